@@ -1,0 +1,396 @@
+/*
+ * sv_oracle.c -- float64 CPU oracle for batched speculative-decoding verification.
+ *
+ * TEST INFRASTRUCTURE ONLY. Plain, single-threaded, slow on purpose: every
+ * step is written out in the order the pages give it, in double precision,
+ * with no blocking, fusion or reordering. Only the test-suite, the smoke
+ * check and the benchmark's CPU-baseline leg load this file's library; the
+ * CUDA library shares no code with it and never calls it.
+ *
+ * Pages this follows (cited by title and section):
+ *  [RU] "Как работает speculative decoding на уровне логитов, а не токенов?"
+ *       (aivaro.ru): §5 "Алгоритм ... (пошагово)", step 3 (accept when
+ *       p_target >= p_draft, else reject with probability 1 - p_target/p_draft;
+ *       discard every later draft; resample from max(0, p_target - p_draft)/Z)
+ *       and §6 (accept(x) = min(1, p_target(x)/p_draft(x))).
+ *  [VN] "Speculative decoding" (aihero.vn): section "Chấp nhận bằng tỉ lệ,
+ *       không chỉ bằng argmax" (q = draft, p = target, acceptance
+ *       min(1, p(x)/q(x)), residual proportional to max(0, p - q), normalised;
+ *       verification stops at the first rejection), the paragraph on
+ *       temperature/top-k/top-p (transforms applied consistently to both
+ *       distributions), and "Cùng phân bố không có nghĩa cùng chuỗi" (greedy
+ *       decoding uses a different check from sampling).
+ *  [ZH] Hung-yi Lee, "Introduction to Generative AI 2024 Spring", lecture 16
+ *       notes (CSDN): §4 "推测解码验证流程图", item 1 (target distribution P_i
+ *       is computed at the position before draft token i), item 3 (truncate at
+ *       the failed position, emit the target's own token there) and item 4
+ *       "The Bonus Token" (all k accepted => one more token from the next
+ *       target distribution).
+ *  [PH] Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as
+ *       1, 2, 3", SC'11, §4: the Philox4x32 bijection and its key schedule.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - temperature divides both logit rows before the softmax; greedy ignores it;
+ *  - target row i verifies draft token x_i; target row K is the bonus row;
+ *  - accept iff u < r with u drawn in [0, 1) (the pseudocode's strict test);
+ *  - u_i = lane 0 of Philox(key = seed, counter = (i, b, 0, 0)); the sampling
+ *    uniform at the emitted position j is lane 1 of the same counter (j, b);
+ *    a uniform is (32-bit word >> 8) * 2^-24, exact in float and double;
+ *  - sampling is the inverse CDF in index order: smallest k with C_k > u*Z;
+ *  - if rounding leaves no such k, the largest k with w_k > 0 is taken; if a
+ *    residual sums to 0 (possible only through rounding), p_j is sampled;
+ *  - greedy: lowest index attaining the maximum raw logit; accept while it
+ *    equals the draft token; emit the target's argmax at the first mismatch,
+ *    or the bonus row's argmax when all K match;
+ *  - positions after the emitted token are -1;
+ *  - a row holding NaN or +inf, or all -inf, makes the sequence invalid in
+ *    sampling mode; a NaN in a target row does so in greedy mode; a draft token
+ *    outside [0, V) does so in both modes. Invalid sequences report
+ *    num_accepted = -1, all out_tokens = -1 and a status bit.
+ */
+#include "sv_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------- */
+/* Philox4x32-10 [PH] §4.                                                     */
+/* One round: two 32x32->64 multiplications of words 0 and 2 by the round     */
+/* multipliers; the high halves are xored with the other two words and the    */
+/* round key, and the words are permuted. The key is bumped by the Weyl        */
+/* constants (golden ratio and sqrt(3) - 1, as 32-bit fractions) each round.  */
+/* ------------------------------------------------------------------------- */
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+void svo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4])
+{
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    int round;
+    for (round = 0; round < 10; ++round) {
+        uint64_t prod0 = (uint64_t)PHILOX_M0 * (uint64_t)x0;
+        uint64_t prod1 = (uint64_t)PHILOX_M1 * (uint64_t)x2;
+        uint32_t hi0 = (uint32_t)(prod0 >> 32), lo0 = (uint32_t)prod0;
+        uint32_t hi1 = (uint32_t)(prod1 >> 32), lo1 = (uint32_t)prod1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+        k0 += PHILOX_W0;
+        k1 += PHILOX_W1;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+double svo_uniform(uint64_t seed, uint32_t seq, uint32_t pos, int lane)
+{
+    uint32_t ctr[4], key[2], r[4];
+    ctr[0] = pos; ctr[1] = seq; ctr[2] = 0; ctr[3] = 0;
+    key[0] = (uint32_t)(seed & 0xFFFFFFFFu);
+    key[1] = (uint32_t)(seed >> 32);
+    svo_philox4x32_10(ctr, key, r);
+    return (double)(r[lane & 3] >> 8) * (1.0 / 16777216.0);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Element access. bfloat16 is the upper half of an IEEE binary32, so placing */
+/* its 16 bits in the high half of a 32-bit word gives the float exactly.     */
+/* ------------------------------------------------------------------------- */
+double svo_elem(const void* row, int64_t k, int dtype)
+{
+    float f;
+    if (dtype == SVO_F32) {
+        memcpy(&f, (const unsigned char*)row + 4 * k, 4);
+    } else {
+        uint16_t h;
+        uint32_t bits;
+        memcpy(&h, (const unsigned char*)row + 2 * k, 2);
+        bits = (uint32_t)h << 16;
+        memcpy(&f, &bits, 4);
+    }
+    return (double)f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Softmax of logits / T, through its log-normaliser ([RU] §9 applies a       */
+/* softmax to each row; [VN] asks for the temperature on both rows).          */
+/* lse = m + log(sum_k exp(s_k - m)), s_k = l_k / T, m = max_k s_k.           */
+/* ------------------------------------------------------------------------- */
+int svo_row_lse(const void* row, int64_t V, int dtype, double T, double* lse)
+{
+    double m = -INFINITY, acc = 0.0;
+    int64_t k;
+    for (k = 0; k < V; ++k) {
+        double s = svo_elem(row, k, dtype) / T;
+        if (isnan(s) || s == INFINITY) {
+            *lse = NAN;
+            return SVO_NONFINITE;
+        }
+        if (s > m) m = s;
+    }
+    if (m == -INFINITY) {
+        *lse = NAN;
+        return SVO_NONFINITE;
+    }
+    for (k = 0; k < V; ++k) acc += exp(svo_elem(row, k, dtype) / T - m);
+    *lse = m + log(acc);
+    return 0;
+}
+
+double svo_log_prob(const void* row, int64_t k, int dtype, double T, double lse)
+{
+    return svo_elem(row, k, dtype) / T - lse;
+}
+
+/* [RU] §6, [VN]: accept(x) = min(1, p(x)/q(x)), taken in the log domain so     */
+/* that q(x) underflowing to 0 still gives ratio +inf, i.e. 1.                 */
+double svo_accept_prob(double log_p, double log_q)
+{
+    if (log_p >= log_q) return 1.0;
+    return exp(log_p - log_q);
+}
+
+/* [RU] §5 step 3 / §6 and [VN]: after a rejection the next token comes from    */
+/* max(0, p - q)/Z; [ZH] §4 item 4: after K acceptances it comes from the       */
+/* bonus row's own distribution p.                                              */
+void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
+                        double T, double lse_t, double lse_d, double* w)
+{
+    int64_t k;
+    for (k = 0; k < V; ++k) {
+        double p = exp(svo_log_prob(target_row, k, dtype, T, lse_t));
+        if (draft_row != NULL) {
+            double q = exp(svo_log_prob(draft_row, k, dtype, T, lse_d));
+            w[k] = (p > q) ? (p - q) : 0.0;
+        } else {
+            w[k] = p;
+        }
+    }
+}
+
+int64_t svo_inverse_cdf(const double* w, int64_t V, double u, double* margin)
+{
+    double Z = 0.0, target, C = 0.0, prev;
+    int64_t k;
+    for (k = 0; k < V; ++k) Z += w[k];
+    if (!(Z > 0.0)) {
+        *margin = 0.0;
+        return -1;
+    }
+    target = u * Z;
+    for (k = 0; k < V; ++k) {
+        prev = C;
+        C += w[k];
+        if (C > target) {
+            double lo = target - prev, hi = C - target;
+            *margin = (lo < hi ? lo : hi) / Z;
+            return k;
+        }
+    }
+    /* Rounding left u*Z at or above the total: take the last token with weight. */
+    for (k = V - 1; k >= 0; --k) {
+        if (w[k] > 0.0) {
+            *margin = 0.0;
+            return k;
+        }
+    }
+    *margin = 0.0;
+    return -1;
+}
+
+/* Greedy check ([VN], "Cùng phân bố..."): the raw-logit argmax; the lowest     */
+/* index wins ties.                                                              */
+int64_t svo_row_argmax(const void* row, int64_t V, int dtype, int* has_nan)
+{
+    int64_t k, best_k = 0;
+    double best = -INFINITY;
+    *has_nan = 0;
+    for (k = 0; k < V; ++k) {
+        double v = svo_elem(row, k, dtype);
+        if (isnan(v)) *has_nan = 1;
+        else if (v > best) {
+            best = v;
+            best_k = k;
+        }
+    }
+    return best_k;
+}
+
+/* ------------------------------------------------------------------------- */
+/* One sequence.                                                              */
+/* ------------------------------------------------------------------------- */
+static void fail_sequence(int64_t b, int64_t K, int32_t status, int32_t* out_tokens,
+                          int32_t* num_accepted, int32_t* seq_status)
+{
+    int64_t i;
+    for (i = 0; i <= K; ++i) out_tokens[b * (K + 1) + i] = -1;
+    num_accepted[b] = -1;
+    if (seq_status) seq_status[b] = status;
+}
+
+static void verify_sampling(const void* target, const void* draft, const int32_t* tokens,
+                            int64_t b, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
+                            int32_t* out_tokens, int32_t* num_accepted, double* lse_t_out,
+                            double* lse_d_out, double* log_ratio_out, double* accept_margin,
+                            double* sample_margin, int32_t* seq_status)
+{
+    const size_t esz = (dtype == SVO_F32) ? 4 : 2;
+    const unsigned char* trow0 = (const unsigned char*)target + (size_t)(b * (K + 1)) * V * esz;
+    const unsigned char* drow0 =
+        draft ? (const unsigned char*)draft + (size_t)(b * K) * V * esz : NULL;
+    double* lse_t = (double*)malloc(sizeof(double) * (size_t)(K + 1));
+    double* lse_d = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
+    double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    int32_t status = 0;
+    int64_t i, j;
+    double margin;
+    int64_t token;
+
+    /* Every draft token must name a vocabulary entry. */
+    for (i = 0; i < K; ++i) {
+        int32_t x = tokens[b * K + i];
+        if (x < 0 || (int64_t)x >= V) status |= SVO_BAD_TOKEN;
+    }
+    /* Step 1: the normaliser of every target row (K verify rows + bonus row)   */
+    /* and every draft row.                                                     */
+    for (i = 0; i <= K; ++i)
+        status |= svo_row_lse(trow0 + (size_t)i * V * esz, V, dtype, T, &lse_t[i]);
+    for (i = 0; i < K; ++i)
+        status |= svo_row_lse(drow0 + (size_t)i * V * esz, V, dtype, T, &lse_d[i]);
+    for (i = 0; i <= K; ++i)
+        if (lse_t_out) lse_t_out[b * (K + 1) + i] = lse_t[i];
+    for (i = 0; i < K; ++i)
+        if (lse_d_out) lse_d_out[b * K + i] = lse_d[i];
+    if (accept_margin)
+        for (i = 0; i < K; ++i) accept_margin[b * K + i] = NAN;
+    if (sample_margin) sample_margin[b] = NAN;
+    if (status != 0) {
+        fail_sequence(b, K, status, out_tokens, num_accepted, seq_status);
+        goto done;
+    }
+
+    /* Log ratio log p_i(x_i) - log q_i(x_i) at every position (diagnostic). */
+    for (i = 0; i < K; ++i) {
+        int32_t x = tokens[b * K + i];
+        double lp = svo_log_prob(trow0 + (size_t)i * V * esz, x, dtype, T, lse_t[i]);
+        double lq = svo_log_prob(drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i]);
+        if (log_ratio_out) log_ratio_out[b * K + i] = lp - lq;
+    }
+
+    /* Step 2: positions in order; accept x_i with probability min(1, p/q);     */
+    /* the first rejection ends the scan ([RU] §5 step 3, [VN], [ZH] §4 item 3). */
+    j = K;
+    for (i = 0; i < K; ++i) {
+        int32_t x = tokens[b * K + i];
+        double lp = svo_log_prob(trow0 + (size_t)i * V * esz, x, dtype, T, lse_t[i]);
+        double lq = svo_log_prob(drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i]);
+        double r = svo_accept_prob(lp, lq);
+        double u = svo_uniform(seed, (uint32_t)b, (uint32_t)i, 0);
+        if (accept_margin) accept_margin[b * K + i] = fabs(u - r);
+        if (!(u < r)) {
+            j = i;
+            break;
+        }
+    }
+
+    /* Step 3: the token at position j -- the residual after a rejection, the   */
+    /* bonus row after K acceptances.                                           */
+    if (j < K) {
+        svo_sample_weights(trow0 + (size_t)j * V * esz, drow0 + (size_t)j * V * esz, V, dtype, T,
+                           lse_t[j], lse_d[j], w);
+    } else {
+        svo_sample_weights(trow0 + (size_t)K * V * esz, NULL, V, dtype, T, lse_t[K], 0.0, w);
+    }
+    token = svo_inverse_cdf(w, V, svo_uniform(seed, (uint32_t)b, (uint32_t)j, 1), &margin);
+    if (token < 0) {
+        /* The residual summed to zero through rounding: sample p_j instead. */
+        svo_sample_weights(trow0 + (size_t)j * V * esz, NULL, V, dtype, T, lse_t[j], 0.0, w);
+        token = svo_inverse_cdf(w, V, svo_uniform(seed, (uint32_t)b, (uint32_t)j, 1), &margin);
+        margin = 0.0;
+    }
+    if (sample_margin) sample_margin[b] = margin;
+
+    for (i = 0; i < j; ++i) out_tokens[b * (K + 1) + i] = tokens[b * K + i];
+    out_tokens[b * (K + 1) + j] = (int32_t)token;
+    for (i = j + 1; i <= K; ++i) out_tokens[b * (K + 1) + i] = -1;
+    num_accepted[b] = (int32_t)j;
+    if (seq_status) seq_status[b] = 0;
+
+done:
+    free(lse_t);
+    free(lse_d);
+    free(w);
+}
+
+static void verify_greedy(const void* target, const int32_t* tokens, int64_t b, int64_t K,
+                          int64_t V, int dtype, int32_t* out_tokens, int32_t* num_accepted,
+                          double* accept_margin, double* sample_margin, int32_t* seq_status)
+{
+    const size_t esz = (dtype == SVO_F32) ? 4 : 2;
+    const unsigned char* trow0 = (const unsigned char*)target + (size_t)(b * (K + 1)) * V * esz;
+    int64_t* a = (int64_t*)malloc(sizeof(int64_t) * (size_t)(K + 1));
+    int32_t status = 0;
+    int64_t i, j;
+
+    for (i = 0; i < K; ++i) {
+        int32_t x = tokens[b * K + i];
+        if (x < 0 || (int64_t)x >= V) status |= SVO_BAD_TOKEN;
+    }
+    for (i = 0; i <= K; ++i) {
+        int has_nan;
+        a[i] = svo_row_argmax(trow0 + (size_t)i * V * esz, V, dtype, &has_nan);
+        if (has_nan) status |= SVO_NONFINITE;
+    }
+    if (accept_margin)
+        for (i = 0; i < K; ++i) accept_margin[b * K + i] = NAN;
+    if (sample_margin) sample_margin[b] = NAN;
+    if (status != 0) {
+        fail_sequence(b, K, status, out_tokens, num_accepted, seq_status);
+        free(a);
+        return;
+    }
+    j = K;
+    for (i = 0; i < K; ++i) {
+        if (a[i] != (int64_t)tokens[b * K + i]) {
+            j = i;
+            break;
+        }
+    }
+    for (i = 0; i < j; ++i) out_tokens[b * (K + 1) + i] = tokens[b * K + i];
+    out_tokens[b * (K + 1) + j] = (int32_t)a[j];
+    for (i = j + 1; i <= K; ++i) out_tokens[b * (K + 1) + i] = -1;
+    num_accepted[b] = (int32_t)j;
+    if (seq_status) seq_status[b] = 0;
+    free(a);
+}
+
+int svo_verify(const void* target, const void* draft, const int32_t* tokens,
+               int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed, int mode,
+               int64_t b0, int64_t b1, int32_t* out_tokens, int32_t* num_accepted,
+               double* lse_t, double* lse_d, double* log_ratio,
+               double* accept_margin, double* sample_margin, int32_t* seq_status)
+{
+    int64_t b;
+    if (B < 0 || K < 0 || V < 1 || b0 < 0 || b1 > B || b0 > b1) return -1;
+    if (dtype != SVO_F32 && dtype != SVO_BF16) return -1;
+    if (mode != SVO_SAMPLE && mode != SVO_GREEDY) return -1;
+    if (target == NULL || out_tokens == NULL || num_accepted == NULL) return -1;
+    if (K > 0 && tokens == NULL) return -1;
+    if (mode == SVO_SAMPLE && (K > 0 && draft == NULL)) return -1;
+    if (mode == SVO_SAMPLE && !(T > 0.0 && isfinite(T))) return -1;
+    for (b = b0; b < b1; ++b) {
+        if (mode == SVO_SAMPLE)
+            verify_sampling(target, draft, tokens, b, K, V, dtype, T, seed, out_tokens,
+                            num_accepted, lse_t, lse_d, log_ratio, accept_margin, sample_margin,
+                            seq_status);
+        else
+            verify_greedy(target, tokens, b, K, V, dtype, out_tokens, num_accepted,
+                          accept_margin, sample_margin, seq_status);
+    }
+    return 0;
+}

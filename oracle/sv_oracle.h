@@ -1,0 +1,89 @@
+/*
+ * sv_oracle.h -- declarations of the float64 CPU oracle for speculative-decoding
+ * verification.
+ *
+ * TEST INFRASTRUCTURE ONLY. The oracle is the slow, plain, obviously-correct
+ * statement of what the verification step computes. Only the test-suite, the
+ * smoke check and the benchmark's CPU-baseline leg load it. The CUDA library
+ * never includes, links or calls anything declared here, and this header shares
+ * nothing with the library's own header.
+ *
+ * Conventions (fixed by the pages, see sv_oracle.c for the citations):
+ *   p = target distribution, q = draft distribution, both softmax(logits / T).
+ *   target rows: [B, K+1, V]; row i < K verifies draft token x_i, row K is the
+ *   bonus row. draft rows: [B, K, V]. Row-major, contiguous.
+ *   dtype 0 = IEEE binary32, dtype 1 = bfloat16 (raw 16-bit patterns).
+ */
+#ifndef SV_ORACLE_H
+#define SV_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { SVO_F32 = 0, SVO_BF16 = 1 };
+enum { SVO_SAMPLE = 0, SVO_GREEDY = 1 };
+
+/* Per-sequence status bits written by svo_verify. */
+enum { SVO_BAD_TOKEN = 1, SVO_NONFINITE = 2 };
+
+/* Philox4x32 with 10 rounds, one block: out = Philox(ctr, key). */
+void svo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* Uniform in [0, 1 - 2^-24] from lane `lane` (0..3) of Philox4x32-10 with
+ * key = (lo32(seed), hi32(seed)) and counter = (pos, seq, 0, 0). */
+double svo_uniform(uint64_t seed, uint32_t seq, uint32_t pos, int lane);
+
+/* Value of element k of a row, exactly widened to double. */
+double svo_elem(const void* row, int64_t k, int dtype);
+
+/* Natural-log log-sum-exp of the row scaled by 1/T. Returns 0 on success, or
+ * SVO_NONFINITE (and *lse = NaN) when the row holds a NaN or +inf, or is all -inf. */
+int svo_row_lse(const void* row, int64_t V, int dtype, double T, double* lse);
+
+/* log p(k) = l_k / T - lse for one row. */
+double svo_log_prob(const void* row, int64_t k, int dtype, double T, double lse);
+
+/* Acceptance probability min(1, p/q) from the two log-probabilities. */
+double svo_accept_prob(double log_p, double log_q);
+
+/* Sampling weights: w_k = max(0, p_k - q_k) when draft_row != NULL (residual
+ * after a rejection), else w_k = p_k (bonus row). */
+void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
+                        double T, double lse_t, double lse_d, double* w);
+
+/* Inverse CDF: smallest k with C_k > u * Z, C the running sum of w in index
+ * order and Z = C_{V-1}. *margin receives the distance from u*Z to the nearer
+ * edge of the chosen token's interval, divided by Z. Returns -1 if Z is 0. */
+int64_t svo_inverse_cdf(const double* w, int64_t V, double u, double* margin);
+
+/* Lowest index attaining the maximum of the raw row; *has_nan set to 1 when the
+ * row holds a NaN (the index is then meaningless). */
+int64_t svo_row_argmax(const void* row, int64_t V, int dtype, int* has_nan);
+
+/*
+ * Verify sequences b in [b0, b1) of a batch of B.
+ *   target      [B, K+1, V]       draft [B, K, V] (unused, may be NULL, when greedy)
+ *   tokens      [B, K] int32 (may be NULL when K == 0)
+ *   out_tokens  [B, K+1] int32    num_accepted [B] int32
+ * Optional outputs (NULL to skip), all indexed like the inputs:
+ *   lse_t [B, K+1], lse_d [B, K], log_ratio [B, K]  (sampling mode only)
+ *   accept_margin [B, K]: |u_i - r_i| for every decision taken, NaN elsewhere
+ *   sample_margin [B]:    normalised distance of u'*Z to the chosen interval's
+ *                         edges (0 when the rounding fall-backs fired; NaN in greedy)
+ *   seq_status [B]
+ * Returns 0, or -1 on an invalid argument.
+ */
+int svo_verify(const void* target, const void* draft, const int32_t* tokens,
+               int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed, int mode,
+               int64_t b0, int64_t b1, int32_t* out_tokens, int32_t* num_accepted,
+               double* lse_t, double* lse_d, double* log_ratio,
+               double* accept_margin, double* sample_margin, int32_t* seq_status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SV_ORACLE_H */

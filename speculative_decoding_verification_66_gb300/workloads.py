@@ -1,0 +1,133 @@
+"""Seeded synthetic inputs for speculative-decoding verification.
+
+This module only draws inputs. It holds none of the verification arithmetic
+(no acceptance ratio, residual or sampling rule), so that both the CUDA path
+and the CPU oracle can be fed from it without sharing any of the method.
+
+The pages' own workload (a TinyLlama draft and a Llama-2-7B target on 50-100
+token prompts) needs trained weights and prompts that are not available. The
+five workloads below stand in for it. Their logits are synthetic, with the
+shapes and value distributions listed in ``WORKLOADS``. Each draft row is a
+noisy copy of its target row. Draft tokens are drawn from the draft's own
+temperature-scaled softmax, as a draft model would draw them. Greedy drafts
+are the argmax of a noisy copy.
+"""
+from __future__ import annotations
+
+import dataclasses
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    B: int
+    K: int
+    V: int
+    dtype: str          # "f32" or "bf16": logits storage type
+    mode: str           # "sample" or "greedy"
+    temperature: float
+    target_std: float
+    spike: float        # added at one uniformly drawn index of every target row (0 = none)
+    draft_scale: float  # draft = draft_scale * target + N(0, draft_noise^2)
+    draft_noise: float
+
+    @property
+    def label(self) -> str:
+        t = f" T={self.temperature:g}" if self.mode == "sample" else ""
+        return f"B={self.B} K={self.K} V={self.V} {self.dtype} {self.mode}{t}"
+
+    def resized(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+WORKLOADS = {
+    # B=8, K=4, V=32000 fp32: target ~ N(0, 2^2); draft = target + N(0, 0.5^2); T = 1.
+    "small_f32": Workload("small_f32", 8, 4, 32000, "f32", "sample", 1.0, 2.0, 0.0, 1.0, 0.5),
+    # B=64, K=4, V=32000 bf16: target ~ N(0, 3^2) + 8 at one index per row; draft = target + N(0, 1).
+    "spiky_bf16": Workload("spiky_bf16", 64, 4, 32000, "bf16", "sample", 1.0, 3.0, 8.0, 1.0, 1.0),
+    # B=256, K=8, V=128256 bf16, T = 0.7 on both: target ~ N(0, 2.5^2); draft = 0.8 target + N(0, 1).
+    "llama3_bf16": Workload("llama3_bf16", 256, 8, 128256, "bf16", "sample", 0.7, 2.5, 0.0, 0.8, 1.0),
+    # B=32, K=16, V=152064 bf16: target ~ N(0, 2^2); draft = target + N(0, 0.3^2) (long accepted runs).
+    "qwen_long_bf16": Workload("qwen_long_bf16", 32, 16, 152064, "bf16", "sample", 1.0, 2.0, 0.0,
+                               1.0, 0.3),
+    # B=512, K=4, V=128256 bf16 greedy: target ~ N(0, 2^2); drafts = argmax(target + N(0, 1.5^2)).
+    "greedy_bf16": Workload("greedy_bf16", 512, 4, 128256, "bf16", "greedy", 1.0, 2.0, 0.0, 1.0, 1.5),
+}
+
+# The workload whose throughput is the headline figure.
+HEADLINE = "llama3_bf16"
+
+
+def torch_dtype(name: str) -> torch.dtype:
+    return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
+
+
+def make_inputs(wl: Workload, seed: int, device="cpu") -> dict:
+    """Draw one batch for ``wl``.
+
+    Returns dict(target [B, K+1, V], draft [B, K, V] or None, tokens [B, K] int32),
+    all on ``device``. Noise is drawn in float32 from a generator seeded with
+    ``seed`` on ``device``, then stored in the workload's dtype. Draft tokens are
+    drawn from the *stored* draft logits, so they follow the draft distribution
+    the verifier sees.
+    """
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    B, K, V = wl.B, wl.K, wl.V
+    dt = torch_dtype(wl.dtype)
+    tgt = torch.randn((B, K + 1, V), generator=g, device=dev, dtype=torch.float32)
+    tgt.mul_(wl.target_std)
+    if wl.spike != 0.0 and B * (K + 1) > 0:
+        idx = torch.randint(0, V, (B, K + 1, 1), generator=g, device=dev)
+        tgt.scatter_add_(2, idx, torch.full((B, K + 1, 1), wl.spike, device=dev))
+    target = tgt.to(dt)
+    if wl.mode == "greedy":
+        noisy = tgt[:, :K] + wl.draft_noise * torch.randn((B, K, V), generator=g, device=dev)
+        tokens = noisy.argmax(dim=-1).to(torch.int32) if K > 0 else torch.zeros(
+            (B, 0), dtype=torch.int32, device=dev)
+        del tgt, noisy
+        return {"target": target, "draft": None, "tokens": tokens.contiguous()}
+    drf = tgt[:, :K] * wl.draft_scale
+    drf.add_(wl.draft_noise * torch.randn((B, K, V), generator=g, device=dev))
+    draft = drf.to(dt)
+    del tgt, drf
+    tokens = draw_from_logits(draft, wl.temperature, g)
+    return {"target": target, "draft": draft, "tokens": tokens}
+
+
+def draw_from_logits(logits: torch.Tensor, temperature: float, g: torch.Generator) -> torch.Tensor:
+    """One token per row from softmax(logits / T): what a draft model's sampler does."""
+    B, K, V = logits.shape
+    if B * K == 0:
+        return torch.zeros((B, K), dtype=torch.int32, device=logits.device)
+    out = torch.empty((B * K,), dtype=torch.int64, device=logits.device)
+    flat = logits.reshape(B * K, V)
+    step = max(1, (1 << 28) // max(V, 1))
+    for s in range(0, B * K, step):
+        probs = torch.softmax(flat[s:s + step].float() / temperature, dim=-1)
+        out[s:s + step] = torch.multinomial(probs, 1, generator=g).squeeze(1)
+    return out.view(B, K).to(torch.int32)
+
+
+def bf16_bits(t: torch.Tensor):
+    """Host numpy view of a bfloat16 tensor's raw 16-bit patterns (uint16)."""
+    import numpy as np
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def to_host_arrays(inputs: dict):
+    """(target, draft, tokens) as numpy arrays in the layout the oracle reads."""
+    import numpy as np
+
+    def conv(t):
+        if t is None:
+            return None
+        if t.dtype == torch.bfloat16:
+            return bf16_bits(t)
+        return t.detach().cpu().contiguous().numpy().astype(np.float32, copy=False)
+
+    return conv(inputs["target"]), conv(inputs["draft"]), \
+        inputs["tokens"].detach().cpu().numpy().astype(np.int32)

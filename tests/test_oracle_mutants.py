@@ -1,0 +1,58 @@
+"""The pins must catch plausible mistakes in the oracle.
+
+Each case below plants one mistake in a copy of ``oracle/sv_oracle.c`` (a
+flipped sign, a swapped operand, a wrong index, a dropped term...), builds the
+copy into a temporary directory and runs the pin suite against it in a fresh
+process. The suite has to fail for every one of them. Nothing here touches the
+real oracle or any GPU.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "sv_oracle.c")
+
+MUTANTS = {
+    "residual_sign_flipped": ("w[k] = (p > q) ? (p - q) : 0.0;", "w[k] = (q > p) ? (q - p) : 0.0;"),
+    "ratio_inverted": ("return exp(log_p - log_q);", "return exp(log_q - log_p);"),
+    "accept_test_inverted": ("if (!(u < r)) {", "if (u < r) {"),
+    "no_truncation": ("            j = i;\n            break;\n        }\n    }\n\n    /* Step 3",
+                      "            j = i;\n        }\n    }\n\n    /* Step 3"),
+    "bonus_row_off_by_one": ("svo_sample_weights(trow0 + (size_t)K * V * esz, NULL",
+                             "svo_sample_weights(trow0 + (size_t)(K - 1) * V * esz, NULL"),
+    "sampling_uses_accept_lane": ("(uint32_t)b, (uint32_t)j, 1), &margin);\n    if (token < 0)",
+                                  "(uint32_t)b, (uint32_t)j, 0), &margin);\n    if (token < 0)"),
+    "temperature_dropped_in_max": ("double s = svo_elem(row, k, dtype) / T;",
+                                   "double s = svo_elem(row, k, dtype);"),
+    "lse_shift_sign": ("acc += exp(svo_elem(row, k, dtype) / T - m);",
+                       "acc += exp(svo_elem(row, k, dtype) / T + m);"),
+    "argmax_last_occurrence": ("else if (v > best) {", "else if (v >= best) {"),
+    "philox_words_swapped": ("uint32_t y1 = lo1;", "uint32_t y1 = lo0;"),
+    "philox_key_schedule_dropped": ("k1 += PHILOX_W1;", ""),
+    "draft_row_index": ("drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i]);\n        double r",
+                        "drow0 + (size_t)0 * V * esz, x, dtype, T, lse_d[i]);\n        double r"),
+    "uniform_shift": ("(r[lane & 3] >> 8)", "(r[lane & 3] >> 9)"),
+}
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_planted_mistake(tmp_path, name):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mutant = tmp_path / "sv_oracle.c"
+    mutant.write_text(src.replace(old, new))
+    (tmp_path / "sv_oracle.h").write_text(open(os.path.join(ROOT, "oracle", "sv_oracle.h")).read())
+    so = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-std=c99", "-O2", "-fPIC", "-shared", "-o", str(so), str(mutant),
+                    "-lm"], check=True)
+    env = dict(os.environ, SVO_LIB_PATH=str(so))
+    p = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
+    assert p.returncode != 0, f"mutant {name} passed every pin:\n{p.stdout[-2000:]}"
+    assert "failed" in p.stdout, p.stdout[-2000:]
