@@ -12,10 +12,11 @@ Parity status of each function (how it is pinned, see ``tests/test_oracle_*.py``
   Philox4x32-10 run in its CPU interpreter, plus a uniformity chi-square.
 * ``row_lse`` / ``log_prob`` -- pinned against ``torch.logsumexp`` /
   ``torch.log_softmax`` in float64 and closed forms on constant rows.
-* ``accept_prob`` / ``sample_weights`` / ``inverse_cdf`` / ``verify`` --
+* ``accept_prob`` / ``sample_weights`` / ``race_sample`` / ``verify`` --
   pinned by the pages' two worked two-token examples, the p == q special case,
   exact path sums on tiny vocabularies (output law == target law), Monte-Carlo
-  chi-square of the output marginal and closed-form acceptance rates.
+  chi-square of the output marginal and of the race alone, the race's
+  near-tie law, and closed-form acceptance rates.
 * ``row_argmax`` -- pinned against ``torch.argmax`` (first occurrence).
 
 Arrays: float32 logits are passed as ``np.float32``; bfloat16 logits as their
@@ -82,8 +83,10 @@ def lib() -> ctypes.CDLL:
             L.svo_accept_prob.restype = dbl
             L.svo_sample_weights.argtypes = [vp, vp, i64, i32, dbl, dbl, dbl, vp]
             L.svo_sample_weights.restype = None
-            L.svo_inverse_cdf.argtypes = [vp, i64, dbl, vp]
-            L.svo_inverse_cdf.restype = i64
+            L.svo_race_uniform.argtypes = [u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
+            L.svo_race_uniform.restype = dbl
+            L.svo_race_sample.argtypes = [vp, i64, u64, ctypes.c_uint32, ctypes.c_uint32, vp]
+            L.svo_race_sample.restype = i64
             L.svo_row_argmax.argtypes = [vp, i64, i32, vp]
             L.svo_row_argmax.restype = i64
             L.svo_verify.argtypes = [vp, vp, vp, i64, i64, i64, i32, dbl, u64, i32, i64, i64,
@@ -150,11 +153,15 @@ def sample_weights(target_row, draft_row, T: float, lse_t: float, lse_d: float) 
     return w
 
 
-def inverse_cdf(w: np.ndarray, u: float):
+def race_uniform(seed: int, seq: int, pos: int, k: int) -> float:
+    return lib().svo_race_uniform(seed, seq, pos, k)
+
+
+def race_sample(w: np.ndarray, seed: int, seq: int, pos: int):
     """Returns (token, margin)."""
     w = np.ascontiguousarray(w, dtype=np.float64)
     m = np.zeros(1, dtype=np.float64)
-    tok = lib().svo_inverse_cdf(_ptr(w), w.shape[0], u, _ptr(m))
+    tok = lib().svo_race_sample(_ptr(w), w.shape[0], seed, seq, pos, _ptr(m))
     return int(tok), float(m[0])
 
 

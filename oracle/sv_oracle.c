@@ -33,12 +33,17 @@
  *  - temperature divides both logit rows before the softmax; greedy ignores it;
  *  - target row i verifies draft token x_i; target row K is the bonus row;
  *  - accept iff u < r with u drawn in [0, 1) (the pseudocode's strict test);
- *  - u_i = lane 0 of Philox(key = seed, counter = (i, b, 0, 0)); the sampling
- *    uniform at the emitted position j is lane 1 of the same counter (j, b);
- *    a uniform is (32-bit word >> 8) * 2^-24, exact in float and double;
- *  - sampling is the inverse CDF in index order: smallest k with C_k > u*Z;
- *  - if rounding leaves no such k, the largest k with w_k > 0 is taken; if a
- *    residual sums to 0 (possible only through rounding), p_j is sampled;
+ *  - u_i = lane 0 of Philox(key = seed, counter = (i, b, 0, 0)), mapped to
+ *    (32-bit word >> 8) * 2^-24, exact in float and double;
+ *  - the pages draw the corrected token with a generic multinomial draw; it is
+ *    read here as an exponential race: token = argmax_k w_k / E_k over the
+ *    tokens with w_k > 0, E_k = -ln v_k, v_k the race uniform of token k at
+ *    emitted position j (lane k mod 4 of counter (j, b, 1 + k div 4, 0), mapped
+ *    to (2 (word >> 9) + 1) * 2^-24 in (0, 1)); the lowest index wins an exact
+ *    tie. The first arrival of independent exponential clocks with rates w_k is
+ *    token k with probability w_k / sum(w), so this is a draw from w / Z;
+ *  - if every residual weight rounds to 0 (possible only through rounding),
+ *    p_j is raced instead;
  *  - greedy: lowest index attaining the maximum raw logit; accept while it
  *    equals the draft token; emit the target's argmax at the first mismatch,
  *    or the bonus row's argmax when all K match;
@@ -173,34 +178,37 @@ void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V
     }
 }
 
-int64_t svo_inverse_cdf(const double* w, int64_t V, double u, double* margin)
+double svo_race_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t k)
 {
-    double Z = 0.0, target, C = 0.0, prev;
-    int64_t k;
-    for (k = 0; k < V; ++k) Z += w[k];
-    if (!(Z > 0.0)) {
-        *margin = 0.0;
-        return -1;
-    }
-    target = u * Z;
+    uint32_t ctr[4], key[2], r[4];
+    ctr[0] = pos; ctr[1] = seq; ctr[2] = 1u + (k >> 2); ctr[3] = 0;
+    key[0] = (uint32_t)(seed & 0xFFFFFFFFu);
+    key[1] = (uint32_t)(seed >> 32);
+    svo_philox4x32_10(ctr, key, r);
+    return (double)(2u * (r[k & 3u] >> 9) + 1u) * (1.0 / 16777216.0);
+}
+
+int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq, uint32_t pos,
+                        double* margin)
+{
+    double best = -INFINITY, second = 0.0;
+    int64_t k, best_k = -1;
     for (k = 0; k < V; ++k) {
-        prev = C;
-        C += w[k];
-        if (C > target) {
-            double lo = target - prev, hi = C - target;
-            *margin = (lo < hi ? lo : hi) / Z;
-            return k;
+        double v, E, score;
+        if (!(w[k] > 0.0)) continue;
+        v = svo_race_uniform(seed, seq, pos, (uint32_t)k);
+        E = -log(v);
+        score = w[k] / E;
+        if (score > best) {
+            if (best_k >= 0) second = best;
+            best = score;
+            best_k = k;
+        } else if (score > second) {
+            second = score;
         }
     }
-    /* Rounding left u*Z at or above the total: take the last token with weight. */
-    for (k = V - 1; k >= 0; --k) {
-        if (w[k] > 0.0) {
-            *margin = 0.0;
-            return k;
-        }
-    }
-    *margin = 0.0;
-    return -1;
+    *margin = (best_k >= 0) ? (best - second) / best : 0.0;
+    return best_k;
 }
 
 /* Greedy check ([VN], "Cùng phân bố..."): the raw-logit argmax; the lowest     */
@@ -306,11 +314,11 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
     } else {
         svo_sample_weights(trow0 + (size_t)K * V * esz, NULL, V, dtype, T, lse_t[K], 0.0, w);
     }
-    token = svo_inverse_cdf(w, V, svo_uniform(seed, (uint32_t)b, (uint32_t)j, 1), &margin);
+    token = svo_race_sample(w, V, seed, (uint32_t)b, (uint32_t)j, &margin);
     if (token < 0) {
-        /* The residual summed to zero through rounding: sample p_j instead. */
+        /* Every residual weight rounded to zero: race p_j instead. */
         svo_sample_weights(trow0 + (size_t)j * V * esz, NULL, V, dtype, T, lse_t[j], 0.0, w);
-        token = svo_inverse_cdf(w, V, svo_uniform(seed, (uint32_t)b, (uint32_t)j, 1), &margin);
+        token = svo_race_sample(w, V, seed, (uint32_t)b, (uint32_t)j, &margin);
         margin = 0.0;
     }
     if (sample_margin) sample_margin[b] = margin;

@@ -54,10 +54,17 @@ double svo_accept_prob(double log_p, double log_q);
 void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
                         double T, double lse_t, double lse_d, double* w);
 
-/* Inverse CDF: smallest k with C_k > u * Z, C the running sum of w in index
- * order and Z = C_{V-1}. *margin receives the distance from u*Z to the nearer
- * edge of the chosen token's interval, divided by Z. Returns -1 if Z is 0. */
-int64_t svo_inverse_cdf(const double* w, int64_t V, double u, double* margin);
+/* Race uniform of token k at emitted position `pos` of sequence `seq`: lane
+ * k mod 4 of Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter
+ * (pos, seq, 1 + k div 4, 0), mapped to (2 (word >> 9) + 1) * 2^-24 in (0, 1). */
+double svo_race_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t k);
+
+/* Exponential race: argmax over k with w_k > 0 of w_k / E_k, E_k = -ln(v_k),
+ * v_k the race uniform of token k; lowest index wins exact ties. *margin gets
+ * (best - second best) / best (1 when one token has weight, 0 when none).
+ * Returns -1 if no weight is positive. */
+int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq, uint32_t pos,
+                        double* margin);
 
 /* Lowest index attaining the maximum of the raw row; *has_nan set to 1 when the
  * row holds a NaN (the index is then meaningless). */
@@ -71,8 +78,9 @@ int64_t svo_row_argmax(const void* row, int64_t V, int dtype, int* has_nan);
  * Optional outputs (NULL to skip), all indexed like the inputs:
  *   lse_t [B, K+1], lse_d [B, K], log_ratio [B, K]  (sampling mode only)
  *   accept_margin [B, K]: |u_i - r_i| for every decision taken, NaN elsewhere
- *   sample_margin [B]:    normalised distance of u'*Z to the chosen interval's
- *                         edges (0 when the rounding fall-backs fired; NaN in greedy)
+ *   sample_margin [B]:    relative gap (best - second) / best of the race's two
+ *                         top scores (0 when the zero-residual fall-back fired;
+ *                         NaN in greedy)
  *   seq_status [B]
  * Returns 0, or -1 on an invalid argument.
  */

@@ -1,0 +1,89 @@
+"""Comparison of the CUDA path with the float64 oracle (test infrastructure).
+
+Bit-exact where the method is discrete (accepted counts, tokens, argmaxes,
+status), except for decisions the oracle flags as near-ties: an acceptance
+draw with |u - r| < 1e-5 or a sampling draw within 1e-5 * Z of an edge of the
+chosen token's CDF interval. A flagged sequence is compared exactly up to its
+first flagged decision; past it, either branch is correct, so the GPU output
+is only checked to be a valid verification result. Normalisers and
+log-ratios must agree to 1e-5 relative (absolute below magnitude 1).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+FLAG = 1e-5
+RTOL = 1e-5
+
+
+def close(a, b, tol=RTOL):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.abs(a - b) <= tol * np.maximum(1.0, np.abs(b))
+
+
+def valid_output(out, nacc, x, K, V):
+    if not (0 <= nacc <= K):
+        return False
+    if nacc > 0 and not np.array_equal(out[:nacc], x[:nacc]):
+        return False
+    if not (0 <= out[nacc] < V):
+        return False
+    return bool(np.all(out[nacc + 1:] == -1))
+
+
+def compare(gpu: dict, orc: dict, tokens: np.ndarray, K: int, V: int, rows=None, greedy=False,
+            check_stats=True) -> dict:
+    """Compare GPU outputs with oracle outputs on sequences ``rows`` (all by default).
+
+    ``gpu`` holds numpy arrays for the whole batch; ``orc`` holds the oracle's
+    arrays for the whole batch (only ``rows`` need to be filled). Raises
+    AssertionError on a mismatch; returns counts of decisions and flags.
+    """
+    B = gpu["num_accepted"].shape[0]
+    rows = range(B) if rows is None else rows
+    n_dec = n_flag_dec = n_flag_seq = n_flag_diff = 0
+    for b in rows:
+        sg, so = int(gpu["seq_status"][b]), int(orc["seq_status"][b])
+        assert sg == so, f"seq {b}: status gpu {sg} oracle {so}"
+        og, oo = gpu["out_tokens"][b], orc["out_tokens"][b]
+        ng, no = int(gpu["num_accepted"][b]), int(orc["num_accepted"][b])
+        if so != 0:
+            assert ng == -1 and np.all(og == -1), f"seq {b}: invalid sequence not reported"
+            continue
+        x = tokens[b]
+        if check_stats and not greedy:
+            lt_ok = close(gpu["lse_t"][b], orc["lse_t"][b])
+            assert lt_ok.all(), f"seq {b}: lse_t {gpu['lse_t'][b]} vs {orc['lse_t'][b]}"
+            if K > 0:
+                assert close(gpu["lse_d"][b], orc["lse_d"][b]).all(), f"seq {b}: lse_d"
+                assert close(gpu["log_ratio"][b], orc["log_ratio"][b]).all(), \
+                    f"seq {b}: log_ratio {gpu['log_ratio'][b]} vs {orc['log_ratio'][b]}"
+        if greedy:
+            n_dec += min(no + 1, K) + 1
+            assert ng == no and np.array_equal(og, oo), f"seq {b}: greedy gpu {og} oracle {oo}"
+            continue
+        am = orc["accept_margin"][b]
+        decisions = list(range(min(no + 1, K)))
+        n_dec += len(decisions) + 1
+        first_flag = next((i for i in decisions if am[i] < FLAG), None)
+        s_flag = orc["sample_margin"][b] < FLAG
+        if first_flag is not None:
+            n_flag_seq += 1
+            n_flag_dec += 1
+            assert ng >= first_flag, f"seq {b}: diverged before flagged position {first_flag}"
+            assert np.array_equal(og[:first_flag], oo[:first_flag])
+            assert valid_output(og, ng, x, K, V), f"seq {b}: invalid GPU output {og}"
+            n_flag_diff += int(ng != no or not np.array_equal(og, oo))
+        elif s_flag:
+            n_flag_seq += 1
+            n_flag_dec += 1
+            assert ng == no, f"seq {b}: num_accepted gpu {ng} oracle {no}"
+            assert np.array_equal(og[:no], oo[:no])
+            assert valid_output(og, ng, x, K, V), f"seq {b}: invalid GPU output {og}"
+            n_flag_diff += int(og[no] != oo[no])
+        else:
+            assert ng == no, f"seq {b}: num_accepted gpu {ng} oracle {no} (out {og} vs {oo})"
+            assert np.array_equal(og, oo), f"seq {b}: tokens gpu {og} oracle {oo}"
+    return {"decisions": n_dec, "flagged_decisions": n_flag_dec, "flagged_sequences": n_flag_seq,
+            "flagged_differing": n_flag_diff}

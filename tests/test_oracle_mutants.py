@@ -23,8 +23,11 @@ MUTANTS = {
                       "            j = i;\n        }\n    }\n\n    /* Step 3"),
     "bonus_row_off_by_one": ("svo_sample_weights(trow0 + (size_t)K * V * esz, NULL",
                              "svo_sample_weights(trow0 + (size_t)(K - 1) * V * esz, NULL"),
-    "sampling_uses_accept_lane": ("(uint32_t)b, (uint32_t)j, 1), &margin);\n    if (token < 0)",
-                                  "(uint32_t)b, (uint32_t)j, 0), &margin);\n    if (token < 0)"),
+    "race_score_inverted": ("score = w[k] / E;", "score = w[k] * E;"),
+    "race_clock_sign": ("E = -log(v);", "E = log(v);"),
+    "race_lane_fixed": ("r[k & 3u] >> 9", "r[0] >> 9"),
+    "race_shares_accept_counter": ("ctr[2] = 1u + (k >> 2);", "ctr[2] = (k >> 2);"),
+    "race_keeps_last_tie": ("if (score > best) {", "if (score >= best) {"),
     "temperature_dropped_in_max": ("double s = svo_elem(row, k, dtype) / T;",
                                    "double s = svo_elem(row, k, dtype);"),
     "lse_shift_sign": ("acc += exp(svo_elem(row, k, dtype) / T - m);",

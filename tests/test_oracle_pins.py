@@ -215,16 +215,69 @@ def test_philox_against_triton_interpreter(oracle_mod):
 def test_uniform_is_24bit_and_uniform(oracle_mod):
     from scipy import stats
     n = 200_000
-    u = np.array([oracle_mod.uniform(77, b, i, lane)
-                  for b in range(n // 8) for i in range(4) for lane in (0, 1)])
+    u = np.array([oracle_mod.uniform(77, b, i, 0) for b in range(n // 4) for i in range(4)])
     assert u.min() >= 0.0 and u.max() <= 1.0 - 2.0 ** -24
     assert np.all(u * 2**24 == np.floor(u * 2**24))  # exact multiples of 2^-24
     counts = np.histogram(u, bins=256, range=(0.0, 1.0))[0]
     assert stats.chisquare(counts).pvalue > 1e-4
-    # lanes 0 and 1 of the same counter are not the same stream
-    a = np.array([oracle_mod.uniform(9, b, 0, 0) for b in range(4000)])
-    c = np.array([oracle_mod.uniform(9, b, 0, 1) for b in range(4000)])
-    assert abs(np.corrcoef(a, c)[0, 1]) < 0.1
+
+
+def test_race_uniform_open_interval_and_uniform(oracle_mod):
+    from scipy import stats
+    v = np.array([oracle_mod.race_uniform(5, b, j, k)
+                  for b in range(50) for j in range(4) for k in range(1000)])
+    assert v.min() > 0.0 and v.max() < 1.0
+    m = v * 2**24
+    assert np.all(m == np.floor(m)) and np.all(m % 2 == 1)  # odd multiples of 2^-24
+    counts = np.histogram(v, bins=200, range=(0.0, 1.0))[0]
+    assert stats.chisquare(counts).pvalue > 1e-4
+    # the race stream does not reuse the acceptance uniforms of the same position
+    a = np.array([oracle_mod.uniform(5, b, 0, 0) for b in range(3000)])
+    r = np.array([oracle_mod.race_uniform(5, b, 0, 0) for b in range(3000)])
+    assert abs(np.corrcoef(a, r)[0, 1]) < 0.1
+
+
+@pytest.mark.parametrize("V", [2, 7, 300])
+def test_race_draws_proportional_to_weight(oracle_mod, V):
+    """The exponential race picks token k with probability w_k / sum(w);
+    zero-weight tokens are never picked."""
+    from scipy import stats
+    rng = np.random.default_rng(V)
+    w = rng.gamma(0.7, size=V)
+    if V > 2:
+        w[rng.integers(V)] = 0.0
+    n = 60_000 if V > 10 else 40_000
+    toks = np.array([oracle_mod.race_sample(w, 31, b, 2)[0] for b in range(n)])
+    counts = np.bincount(toks, minlength=V)
+    assert counts[w == 0].sum() == 0
+    keep = w > 0
+    exp = w[keep] / w.sum() * n
+    if V > 10:  # pool sparse cells
+        order = np.argsort(exp)
+        grp = np.cumsum(exp[order]) // 50
+        c2 = np.bincount(grp.astype(int), weights=counts[keep][order])
+        e2 = np.bincount(grp.astype(int), weights=exp[order])
+        nz = e2 > 0
+        assert stats.chisquare(c2[nz], e2[nz]).pvalue > 1e-3
+    else:
+        assert stats.chisquare(counts[keep], exp).pvalue > 1e-3
+
+
+def test_race_near_tie_law(oracle_mod):
+    """Closed form: the relative gap between the race's two best scores is below
+    tau with probability at most tau (memorylessness of the exponential clocks),
+    whatever the number of tokens. This is what keeps near-ties rare at V = 128k."""
+    rng = np.random.default_rng(1)
+    V = 2000
+    w = rng.lognormal(sigma=2.0, size=V)
+    n = 20_000
+    margins = np.array([oracle_mod.race_sample(w, 77, b, 0)[1] for b in range(n)])
+    tau = 0.02
+    frac = np.mean(margins < tau)
+    sd = math.sqrt(tau * (1 - tau) / n)
+    assert frac < tau + 5 * sd
+    assert frac > 0.3 * tau  # and it is not degenerate
+    assert np.all((margins >= 0) & (margins <= 1))
 
 
 # --------------------------------------------------------------------------
