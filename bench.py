@@ -1,0 +1,357 @@
+"""Throughput of batched speculative-decoding verification on GB300.
+
+One step = one spec_verify call over one batch of the headline workload
+(B=256 sequences, K=8 drafts, V=128256, bf16 logits, sampling at T=0.7):
+row statistics over every target and draft row, the acceptance scan, and the
+residual/bonus draw. Inputs are synthetic (seeded generators), resident in
+HBM; two copies of 1.12 GB each are rotated, so no step finds its inputs in
+the 129 MB L2.
+
+Prints one JSON line. `value` = verified sequences per second over all ranks.
+`roofline` is the row-statistics kernel (pass 1, the dominant one), timed with
+CUDA events on its own stream inside the timed loop. `e2e` is the same metric
+through spec_verify_host (host buffers, copies in the timed region).
+`cpu_baseline` is the float64 oracle on this host's cores, on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference      # the oracle as the reference arm
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verified seqs/s and logits HBM GB/s (fraction of GB300 peak) per B×(K+1)×V"
+FALLBACK_HBM_GBS = 6800.0
+PROFILE = os.path.join(ROOT, "profiles", "row_stats_llama3_bf16.md")
+KERNEL_SOURCES = ["row_stats.cu", "sv_device.cuh", "sv_internal.h"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=3000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default=None)
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--e2e-steps", type=int, default=None)
+    p.add_argument("--cpu-seconds", type=float, default=10.0,
+                   help="wall-clock budget of the CPU-baseline sample")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_sha():
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "speculative_decoding_verification_66_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per pass-1 launch from the committed ncu summary, if it was
+    taken on the current kernel source."""
+    if not os.path.exists(PROFILE):
+        return None
+    text = open(PROFILE).read()
+    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+    if not m_sha or not m_tr or m_sha.group(1) != kernel_sha():
+        return None
+    return float(m_tr.group(1))
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[4:8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i] == "Active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": rows[0][1],
+                "reasons": reasons, "samples": len(rows)}
+
+
+def cpu_baseline(wl, host_fn, budget_s: float):
+    """Time the oracle (as it stands) on this host's cores on a bounded sample of
+    the workload: the batch's sequences split over threads, repeated until about
+    `budget_s` seconds of wall time have passed."""
+    import oracle
+    cores = len(os.sched_getaffinity(0))
+    mode = 0 if wl.mode == "sample" else 1
+    t, d, x = host_fn(wl.B)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.verify(t, d, x, wl.temperature, 0x5EED0000 + reps, mode, threads=cores)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 1000:
+            break
+    return {"value": wl.B * reps / el, "unit": "seqs/s", "cores": cores, "kind": "oracle",
+            "sample": f"{reps} pass(es) over the {wl.B} sequences of one batch ({wl.label}), "
+                      f"float64 C oracle, {cores} threads splitting the sequences, {el:.1f} s wall"}
+
+
+def reference_arm(args, wl):
+    """The oracle timed as the reference arm: each step verifies a bounded
+    sample of the workload's sequences on the host's cores."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import torch
+
+    import oracle
+    from speculative_decoding_verification_66_gb300.workloads import make_inputs, to_host_arrays
+    cores = len(os.sched_getaffinity(0))
+    inputs = make_inputs(wl.resized(B=max(cores, 1)), 0, "cpu")
+    t, d, x = to_host_arrays(inputs)
+    mode = 0 if wl.mode == "sample" else 1
+    t0 = time.perf_counter()
+    oracle.verify(t[:1], None if d is None else d[:1], x[:1], wl.temperature, 1, mode)
+    one = time.perf_counter() - t0
+    # Size each step so that warm-up plus timed steps stay near two minutes.
+    per_step = 120.0 / max(1, args.steps + args.warmup)
+    n = int(max(1, min(cores, per_step * cores / max(one, 1e-6))))
+    for w in range(args.warmup):
+        oracle.verify(t[:n], None if d is None else d[:n], x[:n], wl.temperature, w, mode,
+                      threads=min(n, cores))
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        oracle.verify(t[:n], None if d is None else d[:n], x[:n], wl.temperature, 100 + s, mode,
+                      threads=min(n, cores))
+    el = time.perf_counter() - t0
+    value = n * args.steps / el
+    del torch
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "seqs/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(wl),
+            "cpu_baseline": {"value": value, "unit": "seqs/s", "cores": min(n, cores),
+                             "kind": "oracle",
+                             "sample": f"{n} sequence(s) of {wl.label} per step"},
+            "e2e": {"value": value, "unit": "seqs/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_of(wl):
+    return {"workload": wl.label, "B": wl.B, "K": wl.K, "V": wl.V, "logits_dtype": wl.dtype,
+            "mode": wl.mode, "temperature": wl.temperature,
+            "l2": "inputs larger than L2: two 1.1 GB input sets rotated between steps",
+            "parallelism": "independent replicas per GPU (weak scaling, no collective)"}
+
+
+def main():
+    args = parse()
+    from speculative_decoding_verification_66_gb300.workloads import HEADLINE, WORKLOADS
+    wl = WORKLOADS[args.workload or HEADLINE]
+    if args.impl == "reference":
+        reference_arm(args, wl)
+        return
+
+    import torch
+
+    import speculative_decoding_verification_66_gb300 as sv
+    from speculative_decoding_verification_66_gb300.workloads import make_inputs, to_host_arrays
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    sv.load()
+
+    copies = [make_inputs(wl, 1000 * rank + c, dev) for c in range(2)]
+    seeds = [0x5EED0002 + c for c in range(2)]
+    B, K, V = wl.B, wl.K, wl.V
+    es = 2 if wl.dtype == "bf16" else 4
+    mode = wl.mode
+    out = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    nacc = torch.empty((B,), dtype=torch.int32, device=dev)
+    ws = torch.empty(sv.sv_workspace_bytes(B, K, V, copies[0]["target"].dtype, mode),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # Per-copy outcome (deterministic for a fixed seed): bytes the step must move.
+    rows_pass1 = B * (K + 1) + (B * K if mode == "sample" else 0)
+    step_bytes = []
+    accepted = []
+    for c, inp in enumerate(copies):
+        sv.spec_verify(inp["target"], inp["draft"], inp["tokens"], wl.temperature, seeds[c], mode,
+                       out_tokens=out, num_accepted=nacc, workspace=ws)
+        n = nacc.cpu()
+        accepted.append(n.float().mean().item())
+        rejected = int(((n >= 0) & (n < K)).sum())
+        bonus = int((n == K).sum())
+        reread = (2 * rejected + bonus) if mode == "sample" else 0
+        step_bytes.append(es * V * (rows_pass1 + reread) + 4 * B * K + 4 * B * (K + 2))
+    pass1_bytes = es * V * rows_pass1
+
+    def step(i, ev=None):
+        c = i & 1
+        inp = copies[c]
+        if ev is None:
+            sv.spec_verify(inp["target"], inp["draft"], inp["tokens"], wl.temperature, seeds[c],
+                           mode, out_tokens=out, num_accepted=nacc, workspace=ws, stream=stream)
+        else:
+            sv.spec_verify_timed(inp["target"], inp["draft"], inp["tokens"], ev, wl.temperature,
+                                 seeds[c], mode, out_tokens=out, num_accepted=nacc, workspace=ws,
+                                 stream=stream)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            step(i, events[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+    elapsed_ms = start.elapsed_time(stop)
+    if dist:
+        t = torch.tensor([elapsed_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    pass1_ms = sum(e[0].elapsed_time(e[1]) for e in events) / args.steps
+    scan_ms = sum(e[1].elapsed_time(e[2]) for e in events) / args.steps
+    sample_ms = sum(e[2].elapsed_time(e[3]) for e in events) / args.steps
+    ms_per_step = elapsed_ms / args.steps
+    value = world * B * args.steps / (elapsed_ms / 1e3)
+    mean_bytes = sum(step_bytes[i & 1] for i in range(args.steps)) / args.steps
+    peak, peak_src = peaks()
+    step_gbs = mean_bytes / (ms_per_step / 1e3) / 1e9
+    pass1_gbs = pass1_bytes / (pass1_ms / 1e3) / 1e9
+
+    # End to end through the host entry point: pinned host inputs, copies inside.
+    e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
+    h = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in c.items()}
+         for c in copies]
+    h_out = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    h_nacc = torch.empty((B,), dtype=torch.int32).pin_memory()
+    staging = torch.empty(sv.sv_host_staging_bytes(B, K, V, copies[0]["target"].dtype, mode),
+                          dtype=torch.uint8, device=dev)
+
+    def e2e_step(i):
+        c = i & 1
+        sv.spec_verify_host(h[c]["target"], h[c]["draft"], h[c]["tokens"], wl.temperature,
+                            seeds[c], mode, out_tokens=h_out, num_accepted=h_nacc,
+                            staging=staging, device=dev, stream=stream, synchronize=False)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.synchronize()
+    e2e_s = time.perf_counter() - t0
+    if dist:
+        t = torch.tensor([e2e_s], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in h[0].values() if t is not None)
+    d2h = h_out.numel() * 4 + h_nacc.numel() * 4
+
+    if rank != 0:
+        if dist:
+            dist.barrier()
+        return
+    line = {
+        "metric": METRIC, "value": value, "unit": "seqs/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": config_of(wl),
+        "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak,
+        "stage_ms": {"row_stats": pass1_ms, "scan": scan_ms, "sample": sample_ms},
+        "mean_accepted": sum(accepted) / len(accepted),
+        "roofline": {"kernel": "row_stats", "bound": "hbm", "achieved": pass1_gbs, "peak": peak,
+                     "unit": "GB/s", "frac": pass1_gbs / peak, "traffic": profiled_traffic(),
+                     "algorithmic_bytes": pass1_bytes, "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": world * B * e2e_steps / e2e_s, "unit": "seqs/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "clocks": clocks.summary(),
+        "gpu_launches": sv.LAUNCHES[sv.api.mode_code(mode)] * args.steps,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        def host_fn(n):
+            sub = {k: (v[:n] if v is not None else None) for k, v in copies[0].items()}
+            return to_host_arrays(sub)
+        line["cpu_baseline"] = cpu_baseline(wl, host_fn, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,189 @@
+/*
+ * spec_verify.h -- C ABI of libspecverify, batched speculative-decoding
+ * verification on one NVIDIA GB300 (sm_103a).
+ *
+ * What the library computes (the pages it follows, by title and section):
+ *
+ *  - "Как работает speculative decoding на уровне логитов, а не токенов?"
+ *    (aivaro.ru) §5 step 3 and §6: for each drafted position, the draft token
+ *    x is accepted with probability min(1, p_target(x) / p_draft(x)); at the
+ *    first rejection every later draft is dropped and one token is drawn from
+ *    max(0, p_target - p_draft) / Z.
+ *  - "Speculative decoding" (aihero.vn), section on accepting by ratio:
+ *    q is the draft distribution and p the target distribution at the same
+ *    prefix; verification stops at the first rejection; temperature (and any
+ *    other transform) is applied consistently to both distributions; greedy
+ *    decoding uses a different check from sampling.
+ *  - Hung-yi Lee, "Introduction to Generative AI 2024 Spring", lecture 16
+ *    notes, §4 (verification flowchart), item 4 "The Bonus Token": when all k
+ *    drafts pass, the target's distribution at the next position yields one
+ *    extra token, so a round emits up to k + 1 tokens.
+ *
+ * Layout (all row-major and contiguous; b = sequence, i = position):
+ *   target_logits [B, K+1, V]  row i < K is the target distribution at the
+ *                              position of draft token i; row K is the bonus row.
+ *   draft_logits  [B, K, V]    row i produced draft token i.
+ *   draft_tokens  [B, K]       int32.
+ *   out_tokens    [B, K+1]     int32: x_0 .. x_{j-1}, then the corrected (or
+ *                              bonus) token at j, then -1.
+ *   num_accepted  [B]          int32: j, the number of drafts kept (0..K);
+ *                              -1 when the sequence's inputs are invalid.
+ *
+ * Numbers and reproducibility:
+ *   p = softmax(target_logits / T), q = softmax(draft_logits / T), accumulated
+ *   in float32 (rescaled partial sums, double where partials are merged).
+ *   The acceptance uniform of position i of sequence b is lane 0, and the
+ *   sampling uniform lane 1, of Philox4x32-10 with key (lo32(seed),
+ *   hi32(seed)) and counter (i, b, 0, 0), mapped to (word >> 8) * 2^-24.
+ *   Sampling is the inverse CDF in index order. Results are a pure function of
+ *   (inputs, T, seed, mode) on a given GPU model: no float atomics, fixed
+ *   reduction trees, the same answer on every run.
+ *
+ * Memory and streams:
+ *   Every pointer passed to spec_verify / spec_verify_debug / spec_verify_timed
+ *   is DEVICE memory owned by the caller. The library allocates nothing and
+ *   keeps no state between calls other than a per-device cache of launch
+ *   parameters. Calls are asynchronous and stream-ordered: they enqueue work
+ *   on `stream` (a cudaStream_t, NULL = legacy default stream) and return
+ *   without synchronising. Inputs must stay unchanged, and outputs and
+ *   workspace unread, until the stream has passed the call. Two calls that
+ *   share a workspace must be ordered on the GPU (same stream or events).
+ *
+ * Errors:
+ *   Functions return SV_OK (0) or a negative SV_ERR_* code. Argument errors
+ *   are found on the host before anything is enqueued. Data errors found on
+ *   the device (a draft token outside [0, V), a target or draft row holding a
+ *   NaN or +inf or made only of -inf in sampling mode, a NaN target row in
+ *   greedy mode) make that sequence's num_accepted -1 and its out_tokens all
+ *   -1, and set SV_SEQ_* bits in the optional per-sequence status output. No
+ *   input, however malformed, makes a kernel read outside the buffers
+ *   described here.
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Logits storage type. */
+enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 };
+
+/* SV_SAMPLE: rejection sampling (acceptance min(1, p/q), residual, bonus).
+ * SV_GREEDY: accept while argmax(target row i) == x_i (lowest index wins
+ *            ties, raw logits, temperature unused); at the first mismatch,
+ *            or at the bonus row, emit the target row's argmax. */
+enum sv_mode { SV_SAMPLE = 0, SV_GREEDY = 1 };
+
+enum sv_status {
+    SV_OK = 0,
+    SV_ERR_ARG = -1,       /* bad size, mode, temperature or NULL pointer   */
+    SV_ERR_DTYPE = -2,     /* unknown dtype                                 */
+    SV_ERR_ALIGN = -3,     /* logits not 16-byte aligned, ints not 4-byte   */
+    SV_ERR_WORKSPACE = -4, /* workspace NULL, too small or not 256-aligned  */
+    SV_ERR_CUDA = -5,      /* a CUDA runtime call or launch failed          */
+    SV_ERR_SIZE = -6       /* sizes beyond the supported range              */
+};
+
+/* Per-sequence status bits (spec_verify_debug's seq_status output). */
+enum sv_seq_status {
+    SV_SEQ_BAD_TOKEN = 1,  /* a draft token outside [0, V)                  */
+    SV_SEQ_NONFINITE = 2,  /* a NaN / +inf / all -inf row (see above)       */
+    SV_SEQ_TIMEOUT = 4     /* a bounded wait inside a kernel expired        */
+};
+
+/* Supported ranges: 0 <= B < 2^31, 0 <= K <= 1024, 1 <= V < 2^31,
+ * B * (2K + 1) * V * sizeof(element) < 2^62. Temperature (sampling mode):
+ * finite, > 0, with log2(e)/T finite in float32. */
+
+/*
+ * Workspace needed by spec_verify for these sizes on the CURRENT device.
+ * Writes the byte count to *bytes. Returns SV_OK or an SV_ERR_* code.
+ */
+int sv_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode, size_t* bytes);
+
+/*
+ * Verify B sequences of K drafts each (see the file comment for what that
+ * means and for the layouts).
+ *   target_logits  device, [B, K+1, V] of `dtype`, 16-byte aligned.
+ *   draft_logits   device, [B, K, V] of `dtype`, 16-byte aligned; may be NULL
+ *                  when mode == SV_GREEDY or K == 0.
+ *   draft_tokens   device, [B, K] int32; may be NULL when K == 0.
+ *   temperature    divides both target and draft logits (sampling mode only).
+ *   seed           Philox key.
+ *   out_tokens     device, [B, K+1] int32, written.
+ *   num_accepted   device, [B] int32, written.
+ *   workspace      device, >= sv_workspace_bytes(...) bytes, 256-byte aligned,
+ *                  any contents; overwritten.
+ *   stream         cudaStream_t to enqueue on.
+ * B == 0 enqueues nothing and returns SV_OK.
+ */
+int spec_verify(const void* target_logits, const void* draft_logits, const int32_t* draft_tokens,
+                int64_t B, int64_t K, int64_t V, int dtype, float temperature, uint64_t seed,
+                int mode, int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify plus the intermediate values the parity tests compare. Same
+ * arguments and launches, plus (each device memory, each may be NULL):
+ *   lse_t      [B, K+1] double: natural-log log-sum-exp of target_logits / T.
+ *   lse_d      [B, K]   double: the same for draft rows.
+ *   log_ratio  [B, K]   double: log p_i(x_i) - log q_i(x_i).
+ *   seq_status [B]      int32:  SV_SEQ_* bits, 0 for a valid sequence.
+ * In greedy mode lse_t / lse_d / log_ratio are not written.
+ */
+int spec_verify_debug(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                      float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                      int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                      void* stream, double* lse_t, double* lse_d, double* log_ratio,
+                      int32_t* seq_status);
+
+/*
+ * spec_verify with CUDA events recorded on `stream` between its kernels, for
+ * timing the stages in place: events[0] before the row-statistics kernel,
+ * events[1] after it, events[2] after the acceptance scan, events[3] after
+ * the residual/bonus sampler (equal to events[2]'s position in greedy mode).
+ * `events` holds n_events (>= 4) cudaEvent_t handles created by the caller.
+ */
+int spec_verify_timed(const void* target_logits, const void* draft_logits,
+                      const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                      float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                      int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                      void* stream, void* const* events, int n_events);
+
+/*
+ * Device staging bytes spec_verify_host needs for these sizes on the current
+ * device (inputs + outputs + workspace, each 256-byte aligned).
+ */
+int sv_host_staging_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode, size_t* bytes);
+
+/*
+ * End-to-end call from HOST buffers. Copies target/draft logits and draft
+ * tokens from host memory to `staging` (device, >= sv_host_staging_bytes,
+ * 256-byte aligned), runs spec_verify on `stream`, and copies out_tokens and
+ * num_accepted back to host memory, all enqueued on `stream`. Returns after
+ * enqueueing; the host outputs are valid once the stream has been
+ * synchronised. Host buffers should be page-locked (cudaHostAlloc) for the
+ * copies to be asynchronous; pageable memory works but the copies then
+ * synchronise with the host.
+ */
+int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
+                     const int32_t* h_draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                     float temperature, uint64_t seed, int mode, int32_t* h_out_tokens,
+                     int32_t* h_num_accepted, void* staging, size_t staging_bytes, void* stream);
+
+/* Static description of an SV_* return code. Never NULL. */
+const char* sv_error_string(int code);
+
+/* Library ABI version (major * 100 + minor). */
+int sv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

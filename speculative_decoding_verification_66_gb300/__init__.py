@@ -1,0 +1,28 @@
+"""GB300-native batched speculative-decoding verification.
+
+The verification step of speculative decoding (rejection sampling of K draft
+tokens against target and draft logits, truncation at the first rejection,
+residual or bonus sampling; and the greedy variant) as hand-written CUDA for
+sm_103a behind the C ABI in include/spec_verify.h. This package is the thin
+Python binding: ``spec_verify`` and friends take torch tensors and call the
+library; there is no CPU or eager fallback.
+"""
+from .api import (  # noqa: F401
+    LAUNCHES,
+    SV_BF16,
+    SV_F32,
+    SV_GREEDY,
+    SV_SAMPLE,
+    SV_SEQ_BAD_TOKEN,
+    SV_SEQ_NONFINITE,
+    SV_SEQ_TIMEOUT,
+    SpecVerifyError,
+    spec_verify,
+    spec_verify_debug,
+    spec_verify_host,
+    spec_verify_timed,
+    sv_host_staging_bytes,
+    sv_workspace_bytes,
+    version,
+)
+from ._lib import LIB_PATH, LibraryMissing, load  # noqa: F401

@@ -1,0 +1,230 @@
+"""Python binding of the spec_verify C ABI: the same names, torch tensors in.
+
+Argument marshalling only. Every step of the verification runs in the CUDA
+kernels of libspecverify.so; this module turns tensors into pointers and
+sizes, picks the current CUDA stream, and keeps a workspace buffer per device
+and stream so that repeated calls do not allocate.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import torch
+
+from . import _lib
+
+SV_F32, SV_BF16 = 0, 1
+SV_SAMPLE, SV_GREEDY = 0, 1
+SV_SEQ_BAD_TOKEN, SV_SEQ_NONFINITE, SV_SEQ_TIMEOUT = 1, 2, 4
+
+# Kernel launches one spec_verify call makes (row statistics, scan, sampler).
+LAUNCHES = {SV_SAMPLE: 3, SV_GREEDY: 2}
+
+
+class SpecVerifyError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        msg = _lib.load().sv_error_string(code).decode()
+        super().__init__(f"{where}: {msg} (code {code})")
+        self.code = code
+
+
+def _check(code: int, where: str):
+    if code != 0:
+        raise SpecVerifyError(code, where)
+
+
+def dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return SV_F32
+    if t == torch.bfloat16:
+        return SV_BF16
+    raise TypeError(f"logits must be float32 or bfloat16, got {t}")
+
+
+def mode_code(mode) -> int:
+    if isinstance(mode, str):
+        return {"sample": SV_SAMPLE, "greedy": SV_GREEDY}[mode]
+    return int(mode)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def sv_workspace_bytes(B: int, K: int, V: int, dtype, mode) -> int:
+    n = ctypes.c_size_t(0)
+    d = dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    _check(_lib.load().sv_workspace_bytes(B, K, V, d, mode_code(mode), ctypes.byref(n)),
+           "sv_workspace_bytes")
+    return int(n.value)
+
+
+def sv_host_staging_bytes(B: int, K: int, V: int, dtype, mode) -> int:
+    n = ctypes.c_size_t(0)
+    d = dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    _check(_lib.load().sv_host_staging_bytes(B, K, V, d, mode_code(mode), ctypes.byref(n)),
+           "sv_host_staging_bytes")
+    return int(n.value)
+
+
+_ws_lock = threading.Lock()
+_ws_cache: dict = {}
+
+
+def workspace_for(device: torch.device, stream: torch.cuda.Stream, nbytes: int) -> torch.Tensor:
+    """A reusable workspace of at least nbytes for (device, stream)."""
+    key = (device.index, stream.cuda_stream)
+    with _ws_lock:
+        ws = _ws_cache.get(key)
+        if ws is None or ws.numel() < nbytes:
+            ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+            _ws_cache[key] = ws
+    return ws
+
+
+def _shapes(target_logits, draft_logits, draft_tokens, mode):
+    if target_logits.dim() != 3 or not target_logits.is_cuda:
+        raise ValueError("target_logits must be a CUDA tensor [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if K < 0:
+        raise ValueError("target_logits needs K+1 >= 1 rows per sequence")
+    if not target_logits.is_contiguous():
+        raise ValueError("target_logits must be contiguous")
+    if mode == SV_SAMPLE and K > 0:
+        if draft_logits is None or tuple(draft_logits.shape) != (B, K, V):
+            raise ValueError("draft_logits must be [B, K, V] in sampling mode")
+        if draft_logits.dtype != target_logits.dtype or not draft_logits.is_contiguous():
+            raise ValueError("draft_logits must be contiguous with target_logits' dtype")
+        if draft_logits.device != target_logits.device:
+            raise ValueError("draft_logits must be on target_logits' device")
+    if K > 0:
+        if draft_tokens is None or tuple(draft_tokens.shape) != (B, K):
+            raise ValueError("draft_tokens must be [B, K]")
+        if draft_tokens.dtype != torch.int32 or not draft_tokens.is_contiguous():
+            raise ValueError("draft_tokens must be contiguous int32")
+        if draft_tokens.device != target_logits.device:
+            raise ValueError("draft_tokens must be on target_logits' device")
+    return B, K, V
+
+
+def _prepare(target_logits, draft_logits, draft_tokens, mode, out_tokens, num_accepted,
+             workspace, stream):
+    m = mode_code(mode)
+    B, K, V = _shapes(target_logits, draft_logits, draft_tokens, m)
+    dev = target_logits.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    d = dtype_code(target_logits.dtype)
+    need = sv_workspace_bytes(B, K, V, d, m)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, need)
+    return m, B, K, V, d, stream, out_tokens, num_accepted, workspace
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
+                seed: int = 0, mode="sample", *, out_tokens=None, num_accepted=None,
+                workspace=None, stream=None):
+    """Verify B sequences of K drafts. Returns (out_tokens [B, K+1], num_accepted [B]).
+
+    Asynchronous on ``stream`` (default: the current stream of the logits' device).
+    """
+    m, B, K, V, d, stream, out_tokens, num_accepted, workspace = _prepare(
+        target_logits, draft_logits, draft_tokens, mode, out_tokens, num_accepted, workspace,
+        stream)
+    with torch.cuda.device(target_logits.device):
+        _check(_lib.load().spec_verify(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream)), "spec_verify")
+    return out_tokens, num_accepted
+
+
+def spec_verify_debug(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
+                      seed: int = 0, mode="sample", *, workspace=None, stream=None) -> dict:
+    """spec_verify plus the normalisers, log-ratios and per-sequence status."""
+    m, B, K, V, d, stream, out_tokens, num_accepted, workspace = _prepare(
+        target_logits, draft_logits, draft_tokens, mode, None, None, workspace, stream)
+    dev = target_logits.device
+    lse_t = torch.full((B, K + 1), float("nan"), dtype=torch.float64, device=dev)
+    lse_d = torch.full((B, K), float("nan"), dtype=torch.float64, device=dev)
+    log_ratio = torch.full((B, K), float("nan"), dtype=torch.float64, device=dev)
+    seq_status = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_debug(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream),
+            _ptr(lse_t), _ptr(lse_d), _ptr(log_ratio), _ptr(seq_status)), "spec_verify_debug")
+    return {"out_tokens": out_tokens, "num_accepted": num_accepted, "lse_t": lse_t,
+            "lse_d": lse_d, "log_ratio": log_ratio, "seq_status": seq_status}
+
+
+def spec_verify_timed(target_logits, draft_logits, draft_tokens, events, temperature: float = 1.0,
+                      seed: int = 0, mode="sample", *, out_tokens=None, num_accepted=None,
+                      workspace=None, stream=None):
+    """spec_verify with ``events`` (4 torch.cuda.Event(enable_timing=True)) recorded
+    on the launch stream before pass 1, after pass 1, after the scan and after the
+    sampler."""
+    m, B, K, V, d, stream, out_tokens, num_accepted, workspace = _prepare(
+        target_logits, draft_logits, draft_tokens, mode, out_tokens, num_accepted, workspace,
+        stream)
+    handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    with torch.cuda.device(target_logits.device):
+        _check(_lib.load().spec_verify_timed(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream),
+            handles, len(events)), "spec_verify_timed")
+    return out_tokens, num_accepted
+
+
+def spec_verify_host(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
+                     seed: int = 0, mode="sample", *, out_tokens=None, num_accepted=None,
+                     staging=None, device=None, stream=None, synchronize: bool = True):
+    """End to end from host memory: CPU tensors in (pinned for asynchronous copies),
+    CPU tensors out. The library copies inputs to ``staging`` on the device, verifies,
+    and copies the results back, all on one stream."""
+    m = mode_code(mode)
+    if target_logits.dim() != 3 or target_logits.is_cuda:
+        raise ValueError("target_logits must be a CPU tensor [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    d = dtype_code(target_logits.dtype)
+    dev = torch.device(device if device is not None else "cuda")
+    if dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32).pin_memory()
+    need = sv_host_staging_bytes(B, K, V, d, m)
+    if staging is None:
+        staging = workspace_for(dev, stream, need)
+    for t in (target_logits, draft_logits, draft_tokens):
+        if t is not None and (t.is_cuda or not t.is_contiguous()):
+            raise ValueError("host inputs must be contiguous CPU tensors")
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_host(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(staging), staging.numel(), ctypes.c_void_p(stream.cuda_stream)),
+            "spec_verify_host")
+    if synchronize:
+        stream.synchronize()
+    return out_tokens, num_accepted
+
+
+def version() -> int:
+    return int(_lib.load().sv_version())

@@ -1,0 +1,338 @@
+// sv_api.cu -- the C ABI (include/spec_verify.h): argument checks, launch
+// planning, workspace carving and the three launches.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "spec_verify.h"
+#include "sv_internal.h"
+
+#define SV_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using sv::Geometry;
+
+constexpr size_t kAlign = 256;
+constexpr int kMaxDevices = 64;
+
+size_t round_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
+
+struct DeviceCache {
+    bool ready = false;
+    int sms = 0;
+    int blocks[2][2] = {{0, 0}, {0, 0}};  // [es == 2][mode]
+};
+std::mutex g_mu;
+DeviceCache g_cache[kMaxDevices];
+
+// SM count and resident pass-1 CTAs per SM on the current device.
+int device_limits(int es, int mode, int* sms, int* blocks)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceCache& c = g_cache[dev];
+    if (!c.ready) {
+        if (cudaDeviceGetAttribute(&c.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return SV_ERR_CUDA;
+        for (int e = 0; e < 2; ++e)
+            for (int m = 0; m < 2; ++m)
+                if (sv::row_stats_blocks_per_sm(e ? 2 : 4, m, &c.blocks[e][m]) != cudaSuccess)
+                    return SV_ERR_CUDA;
+        c.ready = true;
+    }
+    *sms = c.sms;
+    *blocks = c.blocks[es == 2][mode];
+    return (*sms > 0 && *blocks > 0) ? SV_OK : SV_ERR_CUDA;
+}
+
+struct Layout {
+    size_t partials = 0, seqs = 0, chunk_best = 0, tickets = 0, total = 0;
+};
+
+int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
+{
+    if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+    if (mode != SV_SAMPLE && mode != SV_GREEDY) return SV_ERR_ARG;
+    if (B < 0 || K < 0 || V < 1) return SV_ERR_ARG;
+    if (B >= (int64_t(1) << 31) || K > sv::kMaxK || V >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+    const int64_t es = dtype == SV_BF16 ? 2 : 4;
+    // B (2K + 1) V es < 2^62, checked without overflow.
+    const int64_t per_seq = (2 * K + 1) * V * es;  // < 2^11 * 2^31 * 4 = 2^44
+    if (B > 0 && per_seq > (int64_t(1) << 62) / B) return SV_ERR_SIZE;
+    return SV_OK;
+}
+
+int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g, Layout* L)
+{
+    int rc = check_sizes(B, K, V, dtype, mode);
+    if (rc != SV_OK) return rc;
+    const int es = dtype == SV_BF16 ? 2 : 4;
+    int sms = 0, blocks = 0;
+    rc = device_limits(es, mode, &sms, &blocks);
+    if (rc != SV_OK) return rc;
+
+    std::memset(g, 0, sizeof(*g));
+    g->B = B;
+    g->K = K;
+    g->V = V;
+    g->es = es;
+    g->mode = mode;
+    g->rows_t = B * (K + 1);
+    g->rows = g->rows_t + (mode == SV_SAMPLE ? B * K : 0);
+    g->aligned = (V * es) % 16 == 0;
+    // Misaligned rows need one extra 16-byte vector per tile in the buffer.
+    g->tile_elems = (g->aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
+    g->tiles_per_row = (V + g->tile_elems - 1) / g->tile_elems;
+    g->tiles = g->rows * g->tiles_per_row;
+    const int64_t want = static_cast<int64_t>(sms) * blocks;
+    g->grid = static_cast<int32_t>(g->tiles < want ? (g->tiles > 0 ? g->tiles : 1) : want);
+    const int64_t per_cta = (g->tiles + g->grid - 1) / g->grid;
+    g->maxseg = static_cast<int32_t>((per_cta + g->tiles_per_row - 1) / g->tiles_per_row + 1);
+    g->chunk_elems = sv::kChunkBytes / es;
+    g->nchunks = (V + g->chunk_elems - 1) / g->chunk_elems;
+    if (B * g->nchunks >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+
+    size_t off = 0;
+    L->partials = off;
+    off += round_up(static_cast<size_t>(g->grid) * g->maxseg * sv::kRowConsumerWarps *
+                    sizeof(sv::Partial));
+    L->seqs = off;
+    off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
+    L->chunk_best = off;
+    if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nchunks) * sizeof(sv::ChunkBest));
+    L->tickets = off;
+    off += round_up(static_cast<size_t>(B) * sizeof(uint32_t));
+    L->total = off > 0 ? off : kAlign;
+    return SV_OK;
+}
+
+bool aligned_to(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int run(const void* target, const void* draft, const int32_t* tokens, int64_t B, int64_t K,
+        int64_t V, int dtype, float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+        int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
+        double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
+        void* const* events, int n_events)
+{
+    int rc = check_sizes(B, K, V, dtype, mode);
+    if (rc != SV_OK) return rc;
+    float c = 0.f;
+    if (mode == SV_SAMPLE) {
+        if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_ARG;
+        c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+        if (!std::isfinite(c) || !(c > 0.f)) return SV_ERR_ARG;
+    }
+    if (events != nullptr && n_events < 4) return SV_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto record = [&](int i) -> bool {
+        return events == nullptr ||
+               cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    };
+    if (B == 0) {
+        for (int i = 0; i < 4; ++i)
+            if (!record(i)) return SV_ERR_CUDA;
+        return SV_OK;
+    }
+    const bool sampling = mode == SV_SAMPLE;
+    if (target == nullptr || out_tokens == nullptr || num_accepted == nullptr) return SV_ERR_ARG;
+    if (K > 0 && tokens == nullptr) return SV_ERR_ARG;
+    if (sampling && K > 0 && draft == nullptr) return SV_ERR_ARG;
+    if (workspace == nullptr) return SV_ERR_WORKSPACE;
+    if (!aligned_to(target, 16) || (sampling && K > 0 && !aligned_to(draft, 16))) return SV_ERR_ALIGN;
+    if ((tokens && !aligned_to(tokens, 4)) || !aligned_to(out_tokens, 4) ||
+        !aligned_to(num_accepted, 4) || (seq_status && !aligned_to(seq_status, 4)))
+        return SV_ERR_ALIGN;
+    if ((lse_t && !aligned_to(lse_t, 8)) || (lse_d && !aligned_to(lse_d, 8)) ||
+        (log_ratio && !aligned_to(log_ratio, 8)))
+        return SV_ERR_ALIGN;
+    if (!aligned_to(workspace, kAlign)) return SV_ERR_WORKSPACE;
+
+    Geometry g;
+    Layout L;
+    rc = make_plan(B, K, V, dtype, mode, &g, &L);
+    if (rc != SV_OK) return rc;
+    if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+
+    const uint8_t* tp = static_cast<const uint8_t*>(target);
+    const uint8_t* dp = sampling ? static_cast<const uint8_t*>(draft) : nullptr;
+    auto* partials = reinterpret_cast<sv::Partial*>(ws + L.partials);
+    auto* seqs = reinterpret_cast<sv::SeqRecord*>(ws + L.seqs);
+    auto* chunk_best = reinterpret_cast<sv::ChunkBest*>(ws + L.chunk_best);
+    auto* tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+
+    sv::RowStatsArgs ra{tp, dp, g, c, partials};
+    sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
+                    tickets, sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
+                    sampling ? log_ratio : nullptr, seq_status};
+    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, chunk_best, tickets, out_tokens, num_accepted,
+                      seq_status};
+
+    if (!record(0)) return SV_ERR_CUDA;
+    if (sv::launch_row_stats(ra, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (!record(1)) return SV_ERR_CUDA;
+    if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (!record(2)) return SV_ERR_CUDA;
+    if (sampling && sv::launch_sample(pa, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (!record(3)) return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+struct HostLayout {
+    size_t target = 0, draft = 0, tokens = 0, out = 0, nacc = 0, ws = 0, total = 0;
+    size_t target_bytes = 0, draft_bytes = 0, tokens_bytes = 0, out_bytes = 0, nacc_bytes = 0;
+    size_t ws_bytes = 0;
+};
+
+int host_layout(int64_t B, int64_t K, int64_t V, int dtype, int mode, HostLayout* h)
+{
+    int rc = check_sizes(B, K, V, dtype, mode);
+    if (rc != SV_OK) return rc;
+    Geometry g;
+    Layout L;
+    rc = make_plan(B, K, V, dtype, mode, &g, &L);
+    if (rc != SV_OK) return rc;
+    const size_t es = dtype == SV_BF16 ? 2 : 4;
+    h->target_bytes = static_cast<size_t>(B * (K + 1) * V) * es;
+    h->draft_bytes = mode == SV_SAMPLE ? static_cast<size_t>(B * K * V) * es : 0;
+    h->tokens_bytes = static_cast<size_t>(B * K) * 4;
+    h->out_bytes = static_cast<size_t>(B * (K + 1)) * 4;
+    h->nacc_bytes = static_cast<size_t>(B) * 4;
+    h->ws_bytes = L.total;
+    size_t off = 0;
+    h->target = off;
+    off += round_up(h->target_bytes);
+    h->draft = off;
+    off += round_up(h->draft_bytes);
+    h->tokens = off;
+    off += round_up(h->tokens_bytes);
+    h->out = off;
+    off += round_up(h->out_bytes);
+    h->nacc = off;
+    off += round_up(h->nacc_bytes);
+    h->ws = off;
+    off += round_up(h->ws_bytes);
+    h->total = off;
+    return SV_OK;
+}
+
+}  // namespace
+
+SV_EXPORT int sv_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode, size_t* bytes)
+{
+    if (bytes == nullptr) return SV_ERR_ARG;
+    Geometry g;
+    Layout L;
+    const int rc = make_plan(B, K, V, dtype, mode, &g, &L);
+    if (rc != SV_OK) return rc;
+    *bytes = L.total;
+    return SV_OK;
+}
+
+SV_EXPORT int spec_verify(const void* target_logits, const void* draft_logits,
+                          const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                          float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                          int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                          void* stream)
+{
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr, nullptr, nullptr, 0);
+}
+
+SV_EXPORT int spec_verify_debug(const void* target_logits, const void* draft_logits,
+                                const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                                int dtype, float temperature, uint64_t seed, int mode,
+                                int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                size_t workspace_bytes, void* stream, double* lse_t, double* lse_d,
+                                double* log_ratio, int32_t* seq_status)
+{
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, lse_t, lse_d,
+               log_ratio, seq_status, nullptr, 0);
+}
+
+SV_EXPORT int spec_verify_timed(const void* target_logits, const void* draft_logits,
+                                const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                                int dtype, float temperature, uint64_t seed, int mode,
+                                int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                size_t workspace_bytes, void* stream, void* const* events,
+                                int n_events)
+{
+    if (events == nullptr) return SV_ERR_ARG;
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr, nullptr, events, n_events);
+}
+
+SV_EXPORT int sv_host_staging_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode,
+                                    size_t* bytes)
+{
+    if (bytes == nullptr) return SV_ERR_ARG;
+    HostLayout h;
+    const int rc = host_layout(B, K, V, dtype, mode, &h);
+    if (rc != SV_OK) return rc;
+    *bytes = h.total;
+    return SV_OK;
+}
+
+SV_EXPORT int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
+                               const int32_t* h_draft_tokens, int64_t B, int64_t K, int64_t V,
+                               int dtype, float temperature, uint64_t seed, int mode,
+                               int32_t* h_out_tokens, int32_t* h_num_accepted, void* staging,
+                               size_t staging_bytes, void* stream)
+{
+    HostLayout h;
+    int rc = host_layout(B, K, V, dtype, mode, &h);
+    if (rc != SV_OK) return rc;
+    if (B == 0) return SV_OK;
+    const bool sampling = mode == SV_SAMPLE;
+    if (h_target_logits == nullptr || h_out_tokens == nullptr || h_num_accepted == nullptr)
+        return SV_ERR_ARG;
+    if (K > 0 && h_draft_tokens == nullptr) return SV_ERR_ARG;
+    if (sampling && K > 0 && h_draft_logits == nullptr) return SV_ERR_ARG;
+    if (staging == nullptr || !aligned_to(staging, kAlign) || staging_bytes < h.total)
+        return SV_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint8_t* st = static_cast<uint8_t*>(staging);
+    if (cudaMemcpyAsync(st + h.target, h_target_logits, h.target_bytes, cudaMemcpyHostToDevice, s) !=
+        cudaSuccess)
+        return SV_ERR_CUDA;
+    if (h.draft_bytes > 0 &&
+        cudaMemcpyAsync(st + h.draft, h_draft_logits, h.draft_bytes, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+        return SV_ERR_CUDA;
+    if (h.tokens_bytes > 0 &&
+        cudaMemcpyAsync(st + h.tokens, h_draft_tokens, h.tokens_bytes, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+        return SV_ERR_CUDA;
+    rc = spec_verify(st + h.target, sampling ? st + h.draft : nullptr,
+                     reinterpret_cast<const int32_t*>(st + h.tokens), B, K, V, dtype, temperature,
+                     seed, mode, reinterpret_cast<int32_t*>(st + h.out),
+                     reinterpret_cast<int32_t*>(st + h.nacc), st + h.ws, h.ws_bytes, stream);
+    if (rc != SV_OK) return rc;
+    if (cudaMemcpyAsync(h_out_tokens, st + h.out, h.out_bytes, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(h_num_accepted, st + h.nacc, h.nacc_bytes, cudaMemcpyDeviceToHost, s) !=
+            cudaSuccess)
+        return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+SV_EXPORT const char* sv_error_string(int code)
+{
+    switch (code) {
+        case SV_OK: return "success";
+        case SV_ERR_ARG: return "invalid argument (size, mode, temperature or NULL pointer)";
+        case SV_ERR_DTYPE: return "unknown logits dtype";
+        case SV_ERR_ALIGN: return "misaligned pointer (logits need 16 bytes, int32 buffers 4)";
+        case SV_ERR_WORKSPACE: return "workspace or staging buffer NULL, too small or not 256-byte aligned";
+        case SV_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+        case SV_ERR_SIZE: return "sizes outside the supported range";
+        default: return "unknown status code";
+    }
+}
+
+SV_EXPORT int sv_version(void) { return 100; }

@@ -1,0 +1,132 @@
+// sv_internal.h -- layouts and launchers shared by the library's translation
+// units (not part of the public ABI; see include/spec_verify.h for that).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace sv {
+
+// ---------------------------------------------------------------------------
+// Row statistics (pass 1). Each CTA streams a contiguous range of fixed-size
+// tiles of the concatenated row space [target rows | draft rows] through a
+// STAGES-deep ring of shared-memory buffers filled by bulk copies. One warp
+// issues the copies; kRowConsumerWarps warps reduce.
+// ---------------------------------------------------------------------------
+constexpr int kRowTileBytes = 16384;
+constexpr int kRowStages = 4;
+constexpr int kRowConsumerWarps = 8;
+constexpr int kRowThreads = (kRowConsumerWarps + 1) * 32;
+
+// Residual / bonus sampling (pass 2): per sequence, the chosen row pair is cut
+// into chunks of kChunkBytes of each row; one CTA per chunk.
+constexpr int kChunkBytes = 16384;
+constexpr int kSampleThreads = 256;
+
+constexpr int kMaxK = 1024;
+
+// Flags carried by partial results and sequence records.
+constexpr int kFlagNonFinite = 2;  // == SV_SEQ_NONFINITE
+constexpr int kFlagTimeout = 4;    // == SV_SEQ_TIMEOUT
+constexpr int kFlagBadToken = 1;   // == SV_SEQ_BAD_TOKEN
+
+// One warp's reduction of one row segment.
+//   sampling: s = sum over the segment of 2^(x*c - m), m an integer-valued
+//             reference exponent (log2 units), -inf when the segment is all -inf.
+//   greedy:   m = largest raw logit, s = its lowest index (exact in double),
+//             or 2^31 - 1 when no element beat -inf.
+//   flags:    kFlagNonFinite / kFlagTimeout.
+struct Partial {
+    double s;
+    float m;
+    int32_t flags;
+};
+static_assert(sizeof(Partial) == 16, "Partial layout");
+
+// Per-sequence record written by the acceptance scan, read by the sampler.
+struct SeqRecord {
+    int32_t j;         // emitted position (0..K)
+    int32_t status;    // SV_SEQ_* bits; 0 = valid
+    float lse_t_hi;    // log2-domain normaliser of target row j, as hi + lo
+    float lse_t_lo;
+    float lse_d_hi;    // same for draft row j (unused when j == K)
+    float lse_d_lo;
+    int32_t pad[2];
+};
+static_assert(sizeof(SeqRecord) == 32, "SeqRecord layout");
+
+// Winner of one chunk's exponential race (score 0 / idx INT_MAX: no candidate).
+struct ChunkBest {
+    float score;
+    int32_t idx;
+    int32_t flags;
+    int32_t pad;
+};
+static_assert(sizeof(ChunkBest) == 16, "ChunkBest layout");
+
+struct Geometry {
+    int64_t B, K, V;
+    int32_t es;             // bytes per element (4 or 2)
+    int32_t mode;           // SV_SAMPLE / SV_GREEDY
+    int64_t rows_t;         // target rows = B (K + 1)
+    int64_t rows;           // rows streamed in pass 1 (target, then draft when sampling)
+    int64_t tile_elems;     // elements per pass-1 tile
+    int64_t tiles_per_row;
+    int64_t tiles;          // rows * tiles_per_row
+    int32_t grid;           // pass-1 CTAs
+    int32_t maxseg;         // most row segments one pass-1 CTA can touch
+    int32_t aligned;        // every row starts on a 16-byte boundary
+    int64_t chunk_elems;    // pass-2 chunk length
+    int64_t nchunks;        // chunks per row
+};
+
+struct RowStatsArgs {
+    const uint8_t* target;
+    const uint8_t* draft;
+    Geometry g;
+    float c;                // log2(e) / T
+    Partial* partials;      // [grid][maxseg][kRowConsumerWarps]
+};
+
+struct ScanArgs {
+    const uint8_t* target;
+    const uint8_t* draft;
+    const int32_t* tokens;
+    Geometry g;
+    float c;
+    uint64_t seed;
+    const Partial* partials;
+    int32_t* out_tokens;
+    int32_t* num_accepted;
+    SeqRecord* seqs;
+    uint32_t* tickets;
+    double* lse_t;          // optional diagnostics
+    double* lse_d;
+    double* log_ratio;
+    int32_t* seq_status;
+};
+
+struct SampleArgs {
+    const uint8_t* target;
+    const uint8_t* draft;
+    Geometry g;
+    float c;
+    uint64_t seed;
+    const SeqRecord* seqs;
+    ChunkBest* chunk_best;  // [B][nchunks]
+    uint32_t* tickets;      // [B], zeroed by the scan
+    int32_t* out_tokens;
+    int32_t* num_accepted;
+    int32_t* seq_status;    // optional
+};
+
+// Launchers (return the launch's cudaError_t).
+cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t s);
+cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
+cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+
+// Resident pass-1 CTAs per SM for this dtype / mode (occupancy query).
+cudaError_t row_stats_blocks_per_sm(int es, int mode, int* blocks);
+
+}  // namespace sv
