@@ -43,6 +43,8 @@ def parse():
     p.add_argument("--steps", type=int, default=3000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--workload", default=None)
+    p.add_argument("--batch", type=int, default=None,
+                   help="override B (smaller cases for profiling; not the headline)")
     p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     p.add_argument("--e2e-steps", type=int, default=None)
     p.add_argument("--cpu-seconds", type=float, default=10.0,
@@ -203,6 +205,8 @@ def main():
     args = parse()
     from speculative_decoding_verification_66_gb300.workloads import HEADLINE, WORKLOADS
     wl = WORKLOADS[args.workload or HEADLINE]
+    if args.batch is not None:
+        wl = wl.resized(B=args.batch)
     if args.impl == "reference":
         reference_arm(args, wl)
         return

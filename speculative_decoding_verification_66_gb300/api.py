@@ -176,6 +176,9 @@ def spec_verify_timed(target_logits, draft_logits, draft_tokens, events, tempera
     m, B, K, V, d, stream, out_tokens, num_accepted, workspace = _prepare(
         target_logits, draft_logits, draft_tokens, mode, out_tokens, num_accepted, workspace,
         stream)
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event lazily, on its first record
+            e.record(stream)
     handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     with torch.cuda.device(target_logits.device):
         _check(_lib.load().spec_verify_timed(
