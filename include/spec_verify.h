@@ -32,12 +32,17 @@
  * Numbers and reproducibility:
  *   p = softmax(target_logits / T), q = softmax(draft_logits / T), accumulated
  *   in float32 (rescaled partial sums, double where partials are merged).
- *   The acceptance uniform of position i of sequence b is lane 0, and the
- *   sampling uniform lane 1, of Philox4x32-10 with key (lo32(seed),
- *   hi32(seed)) and counter (i, b, 0, 0), mapped to (word >> 8) * 2^-24.
- *   Sampling is the inverse CDF in index order. Results are a pure function of
- *   (inputs, T, seed, mode) on a given GPU model: no float atomics, fixed
- *   reduction trees, the same answer on every run.
+ *   The acceptance uniform of position i of sequence b is lane 0 of
+ *   Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter (i, b, 0, 0),
+ *   mapped to (word >> 8) * 2^-24; position i is kept iff that uniform is
+ *   below min(1, p_i(x_i) / q_i(x_i)). The token at the emitted position j is
+ *   drawn from the weights w (max(0, p_j - q_j) after a rejection, p_K for the
+ *   bonus) by an exponential race: the argmax over w_k > 0 of w_k / E_k,
+ *   E_k = -ln v_k, v_k lane (k mod 4) of counter (j, b, 1 + k div 4, 0) mapped
+ *   to (2 (word >> 9) + 1) * 2^-24; the lowest index wins an exact tie. The
+ *   race picks token k with probability w_k / sum(w). Results are a pure
+ *   function of (inputs, T, seed, mode) on a given GPU model: no float
+ *   atomics, fixed reduction trees, the same answer on every run.
  *
  * Memory and streams:
  *   Every pointer passed to spec_verify / spec_verify_debug / spec_verify_timed
