@@ -181,6 +181,34 @@ int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
                      float temperature, uint64_t seed, int mode, int32_t* h_out_tokens,
                      int32_t* h_num_accepted, void* staging, size_t staging_bytes, void* stream);
 
+/*
+ * spec_verify for callers that cannot allocate device memory. The pages have
+ * no counterpart to this entry point; it exists for callers such as code
+ * inside a host framework that owns all device memory through its own pool,
+ * where a cudaMalloc would fail or break the pool's accounting, or code on a
+ * latency-critical path, where cudaMalloc / cudaFree would synchronise the
+ * device.
+ *
+ * Arguments and results are those of spec_verify, without the workspace: the
+ * caller still passes its own (device) inputs and outputs. The scratch is a
+ * fixed array of 8 MiB inside the library's device image, held by every GPU
+ * that loads the library until the process exits. Problems whose
+ * sv_workspace_bytes exceed 8 MiB are rejected with SV_ERR_SIZE before
+ * anything is enqueued. The call allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture. All calls share the one array: two calls whose
+ * work overlaps on the GPU (different streams, no ordering between them) race
+ * on it. The array keeps the last call's contents; nothing in it needs to
+ * start at zero.
+ */
+int spec_verify_static(const void* target_logits, const void* draft_logits,
+                       const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                       float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                       int32_t* num_accepted, void* stream);
+
 /* Static description of an SV_* return code. Never NULL. */
 const char* sv_error_string(int code);
 

@@ -20,6 +20,7 @@ from .api import (  # noqa: F401
     spec_verify,
     spec_verify_debug,
     spec_verify_host,
+    spec_verify_static,
     spec_verify_timed,
     sv_host_staging_bytes,
     sv_workspace_bytes,

@@ -229,5 +229,30 @@ def spec_verify_host(target_logits, draft_logits, draft_tokens, temperature: flo
     return out_tokens, num_accepted
 
 
+def spec_verify_static(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
+                       seed: int = 0, mode="sample", *, out_tokens=None, num_accepted=None,
+                       stream=None):
+    """spec_verify without a workspace, for callers that cannot allocate device
+    memory: the library's fixed 8 MiB device scratch array is used instead. The
+    output tensors are the caller's (allocated here only when not given). Calls
+    that overlap on the GPU share that one array and race on it."""
+    m = mode_code(mode)
+    B, K, V = _shapes(target_logits, draft_logits, draft_tokens, m)
+    dev = target_logits.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_static(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, dtype_code(target_logits.dtype),
+            float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens),
+            _ptr(num_accepted), ctypes.c_void_p(stream.cuda_stream)), "spec_verify_static")
+    return out_tokens, num_accepted
+
+
 def version() -> int:
     return int(_lib.load().sv_version())

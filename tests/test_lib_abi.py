@@ -34,7 +34,8 @@ def lib():
 def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "sv_workspace_bytes", "spec_verify", "spec_verify_debug", "spec_verify_timed",
-        "sv_host_staging_bytes", "spec_verify_host", "sv_error_string", "sv_version"])
+        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static", "sv_error_string",
+        "sv_version"])
 
 
 def test_every_declared_symbol_is_exported(lib):
