@@ -85,6 +85,8 @@ def lib() -> ctypes.CDLL:
             L.svo_sample_weights.restype = None
             L.svo_race_uniform.argtypes = [u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
             L.svo_race_uniform.restype = dbl
+            L.svo_block_uniform.argtypes = [u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
+            L.svo_block_uniform.restype = dbl
             L.svo_race_sample.argtypes = [vp, i64, u64, ctypes.c_uint32, ctypes.c_uint32, vp]
             L.svo_race_sample.restype = i64
             L.svo_row_argmax.argtypes = [vp, i64, i32, vp]
@@ -155,6 +157,13 @@ def sample_weights(target_row, draft_row, T: float, lse_t: float, lse_d: float) 
 
 def race_uniform(seed: int, seq: int, pos: int, k: int) -> float:
     return lib().svo_race_uniform(seed, seq, pos, k)
+
+
+RACE_BLOCK = 8192
+
+
+def block_uniform(seed: int, seq: int, pos: int, c: int) -> float:
+    return lib().svo_block_uniform(seed, seq, pos, c)
 
 
 def race_sample(w: np.ndarray, seed: int, seq: int, pos: int):

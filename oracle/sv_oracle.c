@@ -36,12 +36,16 @@
  *  - u_i = lane 0 of Philox(key = seed, counter = (i, b, 0, 0)), mapped to
  *    (32-bit word >> 8) * 2^-24, exact in float and double;
  *  - the pages draw the corrected token with a generic multinomial draw; it is
- *    read here as an exponential race: token = argmax_k w_k / E_k over the
- *    tokens with w_k > 0, E_k = -ln v_k, v_k the race uniform of token k at
- *    emitted position j (lane k mod 4 of counter (j, b, 1 + k div 4, 0), mapped
- *    to (2 (word >> 9) + 1) * 2^-24 in (0, 1)); the lowest index wins an exact
- *    tie. The first arrival of independent exponential clocks with rates w_k is
- *    token k with probability w_k / sum(w), so this is a draw from w / Z;
+ *    read here as a two-level exponential race over blocks of 8192 tokens.
+ *    Level 1 races the blocks: block c = argmax over blocks with W_c > 0 of
+ *    W_c / E_c, W_c the sum of w over the block, E_c = -ln v_c, v_c lane c mod 4
+ *    of counter (j, b, 1 + c div 4, 1). Level 2 races the tokens of the winning
+ *    block: token = argmax over its k with w_k > 0 of w_k / E_k, E_k = -ln v_k,
+ *    v_k lane k mod 4 of counter (j, b, 1 + k div 4, 0). Uniforms are
+ *    (2 (word >> 9) + 1) * 2^-24 in (0, 1); the lowest index wins an exact tie.
+ *    The first arrival of independent exponential clocks with rates w_k is
+ *    clock k with probability w_k / sum(w), so block c wins with probability
+ *    W_c / Z and token k of it with probability w_k / W_c: a draw from w / Z;
  *  - if every residual weight rounds to 0 (possible only through rounding),
  *    p_j is raced instead;
  *  - greedy: lowest index attaining the maximum raw logit; accept while it
@@ -188,26 +192,57 @@ double svo_race_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t k)
     return (double)(2u * (r[k & 3u] >> 9) + 1u) * (1.0 / 16777216.0);
 }
 
+double svo_block_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t c)
+{
+    uint32_t ctr[4], key[2], r[4];
+    ctr[0] = pos; ctr[1] = seq; ctr[2] = 1u + (c >> 2); ctr[3] = 1;
+    key[0] = (uint32_t)(seed & 0xFFFFFFFFu);
+    key[1] = (uint32_t)(seed >> 32);
+    svo_philox4x32_10(ctr, key, r);
+    return (double)(2u * (r[c & 3u] >> 9) + 1u) * (1.0 / 16777216.0);
+}
+
+/* One exponential race: keep the largest w / E and the second largest. */
+static void race_step(double w, double v, int64_t id, double* best, double* second, int64_t* best_id)
+{
+    double score = w / (-log(v));
+    if (score > *best) {
+        if (*best_id >= 0) *second = *best;
+        *best = score;
+        *best_id = id;
+    } else if (score > *second) {
+        *second = score;
+    }
+}
+
 int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq, uint32_t pos,
                         double* margin)
 {
-    double best = -INFINITY, second = 0.0;
-    int64_t k, best_k = -1;
-    for (k = 0; k < V; ++k) {
-        double v, E, score;
-        if (!(w[k] > 0.0)) continue;
-        v = svo_race_uniform(seed, seq, pos, (uint32_t)k);
-        E = -log(v);
-        score = w[k] / E;
-        if (score > best) {
-            if (best_k >= 0) second = best;
-            best = score;
-            best_k = k;
-        } else if (score > second) {
-            second = score;
-        }
+    const int64_t nblocks = (V + SVO_RACE_BLOCK - 1) / SVO_RACE_BLOCK;
+    double best = -INFINITY, second = 0.0, gap1, gap2;
+    int64_t c, k, best_c = -1, best_k = -1, k0, k1;
+    /* Level 1: the blocks, each with the total weight of its tokens. */
+    for (c = 0; c < nblocks; ++c) {
+        double W = 0.0;
+        k0 = c * SVO_RACE_BLOCK;
+        k1 = k0 + SVO_RACE_BLOCK < V ? k0 + SVO_RACE_BLOCK : V;
+        for (k = k0; k < k1; ++k) W += w[k];
+        if (W > 0.0) race_step(W, svo_block_uniform(seed, seq, pos, (uint32_t)c), c, &best, &second, &best_c);
     }
-    *margin = (best_k >= 0) ? (best - second) / best : 0.0;
+    if (best_c < 0) {
+        *margin = 0.0;
+        return -1;
+    }
+    gap1 = (best - second) / best;
+    /* Level 2: the tokens of the winning block. */
+    best = -INFINITY;
+    second = 0.0;
+    k0 = best_c * SVO_RACE_BLOCK;
+    k1 = k0 + SVO_RACE_BLOCK < V ? k0 + SVO_RACE_BLOCK : V;
+    for (k = k0; k < k1; ++k)
+        if (w[k] > 0.0) race_step(w[k], svo_race_uniform(seed, seq, pos, (uint32_t)k), k, &best, &second, &best_k);
+    gap2 = (best - second) / best;
+    *margin = gap1 < gap2 ? gap1 : gap2;
     return best_k;
 }
 

@@ -54,15 +54,23 @@ double svo_accept_prob(double log_p, double log_q);
 void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
                         double T, double lse_t, double lse_d, double* w);
 
+/* Tokens per block of the two-level race. */
+#define SVO_RACE_BLOCK 8192
+
 /* Race uniform of token k at emitted position `pos` of sequence `seq`: lane
  * k mod 4 of Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter
  * (pos, seq, 1 + k div 4, 0), mapped to (2 (word >> 9) + 1) * 2^-24 in (0, 1). */
 double svo_race_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t k);
 
-/* Exponential race: argmax over k with w_k > 0 of w_k / E_k, E_k = -ln(v_k),
- * v_k the race uniform of token k; lowest index wins exact ties. *margin gets
- * (best - second best) / best (1 when one token has weight, 0 when none).
- * Returns -1 if no weight is positive. */
+/* Race uniform of block c: as above with counter (pos, seq, 1 + c div 4, 1). */
+double svo_block_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t c);
+
+/* Two-level exponential race over blocks of SVO_RACE_BLOCK tokens: the block
+ * with the largest W_c / E_c (W_c = sum of w over the block), then the token of
+ * that block with the largest w_k / E_k, E = -ln(uniform). The lowest index
+ * wins exact ties. *margin gets the smaller of the two levels' relative gaps
+ * (best - second) / best (1 when a level has one candidate, 0 when no weight
+ * is positive). Returns -1 if no weight is positive. */
 int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq, uint32_t pos,
                         double* margin);
 
@@ -78,9 +86,9 @@ int64_t svo_row_argmax(const void* row, int64_t V, int dtype, int* has_nan);
  * Optional outputs (NULL to skip), all indexed like the inputs:
  *   lse_t [B, K+1], lse_d [B, K], log_ratio [B, K]  (sampling mode only)
  *   accept_margin [B, K]: |u_i - r_i| for every decision taken, NaN elsewhere
- *   sample_margin [B]:    relative gap (best - second) / best of the race's two
- *                         top scores (0 when the zero-residual fall-back fired;
- *                         NaN in greedy)
+ *   sample_margin [B]:    smaller relative gap (best - second) / best of the
+ *                         race's two levels (0 when the zero-residual fall-back
+ *                         fired; NaN in greedy)
  *   seq_status [B]
  * Returns 0, or -1 on an invalid argument.
  */

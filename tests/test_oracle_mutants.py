@@ -23,11 +23,15 @@ MUTANTS = {
                       "            j = i;\n        }\n    }\n\n    /* Step 3"),
     "bonus_row_off_by_one": ("svo_sample_weights(trow0 + (size_t)K * V * esz, NULL",
                              "svo_sample_weights(trow0 + (size_t)(K - 1) * V * esz, NULL"),
-    "race_score_inverted": ("score = w[k] / E;", "score = w[k] * E;"),
-    "race_clock_sign": ("E = -log(v);", "E = log(v);"),
-    "race_lane_fixed": ("r[k & 3u] >> 9", "r[0] >> 9"),
-    "race_shares_accept_counter": ("ctr[2] = 1u + (k >> 2);", "ctr[2] = (k >> 2);"),
-    "race_keeps_last_tie": ("if (score > best) {", "if (score >= best) {"),
+    "race_score_inverted": ("double score = w / (-log(v));", "double score = w * (-log(v));"),
+    "race_clock_sign": ("double score = w / (-log(v));", "double score = w / log(v);"),
+    "race_lane_fixed": ("(2u * (r[k & 3u] >> 9) + 1u)", "(2u * (r[0] >> 9) + 1u)"),
+    "race_shares_accept_counter": ("ctr[2] = 1u + (k >> 2); ctr[3] = 0;",
+                                   "ctr[2] = (k >> 2); ctr[3] = 0;"),
+    "block_race_shares_token_stream": ("ctr[2] = 1u + (c >> 2); ctr[3] = 1;",
+                                       "ctr[2] = 1u + (c >> 2); ctr[3] = 0;"),
+    "block_weight_ignored": ("if (W > 0.0) race_step(W,", "if (W > 0.0) race_step(1.0,"),
+    "level2_races_wrong_block": ("k0 = best_c * SVO_RACE_BLOCK;", "k0 = 0;"),
     "temperature_dropped_in_max": ("double s = svo_elem(row, k, dtype) / T;",
                                    "double s = svo_elem(row, k, dtype);"),
     "lse_shift_sign": ("acc += exp(svo_elem(row, k, dtype) / T - m);",

@@ -263,10 +263,49 @@ def test_race_draws_proportional_to_weight(oracle_mod, V):
         assert stats.chisquare(counts[keep], exp).pvalue > 1e-3
 
 
+def test_two_level_race_law(oracle_mod):
+    """Four blocks of the two-level race (V > 3 * 8192): the winning block
+    follows W_c / Z and the token within it w_k / W_c, so every token follows
+    w_k / Z. Weights sit on a few tokens per block (including the first token
+    of block 0 and the last token of the row) so that each race is cheap."""
+    from scipy import stats
+    L = oracle_mod.RACE_BLOCK
+    V = 3 * L + 100
+    w = np.zeros(V)
+    rng = np.random.default_rng(12)
+    block_mass = [0.1, 0.4, 0.2, 0.3]
+    picks = []
+    for c, mass in enumerate(block_mass):
+        lo, hi = c * L, min((c + 1) * L, V)
+        idx = rng.choice(np.arange(lo + 1, hi - 1), size=3, replace=False).tolist()
+        idx += [lo] if c == 0 else []
+        idx += [V - 1] if c == 3 else []
+        share = rng.dirichlet(np.ones(len(idx)))
+        w[idx] = mass * share
+        picks += idx
+    n = 20_000
+    toks = np.array([oracle_mod.race_sample(w, 99, b, 3)[0] for b in range(n)])
+    blocks = np.bincount(toks // L, minlength=4)
+    assert stats.chisquare(blocks, np.array(block_mass) * n).pvalue > 1e-3
+    picks = np.array(sorted(picks))
+    counts = np.array([(toks == k).sum() for k in picks])
+    assert counts.sum() == n
+    assert stats.chisquare(counts, w[picks] / w.sum() * n).pvalue > 1e-3
+
+
+def test_block_uniforms_are_their_own_stream(oracle_mod):
+    b = np.array([oracle_mod.block_uniform(3, s, 1, c) for s in range(500) for c in range(8)])
+    t = np.array([oracle_mod.race_uniform(3, s, 1, c) for s in range(500) for c in range(8)])
+    assert b.min() > 0 and b.max() < 1
+    assert np.all((b * 2**24) % 2 == 1)
+    assert abs(np.corrcoef(b, t)[0, 1]) < 0.1
+
+
 def test_race_near_tie_law(oracle_mod):
-    """Closed form: the relative gap between the race's two best scores is below
+    """Closed form: the relative gap between a race's two best scores is below
     tau with probability at most tau (memorylessness of the exponential clocks),
-    whatever the number of tokens. This is what keeps near-ties rare at V = 128k."""
+    whatever the number of tokens; the two-level race has two such gaps, so at
+    most 2 tau. This is what keeps near-ties rare at V = 128k."""
     rng = np.random.default_rng(1)
     V = 2000
     w = rng.lognormal(sigma=2.0, size=V)
