@@ -345,7 +345,7 @@ def main():
         "e2e": {"value": world * B * e2e_steps / e2e_s, "unit": "seqs/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks.summary(),
-        "gpu_launches": sv.LAUNCHES[sv.api.mode_code(mode)] * args.steps,
+        "gpu_launches": sv.launches(mode, V, copies[0]["target"].dtype) * args.steps,
     }
     if world == 1 and not args.no_cpu_baseline:
         def host_fn(n):

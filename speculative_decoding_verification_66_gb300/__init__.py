@@ -8,7 +8,6 @@ Python binding: ``spec_verify`` and friends take torch tensors and call the
 library; there is no CPU or eager fallback.
 """
 from .api import (  # noqa: F401
-    LAUNCHES,
     SV_BF16,
     SV_F32,
     SV_GREEDY,
@@ -17,6 +16,7 @@ from .api import (  # noqa: F401
     SV_SEQ_NONFINITE,
     SV_SEQ_TIMEOUT,
     SpecVerifyError,
+    launches,
     spec_verify,
     spec_verify_debug,
     spec_verify_host,

@@ -18,8 +18,15 @@ SV_F32, SV_BF16 = 0, 1
 SV_SAMPLE, SV_GREEDY = 0, 1
 SV_SEQ_BAD_TOKEN, SV_SEQ_NONFINITE, SV_SEQ_TIMEOUT = 1, 2, 4
 
-# Kernel launches one spec_verify call makes (row statistics, scan, sampler).
-LAUNCHES = {SV_SAMPLE: 3, SV_GREEDY: 2}
+def launches(mode, V: int, dtype) -> int:
+    """Kernel launches one spec_verify call makes: row statistics and the scan;
+    in sampling mode also the sampler (two launches when rows are 16-byte
+    aligned: streaming and finish)."""
+    m = mode_code(mode)
+    if m == SV_GREEDY:
+        return 2
+    es = 2 if (dtype == torch.bfloat16 or dtype == SV_BF16) else 4
+    return 4 if (V * es) % 16 == 0 else 3
 
 
 class SpecVerifyError(RuntimeError):

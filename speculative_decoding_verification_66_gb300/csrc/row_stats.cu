@@ -26,7 +26,8 @@
 // of the largest scaled logit seen so far), so every rescale is an exact power
 // of two. Per tile a thread adds <= 32 terms in four float accumulators, then
 // folds the tile sum into a float pair (two-sum), keeping the running sum's
-// rounding error. Warps combine their lanes in double.
+// rounding error. Warps combine their lanes as float pairs (no float64: GB300
+// runs it at a small fraction of the float32 rate).
 #include <climits>
 
 #include "sv_device.cuh"
@@ -280,27 +281,25 @@ __device__ __forceinline__ void argmax_tile(GreedyState& st, const uint4 (&v)[kV
     st.idx = found;
 }
 
-// Warp-reduce the lanes' states and have lane 0 store the warp's Partial.
+// Warp-reduce the lanes' states (float pairs, exact power-of-two rescales) and
+// have lane 0 store the warp's Partial.
 __device__ __forceinline__ void flush_sample(const SampleState& st, Partial* out, int lane)
 {
-    float m = st.m;
-    double s = static_cast<double>(st.s_hi) + static_cast<double>(st.s_lo);
+    float m = st.m, hi = st.s_hi, lo = st.s_lo;
     int flags = st.flags;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
         const float om = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-        const double os = __shfl_xor_sync(0xFFFFFFFFu, s, off);
+        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, off);
+        const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, off);
         flags |= __shfl_xor_sync(0xFFFFFFFFu, flags, off);
-        const float M = fmaxf(m, om);
-        s = (M == __uint_as_float(kF32NegInfBits))
-                ? 0.0
-                : s * pow2_neg_int_d(m - M) + os * pow2_neg_int_d(om - M);
-        m = M;
+        merge_scaled(m, hi, lo, om, ohi, olo);
     }
     if (lane == 0) {
         Partial p;
-        p.s = s;
         p.m = m;
+        p.hi = hi;
+        p.lo = lo;
         p.flags = flags;
         *out = p;
     }
@@ -323,8 +322,9 @@ __device__ __forceinline__ void flush_greedy(const GreedyState& st, Partial* out
     }
     if (lane == 0) {
         Partial p;
-        p.s = static_cast<double>(idx);
         p.m = best;
+        p.hi = __int_as_float(idx);
+        p.lo = 0.f;
         p.flags = flags;
         *out = p;
     }
@@ -455,8 +455,9 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
         // Timed out: mark this warp's remaining segments so the scan rejects them.
         for (int64_t r = row; r <= row_last; ++r) {
             Partial p;
-            p.s = 0.0;
             p.m = __uint_as_float(kF32NegInfBits);
+            p.hi = 0.f;
+            p.lo = 0.f;
             p.flags = kFlagTimeout;
             my_partials[(r - row_first) * kRowConsumerWarps] = p;
         }

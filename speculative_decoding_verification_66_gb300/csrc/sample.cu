@@ -8,21 +8,31 @@
 //    max(0, p_j - q_j) / Z.
 //  * Hung-yi Lee, lecture 16 notes, §4 item 4 "The Bonus Token": when all K
 //    drafts pass, the token is drawn from the target row K.
-// The draw is an exponential race: token = argmax over k with w_k > 0 of
-// w_k / E_k, E_k = -ln v_k, v_k the race uniform of token k (lane k mod 4 of
-// Philox counter (j, b, 1 + k div 4, 0), mapped to (2 (word >> 9) + 1) 2^-24).
-// The first of independent exponential clocks with rates w_k to ring is token
-// k with probability w_k / sum(w), so no normaliser and no prefix sum is
-// needed; the lowest index wins an exact tie.
+// The draw is a two-level exponential race over blocks of kRaceBlock tokens.
+// Level 1 picks the block with the largest W_c / E_c, where W_c is the sum of
+// the weights w over block c and E_c = -ln v_c, with v_c lane c mod 4 of Philox
+// counter (j, b, 1 + c div 4, 1). Level 2 picks the token of that block with the
+// largest w_k / E_k, with v_k lane k mod 4 of counter (j, b, 1 + k div 4, 0).
+// Uniforms are (2 (word >> 9) + 1) 2^-24, and the lowest index wins an exact
+// tie. Block c wins with probability W_c / Z and token k within it with
+// w_k / W_c, so the token follows w / Z exactly.
 //
-// Design. Only the one row pair of each sequence is read again. Its V entries
-// are cut into chunks of kChunkBytes per row, one CTA per (sequence, chunk).
-// A CTA stages its chunk with bulk copies, and each thread races four
-// consecutive tokens per Philox call. The block keeps the best (score, index)
-// and stores it per chunk. The last CTA of a sequence to finish takes an atomic
-// ticket (no one waits on it) and merges the chunk winners in index order. If
-// every residual weight rounded to zero, that CTA races p_j over the whole row
-// instead.
+// Design. Only the one row pair of each sequence is read again.
+//  * Rows on 16-byte boundaries (every vocabulary whose row is a multiple of
+//    16 bytes): two launches. sample_stream_kernel is a grid of warps, each
+//    taking a contiguous run of 2 KB-per-row slices of the emitted row pairs
+//    with coalesced 16-byte loads and writing one float-pair weight sum per
+//    slice; it has no shared memory, no atomics and no barriers.
+//    sample_finish_kernel, one CTA per sequence, adds the slice sums of each
+//    block in a fixed order, runs level 1, re-reads the winning block and runs
+//    level 2.
+//  * Other rows: sample_kernel, one CTA per (sequence, block), stages its block
+//    in shared memory with bulk copies; the last CTA of a sequence (an atomic
+//    ticket: no one waits on it) runs the two levels.
+// Weights are float; block sums are float pairs (no float64, which GB300 runs
+// at a small fraction of the float32 rate). Per-token random numbers are drawn
+// in the winning block only. If every residual weight rounded to zero, p_j is
+// raced instead.
 #include <climits>
 
 #include "sv_device.cuh"
@@ -33,7 +43,13 @@ namespace {
 
 constexpr int kT = kSampleThreads;
 constexpr int kWarps = kT / 32;
-constexpr int kBufBytes = kChunkBytes + 32;
+
+// Shared-memory bytes of one staged row block (tokens plus 16-byte cover).
+template <int ES>
+constexpr int buf_bytes()
+{
+    return kRaceBlock * ES + 32;
+}
 
 __device__ __forceinline__ const uint8_t* down16(const uint8_t* p)
 {
@@ -44,10 +60,198 @@ __device__ __forceinline__ const uint8_t* up16(const uint8_t* p)
     return reinterpret_cast<const uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
 }
 
-// One row's share of a staged chunk: the bulk engine moves the 16-byte-aligned
-// range [a0, a0 + bulk) that covers row bytes [s, e); bytes it cannot take
-// (the last < 16 bytes of a tensor whose size is not a multiple of 16) are
-// loaded one element at a time. Byte s lands at buf + off.
+// Everything about the row pair a CTA works on.
+struct RowPair {
+    const uint8_t* trow;   // target row j
+    const uint8_t* drow;   // draft row j, or nullptr for the bonus row
+    const uint8_t* t_end;  // aligned tensor ends
+    const uint8_t* d_end;
+    float c, mt, lt, md, ld;
+    uint64_t seed;
+    uint32_t seq, pos;
+};
+
+// Sampling weight of one token from its logits: max(0, p - q) after a
+// rejection, p for the bonus. log2 p = x c - m - l (see SeqRecord).
+__device__ __forceinline__ float weight_of(const RowPair& rp, float xt, float xd)
+{
+    const float p = ex2(fmaf(xt, rp.c, -rp.mt) - rp.lt);
+    if (rp.drow == nullptr) return p;
+    const float q = ex2(fmaf(xd, rp.c, -rp.md) - rp.ld);
+    return fmaxf(p - q, 0.0f);
+}
+
+struct Best {
+    float score;  // 0 = no candidate yet (every real score is > 0)
+    int idx;      // INT_MAX = none
+};
+
+__device__ __forceinline__ void take(Best& a, float s, int i)
+{
+    if (s > a.score || (s == a.score && i < a.idx)) {
+        a.score = s;
+        a.idx = i;
+    }
+}
+
+// One group of four consecutive tokens k0..k0+3 (k0 a multiple of 4) in the
+// race of level 2: one Philox block gives their four clocks.
+__device__ __forceinline__ void race_group(Best& best, const RowPair& rp, int64_t k0,
+                                           const float (&w)[4])
+{
+    if (!(w[0] > 0.f || w[1] > 0.f || w[2] > 0.f || w[3] > 0.f)) return;
+    const uint2 key = make_uint2(static_cast<uint32_t>(rp.seed), static_cast<uint32_t>(rp.seed >> 32));
+    const uint4 r = philox4x32_10(
+        make_uint4(rp.pos, rp.seq, 1u + static_cast<uint32_t>(k0 >> 2), 0u), key);
+    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (w[q] > 0.f)
+            take(best, __fdividef(w[q], exp_clock(word_to_open_uniform(words[q]))),
+                 static_cast<int>(k0 + q));
+}
+
+// Block-wide float-pair sum (fixed tree); every thread gets the total.
+__device__ __forceinline__ float2 block_sum2(float hi, float lo, float2* red)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, off);
+        const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, off);
+        float err;
+        const float s = two_sum(hi, ohi, &err);
+        lo = __fadd_rn(__fadd_rn(lo, olo), err);
+        hi = s;
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float2(hi, lo);
+    __syncthreads();
+    float th = red[0].x, tl = red[0].y;
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) {
+        float err;
+        const float s = two_sum(th, red[i].x, &err);
+        tl = __fadd_rn(__fadd_rn(tl, red[i].y), err);
+        th = s;
+    }
+    return make_float2(th, tl);
+}
+
+// Block-wide best (largest score, lowest index), fixed tree.
+__device__ __forceinline__ Best block_best(Best b, Best* red)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float os = __shfl_xor_sync(0xFFFFFFFFu, b.score, off);
+        const int oi = __shfl_xor_sync(0xFFFFFFFFu, b.idx, off);
+        take(b, os, oi);
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
+    __syncthreads();
+    Best t = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) take(t, red[i].score, red[i].idx);
+    return t;
+}
+
+// ---------------------------------------------------------------------------
+// Direct path: rows 16-byte aligned, a block is read with 16-byte loads.
+// Thread t takes vectors t, t + kT, ... of the block (coalesced).
+// ---------------------------------------------------------------------------
+template <int ES>
+struct Direct {
+    static constexpr int kEPV = 16 / ES;                  // elements per vector
+    static constexpr int kVPT = kRaceBlock / kEPV / kT;   // vectors per thread
+
+    // Elements of one 16-byte vector, widened exactly to float.
+    __device__ static __forceinline__ void unpack(const uint4& v, float (&x)[kEPV])
+    {
+        if constexpr (ES == 2) {
+            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+        } else {
+            x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+            x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+        }
+    }
+
+    __device__ static __forceinline__ void load(const RowPair& rp, int64_t e0, int n,
+                                                uint4 (&tv)[kVPT], uint4 (&dv)[kVPT])
+    {
+        const uint4* tp = reinterpret_cast<const uint4*>(rp.trow + e0 * ES);
+        const uint4* dp = rp.drow ? reinterpret_cast<const uint4*>(rp.drow + e0 * ES) : nullptr;
+        const int nvec = n / kEPV;
+#pragma unroll
+        for (int q = 0; q < kVPT; ++q) {
+            const int vi = static_cast<int>(threadIdx.x) + q * kT;
+            tv[q] = vi < nvec ? __ldg(tp + vi) : make_uint4(0, 0, 0, 0);
+            dv[q] = (dp != nullptr && vi < nvec) ? __ldg(dp + vi) : make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // Per-thread weights of the block (zero past its end).
+    __device__ static __forceinline__ void weights(const RowPair& rp, int n, const uint4 (&tv)[kVPT],
+                                                   const uint4 (&dv)[kVPT],
+                                                   float (&w)[kVPT][kEPV])
+    {
+        const int nvec = n / kEPV;
+#pragma unroll
+        for (int q = 0; q < kVPT; ++q) {
+            float xt[kEPV], xd[kEPV];
+            unpack(tv[q], xt);
+            unpack(dv[q], xd);
+            const bool in = static_cast<int>(threadIdx.x) + q * kT < nvec;
+#pragma unroll
+            for (int e = 0; e < kEPV; ++e) w[q][e] = in ? weight_of(rp, xt[e], xd[e]) : 0.f;
+        }
+    }
+
+    __device__ static float2 block_weight(const RowPair& rp, int64_t e0, int n, float2* red)
+    {
+        uint4 tv[kVPT], dv[kVPT];
+        load(rp, e0, n, tv, dv);
+        float w[kVPT][kEPV];
+        weights(rp, n, tv, dv, w);
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < kVPT; ++q)
+#pragma unroll
+            for (int e = 0; e < kEPV; e += 2) {
+                a0 += w[q][e];
+                a1 += w[q][e + 1];
+            }
+        float err;
+        const float hi = two_sum(a0, a1, &err);
+        return block_sum2(hi, err, red);
+    }
+
+    __device__ static Best race(const RowPair& rp, int64_t e0, int n, Best* red)
+    {
+        uint4 tv[kVPT], dv[kVPT];
+        load(rp, e0, n, tv, dv);
+        float w[kVPT][kEPV];
+        weights(rp, n, tv, dv, w);
+        Best best{0.0f, INT_MAX};
+#pragma unroll
+        for (int q = 0; q < kVPT; ++q) {
+            const int64_t k = e0 + static_cast<int64_t>(threadIdx.x + q * kT) * kEPV;
+#pragma unroll
+            for (int g = 0; g < kEPV; g += 4) {
+                const float wg[4] = {w[q][g], w[q][g + 1], w[q][g + 2], w[q][g + 3]};
+                race_group(best, rp, k + g, wg);
+            }
+        }
+        return block_best(best, red);
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Staged path: rows not 16-byte aligned. The bulk engine moves the aligned
+// cover [a0, a0 + bulk) of row bytes [s, e); the last < 16 bytes of a tensor
+// whose size is not a multiple of 16 are loaded one element at a time. Byte s
+// lands at buf + off.
+// ---------------------------------------------------------------------------
 struct CopyPlan {
     const uint8_t* a0;
     uint32_t bulk;
@@ -76,17 +280,6 @@ __device__ __forceinline__ CopyPlan plan_copy(uint8_t* buf, const uint8_t* s, co
     return cp;
 }
 
-// Everything about the row pair a CTA works on.
-struct RowPair {
-    const uint8_t* trow;   // target row j
-    const uint8_t* drow;   // draft row j, or nullptr for the bonus row
-    const uint8_t* t_end;  // aligned tensor ends
-    const uint8_t* d_end;
-    float c, lt_hi, lt_lo, ld_hi, ld_lo;
-    uint64_t seed;
-    uint32_t seq, pos;
-};
-
 template <int ES>
 __device__ __forceinline__ float elem(const uint8_t* p)
 {
@@ -94,117 +287,104 @@ __device__ __forceinline__ float elem(const uint8_t* p)
                    : *reinterpret_cast<const float*>(p);
 }
 
-// Weight of staged element e: max(0, p - q) after a rejection, p for the bonus.
 template <int ES>
-__device__ __forceinline__ float weight(const RowPair& rp, const uint8_t* bt, const uint8_t* bd,
-                                        int e)
-{
-    const float p = ex2(fmaf(elem<ES>(bt + e * ES), rp.c, -rp.lt_hi) - rp.lt_lo);
-    if (rp.drow == nullptr) return p;
-    const float q = ex2(fmaf(elem<ES>(bd + e * ES), rp.c, -rp.ld_hi) - rp.ld_lo);
-    return fmaxf(p - q, 0.0f);
-}
+struct Staged {
+    uint8_t* buf_t;
+    uint8_t* buf_d;
+    uint64_t* bar;
+    uint32_t phase;
+    int off_t, off_d;
 
-// Stage chunk [e0, e1) of the pair; false if the copy did not land in time.
-// Thread 0 registers the expected bytes, then issues the copies.
-template <int ES>
-__device__ bool stage_chunk(const RowPair& rp, int64_t e0, int64_t e1, uint8_t* buf_t,
-                            uint8_t* buf_d, uint64_t* bar, uint32_t* phase, int* off_t,
-                            int* off_d)
-{
-    const CopyPlan ct = plan_copy<ES>(buf_t, rp.trow + e0 * ES, rp.trow + e1 * ES, rp.t_end);
-    CopyPlan cd;
-    cd.a0 = nullptr;
-    cd.bulk = 0;
-    cd.off = 0;
-    if (rp.drow != nullptr)
-        cd = plan_copy<ES>(buf_d, rp.drow + e0 * ES, rp.drow + e1 * ES, rp.d_end);
-    if (threadIdx.x == 0) {
-        mbar_arrive_expect_tx(bar, ct.bulk + cd.bulk);
-        if (ct.bulk > 0) bulk_copy_g2s(buf_t, ct.a0, ct.bulk, bar);
-        if (cd.bulk > 0) bulk_copy_g2s(buf_d, cd.a0, cd.bulk, bar);
+    // Stage block [e0, e0 + n); false if the copy did not land in time.
+    __device__ bool stage(const RowPair& rp, int64_t e0, int n)
+    {
+        const int64_t e1 = e0 + n;
+        const CopyPlan ct = plan_copy<ES>(buf_t, rp.trow + e0 * ES, rp.trow + e1 * ES, rp.t_end);
+        CopyPlan cd;
+        cd.a0 = nullptr;
+        cd.bulk = 0;
+        cd.off = 0;
+        if (rp.drow != nullptr)
+            cd = plan_copy<ES>(buf_d, rp.drow + e0 * ES, rp.drow + e1 * ES, rp.d_end);
+        if (threadIdx.x == 0) {
+            mbar_arrive_expect_tx(bar, ct.bulk + cd.bulk);
+            if (ct.bulk > 0) bulk_copy_g2s(buf_t, ct.a0, ct.bulk, bar);
+            if (cd.bulk > 0) bulk_copy_g2s(buf_d, cd.a0, cd.bulk, bar);
+        }
+        const bool ok = mbar_wait_bounded(bar, phase & 1u, nullptr);
+        phase += 1;
+        off_t = ct.off;
+        off_d = cd.off;
+        // Orders the element-wise tail stores before every thread's reads, and
+        // agrees on whether the copy landed.
+        return __syncthreads_and(ok ? 1 : 0) != 0;
     }
-    const bool ok = mbar_wait_bounded(bar, *phase & 1u, nullptr);
-    *phase += 1;
-    *off_t = ct.off;
-    *off_d = cd.off;
-    // Orders the element-wise tail stores before every thread's reads, and
-    // agrees on whether the copy landed.
-    return __syncthreads_and(ok ? 1 : 0) != 0;
-}
 
-struct Best {
-    float score;  // 0 = no candidate yet (every real score is > 0)
-    int idx;      // INT_MAX = none
+    __device__ float w_at(const RowPair& rp, int e) const
+    {
+        const float xt = elem<ES>(buf_t + off_t + e * ES);
+        const float xd = rp.drow ? elem<ES>(buf_d + off_d + e * ES) : 0.f;
+        return weight_of(rp, xt, xd);
+    }
+
+    __device__ float2 block_weight(const RowPair& rp, int n, float2* red) const
+    {
+        float a0 = 0.f;
+        for (int e = threadIdx.x; e < n; e += kT) a0 += w_at(rp, e);
+        return block_sum2(a0, 0.f, red);
+    }
+
+    __device__ Best race(const RowPair& rp, int64_t e0, int n, Best* red) const
+    {
+        Best best{0.0f, INT_MAX};
+        for (int g = threadIdx.x; 4 * g < n; g += kT) {
+            float w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) w[q] = 4 * g + q < n ? w_at(rp, 4 * g + q) : 0.f;
+            race_group(best, rp, e0 + 4 * g, w);
+        }
+        return block_best(best, red);
+    }
 };
 
-__device__ __forceinline__ void take(Best& a, float s, int i)
-{
-    if (s > a.score || (s == a.score && i < a.idx)) {
-        a.score = s;
-        a.idx = i;
-    }
-}
-
-// Race the tokens of the staged chunk whose first row index is e0.
-template <int ES>
-__device__ Best race_chunk(const RowPair& rp, const uint8_t* bt, const uint8_t* bd, int64_t e0,
-                           int n)
+// Level 1: the block with the largest W_c / E_c over blocks with W_c > 0
+// (lowest index on a tie); INT_MAX when no block has weight. The flags of all
+// block records are OR-ed into *flags.
+__device__ int race_blocks(const volatile ChunkSum* cs, int64_t nch, const RowPair& rp,
+                           int* flags, Best* red, int* red_flags)
 {
     Best best{0.0f, INT_MAX};
+    int fl = 0;
     const uint2 key = make_uint2(static_cast<uint32_t>(rp.seed), static_cast<uint32_t>(rp.seed >> 32));
-    for (int g = threadIdx.x; 4 * g < n; g += kT) {
-        float w[4];
-        bool any = false;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = 4 * g + q;
-            w[q] = e < n ? weight<ES>(rp, bt, bd, e) : 0.0f;
-            any |= w[q] > 0.0f;
-        }
-        if (!any) continue;
-        const int64_t k0 = e0 + 4 * g;  // multiple of 4: one Philox block per group
+    for (int64_t c = threadIdx.x; c < nch; c += kT) {
+        const float W = cs[c].hi + cs[c].lo;
+        fl |= cs[c].flags;
+        if (!(W > 0.f)) continue;
         const uint4 r = philox4x32_10(
-            make_uint4(rp.pos, rp.seq, 1u + static_cast<uint32_t>(k0 >> 2), 0u), key);
-        const uint32_t words[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            if (!(w[q] > 0.0f)) continue;
-            // v in (0, 1), exact in float; E = -ln v, taken as -log1p(v - 1) so
-            // that clocks near 0 (v near 1) keep full relative precision.
-            const float v = static_cast<float>(2u * (words[q] >> 9) + 1u) * 5.9604644775390625e-8f;
-            const float E = -log1pf(v - 1.0f);
-            take(best, __fdividef(w[q], E), static_cast<int>(k0 + q));
-        }
+            make_uint4(rp.pos, rp.seq, 1u + static_cast<uint32_t>(c >> 2), 1u), key);
+        const uint32_t lane = static_cast<uint32_t>(c & 3);
+        const uint32_t word = lane == 0 ? r.x : lane == 1 ? r.y : lane == 2 ? r.z : r.w;
+        take(best, W / exp_clock(word_to_open_uniform(word)), static_cast<int>(c));
     }
-    return best;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, off);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red_flags[threadIdx.x >> 5] = fl;
+    const Best t = block_best(best, red);  // its barriers also publish red_flags
+    int f = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) f |= red_flags[i];
+    *flags = f;
+    return t.idx;
 }
 
-// Block-wide best (largest score, lowest index), fixed tree.
-__device__ __forceinline__ Best block_best(Best b, Best* red)
+template <int ES, bool STAGED>
+__device__ void sample_block(const SampleArgs& a, uint8_t* dyn)
 {
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float os = __shfl_xor_sync(0xFFFFFFFFu, b.score, off);
-        const int oi = __shfl_xor_sync(0xFFFFFFFFu, b.idx, off);
-        take(b, os, oi);
-    }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
-    __syncthreads();
-    Best t = red[0];
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) take(t, red[i].score, red[i].idx);
-    return t;
-}
-
-template <int ES>
-__global__ void __launch_bounds__(kT) sample_kernel(const SampleArgs a)
-{
-    __shared__ __align__(128) uint8_t buf_t[kBufBytes];
-    __shared__ __align__(128) uint8_t buf_d[kBufBytes];
     __shared__ __align__(8) uint64_t bar;
     __shared__ Best red[kWarps];
+    __shared__ float2 red2[kWarps];
+    __shared__ int red_flags[kWarps];
     __shared__ int s_last;
 
     const Geometry& g = a.g;
@@ -223,39 +403,46 @@ __global__ void __launch_bounds__(kT) sample_kernel(const SampleArgs a)
     rp.drow = j < K ? a.draft + (b * K + j) * row_bytes : nullptr;
     rp.d_end = j < K ? down16(a.draft + g.B * K * row_bytes) : nullptr;
     rp.c = a.c;
-    rp.lt_hi = rec.lse_t_hi;
-    rp.lt_lo = rec.lse_t_lo;
-    rp.ld_hi = rec.lse_d_hi;
-    rp.ld_lo = rec.lse_d_lo;
+    rp.mt = rec.mt;
+    rp.lt = rec.lt;
+    rp.md = rec.md;
+    rp.ld = rec.ld;
     rp.seed = a.seed;
     rp.seq = static_cast<uint32_t>(b);
     rp.pos = static_cast<uint32_t>(j);
 
-    if (threadIdx.x == 0) {
-        mbar_init(&bar, 1);
-        fence_barrier_init();
+    Staged<ES> st{dyn, dyn + buf_bytes<ES>(), &bar, 0u, 0, 0};
+    if (STAGED) {
+        if (threadIdx.x == 0) {
+            mbar_init(&bar, 1);
+            fence_barrier_init();
+        }
+        __syncthreads();
     }
-    __syncthreads();
-    uint32_t phase = 0;
+    ChunkSum* sums = a.chunk_sums + b * nch;
+    auto block_len = [&](int64_t blk) {
+        return static_cast<int>(min(static_cast<int64_t>(kRaceBlock), V - blk * kRaceBlock));
+    };
 
-    const int64_t e0 = c * g.chunk_elems;
-    const int64_t e1 = min(e0 + g.chunk_elems, V);
-    int off_t = 0, off_d = 0;
-    Best mine{0.0f, INT_MAX};
+    // ---- every CTA: the total weight of its block ----
+    float2 W = make_float2(0.f, 0.f);
     int flags = 0;
-    if (stage_chunk<ES>(rp, e0, e1, buf_t, buf_d, &bar, &phase, &off_t, &off_d))
-        mine = race_chunk<ES>(rp, buf_t + off_t, buf_d + off_d, e0, static_cast<int>(e1 - e0));
-    else
-        flags = kFlagTimeout;
-    mine = block_best(mine, red);
-
+    const int n = block_len(c);
+    if (STAGED) {
+        if (st.stage(rp, c * kRaceBlock, n))
+            W = st.block_weight(rp, n, red2);
+        else
+            flags = kFlagTimeout;
+    } else {
+        W = Direct<ES>::block_weight(rp, c * kRaceBlock, n, red2);
+    }
     if (threadIdx.x == 0) {
-        ChunkBest cb;
-        cb.score = mine.score;
-        cb.idx = mine.idx;
-        cb.flags = flags;
-        cb.pad = 0;
-        a.chunk_best[b * nch + c] = cb;
+        ChunkSum cs;
+        cs.hi = W.x;
+        cs.lo = W.y;
+        cs.flags = flags;
+        cs.pad = 0;
+        sums[c] = cs;
         __threadfence();
         const uint32_t ticket = atomicAdd(&a.tickets[b], 1u);
         s_last = ticket == static_cast<uint32_t>(nch - 1);
@@ -264,62 +451,292 @@ __global__ void __launch_bounds__(kT) sample_kernel(const SampleArgs a)
     if (!s_last) return;
     __threadfence();
 
-    // ---- the last CTA of this sequence: merge the chunk winners ----
-    Best win{0.0f, INT_MAX};
+    // ---- the last CTA of this sequence: level 1 over the blocks ----
     int any_flags = 0;
-    if (threadIdx.x == 0) {
-        const volatile ChunkBest* cbs = a.chunk_best + b * nch;
-        for (int64_t i = 0; i < nch; ++i) {
-            take(win, cbs[i].score, cbs[i].idx);
-            any_flags |= cbs[i].flags;
-        }
-        red[0] = win;
-        s_last = any_flags;
-    }
-    __syncthreads();
-    win = red[0];
-    any_flags = s_last;
-    __syncthreads();
-
-    if (any_flags == 0 && win.idx == INT_MAX) {
-        // Every residual weight rounded to zero: race p_j over the whole row.
+    bool fallback = false;
+    int win = race_blocks(sums, nch, rp, &any_flags, red, red_flags);
+    if (any_flags == 0 && win == INT_MAX) {
+        // Every residual weight rounded to zero: race p_j instead, block sums first.
+        fallback = true;
         rp.drow = nullptr;
-        Best all{0.0f, INT_MAX};
-        for (int64_t i = 0; i < nch; ++i) {
-            const int64_t q0 = i * g.chunk_elems, q1 = min(q0 + g.chunk_elems, V);
-            if (!stage_chunk<ES>(rp, q0, q1, buf_t, buf_d, &bar, &phase, &off_t, &off_d)) {
-                any_flags = kFlagTimeout;
-                break;
+        for (int64_t i = 0; i < nch && any_flags == 0; ++i) {
+            const int ni = block_len(i);
+            float2 Wp = make_float2(0.f, 0.f);
+            if (STAGED) {
+                if (st.stage(rp, i * kRaceBlock, ni))
+                    Wp = st.block_weight(rp, ni, red2);
+                else
+                    any_flags = kFlagTimeout;
+            } else {
+                Wp = Direct<ES>::block_weight(rp, i * kRaceBlock, ni, red2);
             }
-            Best cb = race_chunk<ES>(rp, buf_t + off_t, buf_d, q0, static_cast<int>(q1 - q0));
-            cb = block_best(cb, red);
-            take(all, cb.score, cb.idx);
+            if (threadIdx.x == 0) {
+                ChunkSum cs;
+                cs.hi = Wp.x;
+                cs.lo = Wp.y;
+                cs.flags = 0;
+                cs.pad = 0;
+                sums[i] = cs;
+            }
+            __syncthreads();
         }
-        win = all;
+        if (any_flags == 0) {
+            int f2 = 0;
+            win = race_blocks(sums, nch, rp, &f2, red, red_flags);
+        }
+    }
+
+    // ---- level 2 over the tokens of the winning block ----
+    Best tok{0.0f, INT_MAX};
+    if (any_flags == 0 && win != INT_MAX) {
+        const int64_t p0 = static_cast<int64_t>(win) * kRaceBlock;
+        const int np = block_len(win);
+        if (STAGED) {
+            bool ok = true;
+            if (win != c || fallback) ok = st.stage(rp, p0, np);
+            if (ok)
+                tok = st.race(rp, p0, np, red);
+            else
+                any_flags = kFlagTimeout;
+        } else {
+            tok = Direct<ES>::race(rp, p0, np, red);
+        }
     }
 
     if (threadIdx.x == 0) {
         const int64_t K1 = K + 1;
-        if (any_flags != 0 || win.idx == INT_MAX) {
+        if (any_flags != 0 || tok.idx == INT_MAX) {
             for (int64_t i = 0; i < K1; ++i) a.out_tokens[b * K1 + i] = -1;
             a.num_accepted[b] = -1;
             if (a.seq_status) a.seq_status[b] = kFlagTimeout;
         } else {
-            a.out_tokens[b * K1 + j] = win.idx;
+            a.out_tokens[b * K1 + j] = tok.idx;
         }
     }
+}
+
+template <int ES, bool STAGED>
+__global__ void __launch_bounds__(kT) sample_kernel(const SampleArgs a)
+{
+    extern __shared__ __align__(128) uint8_t dyn[];
+    sample_block<ES, STAGED>(a, dyn);
+}
+
+template <int ES, bool STAGED>
+cudaError_t launch_one(const SampleArgs& a, cudaStream_t s)
+{
+    const unsigned grid = static_cast<unsigned>(a.g.B * a.g.nchunks);
+    const int smem = STAGED ? 2 * buf_bytes<ES>() : 0;
+    if (STAGED) {
+        const cudaError_t e = cudaFuncSetAttribute(
+            sample_kernel<ES, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        if (e != cudaSuccess) return e;
+    }
+    sample_kernel<ES, STAGED><<<grid, kT, smem, s>>>(a);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Aligned rows, launch 1 of 2: weight sums of 2 KB-per-row slices.
+// ---------------------------------------------------------------------------
+template <int ES>
+struct Slices {
+    static constexpr int kEPV = 16 / ES;                    // elements per vector
+    static constexpr int kTok = kSliceBytes / ES;           // tokens per slice
+    static constexpr int kPerBlock = kRaceBlock / kTok;     // slices per race block
+    static constexpr int kVPL = kSliceBytes / 16 / 32;      // vectors per lane per row
+};
+
+__device__ __forceinline__ void warp_sum2(float& hi, float& lo)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, off);
+        const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, off);
+        float err;
+        const float s = two_sum(hi, ohi, &err);
+        lo = __fadd_rn(__fadd_rn(lo, olo), err);
+        hi = s;
+    }
+}
+
+__device__ __forceinline__ void row_pair_of(RowPair& rp, const SampleArgs& a, const SeqRecord& rec,
+                                            int64_t b, int es)
+{
+    const Geometry& g = a.g;
+    const int64_t K = g.K, row_bytes = g.V * es;
+    const int64_t j = rec.j;
+    rp.trow = a.target + (b * (K + 1) + j) * row_bytes;
+    rp.t_end = down16(a.target + g.rows_t * row_bytes);
+    rp.drow = j < K ? a.draft + (b * K + j) * row_bytes : nullptr;
+    rp.d_end = j < K ? down16(a.draft + g.B * K * row_bytes) : nullptr;
+    rp.c = a.c;
+    rp.mt = rec.mt;
+    rp.lt = rec.lt;
+    rp.md = rec.md;
+    rp.ld = rec.ld;
+    rp.seed = a.seed;
+    rp.seq = static_cast<uint32_t>(b);
+    rp.pos = static_cast<uint32_t>(j);
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
+{
+    using S = Slices<ES>;
+    const Geometry& g = a.g;
+    const int64_t per_seq = g.nchunks * S::kPerBlock;
+    const int64_t total = g.B * per_seq;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kT / 32);
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * (kT / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    // Each warp takes a contiguous run of slices, so consecutive slices
+    // usually share a sequence and its record.
+    const int64_t i0 = w * total / nwarps, i1 = (w + 1) * total / nwarps;
+    int64_t cur_b = -1;
+    bool valid = false;
+    RowPair rp;
+    for (int64_t i = i0; i < i1; ++i) {
+        const int64_t b = i / per_seq;
+        const int64_t e0 = (i - b * per_seq) * S::kTok;
+        if (b != cur_b) {
+            cur_b = b;
+            const SeqRecord rec = a.seqs[b];
+            valid = rec.status == 0;
+            if (valid) row_pair_of(rp, a, rec, b, ES);
+        }
+        if (!valid) continue;  // the finish kernel skips this sequence
+        float hi = 0.f, lo = 0.f;
+        if (e0 < g.V) {
+            const int nvec = static_cast<int>(min(static_cast<int64_t>(S::kTok), g.V - e0)) / S::kEPV;
+            const uint4* tp = reinterpret_cast<const uint4*>(rp.trow + e0 * ES);
+            const uint4* dp = rp.drow ? reinterpret_cast<const uint4*>(rp.drow + e0 * ES) : nullptr;
+            uint4 tv[S::kVPL], dv[S::kVPL];
+#pragma unroll
+            for (int q = 0; q < S::kVPL; ++q) {
+                const int vi = lane + 32 * q;
+                tv[q] = vi < nvec ? __ldg(tp + vi) : make_uint4(0, 0, 0, 0);
+                dv[q] = (dp != nullptr && vi < nvec) ? __ldg(dp + vi) : make_uint4(0, 0, 0, 0);
+            }
+            float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+            for (int q = 0; q < S::kVPL; ++q) {
+                if (lane + 32 * q >= nvec) continue;
+                float xt[S::kEPV], xd[S::kEPV];
+                Direct<ES>::unpack(tv[q], xt);
+                Direct<ES>::unpack(dv[q], xd);
+#pragma unroll
+                for (int e = 0; e < S::kEPV; e += 2) {
+                    a0 += weight_of(rp, xt[e], xd[e]);
+                    a1 += weight_of(rp, xt[e + 1], xd[e + 1]);
+                }
+            }
+            hi = two_sum(a0, a1, &lo);
+            warp_sum2(hi, lo);
+        }
+        if (lane == 0) a.slice_sums[i] = make_float2(hi, lo);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Aligned rows, launch 2 of 2: one CTA per sequence runs the two levels.
+// ---------------------------------------------------------------------------
+template <int ES>
+__global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
+{
+    using S = Slices<ES>;
+    __shared__ Best red[kWarps];
+    __shared__ float2 red2[kWarps];
+    __shared__ int red_flags[kWarps];
+    const Geometry& g = a.g;
+    const int64_t b = blockIdx.x;
+    const SeqRecord rec = a.seqs[b];
+    if (rec.status != 0) return;
+    RowPair rp;
+    row_pair_of(rp, a, rec, b, ES);
+    const int64_t nch = g.nchunks, V = g.V, K1 = g.K + 1;
+    ChunkSum* sums = a.chunk_sums + b * nch;
+    auto block_len = [&](int64_t blk) {
+        return static_cast<int>(min(static_cast<int64_t>(kRaceBlock), V - blk * kRaceBlock));
+    };
+
+    // Block sums: the slice sums of each block, added in slice order.
+    for (int64_t c = threadIdx.x; c < nch; c += kT) {
+        const float2* sl = a.slice_sums + (b * nch + c) * S::kPerBlock;
+        float hi = 0.f, lo = 0.f;
+        for (int q = 0; q < S::kPerBlock; ++q) {
+            const float2 v = sl[q];
+            float err;
+            const float s2 = two_sum(hi, v.x, &err);
+            lo = __fadd_rn(__fadd_rn(lo, v.y), err);
+            hi = s2;
+        }
+        ChunkSum cs;
+        cs.hi = hi;
+        cs.lo = lo;
+        cs.flags = 0;
+        cs.pad = 0;
+        sums[c] = cs;
+    }
+    __syncthreads();
+
+    int flags = 0;
+    int win = race_blocks(sums, nch, rp, &flags, red, red_flags);
+    if (win == INT_MAX) {
+        // Every residual weight rounded to zero: race p_j instead, block sums first.
+        rp.drow = nullptr;
+        for (int64_t c = 0; c < nch; ++c) {
+            const float2 Wp = Direct<ES>::block_weight(rp, c * kRaceBlock, block_len(c), red2);
+            if (threadIdx.x == 0) {
+                ChunkSum cs;
+                cs.hi = Wp.x;
+                cs.lo = Wp.y;
+                cs.flags = 0;
+                cs.pad = 0;
+                sums[c] = cs;
+            }
+            __syncthreads();
+        }
+        win = race_blocks(sums, nch, rp, &flags, red, red_flags);
+    }
+    Best tok{0.0f, INT_MAX};
+    if (win != INT_MAX)
+        tok = Direct<ES>::race(rp, static_cast<int64_t>(win) * kRaceBlock, block_len(win), red);
+    if (threadIdx.x == 0) {
+        if (tok.idx == INT_MAX) {
+            for (int64_t i = 0; i < K1; ++i) a.out_tokens[b * K1 + i] = -1;
+            a.num_accepted[b] = -1;
+            if (a.seq_status) a.seq_status[b] = kFlagTimeout;
+        } else {
+            a.out_tokens[b * K1 + rec.j] = tok.idx;
+        }
+    }
+}
+
+template <int ES>
+cudaError_t launch_direct(const SampleArgs& a, cudaStream_t s)
+{
+    sample_stream_kernel<ES><<<a.g.sample_grid, kT, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    sample_finish_kernel<ES><<<static_cast<unsigned>(a.g.B), kT, 0, s>>>(a);
+    return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s)
 {
-    const unsigned grid = static_cast<unsigned>(a.g.B * a.g.nchunks);
-    if (a.g.es == 2)
-        sample_kernel<2><<<grid, kT, 0, s>>>(a);
-    else
-        sample_kernel<4><<<grid, kT, 0, s>>>(a);
-    return cudaGetLastError();
+    if (a.g.aligned) return a.g.es == 2 ? launch_direct<2>(a, s) : launch_direct<4>(a, s);
+    return a.g.es == 2 ? launch_one<2, true>(a, s) : launch_one<4, true>(a, s);
+}
+
+int sample_slices_per_block(int es) { return es == 2 ? Slices<2>::kPerBlock : Slices<4>::kPerBlock; }
+
+cudaError_t sample_stream_blocks_per_sm(int es, int* blocks)
+{
+    return es == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, sample_stream_kernel<2>, kT, 0)
+                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, sample_stream_kernel<4>, kT, 0);
 }
 
 }  // namespace sv

@@ -21,13 +21,15 @@ size_t round_up(size_t x) { return (x + kAlign - 1) & ~(kAlign - 1); }
 struct DeviceCache {
     bool ready = false;
     int sms = 0;
-    int blocks[2][2] = {{0, 0}, {0, 0}};  // [es == 2][mode]
+    int blocks[2][2] = {{0, 0}, {0, 0}};  // pass-1 CTAs per SM, [es == 2][mode]
+    int sample_blocks[2] = {0, 0};        // sampler streaming CTAs per SM, [es == 2]
 };
 std::mutex g_mu;
 DeviceCache g_cache[kMaxDevices];
 
-// SM count and resident pass-1 CTAs per SM on the current device.
-int device_limits(int es, int mode, int* sms, int* blocks)
+// SM count, resident pass-1 CTAs per SM and resident sampler-streaming CTAs
+// per SM on the current device.
+int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
 {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SV_ERR_CUDA;
@@ -40,15 +42,19 @@ int device_limits(int es, int mode, int* sms, int* blocks)
             for (int m = 0; m < 2; ++m)
                 if (sv::row_stats_blocks_per_sm(e ? 2 : 4, m, &c.blocks[e][m]) != cudaSuccess)
                     return SV_ERR_CUDA;
+        for (int e = 0; e < 2; ++e)
+            if (sv::sample_stream_blocks_per_sm(e ? 2 : 4, &c.sample_blocks[e]) != cudaSuccess)
+                return SV_ERR_CUDA;
         c.ready = true;
     }
     *sms = c.sms;
     *blocks = c.blocks[es == 2][mode];
-    return (*sms > 0 && *blocks > 0) ? SV_OK : SV_ERR_CUDA;
+    *sample_blocks = c.sample_blocks[es == 2];
+    return (*sms > 0 && *blocks > 0 && *sample_blocks > 0) ? SV_OK : SV_ERR_CUDA;
 }
 
 struct Layout {
-    size_t partials = 0, seqs = 0, chunk_best = 0, tickets = 0, total = 0;
+    size_t partials = 0, seqs = 0, chunk_sums = 0, slice_sums = 0, tickets = 0, total = 0;
 };
 
 int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
@@ -69,8 +75,8 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
     const int es = dtype == SV_BF16 ? 2 : 4;
-    int sms = 0, blocks = 0;
-    rc = device_limits(es, mode, &sms, &blocks);
+    int sms = 0, blocks = 0, sample_blocks = 0;
+    rc = device_limits(es, mode, &sms, &blocks, &sample_blocks);
     if (rc != SV_OK) return rc;
 
     std::memset(g, 0, sizeof(*g));
@@ -90,9 +96,14 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     g->grid = static_cast<int32_t>(g->tiles < want ? (g->tiles > 0 ? g->tiles : 1) : want);
     const int64_t per_cta = (g->tiles + g->grid - 1) / g->grid;
     g->maxseg = static_cast<int32_t>((per_cta + g->tiles_per_row - 1) / g->tiles_per_row + 1);
-    g->chunk_elems = sv::kChunkBytes / es;
-    g->nchunks = (V + g->chunk_elems - 1) / g->chunk_elems;
+    g->nchunks = (V + sv::kRaceBlock - 1) / sv::kRaceBlock;
     if (B * g->nchunks >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+    const int64_t spb = sv::sample_slices_per_block(es);
+    const int64_t slices = B * g->nchunks * spb;
+    const int64_t warps_per_cta = sv::kSampleThreads / 32;
+    const int64_t want_s = static_cast<int64_t>(sms) * sample_blocks;
+    const int64_t need_s = (slices + warps_per_cta - 1) / warps_per_cta;
+    g->sample_grid = static_cast<int32_t>(need_s < want_s ? (need_s > 0 ? need_s : 1) : want_s);
 
     size_t off = 0;
     L->partials = off;
@@ -100,8 +111,10 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
                     sizeof(sv::Partial));
     L->seqs = off;
     off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
-    L->chunk_best = off;
-    if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nchunks) * sizeof(sv::ChunkBest));
+    L->chunk_sums = off;
+    if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nchunks) * sizeof(sv::ChunkSum));
+    L->slice_sums = off;
+    if (mode == SV_SAMPLE && g->aligned) off += round_up(static_cast<size_t>(slices) * sizeof(float2));
     L->tickets = off;
     off += round_up(static_cast<size_t>(B) * sizeof(uint32_t));
     L->total = off > 0 ? off : kAlign;
@@ -160,15 +173,16 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     const uint8_t* dp = sampling ? static_cast<const uint8_t*>(draft) : nullptr;
     auto* partials = reinterpret_cast<sv::Partial*>(ws + L.partials);
     auto* seqs = reinterpret_cast<sv::SeqRecord*>(ws + L.seqs);
-    auto* chunk_best = reinterpret_cast<sv::ChunkBest*>(ws + L.chunk_best);
+    auto* chunk_sums = reinterpret_cast<sv::ChunkSum*>(ws + L.chunk_sums);
+    auto* slice_sums = reinterpret_cast<float2*>(ws + L.slice_sums);
     auto* tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
 
     sv::RowStatsArgs ra{tp, dp, g, c, partials};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     tickets, sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
                     sampling ? log_ratio : nullptr, seq_status};
-    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, chunk_best, tickets, out_tokens, num_accepted,
-                      seq_status};
+    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, chunk_sums, slice_sums, tickets, out_tokens,
+                      num_accepted, seq_status};
 
     if (!record(0)) return SV_ERR_CUDA;
     if (sv::launch_row_stats(ra, s) != cudaSuccess) return SV_ERR_CUDA;

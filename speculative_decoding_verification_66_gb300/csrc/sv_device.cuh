@@ -53,11 +53,6 @@ __device__ __forceinline__ float pow2_neg_int(float d)
     if (!(d > -126.0f)) return 0.0f;
     return __int_as_float((127 + static_cast<int>(d)) << 23);
 }
-__device__ __forceinline__ double pow2_neg_int_d(float d)
-{
-    if (!(d > -1022.0f)) return 0.0;
-    return __longlong_as_double(static_cast<long long>(1023 + static_cast<int>(d)) << 52);
-}
 
 // hi + lo += x with the rounding error of the high sum kept in lo (Knuth's
 // two-sum; no assumption on the magnitudes).
@@ -68,6 +63,31 @@ __device__ __forceinline__ void two_sum_acc(float& hi, float& lo, float x)
     const float err = __fadd_rn(__fsub_rn(hi, __fsub_rn(s, bp)), __fsub_rn(x, bp));
     hi = s;
     lo = __fadd_rn(lo, err);
+}
+
+// Knuth's two-sum: s + err == a + b exactly (round to nearest, no overflow).
+__device__ __forceinline__ float two_sum(float a, float b, float* err)
+{
+    const float s = __fadd_rn(a, b);
+    const float bp = __fsub_rn(s, a);
+    *err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bp)), __fsub_rn(b, bp));
+    return s;
+}
+
+// (hi + lo) * 2^m  +=  (ohi + olo) * 2^om, both exponents integer-valued or
+// -inf (an empty sum). The rescales are exact powers of two, so the only
+// rounding is the one two-sum keeps in lo.
+__device__ __forceinline__ void merge_scaled(float& m, float& hi, float& lo, float om, float ohi,
+                                             float olo)
+{
+    const float M = fmaxf(m, om);
+    if (M == __uint_as_float(0xFF800000u)) return;  // both empty
+    const float a = pow2_neg_int(m - M), b = pow2_neg_int(om - M);
+    float err;
+    const float s = two_sum(__fmul_rn(hi, a), __fmul_rn(ohi, b), &err);
+    lo = __fadd_rn(__fadd_rn(__fmul_rn(lo, a), __fmul_rn(olo, b)), err);
+    hi = s;
+    m = M;
 }
 
 // ---------------------------------------------------------------------------
@@ -95,11 +115,18 @@ __device__ __forceinline__ uint4 verify_random_words(uint64_t seed, uint32_t seq
     return philox4x32_10(make_uint4(pos, seq, 0u, 0u),
                          make_uint2(static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)));
 }
-// 24-bit uniform in [0, 1 - 2^-24]; exact in float and double.
-__device__ __forceinline__ double word_to_uniform(uint32_t w)
+// 24-bit uniform in [0, 1 - 2^-24]; exact in float.
+__device__ __forceinline__ float word_to_uniform(uint32_t w)
 {
-    return static_cast<double>(w >> 8) * (1.0 / 16777216.0);
+    return static_cast<float>(w >> 8) * 5.9604644775390625e-8f;
 }
+// Race uniform in (0, 1): (2 (w >> 9) + 1) * 2^-24, exact in float.
+__device__ __forceinline__ float word_to_open_uniform(uint32_t w)
+{
+    return static_cast<float>(2u * (w >> 9) + 1u) * 5.9604644775390625e-8f;
+}
+// -ln v for v in (0, 1) with full relative precision near v = 1.
+__device__ __forceinline__ float exp_clock(float v) { return -log1pf(v - 1.0f); }
 
 // ---------------------------------------------------------------------------
 // Shared-memory mbarriers and bulk copies

@@ -19,10 +19,15 @@ constexpr int kRowStages = 4;
 constexpr int kRowConsumerWarps = 8;
 constexpr int kRowThreads = (kRowConsumerWarps + 1) * 32;
 
-// Residual / bonus sampling (pass 2): per sequence, the chosen row pair is cut
-// into chunks of kChunkBytes of each row; one CTA per chunk.
-constexpr int kChunkBytes = 16384;
+// Residual / bonus sampling (pass 3): per sequence, the emitted row pair is cut
+// into the sampler's race blocks of kRaceBlock tokens; one CTA per block. The
+// block length is part of the sampler's definition (it decides which random
+// numbers are drawn), not a tuning knob.
+constexpr int kRaceBlock = 8192;
 constexpr int kSampleThreads = 256;
+// Aligned rows: the sampler's streaming pass sums the weights of slices of
+// kSliceBytes per row, one warp per slice.
+constexpr int kSliceBytes = 2048;
 
 constexpr int kMaxK = 1024;
 
@@ -32,38 +37,42 @@ constexpr int kFlagTimeout = 4;    // == SV_SEQ_TIMEOUT
 constexpr int kFlagBadToken = 1;   // == SV_SEQ_BAD_TOKEN
 
 // One warp's reduction of one row segment.
-//   sampling: s = sum over the segment of 2^(x*c - m), m an integer-valued
-//             reference exponent (log2 units), -inf when the segment is all -inf.
-//   greedy:   m = largest raw logit, s = its lowest index (exact in double),
-//             or 2^31 - 1 when no element beat -inf.
+//   sampling: (hi + lo) * 2^m = sum over the segment of 2^(x*c), kept as a float
+//             pair scaled by an integer-valued reference exponent m (log2
+//             units), m = -inf and hi = lo = 0 when the segment is all -inf.
+//   greedy:   m = largest raw logit, hi = its lowest index (int bits), or
+//             2^31 - 1 when no element beat -inf.
 //   flags:    kFlagNonFinite / kFlagTimeout.
+// No double precision: GB300 runs float64 at a small fraction of its float32
+// rate, so sums that need more than 24 bits are carried as float pairs.
 struct Partial {
-    double s;
     float m;
+    float hi;
+    float lo;
     int32_t flags;
 };
 static_assert(sizeof(Partial) == 16, "Partial layout");
 
 // Per-sequence record written by the acceptance scan, read by the sampler.
+// A row's log2 normaliser log2 sum_k 2^(x_k c) is m + l: m the integer-valued
+// reference exponent, l = log2 of the scaled sum.
 struct SeqRecord {
     int32_t j;         // emitted position (0..K)
     int32_t status;    // SV_SEQ_* bits; 0 = valid
-    float lse_t_hi;    // log2-domain normaliser of target row j, as hi + lo
-    float lse_t_lo;
-    float lse_d_hi;    // same for draft row j (unused when j == K)
-    float lse_d_lo;
+    float mt, lt;      // normaliser of target row j
+    float md, ld;      // normaliser of draft row j (unused when j == K)
     int32_t pad[2];
 };
 static_assert(sizeof(SeqRecord) == 32, "SeqRecord layout");
 
-// Winner of one chunk's exponential race (score 0 / idx INT_MAX: no candidate).
-struct ChunkBest {
-    float score;
-    int32_t idx;
+// Total sampling weight of one race block as a float pair (flags: kFlagTimeout).
+struct ChunkSum {
+    float hi;
+    float lo;
     int32_t flags;
     int32_t pad;
 };
-static_assert(sizeof(ChunkBest) == 16, "ChunkBest layout");
+static_assert(sizeof(ChunkSum) == 16, "ChunkSum layout");
 
 struct Geometry {
     int64_t B, K, V;
@@ -77,8 +86,8 @@ struct Geometry {
     int32_t grid;           // pass-1 CTAs
     int32_t maxseg;         // most row segments one pass-1 CTA can touch
     int32_t aligned;        // every row starts on a 16-byte boundary
-    int64_t chunk_elems;    // pass-2 chunk length
-    int64_t nchunks;        // chunks per row
+    int64_t nchunks;        // race blocks per row
+    int32_t sample_grid;    // CTAs of the sampler's streaming pass (aligned rows)
 };
 
 struct RowStatsArgs {
@@ -114,7 +123,8 @@ struct SampleArgs {
     float c;
     uint64_t seed;
     const SeqRecord* seqs;
-    ChunkBest* chunk_best;  // [B][nchunks]
+    ChunkSum* chunk_sums;   // [B][nchunks]
+    float2* slice_sums;     // [B][nchunks][slices per block] (aligned rows)
     uint32_t* tickets;      // [B], zeroed by the scan
     int32_t* out_tokens;
     int32_t* num_accepted;
@@ -128,5 +138,8 @@ cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 
 // Resident pass-1 CTAs per SM for this dtype / mode (occupancy query).
 cudaError_t row_stats_blocks_per_sm(int es, int mode, int* blocks);
+// Resident CTAs per SM of the sampler's streaming pass, and its slices per block.
+cudaError_t sample_stream_blocks_per_sm(int es, int* blocks);
+int sample_slices_per_block(int es);
 
 }  // namespace sv
