@@ -445,6 +445,8 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
             argmax_tile<ES>(gs, v, sp, tid);
         cursor_next<ES>(cur, a);
     }
+    // The scan may start launching now; it waits for this grid to finish.
+    if (tid == 0) pdl_trigger();
     if (n == ntiles) {
         Partial* out = my_partials + (row - row_first) * kRowConsumerWarps;
         if (MODE == kSampleMode)

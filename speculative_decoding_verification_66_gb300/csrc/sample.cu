@@ -391,6 +391,7 @@ __device__ void sample_block(const SampleArgs& a, uint8_t* dyn)
     const int64_t nch = g.nchunks;
     const int64_t b = blockIdx.x / nch;
     const int64_t c = blockIdx.x - b * nch;
+    pdl_wait();  // the scan has finished and the sequence records are visible
     const SeqRecord rec = a.seqs[b];
     if (rec.status != 0) return;
 
@@ -532,8 +533,7 @@ cudaError_t launch_one(const SampleArgs& a, cudaStream_t s)
             sample_kernel<ES, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
     }
-    sample_kernel<ES, STAGED><<<grid, kT, smem, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(sample_kernel<ES, STAGED>, dim3(grid), dim3(kT), smem, s, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -593,6 +593,7 @@ __global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
     // Each warp takes a contiguous run of slices, so consecutive slices
     // usually share a sequence and its record.
     const int64_t i0 = w * total / nwarps, i1 = (w + 1) * total / nwarps;
+    pdl_wait();  // the scan has finished and the sequence records are visible
     int64_t cur_b = -1;
     bool valid = false;
     RowPair rp;
@@ -636,6 +637,7 @@ __global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
         }
         if (lane == 0) a.slice_sums[i] = make_float2(hi, lo);
     }
+    pdl_trigger();  // the finish kernel may start launching
 }
 
 // ---------------------------------------------------------------------------
@@ -650,6 +652,7 @@ __global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
     __shared__ int red_flags[kWarps];
     const Geometry& g = a.g;
     const int64_t b = blockIdx.x;
+    pdl_wait();  // the slice sums are complete and visible
     const SeqRecord rec = a.seqs[b];
     if (rec.status != 0) return;
     RowPair rp;
@@ -716,11 +719,11 @@ __global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
 template <int ES>
 cudaError_t launch_direct(const SampleArgs& a, cudaStream_t s)
 {
-    sample_stream_kernel<ES><<<a.g.sample_grid, kT, 0, s>>>(a);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_dependent(sample_stream_kernel<ES>, dim3(a.g.sample_grid), dim3(kT), 0,
+                                     s, a);
     if (e != cudaSuccess) return e;
-    sample_finish_kernel<ES><<<static_cast<unsigned>(a.g.B), kT, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch_dependent(sample_finish_kernel<ES>, dim3(static_cast<unsigned>(a.g.B)), dim3(kT),
+                            0, s, a);
 }
 
 }  // namespace

@@ -128,6 +128,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
         s_status = 0;
         s_j = static_cast<int>(K);
     }
+    pdl_trigger();  // the sampler's first kernel may start launching
+    pdl_wait();     // pass 1 has finished and its partials are visible
     __syncthreads();
 
     const int lane = threadIdx.x & 31;
@@ -228,11 +230,9 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s)
 {
     const size_t smem = 8 * static_cast<size_t>(2 * a.g.K + 1);
-    if (a.g.es == 2)
-        scan_kernel<2><<<static_cast<unsigned>(a.g.B), kScanThreads, smem, s>>>(a);
-    else
-        scan_kernel<4><<<static_cast<unsigned>(a.g.B), kScanThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>(a.g.B)), block(kScanThreads);
+    return a.g.es == 2 ? launch_dependent(scan_kernel<2>, grid, block, smem, s, a)
+                       : launch_dependent(scan_kernel<4>, grid, block, smem, s, a);
 }
 
 }  // namespace sv

@@ -129,6 +129,20 @@ __device__ __forceinline__ float word_to_open_uniform(uint32_t w)
 __device__ __forceinline__ float exp_clock(float v) { return -log1pf(v - 1.0f); }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch. A kernel launched with programmatic stream
+// serialization may start while the previous kernel in the stream is still
+// running; pdl_wait() blocks until that kernel has completed and its memory
+// is visible (and returns at once when the kernel was launched normally).
+// pdl_trigger() lets the next kernel start launching once every CTA of this
+// one has issued it or exited.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
 // Shared-memory mbarriers and bulk copies
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t smem_addr(const void* p)

@@ -4,6 +4,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
+
 #include <cuda_runtime.h>
 
 namespace sv {
@@ -130,6 +132,25 @@ struct SampleArgs {
     int32_t* num_accepted;
     int32_t* seq_status;    // optional
 };
+
+// Launch with programmatic stream serialization (the kernel must call
+// pdl_wait() before it reads what the previous kernel in the stream wrote).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers (return the launch's cudaError_t).
 cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t s);
