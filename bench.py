@@ -196,6 +196,23 @@ def reference_arm(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(x: float, dist=None) -> float:
+    """The slowest rank's time: every rank's timed region is bracketed by
+    barriers, and the job is done when the last rank is."""
+    if dist is None:
+        return float(x)
+    import torch
+    t = torch.tensor([float(x)], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, seqs_per_rank: int, steps: int, elapsed_s: float) -> float:
+    """Weak scaling: every rank verifies its own batch each step, so the job
+    verifies world * seqs_per_rank sequences per step."""
+    return world * seqs_per_rank * steps / elapsed_s
+
+
 def config_of(wl):
     return {"workload": wl.label, "B": wl.B, "K": wl.K, "V": wl.V, "logits_dtype": wl.dtype,
             "mode": wl.mode, "temperature": wl.temperature,
@@ -283,11 +300,7 @@ def main():
         torch.cuda.synchronize()
         if dist:
             dist.barrier()
-    elapsed_ms = start.elapsed_time(stop)
-    if dist:
-        t = torch.tensor([elapsed_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(start.elapsed_time(stop), dist)
     # Stage times: the same calls with events recorded on the launch stream
     # between the kernels (this serialises the kernels, so it is timed apart).
     n_staged = max(3, min(args.steps, 300))
@@ -299,7 +312,7 @@ def main():
     scan_ms = sum(e[1].elapsed_time(e[2]) for e in events) / n_staged
     sample_ms = sum(e[2].elapsed_time(e[3]) for e in events) / n_staged
     ms_per_step = elapsed_ms / args.steps
-    value = world * B * args.steps / (elapsed_ms / 1e3)
+    value = job_throughput(world, B, args.steps, elapsed_ms / 1e3)
     mean_bytes = sum(step_bytes[i & 1] for i in range(args.steps)) / args.steps
     peak, peak_src = peaks()
     step_gbs = mean_bytes / (ms_per_step / 1e3) / 1e9
@@ -329,11 +342,7 @@ def main():
     for i in range(e2e_steps):
         e2e_step(i)
     stream.synchronize()
-    e2e_s = time.perf_counter() - t0
-    if dist:
-        t = torch.tensor([e2e_s], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks(time.perf_counter() - t0, dist)
     h2d = sum(t.numel() * t.element_size() for t in h[0].values() if t is not None)
     d2h = h_out.numel() * 4 + h_nacc.numel() * 4
 
@@ -353,7 +362,7 @@ def main():
         "roofline": {"kernel": "row_stats", "bound": "hbm", "achieved": pass1_gbs, "peak": peak,
                      "unit": "GB/s", "frac": pass1_gbs / peak, "traffic": profiled_traffic(),
                      "algorithmic_bytes": pass1_bytes, "peak_source": f"{peak_src} hbm_gbs"},
-        "e2e": {"value": world * B * e2e_steps / e2e_s, "unit": "seqs/s",
+        "e2e": {"value": job_throughput(world, B, e2e_steps, e2e_s), "unit": "seqs/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
         "clocks": clocks.summary(),
         "gpu_launches": sv.launches(mode, V, copies[0]["target"].dtype) * args.steps,
