@@ -153,6 +153,9 @@ int spec_verify_debug(const void* target_logits, const void* draft_logits,
  * events[1] after it, events[2] after the acceptance scan, events[3] after
  * the residual/bonus sampler (equal to events[2]'s position in greedy mode).
  * `events` holds n_events (>= 4) cudaEvent_t handles created by the caller.
+ * spec_verify starts each kernel while the previous one drains (programmatic
+ * dependent launch); this variant runs them strictly one after another so
+ * that the events bracket each stage, so its total can exceed spec_verify's.
  */
 int spec_verify_timed(const void* target_logits, const void* draft_logits,
                       const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,

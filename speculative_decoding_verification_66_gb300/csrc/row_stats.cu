@@ -106,6 +106,19 @@ __device__ __forceinline__ Span tile_span(const Cursor& c, const Geometry& g)
     const int64_t e1 = min(e0 + g.tile_elems, g.V);
     const uint8_t* s = c.rowp + e0 * ES;
     const uint8_t* e = c.rowp + e1 * ES;
+    if (g.aligned) {
+        // Rows, tiles and tensor ends on 16-byte boundaries: no cover, no
+        // masks, no element-wise tail.
+        sp.a0 = s;
+        sp.bulk = static_cast<uint32_t>(e - s);
+        sp.tail = e;
+        sp.e = e;
+        sp.nv = static_cast<int32_t>(sp.bulk >> 4);
+        sp.head = 0;
+        sp.last = 16 / ES;
+        sp.idx0 = e0;
+        return sp;
+    }
     sp.a0 = align_down16(s);
     const uint8_t* up = align_up16(e);
     const uint8_t* bend = up < c.tend ? up : c.tend;

@@ -21,11 +21,12 @@
 //  * Rows on 16-byte boundaries (every vocabulary whose row is a multiple of
 //    16 bytes): two launches. sample_stream_kernel is a grid of warps, each
 //    taking a contiguous run of 2 KB-per-row slices of the emitted row pairs
-//    with coalesced 16-byte loads and writing one float-pair weight sum per
-//    slice; it has no shared memory, no atomics and no barriers.
-//    sample_finish_kernel, one CTA per sequence, adds the slice sums of each
-//    block in a fixed order, runs level 1, re-reads the winning block and runs
-//    level 2.
+//    through its own two-stage ring of bulk copies and writing one float-pair
+//    weight sum per slice; it has no atomics and no CTA-wide barriers.
+//    sample_finish_kernel, kFinishSplit CTAs per sequence, adds the slice
+//    sums of each block in a fixed order and runs level 1 (redundantly, with
+//    one result), then each CTA re-reads a quarter of the winning block and
+//    races it; the last CTA of the sequence keeps the best quarter.
 //  * Other rows: sample_kernel, one CTA per (sequence, block), stages its block
 //    in shared memory with bulk copies; the last CTA of a sequence (an atomic
 //    ticket: no one waits on it) runs the two levels.
@@ -111,7 +112,9 @@ __device__ __forceinline__ void race_group(Best& best, const RowPair& rp, int64_
                  static_cast<int>(k0 + q));
 }
 
-// Block-wide float-pair sum (fixed tree); every thread gets the total.
+// Block-wide float-pair sum over NT threads (fixed tree); every thread gets
+// the total.
+template <int NT = kT>
 __device__ __forceinline__ float2 block_sum2(float hi, float lo, float2* red)
 {
 #pragma unroll
@@ -128,7 +131,7 @@ __device__ __forceinline__ float2 block_sum2(float hi, float lo, float2* red)
     __syncthreads();
     float th = red[0].x, tl = red[0].y;
 #pragma unroll
-    for (int i = 1; i < kWarps; ++i) {
+    for (int i = 1; i < NT / 32; ++i) {
         float err;
         const float s = two_sum(th, red[i].x, &err);
         tl = __fadd_rn(__fadd_rn(tl, red[i].y), err);
@@ -137,7 +140,8 @@ __device__ __forceinline__ float2 block_sum2(float hi, float lo, float2* red)
     return make_float2(th, tl);
 }
 
-// Block-wide best (largest score, lowest index), fixed tree.
+// Block-wide best over NT threads (largest score, lowest index), fixed tree.
+template <int NT = kT>
 __device__ __forceinline__ Best block_best(Best b, Best* red)
 {
 #pragma unroll
@@ -151,18 +155,19 @@ __device__ __forceinline__ Best block_best(Best b, Best* red)
     __syncthreads();
     Best t = red[0];
 #pragma unroll
-    for (int i = 1; i < kWarps; ++i) take(t, red[i].score, red[i].idx);
+    for (int i = 1; i < NT / 32; ++i) take(t, red[i].score, red[i].idx);
     return t;
 }
 
 // ---------------------------------------------------------------------------
-// Direct path: rows 16-byte aligned, a block is read with 16-byte loads.
-// Thread t takes vectors t, t + kT, ... of the block (coalesced).
+// Direct path: rows 16-byte aligned, a span of up to LEN tokens is read with
+// 16-byte loads by NT threads; thread t takes vectors t, t + NT, ... (coalesced).
 // ---------------------------------------------------------------------------
-template <int ES>
+template <int ES, int NT = kT, int LEN = kRaceBlock>
 struct Direct {
-    static constexpr int kEPV = 16 / ES;                  // elements per vector
-    static constexpr int kVPT = kRaceBlock / kEPV / kT;   // vectors per thread
+    static constexpr int kEPV = 16 / ES;            // elements per vector
+    static constexpr int kVPT = LEN / kEPV / NT;    // vectors per thread
+    static_assert(LEN % (kEPV * NT) == 0, "span must split evenly over the threads");
 
     // Elements of one 16-byte vector, widened exactly to float.
     __device__ static __forceinline__ void unpack(const uint4& v, float (&x)[kEPV])
@@ -184,7 +189,7 @@ struct Direct {
         const int nvec = n / kEPV;
 #pragma unroll
         for (int q = 0; q < kVPT; ++q) {
-            const int vi = static_cast<int>(threadIdx.x) + q * kT;
+            const int vi = static_cast<int>(threadIdx.x) + q * NT;
             tv[q] = vi < nvec ? __ldg(tp + vi) : make_uint4(0, 0, 0, 0);
             dv[q] = (dp != nullptr && vi < nvec) ? __ldg(dp + vi) : make_uint4(0, 0, 0, 0);
         }
@@ -201,7 +206,7 @@ struct Direct {
             float xt[kEPV], xd[kEPV];
             unpack(tv[q], xt);
             unpack(dv[q], xd);
-            const bool in = static_cast<int>(threadIdx.x) + q * kT < nvec;
+            const bool in = static_cast<int>(threadIdx.x) + q * NT < nvec;
 #pragma unroll
             for (int e = 0; e < kEPV; ++e) w[q][e] = in ? weight_of(rp, xt[e], xd[e]) : 0.f;
         }
@@ -223,7 +228,7 @@ struct Direct {
             }
         float err;
         const float hi = two_sum(a0, a1, &err);
-        return block_sum2(hi, err, red);
+        return block_sum2<NT>(hi, err, red);
     }
 
     __device__ static Best race(const RowPair& rp, int64_t e0, int n, Best* red)
@@ -235,14 +240,14 @@ struct Direct {
         Best best{0.0f, INT_MAX};
 #pragma unroll
         for (int q = 0; q < kVPT; ++q) {
-            const int64_t k = e0 + static_cast<int64_t>(threadIdx.x + q * kT) * kEPV;
+            const int64_t k = e0 + static_cast<int64_t>(threadIdx.x + q * NT) * kEPV;
 #pragma unroll
             for (int g = 0; g < kEPV; g += 4) {
                 const float wg[4] = {w[q][g], w[q][g + 1], w[q][g + 2], w[q][g + 3]};
                 race_group(best, rp, k + g, wg);
             }
         }
-        return block_best(best, red);
+        return block_best<NT>(best, red);
     }
 };
 
@@ -350,13 +355,14 @@ struct Staged {
 // Level 1: the block with the largest W_c / E_c over blocks with W_c > 0
 // (lowest index on a tie); INT_MAX when no block has weight. The flags of all
 // block records are OR-ed into *flags.
+template <int NT = kT>
 __device__ int race_blocks(const volatile ChunkSum* cs, int64_t nch, const RowPair& rp,
                            int* flags, Best* red, int* red_flags)
 {
     Best best{0.0f, INT_MAX};
     int fl = 0;
     const uint2 key = make_uint2(static_cast<uint32_t>(rp.seed), static_cast<uint32_t>(rp.seed >> 32));
-    for (int64_t c = threadIdx.x; c < nch; c += kT) {
+    for (int64_t c = threadIdx.x; c < nch; c += NT) {
         const float W = cs[c].hi + cs[c].lo;
         fl |= cs[c].flags;
         if (!(W > 0.f)) continue;
@@ -370,10 +376,10 @@ __device__ int race_blocks(const volatile ChunkSum* cs, int64_t nch, const RowPa
     for (int off = 16; off > 0; off >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, off);
     __syncthreads();
     if ((threadIdx.x & 31) == 0) red_flags[threadIdx.x >> 5] = fl;
-    const Best t = block_best(best, red);  // its barriers also publish red_flags
+    const Best t = block_best<NT>(best, red);  // its barriers also publish red_flags
     int f = 0;
 #pragma unroll
-    for (int i = 0; i < kWarps; ++i) f |= red_flags[i];
+    for (int i = 0; i < NT / 32; ++i) f |= red_flags[i];
     *flags = f;
     return t.idx;
 }
@@ -533,7 +539,7 @@ cudaError_t launch_one(const SampleArgs& a, cudaStream_t s)
             sample_kernel<ES, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
         if (e != cudaSuccess) return e;
     }
-    return launch_dependent(sample_kernel<ES, STAGED>, dim3(grid), dim3(kT), smem, s, a);
+    return launch_dependent(a.g.pdl != 0, sample_kernel<ES, STAGED>, dim3(grid), dim3(kT), smem, s, a);
 }
 
 // ---------------------------------------------------------------------------
@@ -580,85 +586,184 @@ __device__ __forceinline__ void row_pair_of(RowPair& rp, const SampleArgs& a, co
     rp.pos = static_cast<uint32_t>(j);
 }
 
+// One slice pair as a warp sees it: where its rows are and how many 16-byte
+// vectors of each row it holds (0 past the vocabulary).
+struct SliceJob {
+    RowPair rp;
+    bool seq_ok;  // the sequence is valid (else nothing is read or written)
+    int nvec;
+};
+
+// Slice `sl` of sequence `b`. Consecutive slices of a warp usually share a
+// sequence, whose record is then read once.
+template <int ES>
+__device__ __forceinline__ void slice_job(SliceJob& job, const SampleArgs& a, int64_t b,
+                                          int64_t sl, int64_t& cached_b, SliceJob& cache)
+{
+    using S = Slices<ES>;
+    const int64_t e0 = sl * S::kTok;
+    if (b != cached_b) {
+        cached_b = b;
+        const SeqRecord rec = a.seqs[b];
+        cache.seq_ok = rec.status == 0;
+        if (cache.seq_ok) row_pair_of(cache.rp, a, rec, b, ES);
+    }
+    job = cache;
+    job.nvec = 0;
+    if (job.seq_ok && e0 < a.g.V) {
+        job.nvec = static_cast<int>(min(static_cast<int64_t>(S::kTok), a.g.V - e0)) / S::kEPV;
+        job.rp.trow += e0 * ES;  // point at the slice
+        if (job.rp.drow) job.rp.drow += e0 * ES;
+    }
+}
+
+// Lane 0 starts the bulk copies of a slice pair into a stage; a pair with
+// nothing to read completes the stage's phase with a plain arrive.
+__device__ __forceinline__ void issue_slice(const SliceJob& job, uint8_t* stage, uint64_t* bar)
+{
+    const uint32_t bytes = static_cast<uint32_t>(job.nvec) * 16u;
+    if (bytes == 0) {
+        mbar_arrive(bar);
+        return;
+    }
+    mbar_arrive_expect_tx(bar, job.rp.drow ? 2u * bytes : bytes);
+    bulk_copy_g2s(stage, job.rp.trow, bytes, bar);
+    if (job.rp.drow) bulk_copy_g2s(stage + kSliceBytes, job.rp.drow, bytes, bar);
+}
+
+// Each warp walks a contiguous run of slices with a two-stage ring in shared
+// memory: lane 0 copies slice i + 1 (both rows, bulk copies) while the warp
+// sums the weights of slice i from the other stage. No registers hold data in
+// flight, so every warp keeps a full slice pair moving at all times.
 template <int ES>
 __global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
 {
     using S = Slices<ES>;
+    extern __shared__ __align__(128) uint8_t ring[];  // [warp][stage][target | draft]
+    __shared__ __align__(8) uint64_t bars[kWarps][2];
     const Geometry& g = a.g;
     const int64_t per_seq = g.nchunks * S::kPerBlock;
     const int64_t total = g.B * per_seq;
-    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * (kT / 32);
-    const int64_t w = static_cast<int64_t>(blockIdx.x) * (kT / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
+    const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    // Each warp takes a contiguous run of slices, so consecutive slices
-    // usually share a sequence and its record.
+    const int64_t w = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
     const int64_t i0 = w * total / nwarps, i1 = (w + 1) * total / nwarps;
+    uint8_t* stage0 = ring + static_cast<size_t>(warp) * 4 * kSliceBytes;
+    uint8_t* stage1 = stage0 + 2 * kSliceBytes;
+    if (lane == 0) {
+        mbar_init(&bars[warp][0], 1);
+        mbar_init(&bars[warp][1], 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
     pdl_wait();  // the scan has finished and the sequence records are visible
-    int64_t cur_b = -1;
-    bool valid = false;
-    RowPair rp;
-    for (int64_t i = i0; i < i1; ++i) {
-        const int64_t b = i / per_seq;
-        const int64_t e0 = (i - b * per_seq) * S::kTok;
-        if (b != cur_b) {
-            cur_b = b;
-            const SeqRecord rec = a.seqs[b];
-            valid = rec.status == 0;
-            if (valid) row_pair_of(rp, a, rec, b, ES);
+
+    int64_t cached_b = -1;
+    SliceJob cache, cur, next;
+    cache.seq_ok = false;
+    cache.nvec = 0;
+    uint32_t phases = 0;  // bit s: parity of the next phase of stage s
+    bool failed = false;
+    // Cursor (sequence, slice) of the next slice to issue; one division here,
+    // increments afterwards.
+    int64_t nb = i0 / per_seq, nsl = i0 - nb * per_seq;
+    auto advance = [&]() {
+        if (++nsl == per_seq) {
+            nsl = 0;
+            ++nb;
         }
-        if (!valid) continue;  // the finish kernel skips this sequence
-        float hi = 0.f, lo = 0.f;
-        if (e0 < g.V) {
-            const int nvec = static_cast<int>(min(static_cast<int64_t>(S::kTok), g.V - e0)) / S::kEPV;
-            const uint4* tp = reinterpret_cast<const uint4*>(rp.trow + e0 * ES);
-            const uint4* dp = rp.drow ? reinterpret_cast<const uint4*>(rp.drow + e0 * ES) : nullptr;
-            uint4 tv[S::kVPL], dv[S::kVPL];
-#pragma unroll
-            for (int q = 0; q < S::kVPL; ++q) {
-                const int vi = lane + 32 * q;
-                tv[q] = vi < nvec ? __ldg(tp + vi) : make_uint4(0, 0, 0, 0);
-                dv[q] = (dp != nullptr && vi < nvec) ? __ldg(dp + vi) : make_uint4(0, 0, 0, 0);
-            }
+    };
+    if (i0 < i1) {
+        slice_job<ES>(cur, a, nb, nsl, cached_b, cache);
+        if (lane == 0) issue_slice(cur, stage0, &bars[warp][0]);
+        advance();
+    }
+    int64_t i = i0;
+    for (; i < i1; ++i) {
+        const int s = static_cast<int>((i - i0) & 1);
+        uint8_t* buf = s ? stage1 : stage0;
+        if (i + 1 < i1) {
+            slice_job<ES>(next, a, nb, nsl, cached_b, cache);
+            if (lane == 0) issue_slice(next, s ? stage0 : stage1, &bars[warp][s ^ 1]);
+            advance();
+        }
+        const bool ok = mbar_wait_bounded(&bars[warp][s], (phases >> s) & 1u, nullptr);
+        phases ^= 1u << s;
+        if (!__all_sync(0xFFFFFFFFu, ok)) {
+            failed = true;
+            break;
+        }
+        if (cur.seq_ok) {
             float a0 = 0.f, a1 = 0.f;
 #pragma unroll
             for (int q = 0; q < S::kVPL; ++q) {
-                if (lane + 32 * q >= nvec) continue;
+                const int vi = lane + 32 * q;
+                if (vi >= cur.nvec) continue;
                 float xt[S::kEPV], xd[S::kEPV];
-                Direct<ES>::unpack(tv[q], xt);
-                Direct<ES>::unpack(dv[q], xd);
+                Direct<ES>::unpack(ld_shared_v4(buf + 16 * vi), xt);
+                if (cur.rp.drow)
+                    Direct<ES>::unpack(ld_shared_v4(buf + kSliceBytes + 16 * vi), xd);
+                else
+#pragma unroll
+                    for (int e = 0; e < S::kEPV; ++e) xd[e] = 0.f;
 #pragma unroll
                 for (int e = 0; e < S::kEPV; e += 2) {
-                    a0 += weight_of(rp, xt[e], xd[e]);
-                    a1 += weight_of(rp, xt[e + 1], xd[e + 1]);
+                    a0 += weight_of(cur.rp, xt[e], xd[e]);
+                    a1 += weight_of(cur.rp, xt[e + 1], xd[e + 1]);
                 }
             }
-            hi = two_sum(a0, a1, &lo);
+            float lo;
+            float hi = two_sum(a0, a1, &lo);
             warp_sum2(hi, lo);
+            if (lane == 0) a.slice_sums[i] = make_float2(hi, lo);
         }
-        if (lane == 0) a.slice_sums[i] = make_float2(hi, lo);
+        __syncwarp();  // the stage is read out before it is refilled
+        cur = next;
+    }
+    if (failed) {
+        // Mark the rest of this warp's slices, then let the copy already
+        // issued into the other stage land before the CTA exits.
+        const float nan = __uint_as_float(0x7FC00000u);
+        for (int64_t k = i + lane; k < i1; k += 32) a.slice_sums[k] = make_float2(nan, nan);
+        const int s = static_cast<int>((i - i0) & 1);
+        mbar_wait_bounded(&bars[warp][s], ((phases >> s) & 1u) ^ 1u, nullptr);
+        if (i + 1 < i1) {
+            const int o = s ^ 1;
+            mbar_wait_bounded(&bars[warp][o], (phases >> o) & 1u, nullptr);
+        }
     }
     pdl_trigger();  // the finish kernel may start launching
 }
 
 // ---------------------------------------------------------------------------
-// Aligned rows, launch 2 of 2: one CTA per sequence runs the two levels.
+// Aligned rows, launch 2 of 2: kFinishSplit CTAs per sequence. Each adds the
+// slice sums into block sums and runs level 1 (the same computation, so the
+// same winning block, in every CTA of the sequence), then races its quarter
+// of the winning block. The last of them to finish (an atomic ticket; no one
+// waits) keeps the best of the quarters, the lowest index on a tie.
 // ---------------------------------------------------------------------------
 template <int ES>
 __global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
 {
     using S = Slices<ES>;
+    constexpr int kQuarter = kRaceBlock / kFinishSplit;
+    using DB = Direct<ES, kT, kRaceBlock>;  // whole blocks (zero-residual fall-back)
+    using DQ = Direct<ES, kT, kQuarter>;    // one quarter of the winning block
     __shared__ Best red[kWarps];
     __shared__ float2 red2[kWarps];
     __shared__ int red_flags[kWarps];
+    __shared__ int s_last;
     const Geometry& g = a.g;
-    const int64_t b = blockIdx.x;
+    const int64_t b = blockIdx.x / kFinishSplit;
+    const int part = static_cast<int>(blockIdx.x - b * kFinishSplit);
     pdl_wait();  // the slice sums are complete and visible
     const SeqRecord rec = a.seqs[b];
     if (rec.status != 0) return;
     RowPair rp;
     row_pair_of(rp, a, rec, b, ES);
     const int64_t nch = g.nchunks, V = g.V, K1 = g.K + 1;
-    ChunkSum* sums = a.chunk_sums + b * nch;
+    ChunkSum* sums = a.chunk_sums + (b * kFinishSplit + part) * nch;  // this CTA's own copy
     auto block_len = [&](int64_t blk) {
         return static_cast<int>(min(static_cast<int64_t>(kRaceBlock), V - blk * kRaceBlock));
     };
@@ -677,19 +782,20 @@ __global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
         ChunkSum cs;
         cs.hi = hi;
         cs.lo = lo;
-        cs.flags = 0;
+        cs.flags = (hi == hi) ? 0 : kFlagTimeout;  // NaN: a streaming wait gave up
         cs.pad = 0;
         sums[c] = cs;
     }
     __syncthreads();
 
     int flags = 0;
-    int win = race_blocks(sums, nch, rp, &flags, red, red_flags);
-    if (win == INT_MAX) {
+    int win = race_blocks<kT>(sums, nch, rp, &flags, red, red_flags);
+    if (flags != 0) win = INT_MAX;
+    if (flags == 0 && win == INT_MAX) {
         // Every residual weight rounded to zero: race p_j instead, block sums first.
         rp.drow = nullptr;
         for (int64_t c = 0; c < nch; ++c) {
-            const float2 Wp = Direct<ES>::block_weight(rp, c * kRaceBlock, block_len(c), red2);
+            const float2 Wp = DB::block_weight(rp, c * kRaceBlock, block_len(c), red2);
             if (threadIdx.x == 0) {
                 ChunkSum cs;
                 cs.hi = Wp.x;
@@ -700,30 +806,59 @@ __global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
             }
             __syncthreads();
         }
-        win = race_blocks(sums, nch, rp, &flags, red, red_flags);
+        win = race_blocks<kT>(sums, nch, rp, &flags, red, red_flags);
     }
     Best tok{0.0f, INT_MAX};
-    if (win != INT_MAX)
-        tok = Direct<ES>::race(rp, static_cast<int64_t>(win) * kRaceBlock, block_len(win), red);
+    if (flags == 0 && win != INT_MAX) {
+        const int64_t q0 = static_cast<int64_t>(win) * kRaceBlock + part * kQuarter;
+        const int nq = static_cast<int>(
+            min(static_cast<int64_t>(kQuarter), static_cast<int64_t>(win) * kRaceBlock +
+                                                    block_len(win) - q0));
+        if (nq > 0) tok = DQ::race(rp, q0, nq, red);
+    }
+
     if (threadIdx.x == 0) {
-        if (tok.idx == INT_MAX) {
-            for (int64_t i = 0; i < K1; ++i) a.out_tokens[b * K1 + i] = -1;
-            a.num_accepted[b] = -1;
-            if (a.seq_status) a.seq_status[b] = kFlagTimeout;
-        } else {
-            a.out_tokens[b * K1 + rec.j] = tok.idx;
-        }
+        FinishPart fp;
+        fp.score = tok.score;
+        fp.idx = tok.idx;
+        fp.flags = flags;
+        fp.pad = win == INT_MAX ? 1 : 0;  // level 1 found nothing
+        a.parts[b * kFinishSplit + part] = fp;
+        __threadfence();
+        s_last = atomicAdd(&a.tickets[b], 1u) == static_cast<uint32_t>(kFinishSplit - 1);
+    }
+    __syncthreads();
+    if (!s_last || threadIdx.x != 0) return;
+    __threadfence();
+    const volatile FinishPart* parts = a.parts + b * kFinishSplit;
+    Best best{0.0f, INT_MAX};
+    int any_flags = 0, none = 0;
+    for (int q = 0; q < kFinishSplit; ++q) {
+        take(best, parts[q].score, parts[q].idx);
+        any_flags |= parts[q].flags;
+        none |= parts[q].pad;
+    }
+    if (any_flags != 0 || none != 0 || best.idx == INT_MAX) {
+        for (int64_t i = 0; i < K1; ++i) a.out_tokens[b * K1 + i] = -1;
+        a.num_accepted[b] = -1;
+        if (a.seq_status) a.seq_status[b] = kFlagTimeout;
+    } else {
+        a.out_tokens[b * K1 + rec.j] = best.idx;
     }
 }
 
 template <int ES>
 cudaError_t launch_direct(const SampleArgs& a, cudaStream_t s)
 {
-    cudaError_t e = launch_dependent(sample_stream_kernel<ES>, dim3(a.g.sample_grid), dim3(kT), 0,
-                                     s, a);
+    const int smem = kWarps * 4 * kSliceBytes;
+    cudaError_t e = cudaFuncSetAttribute(sample_stream_kernel<ES>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return launch_dependent(sample_finish_kernel<ES>, dim3(static_cast<unsigned>(a.g.B)), dim3(kT),
-                            0, s, a);
+    e = launch_dependent(a.g.pdl != 0, sample_stream_kernel<ES>, dim3(a.g.sample_grid), dim3(kT),
+                         static_cast<size_t>(smem), s, a);
+    if (e != cudaSuccess) return e;
+    return launch_dependent(a.g.pdl != 0, sample_finish_kernel<ES>,
+                            dim3(static_cast<unsigned>(a.g.B * kFinishSplit)), dim3(kT), 0, s, a);
 }
 
 }  // namespace
@@ -738,8 +873,12 @@ int sample_slices_per_block(int es) { return es == 2 ? Slices<2>::kPerBlock : Sl
 
 cudaError_t sample_stream_blocks_per_sm(int es, int* blocks)
 {
-    return es == 2 ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, sample_stream_kernel<2>, kT, 0)
-                   : cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, sample_stream_kernel<4>, kT, 0);
+    const int smem = kWarps * 4 * kSliceBytes;
+    auto* k = es == 2 ? sample_stream_kernel<2> : sample_stream_kernel<4>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k, kT, smem);
 }
 
 }  // namespace sv

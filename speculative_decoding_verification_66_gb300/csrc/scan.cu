@@ -29,7 +29,7 @@
 namespace sv {
 namespace {
 
-constexpr int kScanThreads = 256;
+constexpr int kScanMaxThreads = 1024;  // a warp per row, up to 32 rows per round
 constexpr double kLn2 = 0.69314718055994530942;
 
 __device__ __forceinline__ int cta_of_tile(int64_t t, const Geometry& g)
@@ -114,9 +114,11 @@ __device__ __forceinline__ float load_logit(const uint8_t* p)
 }
 
 template <int ES>
-__global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
+__global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs a)
 {
-    extern __shared__ RowNorm sh[];  // [2K+1]: normalisers (sampling) or argmaxes (greedy, in .m)
+    // Dynamic shared memory: [2K+1] row normalisers (sampling) or argmaxes
+    // (greedy, in .m), then the K draft tokens and their target / draft logits.
+    extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_status;
     __shared__ int s_j;
     const Geometry& g = a.g;
@@ -124,9 +126,27 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
     const int64_t K = g.K, V = g.V;
     const bool sampling = g.mode == 0;
     const int64_t nrows = sampling ? 2 * K + 1 : K + 1;
+    RowNorm* sh = reinterpret_cast<RowNorm*>(smem_raw);
+    int32_t* sx = reinterpret_cast<int32_t*>(sh + (2 * K + 1));
+    float* stx = reinterpret_cast<float*>(sx + K);
+    float* sdx = stx + K;
     if (threadIdx.x == 0) {
         s_status = 0;
         s_j = static_cast<int>(K);
+    }
+    __syncthreads();
+
+    // Inputs only (complete before pass 1 started): the draft tokens and the
+    // logits they select. This overlaps the tail of pass 1.
+    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+        const int32_t x = a.tokens[b * K + i];
+        sx[i] = x;
+        if (x < 0 || static_cast<int64_t>(x) >= V) {
+            atomicOr(&s_status, kFlagBadToken);
+        } else if (sampling) {
+            stx[i] = load_logit<ES>(a.target + ((b * (K + 1) + i) * V + x) * ES);
+            sdx[i] = load_logit<ES>(a.draft + ((b * K + i) * V + x) * ES);
+        }
     }
     pdl_trigger();  // the sampler's first kernel may start launching
     pdl_wait();     // pass 1 has finished and its partials are visible
@@ -144,24 +164,18 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
             if (fl) atomicOr(&s_status, fl);
         }
     }
-    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
-        const int32_t x = a.tokens[b * K + i];
-        if (x < 0 || static_cast<int64_t>(x) >= V) atomicOr(&s_status, kFlagBadToken);
-    }
     __syncthreads();
 
     if (s_status == 0) {
         for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
-            const int32_t x = a.tokens[b * K + i];
+            const int32_t x = sx[i];
             bool reject;
             if (sampling) {
-                const float tx = load_logit<ES>(a.target + ((b * (K + 1) + i) * V + x) * ES);
-                const float dx = load_logit<ES>(a.draft + ((b * K + i) * V + x) * ES);
                 const RowNorm nt = sh[i], nd = sh[K + 1 + i];
                 // log2 p_i(x) and log2 q_i(x): the fma is exact before its one
                 // rounding, and the normaliser's parts enter separately.
-                const float lp2 = fmaf(tx, a.c, -nt.m) - nt.l;
-                const float lq2 = fmaf(dx, a.c, -nd.m) - nd.l;
+                const float lp2 = fmaf(stx[i], a.c, -nt.m) - nt.l;
+                const float lq2 = fmaf(sdx[i], a.c, -nd.m) - nd.l;
                 const float lr2 = lp2 - lq2;
                 if (a.log_ratio) a.log_ratio[b * K + i] = static_cast<double>(lr2) * kLn2;
                 const float r = lr2 >= 0.f ? 1.f : ex2(lr2);
@@ -195,7 +209,7 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
     } else {
         for (int64_t i = threadIdx.x; i <= K; i += blockDim.x) {
             if (i < j)
-                out[i] = a.tokens[b * K + i];
+                out[i] = sx[i];
             else if (i > j)
                 out[i] = -1;
             else if (!sampling)
@@ -229,10 +243,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(const ScanArgs a)
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s)
 {
-    const size_t smem = 8 * static_cast<size_t>(2 * a.g.K + 1);
-    const dim3 grid(static_cast<unsigned>(a.g.B)), block(kScanThreads);
-    return a.g.es == 2 ? launch_dependent(scan_kernel<2>, grid, block, smem, s, a)
-                       : launch_dependent(scan_kernel<4>, grid, block, smem, s, a);
+    const size_t smem = sizeof(RowNorm) * static_cast<size_t>(2 * a.g.K + 1) + 12 * static_cast<size_t>(a.g.K);
+    const int64_t rows = a.g.mode == 0 ? 2 * a.g.K + 1 : a.g.K + 1;
+    const int warps = static_cast<int>(rows < 2 ? 2 : (rows > 32 ? 32 : rows));
+    const dim3 grid(static_cast<unsigned>(a.g.B)), block(32 * warps);
+    return a.g.es == 2 ? launch_dependent(a.g.pdl != 0, scan_kernel<2>, grid, block, smem, s, a)
+                       : launch_dependent(a.g.pdl != 0, scan_kernel<4>, grid, block, smem, s, a);
 }
 
 }  // namespace sv

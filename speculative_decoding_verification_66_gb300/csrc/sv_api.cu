@@ -54,7 +54,8 @@ int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
 }
 
 struct Layout {
-    size_t partials = 0, seqs = 0, chunk_sums = 0, slice_sums = 0, tickets = 0, total = 0;
+    size_t partials = 0, seqs = 0, chunk_sums = 0, slice_sums = 0, parts = 0, tickets = 0,
+           total = 0;
 };
 
 int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
@@ -112,7 +113,11 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     L->seqs = off;
     off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
     L->chunk_sums = off;
-    if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nchunks) * sizeof(sv::ChunkSum));
+    if (mode == SV_SAMPLE)
+        off += round_up(static_cast<size_t>(B * g->nchunks) * sv::kFinishSplit * sizeof(sv::ChunkSum));
+    L->parts = off;
+    if (mode == SV_SAMPLE)
+        off += round_up(static_cast<size_t>(B) * sv::kFinishSplit * sizeof(sv::FinishPart));
     L->slice_sums = off;
     if (mode == SV_SAMPLE && g->aligned) off += round_up(static_cast<size_t>(slices) * sizeof(float2));
     L->tickets = off;
@@ -167,6 +172,9 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     rc = make_plan(B, K, V, dtype, mode, &g, &L);
     if (rc != SV_OK) return rc;
     if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+    // Events between the kernels would sit between programmatically chained
+    // launches; the timed variant launches them one after the other instead.
+    g.pdl = events == nullptr ? 1 : 0;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
 
     const uint8_t* tp = static_cast<const uint8_t*>(target);
@@ -175,14 +183,15 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     auto* seqs = reinterpret_cast<sv::SeqRecord*>(ws + L.seqs);
     auto* chunk_sums = reinterpret_cast<sv::ChunkSum*>(ws + L.chunk_sums);
     auto* slice_sums = reinterpret_cast<float2*>(ws + L.slice_sums);
+    auto* parts = reinterpret_cast<sv::FinishPart*>(ws + L.parts);
     auto* tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
 
     sv::RowStatsArgs ra{tp, dp, g, c, partials};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     tickets, sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
                     sampling ? log_ratio : nullptr, seq_status};
-    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, chunk_sums, slice_sums, tickets, out_tokens,
-                      num_accepted, seq_status};
+    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, chunk_sums, parts, slice_sums, tickets,
+                      out_tokens, num_accepted, seq_status};
 
     if (!record(0)) return SV_ERR_CUDA;
     if (sv::launch_row_stats(ra, s) != cudaSuccess) return SV_ERR_CUDA;

@@ -28,8 +28,10 @@ constexpr int kRowThreads = (kRowConsumerWarps + 1) * 32;
 constexpr int kRaceBlock = 8192;
 constexpr int kSampleThreads = 256;
 // Aligned rows: the sampler's streaming pass sums the weights of slices of
-// kSliceBytes per row, one warp per slice.
+// kSliceBytes per row, one warp per slice. Its finish pass splits the race of
+// the winning block over kFinishSplit CTAs per sequence.
 constexpr int kSliceBytes = 2048;
+constexpr int kFinishSplit = 4;
 
 constexpr int kMaxK = 1024;
 
@@ -76,6 +78,16 @@ struct ChunkSum {
 };
 static_assert(sizeof(ChunkSum) == 16, "ChunkSum layout");
 
+// One finish CTA's best token in its share of the winning block
+// (score 0 / idx 2^31 - 1: none; flags: kFlagTimeout).
+struct FinishPart {
+    float score;
+    int32_t idx;
+    int32_t flags;
+    int32_t pad;
+};
+static_assert(sizeof(FinishPart) == 16, "FinishPart layout");
+
 struct Geometry {
     int64_t B, K, V;
     int32_t es;             // bytes per element (4 or 2)
@@ -90,6 +102,7 @@ struct Geometry {
     int32_t aligned;        // every row starts on a 16-byte boundary
     int64_t nchunks;        // race blocks per row
     int32_t sample_grid;    // CTAs of the sampler's streaming pass (aligned rows)
+    int32_t pdl;            // chain the kernels with programmatic dependent launch
 };
 
 struct RowStatsArgs {
@@ -125,7 +138,8 @@ struct SampleArgs {
     float c;
     uint64_t seed;
     const SeqRecord* seqs;
-    ChunkSum* chunk_sums;   // [B][nchunks]
+    ChunkSum* chunk_sums;   // [B][kFinishSplit][nchunks] (the staged path uses [B][nchunks])
+    FinishPart* parts;      // [B][kFinishSplit]
     float2* slice_sums;     // [B][nchunks][slices per block] (aligned rows)
     uint32_t* tickets;      // [B], zeroed by the scan
     int32_t* out_tokens;
@@ -135,9 +149,10 @@ struct SampleArgs {
 
 // Launch with programmatic stream serialization (the kernel must call
 // pdl_wait() before it reads what the previous kernel in the stream wrote).
+// With pdl == false it is an ordinary launch (the wait then returns at once).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                             cudaStream_t s, Args&&... args)
+cudaError_t launch_dependent(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                             size_t smem, cudaStream_t s, Args&&... args)
 {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
@@ -148,7 +163,7 @@ cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
