@@ -98,6 +98,16 @@ struct Span {
     int64_t idx0;        // row index of vector 0's first element
 };
 
+// What consumers need to know about the tile in a stage. The producer, which
+// computes the span anyway, writes it next to the data before its arrive.
+struct TileRec {
+    int32_t seg;      // row - first row of the CTA
+    int32_t nv;       // vectors in the buffer
+    int32_t head;     // elements of vector 0 before the tile
+    int32_t last;     // valid elements of vector nv - 1
+    long long idx0;   // row index of vector 0's first element
+};
+
 template <int ES>
 __device__ __forceinline__ Span tile_span(const Cursor& c, const Geometry& g)
 {
@@ -154,7 +164,7 @@ __device__ __forceinline__ void mask_vector(uint4& v, int lo, int hi)
 }
 
 template <int ES>
-__device__ __forceinline__ void load_tile(uint4 (&v)[kVPT], const uint8_t* buf, const Span& sp,
+__device__ __forceinline__ void load_tile(uint4 (&v)[kVPT], const uint8_t* buf, const TileRec& sp,
                                           int tid, bool aligned)
 {
     const uint32_t fill = ES == 2 ? kBf16NegInfPair : kF32NegInfBits;
@@ -266,8 +276,8 @@ __device__ __forceinline__ void accumulate_tile(SampleState& st, const uint4 (&v
 }
 
 template <int ES>
-__device__ __forceinline__ void argmax_tile(GreedyState& st, const uint4 (&v)[kVPT], const Span& sp,
-                                            int tid)
+__device__ __forceinline__ void argmax_tile(GreedyState& st, const uint4 (&v)[kVPT],
+                                            const TileRec& sp, int tid)
 {
     const float tmax = tile_max<ES>(v);
     if (tmax != tmax) {
@@ -349,6 +359,7 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t full_bar[kRowStages];
     __shared__ __align__(8) uint64_t empty_bar[kRowStages];
+    __shared__ __align__(8) TileRec recs[kRowStages];
     __shared__ int abort_flag;
 
     const Geometry& g = a.g;
@@ -391,6 +402,13 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
             }
             const Span sp = tile_span<ES>(cur, g);
             uint8_t* dst = ring + static_cast<size_t>(stage) * kRowTileBytes;
+            TileRec rec;
+            rec.seg = static_cast<int32_t>(cur.row - row_first);
+            rec.nv = sp.nv;
+            rec.head = sp.head;
+            rec.last = sp.last;
+            rec.idx0 = sp.idx0;
+            recs[stage] = rec;  // published by the arrive below (release)
             // Bytes the bulk copy cannot take (the last <16 bytes of a tensor
             // whose size is not a multiple of 16) go through plain loads.
             for (const uint8_t* p = sp.tail; p < sp.e; p += ES) {
@@ -427,11 +445,18 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
     GreedyState gs;
     ss.reset();
     gs.reset();
-    int64_t row = cur.row;
+    int seg = 0;  // the row segment being reduced (row - row_first)
     int64_t n = 0;
+    int stage = 0;
+    uint32_t parity = 0;
     for (; n < ntiles; ++n) {
-        if (cur.row != row) {
-            Partial* out = my_partials + (row - row_first) * kRowConsumerWarps;
+        if (!mbar_wait_bounded(&full_bar[stage], parity, &abort_flag)) {
+            abort_flag = 1;
+            break;
+        }
+        const TileRec sp = recs[stage];
+        if (sp.seg != seg) {
+            Partial* out = my_partials + static_cast<int64_t>(seg) * kRowConsumerWarps;
             if (MODE == kSampleMode) {
                 flush_sample(ss, out, lane);
                 ss.reset();
@@ -439,15 +464,8 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
                 flush_greedy(gs, out, lane);
                 gs.reset();
             }
-            row = cur.row;
+            seg = sp.seg;
         }
-        const int stage = static_cast<int>(n % kRowStages);
-        if (!mbar_wait_bounded(&full_bar[stage], static_cast<uint32_t>((n / kRowStages) & 1),
-                               &abort_flag)) {
-            abort_flag = 1;
-            break;
-        }
-        const Span sp = tile_span<ES>(cur, g);
         uint4 v[kVPT];
         load_tile<ES>(v, ring + static_cast<size_t>(stage) * kRowTileBytes, sp, tid, aligned);
         __syncwarp();
@@ -456,19 +474,22 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
             accumulate_tile<ES>(ss, v, a.c);
         else
             argmax_tile<ES>(gs, v, sp, tid);
-        cursor_next<ES>(cur, a);
+        if (++stage == kRowStages) {
+            stage = 0;
+            parity ^= 1u;
+        }
     }
     // The scan may start launching now; it waits for this grid to finish.
     if (tid == 0) pdl_trigger();
     if (n == ntiles) {
-        Partial* out = my_partials + (row - row_first) * kRowConsumerWarps;
+        Partial* out = my_partials + static_cast<int64_t>(seg) * kRowConsumerWarps;
         if (MODE == kSampleMode)
             flush_sample(ss, out, lane);
         else
             flush_greedy(gs, out, lane);
     } else if (lane == 0) {
         // Timed out: mark this warp's remaining segments so the scan rejects them.
-        for (int64_t r = row; r <= row_last; ++r) {
+        for (int64_t r = row_first + seg; r <= row_last; ++r) {
             Partial p;
             p.m = __uint_as_float(kF32NegInfBits);
             p.hi = 0.f;

@@ -188,22 +188,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
     return ok != 0;
 }
 
-// As mbar_try_wait, but a thread whose phase is not complete is suspended in
-// hardware until it completes or `ns` nanoseconds pass, instead of returning
-// at once: waiting warps stop competing for issue slots.
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
 // Upper bound on any wait inside the kernels, in SM clock cycles (about two
 // seconds at 2 GHz). A wait that runs out returns false; the caller records a
 // timeout status and winds down instead of spinning forever.
@@ -216,10 +200,13 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
 {
     if (mbar_try_wait(bar, parity)) return true;
     const long long t0 = clock64();
+    unsigned backoff = 32;
     for (;;) {
-        // Sleep up to 100 us per try: the abort flag and the overall limit
-        // are still checked regularly.
-        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        // Back off between tries (32 ns doubling to 256 ns) so that waiting
+        // warps leave the issue slots to the warps that have work.
+        __nanosleep(backoff);
+        if (backoff < 256) backoff <<= 1;
+        if (mbar_try_wait(bar, parity)) return true;
         if (abort != nullptr && *abort != 0) return false;
         if (clock64() - t0 > kWaitLimitCycles) return false;
     }
