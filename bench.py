@@ -52,6 +52,8 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="wall-clock budget of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-threads", type=int, default=0,
+                   help="threads for the CPU baseline (0: every core this process may use)")
     return p.parse_args()
 
 
@@ -133,12 +135,14 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(rows)}
 
 
-def cpu_baseline(wl, host_fn, budget_s: float):
+def cpu_baseline(wl, host_fn, budget_s: float, threads: int = 0):
     """Time the oracle (as it stands) on this host's cores on a bounded sample of
     the workload: the batch's sequences split over threads, repeated until about
     `budget_s` seconds of wall time have passed."""
     import oracle
     cores = len(os.sched_getaffinity(0))
+    if threads > 0:
+        cores = min(cores, threads)
     mode = 0 if wl.mode == "sample" else 1
     t, d, x = host_fn(wl.B)
     reps, t0 = 0, time.perf_counter()
@@ -371,7 +375,7 @@ def main():
         def host_fn(n):
             sub = {k: (v[:n] if v is not None else None) for k, v in copies[0].items()}
             return to_host_arrays(sub)
-        line["cpu_baseline"] = cpu_baseline(wl, host_fn, args.cpu_seconds)
+        line["cpu_baseline"] = cpu_baseline(wl, host_fn, args.cpu_seconds, args.cpu_threads)
     print(json.dumps(line), flush=True)
     if dist:
         dist.barrier()

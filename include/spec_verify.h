@@ -30,19 +30,25 @@
  *                              -1 when the sequence's inputs are invalid.
  *
  * Numbers and reproducibility:
- *   p = softmax(target_logits / T), q = softmax(draft_logits / T), accumulated
- *   in float32 (rescaled partial sums, double where partials are merged).
- *   The acceptance uniform of position i of sequence b is lane 0 of
- *   Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter (i, b, 0, 0),
- *   mapped to (word >> 8) * 2^-24; position i is kept iff that uniform is
- *   below min(1, p_i(x_i) / q_i(x_i)). The token at the emitted position j is
- *   drawn from the weights w (max(0, p_j - q_j) after a rejection, p_K for the
- *   bonus) by an exponential race: the argmax over w_k > 0 of w_k / E_k,
- *   E_k = -ln v_k, v_k lane (k mod 4) of counter (j, b, 1 + k div 4, 0) mapped
- *   to (2 (word >> 9) + 1) * 2^-24; the lowest index wins an exact tie. The
- *   race picks token k with probability w_k / sum(w). Results are a pure
- *   function of (inputs, T, seed, mode) on a given GPU model: no float
- *   atomics, fixed reduction trees, the same answer on every run.
+ *   p = softmax(target_logits / T), q = softmax(draft_logits / T). Sums of
+ *   2^(x log2(e) / T) are carried on the device as float pairs (hi + lo)
+ *   scaled by integer powers of two; the device path uses no double precision
+ *   except to write the optional diagnostic outputs. The acceptance uniform of
+ *   position i of sequence b is lane 0 of Philox4x32-10 with key
+ *   (lo32(seed), hi32(seed)) and counter (i, b, 0, 0), mapped to
+ *   (word >> 8) * 2^-24; position i is kept iff that uniform is below
+ *   min(1, p_i(x_i) / q_i(x_i)). The token at the emitted position j is drawn
+ *   from the weights w (max(0, p_j - q_j) after a rejection, p_K for the
+ *   bonus) by a two-level exponential race over blocks of 8192 tokens. Level 1
+ *   takes the block c with the largest W_c / E_c over blocks with weight
+ *   W_c = sum of w over the block > 0, E_c = -ln v_c, v_c lane (c mod 4) of
+ *   counter (j, b, 1 + c div 4, 1). Level 2 takes the token k of that block
+ *   with the largest w_k / E_k over w_k > 0, v_k lane (k mod 4) of counter
+ *   (j, b, 1 + k div 4, 0). Both levels map a word to (2 (word >> 9) + 1) 2^-24
+ *   and let the lowest index win an exact tie. The race picks token k with
+ *   probability w_k / sum(w). Results are a pure function of (inputs, T, seed,
+ *   mode) on a given GPU model: no float atomics, fixed reduction trees, the
+ *   same answer on every run.
  *
  * Memory and streams:
  *   Every pointer passed to spec_verify / spec_verify_debug / spec_verify_timed
@@ -211,6 +217,25 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
                        float temperature, uint64_t seed, int mode, int32_t* out_tokens,
                        int32_t* num_accepted, void* stream);
+
+/*
+ * The Philox4x32-10 generator the verification kernels draw from, evaluated on
+ * the device for caller-chosen counters. The pages have no counterpart to this
+ * entry point: it exists so that the device generator can be checked word for
+ * word against an independent implementation of the published definition
+ * (Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3",
+ * SC'11: ten rounds of the 4x32 Philox bijection under the key schedule).
+ *   seed      the key, (lo32(seed), hi32(seed)), as in spec_verify.
+ *   counters  device, [n][4] uint32, 16-byte aligned: counter words x0..x3.
+ *   out       device, [n][4] uint32, 16-byte aligned: the four output words
+ *             of each counter, written.
+ *   n         number of counters, 0 <= n < 2^40; n == 0 enqueues nothing.
+ *   stream    cudaStream_t to enqueue on.
+ * Stream-ordered; allocates nothing. Returns SV_OK, SV_ERR_ARG (n < 0, or a
+ * NULL pointer with n > 0), SV_ERR_SIZE (n too large), SV_ERR_ALIGN or
+ * SV_ERR_CUDA.
+ */
+int sv_philox(uint64_t seed, const uint32_t* counters, uint32_t* out, int64_t n, void* stream);
 
 /* Static description of an SV_* return code. Never NULL. */
 const char* sv_error_string(int code);

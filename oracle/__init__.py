@@ -70,7 +70,9 @@ def lib() -> ctypes.CDLL:
             vp, i64, i32, dbl, u64 = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
                                       ctypes.c_double, ctypes.c_uint64)
             L.svo_philox4x32_10.argtypes = [vp, vp, vp]
+            L.svo_philox_many.argtypes = [vp, i64, vp, vp]
             L.svo_philox4x32_10.restype = None
+            L.svo_philox_many.restype = None
             L.svo_uniform.argtypes = [u64, ctypes.c_uint32, ctypes.c_uint32, i32]
             L.svo_uniform.restype = dbl
             L.svo_elem.argtypes = [vp, i64, i32]
@@ -115,6 +117,15 @@ def philox(ctr, key) -> np.ndarray:
     k = np.ascontiguousarray(key, dtype=np.uint32)
     out = np.zeros(4, dtype=np.uint32)
     lib().svo_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def philox_many(ctr, key) -> np.ndarray:
+    """Philox4x32-10 of each row of an [n, 4] counter array."""
+    c = np.ascontiguousarray(ctr, dtype=np.uint32).reshape(-1, 4)
+    k = np.ascontiguousarray(key, dtype=np.uint32)
+    out = np.zeros_like(c)
+    lib().svo_philox_many(_ptr(c), c.shape[0], _ptr(k), _ptr(out))
     return out
 
 

@@ -96,6 +96,12 @@ void svo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t ou
     out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
 }
 
+void svo_philox_many(const uint32_t* ctr, int64_t n, const uint32_t key[2], uint32_t* out)
+{
+    int64_t i;
+    for (i = 0; i < n; ++i) svo_philox4x32_10(ctr + 4 * i, key, out + 4 * i);
+}
+
 double svo_uniform(uint64_t seed, uint32_t seq, uint32_t pos, int lane)
 {
     uint32_t ctr[4], key[2], r[4];

@@ -32,6 +32,9 @@ enum { SVO_BAD_TOKEN = 1, SVO_NONFINITE = 2 };
 /* Philox4x32 with 10 rounds, one block: out = Philox(ctr, key). */
 void svo_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 
+/* svo_philox4x32_10 for n counters: ctr and out are [n][4]. */
+void svo_philox_many(const uint32_t* ctr, int64_t n, const uint32_t key[2], uint32_t* out);
+
 /* Uniform in [0, 1 - 2^-24] from lane `lane` (0..3) of Philox4x32-10 with
  * key = (lo32(seed), hi32(seed)) and counter = (pos, seq, 0, 0). */
 double svo_uniform(uint64_t seed, uint32_t seq, uint32_t pos, int lane);

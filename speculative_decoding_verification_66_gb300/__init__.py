@@ -23,6 +23,7 @@ from .api import (  # noqa: F401
     spec_verify_static,
     spec_verify_timed,
     sv_host_staging_bytes,
+    sv_philox,
     sv_workspace_bytes,
     version,
 )

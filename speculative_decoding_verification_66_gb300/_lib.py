@@ -23,6 +23,7 @@ SIGNATURES = {
                                 _vp, _vp, _sz, _vp]),
     "spec_verify_static": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _f32, _u64, _i32, _vp,
                                   _vp, _vp]),
+    "sv_philox": (_i32, [_u64, _vp, _vp, _i64, _vp]),
     "sv_error_string": (ctypes.c_char_p, [_i32]),
     "sv_version": (_i32, []),
 }

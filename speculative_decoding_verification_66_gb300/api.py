@@ -261,5 +261,24 @@ def spec_verify_static(target_logits, draft_logits, draft_tokens, temperature: f
     return out_tokens, num_accepted
 
 
+def sv_philox(seed: int, counters: torch.Tensor, out=None, stream=None) -> torch.Tensor:
+    """The device Philox4x32-10 words of each counter: counters is an [n, 4]
+    int32 CUDA tensor (the words' bit patterns), the result the same shape."""
+    if counters.dim() != 2 or counters.shape[1] != 4 or counters.dtype != torch.int32:
+        raise ValueError("counters must be an [n, 4] int32 tensor")
+    if not counters.is_cuda or not counters.is_contiguous():
+        raise ValueError("counters must be a contiguous CUDA tensor")
+    dev = counters.device
+    if out is None:
+        out = torch.empty_like(counters)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        _check(_lib.load().sv_philox(int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(counters), _ptr(out),
+                                     counters.shape[0], ctypes.c_void_p(stream.cuda_stream)),
+               "sv_philox")
+    return out
+
+
 def version() -> int:
     return int(_lib.load().sv_version())

@@ -358,4 +358,4 @@ SV_EXPORT const char* sv_error_string(int code)
     }
 }
 
-SV_EXPORT int sv_version(void) { return 100; }
+SV_EXPORT int sv_version(void) { return 101; }

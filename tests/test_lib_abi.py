@@ -34,7 +34,8 @@ def lib():
 def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "sv_workspace_bytes", "spec_verify", "spec_verify_debug", "spec_verify_timed",
-        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static", "sv_error_string",
+        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static", "sv_philox",
+        "sv_error_string",
         "sv_version"])
 
 
@@ -68,7 +69,7 @@ def test_error_strings_and_version(lib):
                  SV_ERR_SIZE, 12345):
         s = lib.sv_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
-    assert lib.sv_version() == 100
+    assert lib.sv_version() == 101
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails before any device work
@@ -145,6 +146,15 @@ def test_host_entry_validates_before_copying(lib):
     assert lib.sv_workspace_bytes(2, 3, 0, 1, 0, ctypes.byref(n)) == SV_ERR_ARG
     assert lib.spec_verify_host(FAKE, FAKE, FAKE, 2, 2000, 64, 1, 1.0, 7, 0, FAKE, FAKE, FAKE,
                                 1 << 20, None) == SV_ERR_SIZE
+
+
+def test_philox_entry_validates_on_the_host(lib):
+    """sv_philox checks its arguments before any CUDA call (no GPU needed)."""
+    assert lib.sv_philox(0, None, None, 0, None) == 0      # nothing to do
+    assert lib.sv_philox(0, None, None, -1, None) == -1    # SV_ERR_ARG
+    assert lib.sv_philox(0, None, None, 4, None) == -1     # NULL pointers
+    assert lib.sv_philox(0, 16, 32, 1 << 40, None) == -6   # SV_ERR_SIZE
+    assert lib.sv_philox(0, 16 + 4, 32, 1, None) == -3     # SV_ERR_ALIGN
 
 
 def test_binding_fails_loudly_without_the_library(monkeypatch, tmp_path):

@@ -560,3 +560,12 @@ def test_threads_do_not_change_results(oracle_mod):
     b = oracle_mod.verify(t, d, tok, 1.0, seed=4, threads=5)
     for k in a:
         np.testing.assert_array_equal(a[k], b[k])
+
+
+def test_philox_many_is_philox_per_counter(oracle_mod):
+    rng = np.random.default_rng(5)
+    ctr = rng.integers(0, 2**32, size=(257, 4), dtype=np.uint64).astype(np.uint32)
+    key = np.array([0x89ABCDEF, 0x01234567], dtype=np.uint32)
+    many = oracle_mod.philox_many(ctr, key)
+    for r in range(ctr.shape[0]):
+        assert np.array_equal(many[r], oracle_mod.philox(ctr[r], key))
