@@ -68,10 +68,10 @@ def _law_case(V, K, B, seed):
     p = np.empty((K + 1, V))
     q = np.empty((K, V))
     for i in range(K + 1):
-        lse = oracle.row_lse(t[i], 1.0)
+        _, lse = oracle.row_lse(t[i], 1.0)
         p[i] = [np.exp(oracle.log_prob(t[i], k, 1.0, lse)) for k in range(V)]
     for i in range(K):
-        lse = oracle.row_lse(d[i], 1.0)
+        _, lse = oracle.row_lse(d[i], 1.0)
         q[i] = [np.exp(oracle.log_prob(d[i], k, 1.0, lse)) for k in range(V)]
     x = np.stack([rng.choice(V, size=B, p=q[i] / q[i].sum()) for i in range(K)], 1).astype(np.int32)
     return t, d, x, p, q
