@@ -21,6 +21,7 @@ through spec_verify_host (host buffers, copies in the timed region).
 from __future__ import annotations
 
 import argparse
+import glob
 import hashlib
 import json
 import os
@@ -35,7 +36,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified seqs/s and logits HBM GB/s (fraction of GB300 peak) per B×(K+1)×V"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE = os.path.join(ROOT, "profiles", "row_stats_llama3_bf16.md")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["row_stats.cu", "sv_device.cuh", "sv_internal.h"]
 
 
@@ -73,17 +74,20 @@ def kernel_sha():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per pass-1 launch from the committed ncu summary, if it was
-    taken on the current kernel source."""
-    if not os.path.exists(PROFILE):
-        return None
-    text = open(PROFILE).read()
-    m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
-    m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
-    if not m_sha or not m_tr or m_sha.group(1) != kernel_sha():
-        return None
-    return float(m_tr.group(1))
+def profiled_traffic(wl):
+    """DRAM bytes per pass-1 launch for this workload, from a committed ncu
+    summary (profiles/row_stats_*.md) that names the workload and batch it was
+    scaled to and was taken on the current kernel source; None otherwise."""
+    want = f"{wl.name} B={wl.B}"
+    sha = kernel_sha()
+    for path in sorted(glob.glob(os.path.join(PROFILE_DIR, "row_stats_*.md"))):
+        text = open(path).read()
+        m_wl = re.search(r"traffic_workload:\s*(.+)", text)
+        m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+        if m_wl and m_sha and m_tr and m_wl.group(1).strip() == want and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    return None
 
 
 class ClockSampler:
@@ -143,6 +147,7 @@ def cpu_baseline(wl, host_fn, budget_s: float, threads: int = 0):
     cores = len(os.sched_getaffinity(0))
     if threads > 0:
         cores = min(cores, threads)
+    cores = max(1, min(cores, wl.B))  # the oracle splits by sequence
     mode = 0 if wl.mode == "sample" else 1
     t, d, x = host_fn(wl.B)
     reps, t0 = 0, time.perf_counter()
@@ -364,7 +369,7 @@ def main():
                      "steps_timed": n_staged},
         "mean_accepted": sum(accepted) / len(accepted),
         "roofline": {"kernel": "row_stats", "bound": "hbm", "achieved": pass1_gbs, "peak": peak,
-                     "unit": "GB/s", "frac": pass1_gbs / peak, "traffic": profiled_traffic(),
+                     "unit": "GB/s", "frac": pass1_gbs / peak, "traffic": profiled_traffic(wl),
                      "algorithmic_bytes": pass1_bytes, "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": job_throughput(world, B, e2e_steps, e2e_s), "unit": "seqs/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps},
