@@ -170,7 +170,7 @@ def race_uniform(seed: int, seq: int, pos: int, k: int) -> float:
     return lib().svo_race_uniform(seed, seq, pos, k)
 
 
-RACE_BLOCK = 8192
+RACE_BLOCK = 512  # SVO_RACE_BLOCK in sv_oracle.h
 
 
 def block_uniform(seed: int, seq: int, pos: int, c: int) -> float:

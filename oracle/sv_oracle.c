@@ -36,7 +36,7 @@
  *  - u_i = lane 0 of Philox(key = seed, counter = (i, b, 0, 0)), mapped to
  *    (32-bit word >> 8) * 2^-24, exact in float and double;
  *  - the pages draw the corrected token with a generic multinomial draw; it is
- *    read here as a two-level exponential race over blocks of 8192 tokens.
+ *    read here as a two-level exponential race over blocks of 512 tokens.
  *    Level 1 races the blocks: block c = argmax over blocks with W_c > 0 of
  *    W_c / E_c, W_c the sum of w over the block, E_c = -ln v_c, v_c lane c mod 4
  *    of counter (j, b, 1 + c div 4, 1). Level 2 races the tokens of the winning

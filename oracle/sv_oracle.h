@@ -57,8 +57,10 @@ double svo_accept_prob(double log_p, double log_q);
 void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
                         double T, double lse_t, double lse_d, double* w);
 
-/* Tokens per block of the two-level race. */
-#define SVO_RACE_BLOCK 8192
+/* Tokens per block of the two-level race. The pages fix only the law of the
+ * draw, which the race meets for any block length; this length is part of the
+ * reading (it decides which random numbers are drawn). */
+#define SVO_RACE_BLOCK 512
 
 /* Race uniform of token k at emitted position `pos` of sequence `seq`: lane
  * k mod 4 of Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter

@@ -264,7 +264,7 @@ def test_race_draws_proportional_to_weight(oracle_mod, V):
 
 
 def test_two_level_race_law(oracle_mod):
-    """Four blocks of the two-level race (V > 3 * 8192): the winning block
+    """Four blocks of the two-level race (V > 3 blocks): the winning block
     follows W_c / Z and the token within it w_k / W_c, so every token follows
     w_k / Z. Weights sit on a few tokens per block (including the first token
     of block 0 and the last token of the row) so that each race is cheap."""
@@ -301,20 +301,23 @@ def test_block_uniforms_are_their_own_stream(oracle_mod):
     assert abs(np.corrcoef(b, t)[0, 1]) < 0.1
 
 
-def test_race_near_tie_law(oracle_mod):
+@pytest.mark.parametrize("V, levels", [(500, 1), (2000, 2)])
+def test_race_near_tie_law(oracle_mod, V, levels):
     """Closed form: the relative gap between a race's two best scores is below
     tau with probability at most tau (memorylessness of the exponential clocks),
-    whatever the number of tokens; the two-level race has two such gaps, so at
+    whatever the number of tokens. A row of one block has one such gap (level 1
+    has a single candidate, margin 1); a row of several blocks has two, so at
     most 2 tau. This is what keeps near-ties rare at V = 128k."""
+    assert (V <= oracle_mod.RACE_BLOCK) == (levels == 1)
     rng = np.random.default_rng(1)
-    V = 2000
     w = rng.lognormal(sigma=2.0, size=V)
     n = 20_000
     margins = np.array([oracle_mod.race_sample(w, 77, b, 0)[1] for b in range(n)])
     tau = 0.02
     frac = np.mean(margins < tau)
-    sd = math.sqrt(tau * (1 - tau) / n)
-    assert frac < tau + 5 * sd
+    bound = levels * tau
+    sd = math.sqrt(bound * (1 - bound) / n)
+    assert frac < bound + 5 * sd
     assert frac > 0.3 * tau  # and it is not degenerate
     assert np.all((margins >= 0) & (margins <= 1))
 
