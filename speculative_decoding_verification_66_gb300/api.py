@@ -19,14 +19,9 @@ SV_SAMPLE, SV_GREEDY = 0, 1
 SV_SEQ_BAD_TOKEN, SV_SEQ_NONFINITE, SV_SEQ_TIMEOUT = 1, 2, 4
 
 def launches(mode, V: int, dtype) -> int:
-    """Kernel launches one spec_verify call makes: row statistics and the scan;
-    in sampling mode also the sampler (two launches when rows are 16-byte
-    aligned: streaming and finish)."""
-    m = mode_code(mode)
-    if m == SV_GREEDY:
-        return 2
-    es = 2 if (dtype == torch.bfloat16 or dtype == SV_BF16) else 4
-    return 4 if (V * es) % 16 == 0 else 3
+    """Kernel launches one spec_verify call makes: row statistics and the scan,
+    and in sampling mode the sampler. V and dtype do not change the count."""
+    return 2 if mode_code(mode) == SV_GREEDY else 4
 
 
 class SpecVerifyError(RuntimeError):

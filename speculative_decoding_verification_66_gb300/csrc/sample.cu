@@ -8,32 +8,34 @@
 //    max(0, p_j - q_j) / Z.
 //  * Hung-yi Lee, lecture 16 notes, §4 item 4 "The Bonus Token": when all K
 //    drafts pass, the token is drawn from the target row K.
-// The draw is a two-level exponential race over blocks of kRaceBlock tokens.
-// Level 1 picks the block with the largest W_c / E_c, where W_c is the sum of
-// the weights w over block c and E_c = -ln v_c, with v_c lane c mod 4 of Philox
-// counter (j, b, 1 + c div 4, 1). Level 2 picks the token of that block with the
-// largest w_k / E_k, with v_k lane k mod 4 of counter (j, b, 1 + k div 4, 0).
-// Uniforms are (2 (word >> 9) + 1) 2^-24, and the lowest index wins an exact
-// tie. Block c wins with probability W_c / Z and token k within it with
-// w_k / W_c, so the token follows w / Z exactly.
+// The draw is a two-level exponential race over blocks of kRaceBlock (512)
+// tokens. Level 1 picks the block with the largest W_c / E_c, where W_c is the
+// sum of the weights w over block c and E_c = -ln v_c, with v_c lane c mod 4 of
+// Philox counter (j, b, 1 + c div 4, 1). Level 2 picks the token of that block
+// with the largest w_k / E_k, with v_k lane k mod 4 of counter
+// (j, b, 1 + k div 4, 0). Uniforms are (2 (word >> 9) + 1) 2^-24, and the
+// lowest index wins an exact tie. Block c wins with probability W_c / Z and
+// token k within it with w_k / W_c, so the token follows w / Z exactly.
 //
-// Design. Only the one row pair of each sequence is read again.
-//  * Rows on 16-byte boundaries (every vocabulary whose row is a multiple of
-//    16 bytes): two launches. sample_stream_kernel is a grid of warps, each
-//    taking a contiguous run of 2 KB-per-row slices of the emitted row pairs
-//    through its own two-stage ring of bulk copies and writing one float-pair
-//    weight sum per slice; it has no atomics and no CTA-wide barriers.
-//    sample_finish_kernel, kFinishSplit CTAs per sequence, adds the slice
-//    sums of each block in a fixed order and runs level 1 (redundantly, with
-//    one result), then each CTA re-reads a quarter of the winning block and
-//    races it; the last CTA of the sequence keeps the best quarter.
-//  * Other rows: sample_kernel, one CTA per (sequence, block), stages its block
-//    in shared memory with bulk copies; the last CTA of a sequence (an atomic
-//    ticket: no one waits on it) runs the two levels.
-// Weights are float; block sums are float pairs (no float64, which GB300 runs
-// at a small fraction of the float32 rate). Per-token random numbers are drawn
-// in the winning block only. If every residual weight rounded to zero, p_j is
-// raced instead.
+// Design: two launches, chained by programmatic dependent launch.
+//  * sample_stream_kernel: the emitted row pairs of all sequences are cut into
+//    slices of kSliceBytes per row (whole race blocks: two of bf16, one of
+//    fp32). A grid of warps, no CTA-wide barriers: each warp takes a
+//    contiguous run of slices through its own two-stage ring of bulk copies
+//    and writes the weight sum of every race block it covers.
+//  * sample_race_kernel: one CTA per sequence runs both levels: level 1 over
+//    the block sums (one Philox block per four blocks per thread), then
+//    level 2 over the 512 tokens of the winning block, one four-token group
+//    per thread, read again from global memory. A kernel of its own keeps this
+//    code small and warm in the instruction cache (run inside the streaming
+//    kernel, at the end of a warp's run, it stalled on instruction fetches).
+//  * Rows that do not start on 16-byte boundaries are copied as the aligned
+//    cover of each slice (the last < 16 bytes of a tensor whose size is not a
+//    multiple of 16 by element loads) and read one element at a time.
+// Weights and block sums are float: a block sum adds at most 512 terms, whose
+// rounding stays far inside the 1e-5 near-tie band. The weights carry a factor
+// 2^lt common to the row pair (see weight_of). If every residual weight rounded
+// to zero, p_j is raced instead.
 #include <climits>
 
 #include "sv_device.cuh"
@@ -44,13 +46,8 @@ namespace {
 
 constexpr int kT = kSampleThreads;
 constexpr int kWarps = kT / 32;
-
-// Shared-memory bytes of one staged row block (tokens plus 16-byte cover).
-template <int ES>
-constexpr int buf_bytes()
-{
-    return kRaceBlock * ES + 32;
-}
+constexpr int kStageRow = kSliceBytes + 16;   // a slice's bytes plus its 16-byte cover
+constexpr int kWarpRing = 2 * 2 * kStageRow;  // two stages of (target | draft)
 
 __device__ __forceinline__ const uint8_t* down16(const uint8_t* p)
 {
@@ -61,25 +58,38 @@ __device__ __forceinline__ const uint8_t* up16(const uint8_t* p)
     return reinterpret_cast<const uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
 }
 
-// Everything about the row pair a CTA works on.
+// Slice geometry for one element size.
+template <int ES>
+struct Geo {
+    static constexpr int kEPV = 16 / ES;                // elements per 16-byte vector
+    static constexpr int kTok = kSliceBytes / ES;       // tokens per slice
+    static constexpr int kBlocks = kTok / kRaceBlock;   // race blocks per slice
+    static constexpr int kVPL = kSliceBytes / 16 / 32;  // vectors per lane and row (aligned rows)
+    static constexpr int kQPB = kVPL / kBlocks;         // consecutive vectors of a lane per block
+    static constexpr int kIPB = kRaceBlock / 32;        // consecutive elements of a lane per block
+    static_assert(kTok % kRaceBlock == 0, "a slice holds whole race blocks");
+    static_assert(kVPL % kBlocks == 0 && kQPB * 32 * kEPV == kRaceBlock, "vector to block map");
+};
+
+// The emitted row pair of one sequence and its normalisers.
 struct RowPair {
     const uint8_t* trow;   // target row j
     const uint8_t* drow;   // draft row j, or nullptr for the bonus row
-    const uint8_t* t_end;  // aligned tensor ends
-    const uint8_t* d_end;
-    float c, mt, lt, md, ld;
-    uint64_t seed;
-    uint32_t seq, pos;
+    float c, mt, md;       // c = log2(e) / T; mt, md: the rows' reference exponents
+    float r;               // 2^(lt - ld): the draft term's scale relative to the target's
 };
 
-// Sampling weight of one token from its logits: max(0, p - q) after a
-// rejection, p for the bonus. log2 p = x c - m - l (see SeqRecord).
+// Sampling weight of one token from its logits, up to a factor common to the
+// whole row pair: max(0, p - q) 2^lt after a rejection, p 2^lt for the bonus
+// (log2 p = x c - mt - lt, see SeqRecord). Both race levels compare weights of
+// one row pair only, so the common factor changes no decision; it saves the
+// per-token subtraction of lt and ld.
 __device__ __forceinline__ float weight_of(const RowPair& rp, float xt, float xd)
 {
-    const float p = ex2(fmaf(xt, rp.c, -rp.mt) - rp.lt);
+    const float p = ex2(fmaf(xt, rp.c, -rp.mt));
     if (rp.drow == nullptr) return p;
-    const float q = ex2(fmaf(xd, rp.c, -rp.md) - rp.ld);
-    return fmaxf(p - q, 0.0f);
+    const float q = ex2(fmaf(xd, rp.c, -rp.md));
+    return fmaxf(fmaf(-q, rp.r, p), 0.0f);
 }
 
 struct Best {
@@ -95,54 +105,8 @@ __device__ __forceinline__ void take(Best& a, float s, int i)
     }
 }
 
-// One group of four consecutive tokens k0..k0+3 (k0 a multiple of 4) in the
-// race of level 2: one Philox block gives their four clocks.
-__device__ __forceinline__ void race_group(Best& best, const RowPair& rp, int64_t k0,
-                                           const float (&w)[4])
-{
-    if (!(w[0] > 0.f || w[1] > 0.f || w[2] > 0.f || w[3] > 0.f)) return;
-    const uint2 key = make_uint2(static_cast<uint32_t>(rp.seed), static_cast<uint32_t>(rp.seed >> 32));
-    const uint4 r = philox4x32_10(
-        make_uint4(rp.pos, rp.seq, 1u + static_cast<uint32_t>(k0 >> 2), 0u), key);
-    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        if (w[q] > 0.f)
-            take(best, __fdividef(w[q], exp_clock(word_to_open_uniform(words[q]))),
-                 static_cast<int>(k0 + q));
-}
-
-// Block-wide float-pair sum over NT threads (fixed tree); every thread gets
-// the total.
-template <int NT = kT>
-__device__ __forceinline__ float2 block_sum2(float hi, float lo, float2* red)
-{
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, off);
-        const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, off);
-        float err;
-        const float s = two_sum(hi, ohi, &err);
-        lo = __fadd_rn(__fadd_rn(lo, olo), err);
-        hi = s;
-    }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float2(hi, lo);
-    __syncthreads();
-    float th = red[0].x, tl = red[0].y;
-#pragma unroll
-    for (int i = 1; i < NT / 32; ++i) {
-        float err;
-        const float s = two_sum(th, red[i].x, &err);
-        tl = __fadd_rn(__fadd_rn(tl, red[i].y), err);
-        th = s;
-    }
-    return make_float2(th, tl);
-}
-
-// Block-wide best over NT threads (largest score, lowest index), fixed tree.
-template <int NT = kT>
-__device__ __forceinline__ Best block_best(Best b, Best* red)
+// Best over the warp (largest score, lowest index); every lane gets it.
+__device__ __forceinline__ Best warp_best(Best b)
 {
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -150,140 +114,18 @@ __device__ __forceinline__ Best block_best(Best b, Best* red)
         const int oi = __shfl_xor_sync(0xFFFFFFFFu, b.idx, off);
         take(b, os, oi);
     }
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
-    __syncthreads();
-    Best t = red[0];
-#pragma unroll
-    for (int i = 1; i < NT / 32; ++i) take(t, red[i].score, red[i].idx);
-    return t;
+    return b;
 }
 
-// ---------------------------------------------------------------------------
-// Direct path: rows 16-byte aligned, a span of up to LEN tokens is read with
-// 16-byte loads by NT threads; thread t takes vectors t, t + NT, ... (coalesced).
-// ---------------------------------------------------------------------------
-template <int ES, int NT = kT, int LEN = kRaceBlock>
-struct Direct {
-    static constexpr int kEPV = 16 / ES;            // elements per vector
-    static constexpr int kVPT = LEN / kEPV / NT;    // vectors per thread
-    static_assert(LEN % (kEPV * NT) == 0, "span must split evenly over the threads");
-
-    // Elements of one 16-byte vector, widened exactly to float.
-    __device__ static __forceinline__ void unpack(const uint4& v, float (&x)[kEPV])
-    {
-        if constexpr (ES == 2) {
-            x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
-            x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
-        } else {
-            x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
-            x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
-        }
-    }
-
-    __device__ static __forceinline__ void load(const RowPair& rp, int64_t e0, int n,
-                                                uint4 (&tv)[kVPT], uint4 (&dv)[kVPT])
-    {
-        const uint4* tp = reinterpret_cast<const uint4*>(rp.trow + e0 * ES);
-        const uint4* dp = rp.drow ? reinterpret_cast<const uint4*>(rp.drow + e0 * ES) : nullptr;
-        const int nvec = n / kEPV;
-#pragma unroll
-        for (int q = 0; q < kVPT; ++q) {
-            const int vi = static_cast<int>(threadIdx.x) + q * NT;
-            tv[q] = vi < nvec ? __ldg(tp + vi) : make_uint4(0, 0, 0, 0);
-            dv[q] = (dp != nullptr && vi < nvec) ? __ldg(dp + vi) : make_uint4(0, 0, 0, 0);
-        }
-    }
-
-    // Per-thread weights of the block (zero past its end).
-    __device__ static __forceinline__ void weights(const RowPair& rp, int n, const uint4 (&tv)[kVPT],
-                                                   const uint4 (&dv)[kVPT],
-                                                   float (&w)[kVPT][kEPV])
-    {
-        const int nvec = n / kEPV;
-#pragma unroll
-        for (int q = 0; q < kVPT; ++q) {
-            float xt[kEPV], xd[kEPV];
-            unpack(tv[q], xt);
-            unpack(dv[q], xd);
-            const bool in = static_cast<int>(threadIdx.x) + q * NT < nvec;
-#pragma unroll
-            for (int e = 0; e < kEPV; ++e) w[q][e] = in ? weight_of(rp, xt[e], xd[e]) : 0.f;
-        }
-    }
-
-    __device__ static float2 block_weight(const RowPair& rp, int64_t e0, int n, float2* red)
-    {
-        uint4 tv[kVPT], dv[kVPT];
-        load(rp, e0, n, tv, dv);
-        float w[kVPT][kEPV];
-        weights(rp, n, tv, dv, w);
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int q = 0; q < kVPT; ++q)
-#pragma unroll
-            for (int e = 0; e < kEPV; e += 2) {
-                a0 += w[q][e];
-                a1 += w[q][e + 1];
-            }
-        float err;
-        const float hi = two_sum(a0, a1, &err);
-        return block_sum2<NT>(hi, err, red);
-    }
-
-    __device__ static Best race(const RowPair& rp, int64_t e0, int n, Best* red)
-    {
-        uint4 tv[kVPT], dv[kVPT];
-        load(rp, e0, n, tv, dv);
-        float w[kVPT][kEPV];
-        weights(rp, n, tv, dv, w);
-        Best best{0.0f, INT_MAX};
-#pragma unroll
-        for (int q = 0; q < kVPT; ++q) {
-            const int64_t k = e0 + static_cast<int64_t>(threadIdx.x + q * NT) * kEPV;
-#pragma unroll
-            for (int g = 0; g < kEPV; g += 4) {
-                const float wg[4] = {w[q][g], w[q][g + 1], w[q][g + 2], w[q][g + 3]};
-                race_group(best, rp, k + g, wg);
-            }
-        }
-        return block_best<NT>(best, red);
-    }
-};
-
-// ---------------------------------------------------------------------------
-// Staged path: rows not 16-byte aligned. The bulk engine moves the aligned
-// cover [a0, a0 + bulk) of row bytes [s, e); the last < 16 bytes of a tensor
-// whose size is not a multiple of 16 are loaded one element at a time. Byte s
-// lands at buf + off.
-// ---------------------------------------------------------------------------
-struct CopyPlan {
-    const uint8_t* a0;
-    uint32_t bulk;
-    int off;
-};
-
-template <int ES>
-__device__ __forceinline__ CopyPlan plan_copy(uint8_t* buf, const uint8_t* s, const uint8_t* e,
-                                              const uint8_t* tend)
+// Sum over the warp by a fixed butterfly; every lane gets the same value.
+__device__ __forceinline__ float warp_sum(float x)
 {
-    CopyPlan cp;
-    cp.a0 = down16(s);
-    const uint8_t* up = up16(e);
-    const uint8_t* bend = up < tend ? up : tend;
-    cp.bulk = bend > cp.a0 ? static_cast<uint32_t>(bend - cp.a0) : 0u;
-    cp.off = static_cast<int>(s - cp.a0);
-    const uint8_t* tail = bend >= e ? e : (bend > s ? bend : s);
-    for (const uint8_t* p = tail + threadIdx.x * ES; p < e; p += kT * ES) {
-        if (ES == 2)
-            *reinterpret_cast<uint16_t*>(buf + (p - cp.a0)) =
-                __ldg(reinterpret_cast<const unsigned short*>(p));
-        else
-            *reinterpret_cast<uint32_t*>(buf + (p - cp.a0)) =
-                __ldg(reinterpret_cast<const unsigned int*>(p));
-    }
-    return cp;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+    return x;
 }
+
+__device__ __forceinline__ int64_t lmin(int64_t x, int64_t y) { return x < y ? x : y; }
 
 template <int ES>
 __device__ __forceinline__ float elem(const uint8_t* p)
@@ -292,365 +134,255 @@ __device__ __forceinline__ float elem(const uint8_t* p)
                    : *reinterpret_cast<const float*>(p);
 }
 
-template <int ES>
-struct Staged {
-    uint8_t* buf_t;
-    uint8_t* buf_d;
-    uint64_t* bar;
-    uint32_t phase;
-    int off_t, off_d;
-
-    // Stage block [e0, e0 + n); false if the copy did not land in time.
-    __device__ bool stage(const RowPair& rp, int64_t e0, int n)
-    {
-        const int64_t e1 = e0 + n;
-        const CopyPlan ct = plan_copy<ES>(buf_t, rp.trow + e0 * ES, rp.trow + e1 * ES, rp.t_end);
-        CopyPlan cd;
-        cd.a0 = nullptr;
-        cd.bulk = 0;
-        cd.off = 0;
-        if (rp.drow != nullptr)
-            cd = plan_copy<ES>(buf_d, rp.drow + e0 * ES, rp.drow + e1 * ES, rp.d_end);
-        if (threadIdx.x == 0) {
-            mbar_arrive_expect_tx(bar, ct.bulk + cd.bulk);
-            if (ct.bulk > 0) bulk_copy_g2s(buf_t, ct.a0, ct.bulk, bar);
-            if (cd.bulk > 0) bulk_copy_g2s(buf_d, cd.a0, cd.bulk, bar);
-        }
-        const bool ok = mbar_wait_bounded(bar, phase & 1u, nullptr);
-        phase += 1;
-        off_t = ct.off;
-        off_d = cd.off;
-        // Orders the element-wise tail stores before every thread's reads, and
-        // agrees on whether the copy landed.
-        return __syncthreads_and(ok ? 1 : 0) != 0;
-    }
-
-    __device__ float w_at(const RowPair& rp, int e) const
-    {
-        const float xt = elem<ES>(buf_t + off_t + e * ES);
-        const float xd = rp.drow ? elem<ES>(buf_d + off_d + e * ES) : 0.f;
-        return weight_of(rp, xt, xd);
-    }
-
-    __device__ float2 block_weight(const RowPair& rp, int n, float2* red) const
-    {
-        float a0 = 0.f;
-        for (int e = threadIdx.x; e < n; e += kT) a0 += w_at(rp, e);
-        return block_sum2(a0, 0.f, red);
-    }
-
-    __device__ Best race(const RowPair& rp, int64_t e0, int n, Best* red) const
-    {
-        Best best{0.0f, INT_MAX};
-        for (int g = threadIdx.x; 4 * g < n; g += kT) {
-            float w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) w[q] = 4 * g + q < n ? w_at(rp, 4 * g + q) : 0.f;
-            race_group(best, rp, e0 + 4 * g, w);
-        }
-        return block_best(best, red);
-    }
+// One sequence as the sampler sees it.
+struct SeqJob {
+    RowPair rp;
+    int64_t b;
+    bool ok;  // the scan found the sequence valid
 };
 
-// Level 1: the block with the largest W_c / E_c over blocks with W_c > 0
-// (lowest index on a tie); INT_MAX when no block has weight. The flags of all
-// block records are OR-ed into *flags.
-template <int NT = kT>
-__device__ int race_blocks(const volatile ChunkSum* cs, int64_t nch, const RowPair& rp,
-                           int* flags, Best* red, int* red_flags)
+// Reads sequence b's record; returns the emitted position j.
+__device__ __forceinline__ int load_seq(SeqJob& s, const SampleArgs& a, int64_t b, int es)
 {
-    Best best{0.0f, INT_MAX};
-    int fl = 0;
-    const uint2 key = make_uint2(static_cast<uint32_t>(rp.seed), static_cast<uint32_t>(rp.seed >> 32));
-    for (int64_t c = threadIdx.x; c < nch; c += NT) {
-        const float W = cs[c].hi + cs[c].lo;
-        fl |= cs[c].flags;
-        if (!(W > 0.f)) continue;
-        const uint4 r = philox4x32_10(
-            make_uint4(rp.pos, rp.seq, 1u + static_cast<uint32_t>(c >> 2), 1u), key);
-        const uint32_t lane = static_cast<uint32_t>(c & 3);
-        const uint32_t word = lane == 0 ? r.x : lane == 1 ? r.y : lane == 2 ? r.z : r.w;
-        take(best, W / exp_clock(word_to_open_uniform(word)), static_cast<int>(c));
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) fl |= __shfl_xor_sync(0xFFFFFFFFu, fl, off);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) red_flags[threadIdx.x >> 5] = fl;
-    const Best t = block_best<NT>(best, red);  // its barriers also publish red_flags
-    int f = 0;
-#pragma unroll
-    for (int i = 0; i < NT / 32; ++i) f |= red_flags[i];
-    *flags = f;
-    return t.idx;
-}
-
-template <int ES, bool STAGED>
-__device__ void sample_block(const SampleArgs& a, uint8_t* dyn)
-{
-    __shared__ __align__(8) uint64_t bar;
-    __shared__ Best red[kWarps];
-    __shared__ float2 red2[kWarps];
-    __shared__ int red_flags[kWarps];
-    __shared__ int s_last;
-
     const Geometry& g = a.g;
-    const int64_t nch = g.nchunks;
-    const int64_t b = blockIdx.x / nch;
-    const int64_t c = blockIdx.x - b * nch;
-    pdl_wait();  // the scan has finished and the sequence records are visible
     const SeqRecord rec = a.seqs[b];
-    if (rec.status != 0) return;
-
-    const int64_t K = g.K, V = g.V;
-    const int64_t j = rec.j;
-    const int64_t row_bytes = V * ES;
-    RowPair rp;
-    rp.trow = a.target + (b * (K + 1) + j) * row_bytes;
-    rp.t_end = down16(a.target + g.rows_t * row_bytes);
-    rp.drow = j < K ? a.draft + (b * K + j) * row_bytes : nullptr;
-    rp.d_end = j < K ? down16(a.draft + g.B * K * row_bytes) : nullptr;
-    rp.c = a.c;
-    rp.mt = rec.mt;
-    rp.lt = rec.lt;
-    rp.md = rec.md;
-    rp.ld = rec.ld;
-    rp.seed = a.seed;
-    rp.seq = static_cast<uint32_t>(b);
-    rp.pos = static_cast<uint32_t>(j);
-
-    Staged<ES> st{dyn, dyn + buf_bytes<ES>(), &bar, 0u, 0, 0};
-    if (STAGED) {
-        if (threadIdx.x == 0) {
-            mbar_init(&bar, 1);
-            fence_barrier_init();
-        }
-        __syncthreads();
-    }
-    ChunkSum* sums = a.chunk_sums + b * nch;
-    auto block_len = [&](int64_t blk) {
-        return static_cast<int>(min(static_cast<int64_t>(kRaceBlock), V - blk * kRaceBlock));
-    };
-
-    // ---- every CTA: the total weight of its block ----
-    float2 W = make_float2(0.f, 0.f);
-    int flags = 0;
-    const int n = block_len(c);
-    if (STAGED) {
-        if (st.stage(rp, c * kRaceBlock, n))
-            W = st.block_weight(rp, n, red2);
-        else
-            flags = kFlagTimeout;
-    } else {
-        W = Direct<ES>::block_weight(rp, c * kRaceBlock, n, red2);
-    }
-    if (threadIdx.x == 0) {
-        ChunkSum cs;
-        cs.hi = W.x;
-        cs.lo = W.y;
-        cs.flags = flags;
-        cs.pad = 0;
-        sums[c] = cs;
-        __threadfence();
-        const uint32_t ticket = atomicAdd(&a.tickets[b], 1u);
-        s_last = ticket == static_cast<uint32_t>(nch - 1);
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
-
-    // ---- the last CTA of this sequence: level 1 over the blocks ----
-    int any_flags = 0;
-    bool fallback = false;
-    int win = race_blocks(sums, nch, rp, &any_flags, red, red_flags);
-    if (any_flags == 0 && win == INT_MAX) {
-        // Every residual weight rounded to zero: race p_j instead, block sums first.
-        fallback = true;
-        rp.drow = nullptr;
-        for (int64_t i = 0; i < nch && any_flags == 0; ++i) {
-            const int ni = block_len(i);
-            float2 Wp = make_float2(0.f, 0.f);
-            if (STAGED) {
-                if (st.stage(rp, i * kRaceBlock, ni))
-                    Wp = st.block_weight(rp, ni, red2);
-                else
-                    any_flags = kFlagTimeout;
-            } else {
-                Wp = Direct<ES>::block_weight(rp, i * kRaceBlock, ni, red2);
-            }
-            if (threadIdx.x == 0) {
-                ChunkSum cs;
-                cs.hi = Wp.x;
-                cs.lo = Wp.y;
-                cs.flags = 0;
-                cs.pad = 0;
-                sums[i] = cs;
-            }
-            __syncthreads();
-        }
-        if (any_flags == 0) {
-            int f2 = 0;
-            win = race_blocks(sums, nch, rp, &f2, red, red_flags);
-        }
-    }
-
-    // ---- level 2 over the tokens of the winning block ----
-    Best tok{0.0f, INT_MAX};
-    if (any_flags == 0 && win != INT_MAX) {
-        const int64_t p0 = static_cast<int64_t>(win) * kRaceBlock;
-        const int np = block_len(win);
-        if (STAGED) {
-            bool ok = true;
-            if (win != c || fallback) ok = st.stage(rp, p0, np);
-            if (ok)
-                tok = st.race(rp, p0, np, red);
-            else
-                any_flags = kFlagTimeout;
-        } else {
-            tok = Direct<ES>::race(rp, p0, np, red);
-        }
-    }
-
-    if (threadIdx.x == 0) {
-        const int64_t K1 = K + 1;
-        if (any_flags != 0 || tok.idx == INT_MAX) {
-            for (int64_t i = 0; i < K1; ++i) a.out_tokens[b * K1 + i] = -1;
-            a.num_accepted[b] = -1;
-            if (a.seq_status) a.seq_status[b] = kFlagTimeout;
-        } else {
-            a.out_tokens[b * K1 + j] = tok.idx;
-        }
-    }
+    s.b = b;
+    s.ok = rec.status == 0;
+    const int64_t K = g.K, row_bytes = g.V * es;
+    s.rp.trow = a.target + (b * (K + 1) + rec.j) * row_bytes;
+    s.rp.drow = rec.j < K ? a.draft + (b * K + rec.j) * row_bytes : nullptr;
+    s.rp.c = a.c;
+    s.rp.mt = rec.mt;
+    s.rp.md = rec.md;
+    s.rp.r = rec.j < K ? exp2f(rec.lt - rec.ld) : 1.0f;
+    return rec.j;
 }
 
-template <int ES, bool STAGED>
-__global__ void __launch_bounds__(kT) sample_kernel(const SampleArgs a)
-{
-    extern __shared__ __align__(128) uint8_t dyn[];
-    sample_block<ES, STAGED>(a, dyn);
-}
-
-template <int ES, bool STAGED>
-cudaError_t launch_one(const SampleArgs& a, cudaStream_t s)
-{
-    const unsigned grid = static_cast<unsigned>(a.g.B * a.g.nchunks);
-    const int smem = STAGED ? 2 * buf_bytes<ES>() : 0;
-    if (STAGED) {
-        const cudaError_t e = cudaFuncSetAttribute(
-            sample_kernel<ES, STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-    }
-    return launch_dependent(a.g.pdl != 0, sample_kernel<ES, STAGED>, dim3(grid), dim3(kT), smem, s, a);
-}
-
-// ---------------------------------------------------------------------------
-// Aligned rows, launch 1 of 2: weight sums of 2 KB-per-row slices.
-// ---------------------------------------------------------------------------
-template <int ES>
-struct Slices {
-    static constexpr int kEPV = 16 / ES;                    // elements per vector
-    static constexpr int kTok = kSliceBytes / ES;           // tokens per slice
-    static constexpr int kPerBlock = kRaceBlock / kTok;     // slices per race block
-    static constexpr int kVPL = kSliceBytes / 16 / 32;      // vectors per lane per row
+// 16-byte-aligned ends of the target and draft tensors (bulk copies of rows
+// that are not 16-byte aligned stop there).
+struct TensorEnds {
+    const uint8_t* t;
+    const uint8_t* d;
 };
 
-__device__ __forceinline__ void warp_sum2(float& hi, float& lo)
+// The logits of the four tokens k0 .. k0 + 3 (k0 a multiple of 4) of both
+// rows, read from global memory (0 past the vocabulary, weighted to 0 below).
+template <int ES, bool ALIGNED>
+__device__ __forceinline__ void group_load(const RowPair& rp, int64_t k0, int64_t V, float (&xt)[4],
+                                           float (&xd)[4])
 {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-        const float ohi = __shfl_xor_sync(0xFFFFFFFFu, hi, off);
-        const float olo = __shfl_xor_sync(0xFFFFFFFFu, lo, off);
-        float err;
-        const float s = two_sum(hi, ohi, &err);
-        lo = __fadd_rn(__fadd_rn(lo, olo), err);
-        hi = s;
+    for (int q = 0; q < 4; ++q) xt[q] = xd[q] = 0.f;
+    if (k0 >= V) return;
+    if (ALIGNED) {
+        // Aligned rows hold a multiple of 16 bytes, so a group that starts
+        // inside the row ends inside it.
+        if (ES == 2) {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(rp.trow + k0 * 2));
+            xt[0] = bf16_lo(v.x); xt[1] = bf16_hi(v.x); xt[2] = bf16_lo(v.y); xt[3] = bf16_hi(v.y);
+            if (rp.drow) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(rp.drow + k0 * 2));
+                xd[0] = bf16_lo(u.x); xd[1] = bf16_hi(u.x); xd[2] = bf16_lo(u.y); xd[3] = bf16_hi(u.y);
+            }
+        } else {
+            const float4 v = __ldg(reinterpret_cast<const float4*>(rp.trow + k0 * 4));
+            xt[0] = v.x; xt[1] = v.y; xt[2] = v.z; xt[3] = v.w;
+            if (rp.drow) {
+                const float4 u = __ldg(reinterpret_cast<const float4*>(rp.drow + k0 * 4));
+                xd[0] = u.x; xd[1] = u.y; xd[2] = u.z; xd[3] = u.w;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            if (k0 + q < V) {
+                xt[q] = elem<ES>(rp.trow + (k0 + q) * ES);
+                if (rp.drow) xd[q] = elem<ES>(rp.drow + (k0 + q) * ES);
+            }
+        }
     }
 }
 
-__device__ __forceinline__ void row_pair_of(RowPair& rp, const SampleArgs& a, const SeqRecord& rec,
-                                            int64_t b, int es)
+// Weights of a loaded group (0 for tokens past the vocabulary).
+__device__ __forceinline__ void group_weights(const RowPair& rp, int64_t k0, int64_t V,
+                                              const float (&xt)[4], const float (&xd)[4], float (&w)[4])
 {
-    const Geometry& g = a.g;
-    const int64_t K = g.K, row_bytes = g.V * es;
-    const int64_t j = rec.j;
-    rp.trow = a.target + (b * (K + 1) + j) * row_bytes;
-    rp.t_end = down16(a.target + g.rows_t * row_bytes);
-    rp.drow = j < K ? a.draft + (b * K + j) * row_bytes : nullptr;
-    rp.d_end = j < K ? down16(a.draft + g.B * K * row_bytes) : nullptr;
-    rp.c = a.c;
-    rp.mt = rec.mt;
-    rp.lt = rec.lt;
-    rp.md = rec.md;
-    rp.ld = rec.ld;
-    rp.seed = a.seed;
-    rp.seq = static_cast<uint32_t>(b);
-    rp.pos = static_cast<uint32_t>(j);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) w[q] = k0 + q < V ? weight_of(rp, xt[q], xd[q]) : 0.f;
 }
 
-// One slice pair as a warp sees it: where its rows are and how many 16-byte
-// vectors of each row it holds (0 past the vocabulary).
-struct SliceJob {
-    RowPair rp;
-    bool seq_ok;  // the sequence is valid (else nothing is read or written)
-    int nvec;
-};
+// Race step over one group of four candidates with weights w (indices
+// i0 .. i0 + 3) and clocks from the Philox block of counter ctr.
+__device__ __forceinline__ void race_group(Best& best, const float (&w)[4], int64_t i0, uint4 ctr,
+                                           uint2 key)
+{
+    if (!(w[0] > 0.f || w[1] > 0.f || w[2] > 0.f || w[3] > 0.f)) return;
+    const uint4 r = philox4x32_10(ctr, key);
+    const uint32_t words[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        if (w[q] > 0.f)
+            take(best, w[q] / exp_clock(word_to_open_uniform(words[q])), static_cast<int>(i0 + q));
+}
 
-// Slice `sl` of sequence `b`. Consecutive slices of a warp usually share a
-// sequence, whose record is then read once.
+// Elements of one 16-byte vector, widened exactly to float.
 template <int ES>
-__device__ __forceinline__ void slice_job(SliceJob& job, const SampleArgs& a, int64_t b,
-                                          int64_t sl, int64_t& cached_b, SliceJob& cache)
+__device__ __forceinline__ void unpack(const uint4& v, float (&x)[16 / ES])
 {
-    using S = Slices<ES>;
-    const int64_t e0 = sl * S::kTok;
-    if (b != cached_b) {
-        cached_b = b;
-        const SeqRecord rec = a.seqs[b];
-        cache.seq_ok = rec.status == 0;
-        if (cache.seq_ok) row_pair_of(cache.rp, a, rec, b, ES);
-    }
-    job = cache;
-    job.nvec = 0;
-    if (job.seq_ok && e0 < a.g.V) {
-        job.nvec = static_cast<int>(min(static_cast<int64_t>(S::kTok), a.g.V - e0)) / S::kEPV;
-        job.rp.trow += e0 * ES;  // point at the slice
-        if (job.rp.drow) job.rp.drow += e0 * ES;
+    if constexpr (ES == 2) {
+        x[0] = bf16_lo(v.x); x[1] = bf16_hi(v.x); x[2] = bf16_lo(v.y); x[3] = bf16_hi(v.y);
+        x[4] = bf16_lo(v.z); x[5] = bf16_hi(v.z); x[6] = bf16_lo(v.w); x[7] = bf16_hi(v.w);
+    } else {
+        x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
     }
 }
 
-// Lane 0 starts the bulk copies of a slice pair into a stage; a pair with
-// nothing to read completes the stage's phase with a plain arrive.
-__device__ __forceinline__ void issue_slice(const SliceJob& job, uint8_t* stage, uint64_t* bar)
+// Byte offset at which a slice starting at token e0 of `row` lands in its
+// stage: 0 for aligned rows, else the row position modulo 16.
+template <bool ALIGNED>
+__device__ __forceinline__ int stage_offset(const uint8_t* row, int64_t e0, int es)
 {
-    const uint32_t bytes = static_cast<uint32_t>(job.nvec) * 16u;
-    if (bytes == 0) {
-        mbar_arrive(bar);
-        return;
-    }
-    mbar_arrive_expect_tx(bar, job.rp.drow ? 2u * bytes : bytes);
-    bulk_copy_g2s(stage, job.rp.trow, bytes, bar);
-    if (job.rp.drow) bulk_copy_g2s(stage + kSliceBytes, job.rp.drow, bytes, bar);
+    return ALIGNED ? 0 : static_cast<int>((reinterpret_cast<uintptr_t>(row) + e0 * es) & 15);
 }
 
-// Each warp walks a contiguous run of slices with a two-stage ring in shared
-// memory: lane 0 copies slice i + 1 (both rows, bulk copies) while the warp
-// sums the weights of slice i from the other stage. No registers hold data in
-// flight, so every warp keeps a full slice pair moving at all times.
+// Starts the copies of one slice (tokens [e0, e0 + n) of both rows) into a
+// stage [target | draft]. Lane 0 issues the bulk copies; for rows that are not
+// 16-byte aligned, the bulk copy moves the slice's aligned cover (clipped at
+// the tensor's aligned end) and the lanes load the few bytes past that end one
+// element at a time. A slice with nothing to read completes the stage's phase
+// with a plain arrive.
+template <int ES, bool ALIGNED>
+__device__ __forceinline__ void issue_slice(const SeqJob& sj, const TensorEnds& ends, int64_t e0, int n,
+                                            uint8_t* stage, uint64_t* bar, int lane)
+{
+    const uint8_t* src[2] = {nullptr, nullptr};
+    uint32_t bytes[2] = {0u, 0u};
+    if (sj.ok && n > 0) {
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const uint8_t* row = r == 0 ? sj.rp.trow : sj.rp.drow;
+            if (row == nullptr) continue;
+            const uint8_t* s = row + e0 * ES;
+            const uint8_t* e = s + static_cast<int64_t>(n) * ES;
+            if (ALIGNED) {
+                src[r] = s;
+                bytes[r] = static_cast<uint32_t>(n) * ES;
+            } else {
+                const uint8_t* tend = r == 0 ? ends.t : ends.d;
+                const uint8_t* a0 = down16(s);
+                const uint8_t* up = up16(e);
+                const uint8_t* bend = up < tend ? up : tend;
+                const uint32_t bulk = bend > a0 ? static_cast<uint32_t>(bend - a0) : 0u;
+                src[r] = a0;
+                bytes[r] = bulk;
+                uint8_t* dst = stage + r * kStageRow;
+                const uint8_t* tail = a0 + bulk > s ? a0 + bulk : s;
+                for (const uint8_t* p = tail + lane * ES; p < e; p += 32 * ES) {
+                    if (ES == 2)
+                        *reinterpret_cast<uint16_t*>(dst + (p - a0)) =
+                            __ldg(reinterpret_cast<const unsigned short*>(p));
+                    else
+                        *reinterpret_cast<uint32_t*>(dst + (p - a0)) =
+                            __ldg(reinterpret_cast<const unsigned int*>(p));
+                }
+            }
+        }
+    }
+    if (lane == 0) {
+        const uint32_t tx = bytes[0] + bytes[1];
+        if (tx == 0) {
+            mbar_arrive(bar);
+        } else {
+            mbar_arrive_expect_tx(bar, tx);
+            if (bytes[0]) bulk_copy_g2s(stage, src[0], bytes[0], bar);
+            if (bytes[1]) bulk_copy_g2s(stage + kStageRow, src[1], bytes[1], bar);
+        }
+    }
+}
+
+// Per-lane weight sums of the race blocks of one staged slice of n tokens
+// (acc[k]: block k of the slice). Aligned rows: lane l reads vectors
+// l, l + 32, ... of each row; other rows: elements l, l + 32, ....
+template <int ES, bool ALIGNED>
+__device__ __forceinline__ void sum_slice(const RowPair& rp, const uint8_t* st, int off_t, int off_d,
+                                          int n, int lane, float (&acc)[Geo<ES>::kBlocks])
+{
+    using G = Geo<ES>;
+    const uint8_t* bt = st + off_t;
+    const uint8_t* bd = st + kStageRow + off_d;
+    if (ALIGNED) {
+        const int nvec = n / G::kEPV;
+#pragma unroll
+        for (int q = 0; q < G::kVPL; ++q) {
+            const int vi = lane + 32 * q;
+            if (vi >= nvec) continue;
+            float xt[G::kEPV], xd[G::kEPV];
+            unpack<ES>(ld_shared_v4(bt + 16 * vi), xt);
+            if (rp.drow)
+                unpack<ES>(ld_shared_v4(bd + 16 * vi), xd);
+            else
+#pragma unroll
+                for (int e = 0; e < G::kEPV; ++e) xd[e] = 0.f;
+#pragma unroll
+            for (int e = 0; e < G::kEPV; ++e) acc[q / G::kQPB] += weight_of(rp, xt[e], xd[e]);
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < G::kBlocks; ++k) {
+#pragma unroll 4
+            for (int i = 0; i < G::kIPB; ++i) {
+                const int e = lane + 32 * (k * G::kIPB + i);
+                if (e >= n) break;
+                const float xt = elem<ES>(bt + e * ES);
+                const float xd = rp.drow ? elem<ES>(bd + e * ES) : 0.f;
+                acc[k] += weight_of(rp, xt, xd);
+            }
+        }
+    }
+}
+
+// Lane 0 writes the block sums of one finished slice (NaN: its copy never
+// landed).
 template <int ES>
-__global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
+__device__ __forceinline__ void store_sums(const SampleArgs& a, int64_t b, int64_t e0, int n,
+                                           const float (&sums)[Geo<ES>::kBlocks], int lane)
 {
-    using S = Slices<ES>;
+    const int64_t nblk = a.g.nblocks;
+    const int64_t c0 = e0 / kRaceBlock;
+    const int nb = (n + kRaceBlock - 1) / kRaceBlock;
+    if (lane == 0) {
+#pragma unroll
+        for (int k = 0; k < Geo<ES>::kBlocks; ++k)
+            if (k < nb) a.block_sums[b * nblk + c0 + k] = sums[k];
+    }
+}
+
+// Launch 1 of 2: a grid of warps over the slices of all sequences' emitted
+// row pairs (slice i is slice i mod per_seq of sequence i div per_seq). Each
+// warp takes a contiguous run of slices with a two-stage ring: lane 0 copies
+// slice i + 1 while the warp sums slice i from the other stage, and writes the
+// weight sum of each race block of the slice.
+template <int ES, bool ALIGNED>
+__global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const SampleArgs a)
+{
+    using G = Geo<ES>;
     extern __shared__ __align__(128) uint8_t ring[];  // [warp][stage][target | draft]
     __shared__ __align__(8) uint64_t bars[kWarps][2];
     const Geometry& g = a.g;
-    const int64_t per_seq = g.nchunks * S::kPerBlock;
+    const int64_t per_seq = (g.V + G::kTok - 1) / G::kTok;
     const int64_t total = g.B * per_seq;
     const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kWarps;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t w = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
-    const int64_t i0 = w * total / nwarps, i1 = (w + 1) * total / nwarps;
-    uint8_t* stage0 = ring + static_cast<size_t>(warp) * 4 * kSliceBytes;
-    uint8_t* stage1 = stage0 + 2 * kSliceBytes;
+    // [i0, i1): this warp's slices, split without overflow (w * total can
+    // exceed 63 bits at the largest sizes).
+    const int64_t qt = total / nwarps, rt = total % nwarps;
+    const int64_t i0 = w * qt + (w * rt) / nwarps;
+    const int64_t i1 = (w + 1) * qt + ((w + 1) * rt) / nwarps;
+    uint8_t* const ring_w = ring + static_cast<size_t>(warp) * kWarpRing;
+    auto stage = [&](int st) { return ring_w + st * (2 * kStageRow); };
     if (lane == 0) {
         mbar_init(&bars[warp][0], 1);
         mbar_init(&bars[warp][1], 1);
@@ -658,35 +390,42 @@ __global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
     }
     __syncwarp();
     pdl_wait();  // the scan has finished and the sequence records are visible
+    pdl_trigger();  // the race kernel may be scheduled; it waits for this grid
 
-    int64_t cached_b = -1;
-    SliceJob cache, cur, next;
-    cache.seq_ok = false;
-    cache.nvec = 0;
-    uint32_t phases = 0;  // bit s: parity of the next phase of stage s
-    bool failed = false;
-    // Cursor (sequence, slice) of the next slice to issue; one division here,
-    // increments afterwards.
+    auto tokens_at = [&](int64_t sl) { return static_cast<int>(lmin(G::kTok, g.V - sl * G::kTok)); };
+    TensorEnds ends{nullptr, nullptr};
+    if (!ALIGNED) {
+        const int64_t row_bytes = g.V * ES;
+        ends.t = down16(a.target + g.rows_t * row_bytes);
+        ends.d = a.draft != nullptr ? down16(a.draft + g.B * g.K * row_bytes) : nullptr;
+    }
+    // Cursor of the next slice to issue: sequence nb, slice nsl of it.
     int64_t nb = i0 / per_seq, nsl = i0 - nb * per_seq;
-    auto advance = [&]() {
+    SeqJob issued, cur;  // the sequence of the slice issued last / being summed
+    issued.b = -1;
+    issued.ok = false;
+    uint32_t phases = 0;  // bit s: parity of the next phase of stage s
+    int64_t i = i0;
+    if (i0 < i1) {
+        load_seq(issued, a, nb, ES);
+        issue_slice<ES, ALIGNED>(issued, ends, nsl * G::kTok, tokens_at(nsl), stage(0), &bars[warp][0],
+                                 lane);
+        __syncwarp();  // element loads into the stage before any lane reads it
+    }
+    bool failed = false;
+    for (; i < i1; ++i) {
+        const int s = static_cast<int>((i - i0) & 1);
+        cur = issued;
+        const int64_t e0 = nsl * G::kTok;
+        const int n = tokens_at(nsl);
         if (++nsl == per_seq) {
             nsl = 0;
             ++nb;
         }
-    };
-    if (i0 < i1) {
-        slice_job<ES>(cur, a, nb, nsl, cached_b, cache);
-        if (lane == 0) issue_slice(cur, stage0, &bars[warp][0]);
-        advance();
-    }
-    int64_t i = i0;
-    for (; i < i1; ++i) {
-        const int s = static_cast<int>((i - i0) & 1);
-        uint8_t* buf = s ? stage1 : stage0;
         if (i + 1 < i1) {
-            slice_job<ES>(next, a, nb, nsl, cached_b, cache);
-            if (lane == 0) issue_slice(next, s ? stage0 : stage1, &bars[warp][s ^ 1]);
-            advance();
+            if (nb != issued.b) load_seq(issued, a, nb, ES);
+            issue_slice<ES, ALIGNED>(issued, ends, nsl * G::kTok, tokens_at(nsl), stage(s ^ 1),
+                                     &bars[warp][s ^ 1], lane);
         }
         const bool ok = mbar_wait_bounded(&bars[warp][s], (phases >> s) & 1u, nullptr);
         phases ^= 1u << s;
@@ -694,191 +433,194 @@ __global__ void __launch_bounds__(kT) sample_stream_kernel(const SampleArgs a)
             failed = true;
             break;
         }
-        if (cur.seq_ok) {
-            float a0 = 0.f, a1 = 0.f;
+        if (cur.ok) {
+            float acc[G::kBlocks];
 #pragma unroll
-            for (int q = 0; q < S::kVPL; ++q) {
-                const int vi = lane + 32 * q;
-                if (vi >= cur.nvec) continue;
-                float xt[S::kEPV], xd[S::kEPV];
-                Direct<ES>::unpack(ld_shared_v4(buf + 16 * vi), xt);
-                if (cur.rp.drow)
-                    Direct<ES>::unpack(ld_shared_v4(buf + kSliceBytes + 16 * vi), xd);
-                else
+            for (int q = 0; q < G::kBlocks; ++q) acc[q] = 0.f;
+            sum_slice<ES, ALIGNED>(cur.rp, stage(s), stage_offset<ALIGNED>(cur.rp.trow, e0, ES),
+                                   cur.rp.drow ? stage_offset<ALIGNED>(cur.rp.drow, e0, ES) : 0, n,
+                                   lane, acc);
 #pragma unroll
-                    for (int e = 0; e < S::kEPV; ++e) xd[e] = 0.f;
-#pragma unroll
-                for (int e = 0; e < S::kEPV; e += 2) {
-                    a0 += weight_of(cur.rp, xt[e], xd[e]);
-                    a1 += weight_of(cur.rp, xt[e + 1], xd[e + 1]);
-                }
-            }
-            float lo;
-            float hi = two_sum(a0, a1, &lo);
-            warp_sum2(hi, lo);
-            if (lane == 0) a.slice_sums[i] = make_float2(hi, lo);
+            for (int q = 0; q < G::kBlocks; ++q) acc[q] = warp_sum(acc[q]);
+            store_sums<ES>(a, cur.b, e0, n, acc, lane);
         }
         __syncwarp();  // the stage is read out before it is refilled
-        cur = next;
     }
     if (failed) {
-        // Mark the rest of this warp's slices, then let the copy already
-        // issued into the other stage land before the CTA exits.
-        const float nan = __uint_as_float(0x7FC00000u);
-        for (int64_t k = i + lane; k < i1; k += 32) a.slice_sums[k] = make_float2(nan, nan);
+        // A copy did not land in time. Mark this warp's remaining slices with
+        // NaN sums, so that the race kernel reports a timeout for their
+        // sequences, then let the copies already issued land before the CTA
+        // exits.
         const int s = static_cast<int>((i - i0) & 1);
-        mbar_wait_bounded(&bars[warp][s], ((phases >> s) & 1u) ^ 1u, nullptr);
-        if (i + 1 < i1) {
-            const int o = s ^ 1;
-            mbar_wait_bounded(&bars[warp][o], (phases >> o) & 1u, nullptr);
+        const float nan = __uint_as_float(0x7FC00000u);
+        float sums[G::kBlocks];
+#pragma unroll
+        for (int q = 0; q < G::kBlocks; ++q) sums[q] = nan;
+        for (int64_t k = i; k < i1; ++k) {
+            const int64_t kb = k / per_seq, ke0 = (k - kb * per_seq) * G::kTok;
+            store_sums<ES>(a, kb, ke0, static_cast<int>(lmin(G::kTok, g.V - ke0)), sums, lane);
         }
+        // Stage s: the phase whose wait gave up (its bit was already flipped).
+        mbar_wait_bounded(&bars[warp][s], ((phases >> s) & 1u) ^ 1u, nullptr);
+        if (i + 1 < i1) mbar_wait_bounded(&bars[warp][s ^ 1], (phases >> (s ^ 1)) & 1u, nullptr);
     }
-    pdl_trigger();  // the finish kernel may start launching
 }
 
-// ---------------------------------------------------------------------------
-// Aligned rows, launch 2 of 2: kFinishSplit CTAs per sequence. Each adds the
-// slice sums into block sums and runs level 1 (the same computation, so the
-// same winning block, in every CTA of the sequence), then races its quarter
-// of the winning block. The last of them to finish (an atomic ticket; no one
-// waits) keeps the best of the quarters, the lowest index on a tie.
-// ---------------------------------------------------------------------------
-template <int ES>
-__global__ void __launch_bounds__(kT) sample_finish_kernel(const SampleArgs a)
+// Level 1 and level 2 of the race run in launch 2, one CTA per sequence: a
+// separate small kernel, so that its code stays warm in the instruction cache
+// and its CTAs, scheduled while the streaming pass still runs, start the
+// moment the block sums are complete.
+constexpr int kRaceThreads = kRaceBlock / 4;  // one four-token group per thread
+constexpr int kRaceWarps = kRaceThreads / 32;
+
+// Best over the CTA (largest score, lowest index); every thread gets it.
+__device__ __forceinline__ Best cta_best(Best b, Best* red)
 {
-    using S = Slices<ES>;
-    constexpr int kQuarter = kRaceBlock / kFinishSplit;
-    using DB = Direct<ES, kT, kRaceBlock>;  // whole blocks (zero-residual fall-back)
-    using DQ = Direct<ES, kT, kQuarter>;    // one quarter of the winning block
-    __shared__ Best red[kWarps];
-    __shared__ float2 red2[kWarps];
-    __shared__ int red_flags[kWarps];
-    __shared__ int s_last;
-    const Geometry& g = a.g;
-    const int64_t b = blockIdx.x / kFinishSplit;
-    const int part = static_cast<int>(blockIdx.x - b * kFinishSplit);
-    pdl_wait();  // the slice sums are complete and visible
-    const SeqRecord rec = a.seqs[b];
-    if (rec.status != 0) return;
-    RowPair rp;
-    row_pair_of(rp, a, rec, b, ES);
-    const int64_t nch = g.nchunks, V = g.V, K1 = g.K + 1;
-    ChunkSum* sums = a.chunk_sums + (b * kFinishSplit + part) * nch;  // this CTA's own copy
-    auto block_len = [&](int64_t blk) {
-        return static_cast<int>(min(static_cast<int64_t>(kRaceBlock), V - blk * kRaceBlock));
-    };
-
-    // Block sums: the slice sums of each block, added in slice order.
-    for (int64_t c = threadIdx.x; c < nch; c += kT) {
-        const float2* sl = a.slice_sums + (b * nch + c) * S::kPerBlock;
-        float hi = 0.f, lo = 0.f;
-        for (int q = 0; q < S::kPerBlock; ++q) {
-            const float2 v = sl[q];
-            float err;
-            const float s2 = two_sum(hi, v.x, &err);
-            lo = __fadd_rn(__fadd_rn(lo, v.y), err);
-            hi = s2;
-        }
-        ChunkSum cs;
-        cs.hi = hi;
-        cs.lo = lo;
-        cs.flags = (hi == hi) ? 0 : kFlagTimeout;  // NaN: a streaming wait gave up
-        cs.pad = 0;
-        sums[c] = cs;
-    }
+    b = warp_best(b);
+    __syncthreads();  // red is free again
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = b;
     __syncthreads();
+    Best t = red[0];
+#pragma unroll
+    for (int i = 1; i < kRaceWarps; ++i) take(t, red[i].score, red[i].idx);
+    return t;
+}
 
-    int flags = 0;
-    int win = race_blocks<kT>(sums, nch, rp, &flags, red, red_flags);
-    if (flags != 0) win = INT_MAX;
-    if (flags == 0 && win == INT_MAX) {
-        // Every residual weight rounded to zero: race p_j instead, block sums first.
-        rp.drow = nullptr;
-        for (int64_t c = 0; c < nch; ++c) {
-            const float2 Wp = DB::block_weight(rp, c * kRaceBlock, block_len(c), red2);
-            if (threadIdx.x == 0) {
-                ChunkSum cs;
-                cs.hi = Wp.x;
-                cs.lo = Wp.y;
-                cs.flags = 0;
-                cs.pad = 0;
-                sums[c] = cs;
-            }
-            __syncthreads();
+// Sum over the CTA in a fixed order; every thread gets it.
+__device__ __forceinline__ float cta_sum(float x, float* red)
+{
+    x = warp_sum(x);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+    __syncthreads();
+    float t = red[0];
+#pragma unroll
+    for (int i = 1; i < kRaceWarps; ++i) t += red[i];
+    return t;
+}
+
+// Launch 2 of 2: the race of sequence blockIdx.x. Level 1: thread t takes the
+// groups of four blocks t, t + kRaceThreads, ... of the block sums (one Philox
+// block per group). Level 2: thread t takes four-token group t of the winning
+// block. Writes out_tokens[b, j].
+template <int ES, bool ALIGNED>
+__global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const SampleArgs a)
+{
+    __shared__ Best red[kRaceWarps];
+    __shared__ float redf[kRaceWarps];
+    __shared__ Best s_fb;
+    const Geometry& g = a.g;
+    const int64_t b = blockIdx.x;
+    const int t = threadIdx.x;
+    pdl_wait();  // the block sums are complete and visible
+    SeqJob sj;
+    const int j = load_seq(sj, a, b, ES);
+    if (!sj.ok) return;  // the scan wrote the outputs of an invalid sequence
+    const int64_t nblk = g.nblocks;
+    const float* W = a.block_sums + b * nblk;
+    const uint2 key = make_uint2(static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
+    const uint32_t seq = static_cast<uint32_t>(b), pos = static_cast<uint32_t>(j);
+
+    Best best{0.0f, INT_MAX};
+    int nan = 0;
+#pragma unroll 1
+    for (int64_t gq = t; 4 * gq < nblk; gq += kRaceThreads) {
+        float w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t c = 4 * gq + q;
+            w[q] = c < nblk ? __ldcg(W + c) : 0.f;
+            nan |= !(w[q] == w[q]);  // a wait of the streaming pass gave up
         }
-        win = race_blocks<kT>(sums, nch, rp, &flags, red, red_flags);
+        race_group(best, w, 4 * gq, make_uint4(pos, seq, 1u + static_cast<uint32_t>(gq), 1u), key);
+    }
+    const bool bad = __syncthreads_or(nan) != 0;
+    Best blk = cta_best(best, red);
+    if (!bad && blk.idx == INT_MAX) {
+        // Every residual weight rounded to zero: race p_j instead (rare; the
+        // target row is read once more, block by block).
+        sj.rp.drow = nullptr;
+        Best fb{0.0f, INT_MAX};
+#pragma unroll 1
+        for (int64_t c = 0; c < nblk; ++c) {
+            const int64_t k0 = c * kRaceBlock + 4 * t;
+            float xt[4], xd[4], w[4];
+            group_load<ES, ALIGNED>(sj.rp, k0, g.V, xt, xd);
+            group_weights(sj.rp, k0, g.V, xt, xd, w);
+            const float sc = cta_sum(((w[0] + w[1]) + w[2]) + w[3], redf);
+            if (t == 0 && sc > 0.f) {
+                const uint4 r = philox4x32_10(
+                    make_uint4(pos, seq, 1u + static_cast<uint32_t>(c >> 2), 1u), key);
+                const uint32_t word = (c & 3) == 0 ? r.x : (c & 3) == 1 ? r.y : (c & 3) == 2 ? r.z : r.w;
+                take(fb, sc / exp_clock(word_to_open_uniform(word)), static_cast<int>(c));
+            }
+        }
+        if (t == 0) s_fb = fb;
+        __syncthreads();
+        blk = s_fb;
     }
     Best tok{0.0f, INT_MAX};
-    if (flags == 0 && win != INT_MAX) {
-        const int64_t q0 = static_cast<int64_t>(win) * kRaceBlock + part * kQuarter;
-        const int nq = static_cast<int>(
-            min(static_cast<int64_t>(kQuarter), static_cast<int64_t>(win) * kRaceBlock +
-                                                    block_len(win) - q0));
-        if (nq > 0) tok = DQ::race(rp, q0, nq, red);
+    if (!bad && blk.idx != INT_MAX) {
+        const int64_t k0 = static_cast<int64_t>(blk.idx) * kRaceBlock + 4 * t;
+        float xt[4], xd[4], w[4];
+        group_load<ES, ALIGNED>(sj.rp, k0, g.V, xt, xd);
+        group_weights(sj.rp, k0, g.V, xt, xd, w);
+        race_group(tok, w, k0, make_uint4(pos, seq, 1u + static_cast<uint32_t>(k0 >> 2), 0u), key);
     }
-
-    if (threadIdx.x == 0) {
-        FinishPart fp;
-        fp.score = tok.score;
-        fp.idx = tok.idx;
-        fp.flags = flags;
-        fp.pad = win == INT_MAX ? 1 : 0;  // level 1 found nothing
-        a.parts[b * kFinishSplit + part] = fp;
-        __threadfence();
-        s_last = atomicAdd(&a.tickets[b], 1u) == static_cast<uint32_t>(kFinishSplit - 1);
-    }
-    __syncthreads();
-    if (!s_last || threadIdx.x != 0) return;
-    __threadfence();
-    const volatile FinishPart* parts = a.parts + b * kFinishSplit;
-    Best best{0.0f, INT_MAX};
-    int any_flags = 0, none = 0;
-    for (int q = 0; q < kFinishSplit; ++q) {
-        take(best, parts[q].score, parts[q].idx);
-        any_flags |= parts[q].flags;
-        none |= parts[q].pad;
-    }
-    if (any_flags != 0 || none != 0 || best.idx == INT_MAX) {
-        for (int64_t i = 0; i < K1; ++i) a.out_tokens[b * K1 + i] = -1;
-        a.num_accepted[b] = -1;
-        if (a.seq_status) a.seq_status[b] = kFlagTimeout;
-    } else {
-        a.out_tokens[b * K1 + rec.j] = best.idx;
+    tok = cta_best(tok, red);
+    const int64_t K1 = g.K + 1;
+    if (bad || tok.idx == INT_MAX) {
+        for (int64_t i = t; i < K1; i += kRaceThreads) a.out_tokens[b * K1 + i] = -1;
+        if (t == 0) {
+            a.num_accepted[b] = -1;
+            if (a.seq_status) a.seq_status[b] = kFlagTimeout;
+        }
+    } else if (t == 0) {
+        a.out_tokens[b * K1 + j] = tok.idx;
     }
 }
 
-template <int ES>
-cudaError_t launch_direct(const SampleArgs& a, cudaStream_t s)
+template <int ES, bool ALIGNED>
+cudaError_t launch_sampler(const SampleArgs& a, cudaStream_t s)
 {
-    const int smem = kWarps * 4 * kSliceBytes;
-    cudaError_t e = cudaFuncSetAttribute(sample_stream_kernel<ES>,
+    const int smem = kWarps * kWarpRing;
+    cudaError_t e = cudaFuncSetAttribute(sample_stream_kernel<ES, ALIGNED>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(a.g.pdl != 0, sample_stream_kernel<ES>, dim3(a.g.sample_grid), dim3(kT),
-                         static_cast<size_t>(smem), s, a);
+    e = launch_dependent(a.g.pdl != 0, sample_stream_kernel<ES, ALIGNED>, dim3(a.g.sample_grid),
+                         dim3(kT), static_cast<size_t>(smem), s, a);
     if (e != cudaSuccess) return e;
-    return launch_dependent(a.g.pdl != 0, sample_finish_kernel<ES>,
-                            dim3(static_cast<unsigned>(a.g.B * kFinishSplit)), dim3(kT), 0, s, a);
+    return launch_dependent(a.g.pdl != 0, sample_race_kernel<ES, ALIGNED>,
+                            dim3(static_cast<unsigned>(a.g.B)), dim3(kRaceThreads), 0, s, a);
 }
 
 }  // namespace
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s)
 {
-    if (a.g.aligned) return a.g.es == 2 ? launch_direct<2>(a, s) : launch_direct<4>(a, s);
-    return a.g.es == 2 ? launch_one<2, true>(a, s) : launch_one<4, true>(a, s);
+    if (a.g.aligned) return a.g.es == 2 ? launch_sampler<2, true>(a, s) : launch_sampler<4, true>(a, s);
+    return a.g.es == 2 ? launch_sampler<2, false>(a, s) : launch_sampler<4, false>(a, s);
 }
 
-int sample_slices_per_block(int es) { return es == 2 ? Slices<2>::kPerBlock : Slices<4>::kPerBlock; }
+int sample_tokens_per_slice(int es) { return es == 2 ? Geo<2>::kTok : Geo<4>::kTok; }
 
-cudaError_t sample_stream_blocks_per_sm(int es, int* blocks)
+cudaError_t sample_blocks_per_sm(int es, int* blocks)
 {
-    const int smem = kWarps * 4 * kSliceBytes;
-    auto* k = es == 2 ? sample_stream_kernel<2> : sample_stream_kernel<4>;
-    const cudaError_t e =
-        cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    const int smem = kWarps * kWarpRing;
+    auto* k = es == 2 ? sample_stream_kernel<2, false> : sample_stream_kernel<4, false>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, k, kT, smem);
+    int b1 = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k, kT, smem);
+    if (e != cudaSuccess) return e;
+    auto* ka = es == 2 ? sample_stream_kernel<2, true> : sample_stream_kernel<4, true>;
+    e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int b2 = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b2, ka, kT, smem);
+    if (e != cudaSuccess) return e;
+    *blocks = b1 < b2 ? b1 : b2;
+    return cudaSuccess;
 }
 
 }  // namespace sv

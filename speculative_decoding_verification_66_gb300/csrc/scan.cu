@@ -19,8 +19,7 @@
 // error, about 1e-6 on the ratio, is far inside the 1e-5 near-tie band. Only
 // the optional diagnostic outputs are widened to double. Everything the
 // sampler needs (the emitted position j and the normalisers of row j) goes to
-// the SeqRecord, and the sampler's ticket counter for the sequence is reset
-// here.
+// the SeqRecord.
 #include <climits>
 
 #include "sv_device.cuh"
@@ -234,7 +233,6 @@ __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs
                 }
             }
             a.seqs[b] = rec;
-            a.tickets[b] = 0u;
         }
     }
 }

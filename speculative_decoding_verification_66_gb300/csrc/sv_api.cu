@@ -22,13 +22,13 @@ struct DeviceCache {
     bool ready = false;
     int sms = 0;
     int blocks[2][2] = {{0, 0}, {0, 0}};  // pass-1 CTAs per SM, [es == 2][mode]
-    int sample_blocks[2] = {0, 0};        // sampler streaming CTAs per SM, [es == 2]
+    int sample_blocks[2] = {0, 0};        // sampler CTAs per SM, [es == 2]
 };
 std::mutex g_mu;
 DeviceCache g_cache[kMaxDevices];
 
-// SM count, resident pass-1 CTAs per SM and resident sampler-streaming CTAs
-// per SM on the current device.
+// SM count, resident pass-1 CTAs per SM and resident sampler CTAs per SM on
+// the current device.
 int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
 {
     int dev = 0;
@@ -43,7 +43,7 @@ int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
                 if (sv::row_stats_blocks_per_sm(e ? 2 : 4, m, &c.blocks[e][m]) != cudaSuccess)
                     return SV_ERR_CUDA;
         for (int e = 0; e < 2; ++e)
-            if (sv::sample_stream_blocks_per_sm(e ? 2 : 4, &c.sample_blocks[e]) != cudaSuccess)
+            if (sv::sample_blocks_per_sm(e ? 2 : 4, &c.sample_blocks[e]) != cudaSuccess)
                 return SV_ERR_CUDA;
         c.ready = true;
     }
@@ -54,8 +54,7 @@ int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
 }
 
 struct Layout {
-    size_t partials = 0, seqs = 0, chunk_sums = 0, slice_sums = 0, parts = 0, tickets = 0,
-           total = 0;
+    size_t partials = 0, seqs = 0, block_sums = 0, total = 0;
 };
 
 int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
@@ -97,10 +96,9 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     g->grid = static_cast<int32_t>(g->tiles < want ? (g->tiles > 0 ? g->tiles : 1) : want);
     const int64_t per_cta = (g->tiles + g->grid - 1) / g->grid;
     g->maxseg = static_cast<int32_t>((per_cta + g->tiles_per_row - 1) / g->tiles_per_row + 1);
-    g->nchunks = (V + sv::kRaceBlock - 1) / sv::kRaceBlock;
-    if (B * g->nchunks >= (int64_t(1) << 31)) return SV_ERR_SIZE;
-    const int64_t spb = sv::sample_slices_per_block(es);
-    const int64_t slices = B * g->nchunks * spb;
+    g->nblocks = (V + sv::kRaceBlock - 1) / sv::kRaceBlock;
+    const int64_t tok = sv::sample_tokens_per_slice(es);
+    const int64_t slices = B * ((V + tok - 1) / tok);  // < 2^62 / 2048: no overflow
     const int64_t warps_per_cta = sv::kSampleThreads / 32;
     const int64_t want_s = static_cast<int64_t>(sms) * sample_blocks;
     const int64_t need_s = (slices + warps_per_cta - 1) / warps_per_cta;
@@ -112,16 +110,8 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
                     sizeof(sv::Partial));
     L->seqs = off;
     off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
-    L->chunk_sums = off;
-    if (mode == SV_SAMPLE)
-        off += round_up(static_cast<size_t>(B * g->nchunks) * sv::kFinishSplit * sizeof(sv::ChunkSum));
-    L->parts = off;
-    if (mode == SV_SAMPLE)
-        off += round_up(static_cast<size_t>(B) * sv::kFinishSplit * sizeof(sv::FinishPart));
-    L->slice_sums = off;
-    if (mode == SV_SAMPLE && g->aligned) off += round_up(static_cast<size_t>(slices) * sizeof(float2));
-    L->tickets = off;
-    off += round_up(static_cast<size_t>(B) * sizeof(uint32_t));
+    L->block_sums = off;
+    if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nblocks) * sizeof(float));
     L->total = off > 0 ? off : kAlign;
     return SV_OK;
 }
@@ -181,16 +171,13 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     const uint8_t* dp = sampling ? static_cast<const uint8_t*>(draft) : nullptr;
     auto* partials = reinterpret_cast<sv::Partial*>(ws + L.partials);
     auto* seqs = reinterpret_cast<sv::SeqRecord*>(ws + L.seqs);
-    auto* chunk_sums = reinterpret_cast<sv::ChunkSum*>(ws + L.chunk_sums);
-    auto* slice_sums = reinterpret_cast<float2*>(ws + L.slice_sums);
-    auto* parts = reinterpret_cast<sv::FinishPart*>(ws + L.parts);
-    auto* tickets = reinterpret_cast<uint32_t*>(ws + L.tickets);
+    auto* block_sums = reinterpret_cast<float*>(ws + L.block_sums);
 
     sv::RowStatsArgs ra{tp, dp, g, c, partials};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
-                    tickets, sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
+                    sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
                     sampling ? log_ratio : nullptr, seq_status};
-    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, chunk_sums, parts, slice_sums, tickets,
+    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, block_sums,
                       out_tokens, num_accepted, seq_status};
 
     if (!record(0)) return SV_ERR_CUDA;

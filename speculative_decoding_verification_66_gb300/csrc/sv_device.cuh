@@ -175,15 +175,19 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+// One wait for phase `parity` of `bar`: the thread may be suspended until the
+// phase completes or about `suspend_ns` nanoseconds have passed (a hint; the
+// hardware wakes the thread when the phase completes, so waiting warps spend
+// no issue slots). True if the phase completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity, uint32_t suspend_ns)
 {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(suspend_ns)
         : "memory");
     return ok != 0;
 }
@@ -192,21 +196,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
 // seconds at 2 GHz). A wait that runs out returns false; the caller records a
 // timeout status and winds down instead of spinning forever.
 constexpr long long kWaitLimitCycles = 4000000000LL;
+// Suspend hint of one try: 1 ms, so the time limit is checked often enough.
+constexpr uint32_t kSuspendHintNs = 1000000u;
 
 // Wait for phase `parity` of `bar`. Gives up when *abort becomes non-zero
 // (another thread of the CTA already gave up) or after kWaitLimitCycles.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
                                                   const volatile int* abort)
 {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity, kSuspendHintNs)) return true;
     const long long t0 = clock64();
-    unsigned backoff = 32;
     for (;;) {
-        // Back off between tries (32 ns doubling to 256 ns) so that waiting
-        // warps leave the issue slots to the warps that have work.
-        __nanosleep(backoff);
-        if (backoff < 256) backoff <<= 1;
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, kSuspendHintNs)) return true;
         if (abort != nullptr && *abort != 0) return false;
         if (clock64() - t0 > kWaitLimitCycles) return false;
     }

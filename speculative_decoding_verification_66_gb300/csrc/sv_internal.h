@@ -21,17 +21,15 @@ constexpr int kRowStages = 4;
 constexpr int kRowConsumerWarps = 8;
 constexpr int kRowThreads = (kRowConsumerWarps + 1) * 32;
 
-// Residual / bonus sampling (pass 3): per sequence, the emitted row pair is cut
-// into the sampler's race blocks of kRaceBlock tokens; one CTA per block. The
-// block length is part of the sampler's definition (it decides which random
-// numbers are drawn), not a tuning knob.
-constexpr int kRaceBlock = 8192;
+// Residual / bonus sampling (pass 3): a two-level exponential race over
+// blocks of kRaceBlock tokens of the emitted row pair. The block length is part
+// of the sampler's definition (it decides which random numbers are drawn), not
+// a tuning knob. The sampler streams the row pairs in slices of kSliceBytes per
+// row, one warp per slice (a slice holds whole race blocks), then races each
+// sequence in a CTA of its own.
+constexpr int kRaceBlock = 512;
 constexpr int kSampleThreads = 256;
-// Aligned rows: the sampler's streaming pass sums the weights of slices of
-// kSliceBytes per row, one warp per slice. Its finish pass splits the race of
-// the winning block over kFinishSplit CTAs per sequence.
 constexpr int kSliceBytes = 2048;
-constexpr int kFinishSplit = 4;
 
 constexpr int kMaxK = 1024;
 
@@ -69,25 +67,6 @@ struct SeqRecord {
 };
 static_assert(sizeof(SeqRecord) == 32, "SeqRecord layout");
 
-// Total sampling weight of one race block as a float pair (flags: kFlagTimeout).
-struct ChunkSum {
-    float hi;
-    float lo;
-    int32_t flags;
-    int32_t pad;
-};
-static_assert(sizeof(ChunkSum) == 16, "ChunkSum layout");
-
-// One finish CTA's best token in its share of the winning block
-// (score 0 / idx 2^31 - 1: none; flags: kFlagTimeout).
-struct FinishPart {
-    float score;
-    int32_t idx;
-    int32_t flags;
-    int32_t pad;
-};
-static_assert(sizeof(FinishPart) == 16, "FinishPart layout");
-
 struct Geometry {
     int64_t B, K, V;
     int32_t es;             // bytes per element (4 or 2)
@@ -100,8 +79,8 @@ struct Geometry {
     int32_t grid;           // pass-1 CTAs
     int32_t maxseg;         // most row segments one pass-1 CTA can touch
     int32_t aligned;        // every row starts on a 16-byte boundary
-    int64_t nchunks;        // race blocks per row
-    int32_t sample_grid;    // CTAs of the sampler's streaming pass (aligned rows)
+    int64_t nblocks;        // race blocks per row
+    int32_t sample_grid;    // CTAs of the sampler
     int32_t pdl;            // chain the kernels with programmatic dependent launch
 };
 
@@ -124,7 +103,6 @@ struct ScanArgs {
     int32_t* out_tokens;
     int32_t* num_accepted;
     SeqRecord* seqs;
-    uint32_t* tickets;
     double* lse_t;          // optional diagnostics
     double* lse_d;
     double* log_ratio;
@@ -138,10 +116,7 @@ struct SampleArgs {
     float c;
     uint64_t seed;
     const SeqRecord* seqs;
-    ChunkSum* chunk_sums;   // [B][kFinishSplit][nchunks] (the staged path uses [B][nchunks])
-    FinishPart* parts;      // [B][kFinishSplit]
-    float2* slice_sums;     // [B][nchunks][slices per block] (aligned rows)
-    uint32_t* tickets;      // [B], zeroed by the scan
+    float* block_sums;      // [B][nblocks]: weight of each race block of the emitted row pair
     int32_t* out_tokens;
     int32_t* num_accepted;
     int32_t* seq_status;    // optional
@@ -174,8 +149,8 @@ cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 
 // Resident pass-1 CTAs per SM for this dtype / mode (occupancy query).
 cudaError_t row_stats_blocks_per_sm(int es, int mode, int* blocks);
-// Resident CTAs per SM of the sampler's streaming pass, and its slices per block.
-cudaError_t sample_stream_blocks_per_sm(int es, int* blocks);
-int sample_slices_per_block(int es);
+// Resident sampler CTAs per SM, and the tokens of one sampler slice.
+cudaError_t sample_blocks_per_sm(int es, int* blocks);
+int sample_tokens_per_slice(int es);
 
 }  // namespace sv
