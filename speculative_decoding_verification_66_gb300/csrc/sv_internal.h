@@ -16,9 +16,9 @@ namespace sv {
 // STAGES-deep ring of shared-memory buffers filled by bulk copies. One warp
 // issues the copies; kRowConsumerWarps warps reduce.
 // ---------------------------------------------------------------------------
-constexpr int kRowTileBytes = 16384;
-constexpr int kRowStages = 4;
-constexpr int kRowConsumerWarps = 8;
+constexpr int kRowTileBytes = 32768;
+constexpr int kRowStages = 3;
+constexpr int kRowConsumerWarps = 16;
 constexpr int kRowThreads = (kRowConsumerWarps + 1) * 32;
 
 // Residual / bonus sampling (pass 3): a two-level exponential race over
