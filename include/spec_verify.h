@@ -219,6 +219,38 @@ int spec_verify_static(const void* target_logits, const void* draft_logits,
                        int32_t* num_accepted, void* stream);
 
 /*
+ * Workspace needed by spec_verify_early_exit for these sizes on the CURRENT
+ * device. Writes the byte count to *bytes. Returns SV_OK or an SV_ERR_* code.
+ */
+int sv_early_exit_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode,
+                                  size_t* bytes);
+
+/*
+ * spec_verify that stops reading a sequence's rows at its first rejection
+ * (Hung-yi Lee, "Introduction to Generative AI 2024 Spring", lecture 16
+ * notes, section on the key engineering optimisations, item 4 "Early Stop":
+ * once a draft is found wrong, the later drafts are not verified). The positions are verified in phases of
+ * 1, 2, 4, ... positions; each phase reads the target and draft rows of its
+ * positions only for the sequences that accepted every earlier draft.
+ *
+ * Arguments, layouts, results and errors are those of spec_verify, with a
+ * workspace of sv_early_exit_workspace_bytes. out_tokens and num_accepted are
+ * the same function of the inputs as spec_verify's, with one exception: rows
+ * after a sequence's emitted position are never read, so a NaN or +inf there
+ * (or a row of only -inf) does not invalidate the sequence. Draft tokens are
+ * all checked. The normalisers of a row are merged in another order than in
+ * spec_verify, so the two can differ on the decisions the near-tie rule
+ * flags (a gap below 1e-5), and only there. Calls make 2 launches per phase
+ * (about log2(K + 1) + 1 phases), a small memset, and in sampling mode the two
+ * sampler launches.
+ */
+int spec_verify_early_exit(const void* target_logits, const void* draft_logits,
+                           const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                           float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                           int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/*
  * The Philox4x32-10 generator the verification kernels draw from, evaluated on
  * the device for caller-chosen counters. The pages have no counterpart to this
  * entry point: it exists so that the device generator can be checked word for

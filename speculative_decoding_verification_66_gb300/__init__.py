@@ -19,9 +19,11 @@ from .api import (  # noqa: F401
     launches,
     spec_verify,
     spec_verify_debug,
+    spec_verify_early_exit,
     spec_verify_host,
     spec_verify_static,
     spec_verify_timed,
+    sv_early_exit_workspace_bytes,
     sv_host_staging_bytes,
     sv_philox,
     sv_workspace_bytes,

@@ -148,6 +148,42 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature: float = 
     return out_tokens, num_accepted
 
 
+def sv_early_exit_workspace_bytes(B: int, K: int, V: int, dtype, mode) -> int:
+    n = ctypes.c_size_t(0)
+    d = dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    _check(_lib.load().sv_early_exit_workspace_bytes(B, K, V, d, mode_code(mode), ctypes.byref(n)),
+           "sv_early_exit_workspace_bytes")
+    return int(n.value)
+
+
+def spec_verify_early_exit(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
+                           seed: int = 0, mode="sample", *, out_tokens=None, num_accepted=None,
+                           workspace=None, stream=None):
+    """spec_verify that reads a sequence's rows only up to its first rejection
+    (phases of 1, 2, 4, ... positions). Same results as spec_verify except
+    that non-finite values in rows after the emitted position go unnoticed."""
+    m = mode_code(mode)
+    B, K, V = _shapes(target_logits, draft_logits, draft_tokens, m)
+    dev = target_logits.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    d = dtype_code(target_logits.dtype)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_early_exit_workspace_bytes(B, K, V, d, m))
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_early_exit(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream)),
+            "spec_verify_early_exit")
+    return out_tokens, num_accepted
+
+
 def spec_verify_debug(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
                       seed: int = 0, mode="sample", *, workspace=None, stream=None) -> dict:
     """spec_verify plus the normalisers, log-ratios and per-sequence status."""

@@ -52,26 +52,45 @@ __device__ __forceinline__ const uint8_t* align_up16(const uint8_t* p)
     return reinterpret_cast<const uint8_t*>((reinterpret_cast<uintptr_t>(p) + 15) & ~uintptr_t(15));
 }
 
-// Walks the tiles of a CTA's range in order, without divisions.
+// Walks the tiles of a CTA's range in order, without divisions per tile.
 struct Cursor {
-    int64_t row;             // row in the concatenated row space
+    int64_t row;             // row in the launch's row space (see RowMap)
     int64_t k;               // tile index within the row
+    int64_t n;               // sequences in the row space
     const uint8_t* rowp;     // first byte of the row
     const uint8_t* tend;     // 16-byte-aligned end of the row's tensor
 };
 
+// Row `row` of the row space [n * nt target rows | n * nd draft rows]: in each
+// part, sequence s of the map contributes its positions p0, p0 + 1, ... in
+// order. With the identity map of the full pass this is the plain
+// concatenation [target rows | draft rows].
 template <int ES>
 __device__ __forceinline__ void cursor_row(Cursor& c, const RowStatsArgs& a, int64_t row)
 {
     const Geometry& g = a.g;
+    const RowMap& m = a.map;
     c.row = row;
     const int64_t row_bytes = g.V * ES;
-    if (row < g.rows_t) {
-        c.rowp = a.target + row * row_bytes;
+    const int64_t nt_rows = c.n * m.nt;
+    if (row >= c.n * (m.nt + m.nd)) {
+        // One past the last row (the cursor steps here after the last tile):
+        // never copied from, and the map has no entry for it.
+        c.rowp = a.target;
+        c.tend = a.target;
+        return;
+    }
+    if (row < nt_rows) {
+        const int64_t sq = row / m.nt, i = m.p0 + (row - sq * m.nt);
+        const int64_t b = m.active != nullptr ? m.active[sq] : sq;
+        c.rowp = a.target + (b * (g.K + 1) + i) * row_bytes;
         c.tend = align_down16(a.target + g.rows_t * row_bytes);
     } else {
-        c.rowp = a.draft + (row - g.rows_t) * row_bytes;
-        c.tend = align_down16(a.draft + (g.rows - g.rows_t) * row_bytes);
+        const int64_t r = row - nt_rows;
+        const int64_t sq = r / m.nd, i = m.p0 + (r - sq * m.nd);
+        const int64_t b = m.active != nullptr ? m.active[sq] : sq;
+        c.rowp = a.draft + (b * g.K + i) * row_bytes;
+        c.tend = align_down16(a.draft + g.B * g.K * row_bytes);
     }
 }
 
@@ -364,8 +383,20 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
 
     const Geometry& g = a.g;
     const int cta = blockIdx.x;
-    const int64_t t_begin = static_cast<int64_t>(cta) * g.tiles / g.grid;
-    const int64_t t_end = static_cast<int64_t>(cta + 1) * g.tiles / g.grid;
+    // Sequences in this launch's row space: all B, or (early exit) those the
+    // previous scan left undecided, known once that scan has finished.
+    int64_t nseq = g.B;
+    if (a.map.count != nullptr) {
+        pdl_wait();
+        nseq = *a.map.count;
+    }
+    const int64_t tiles = map_rows(a.map, nseq) * g.tiles_per_row;
+    // CTAs in use: at most one per tile, so every range below is non-empty
+    // (an early-exit phase can have fewer tiles than the launch has CTAs).
+    const int64_t grid = tiles < g.grid ? tiles : g.grid;
+    if (cta >= grid) return;
+    const int64_t t_begin = static_cast<int64_t>(cta) * tiles / grid;
+    const int64_t t_end = static_cast<int64_t>(cta + 1) * tiles / grid;
     const int64_t ntiles = t_end - t_begin;
     if (ntiles <= 0) return;
     const int warp = threadIdx.x >> 5;
@@ -385,6 +416,7 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
 
     Cursor cur;
     cur.k = t_begin - row_first * g.tiles_per_row;
+    cur.n = nseq;
     cursor_row<ES>(cur, a, row_first);
 
     if (warp == kRowConsumerWarps) {
@@ -507,8 +539,11 @@ cudaError_t launch_one(const RowStatsArgs& a, cudaStream_t s)
     const int smem = kRowStages * kRowTileBytes;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    k<<<a.g.grid, kRowThreads, smem, s>>>(a);
-    return cudaGetLastError();
+    // The first pass of a call starts in plain stream order; an early-exit
+    // phase after the first is chained to the scan it reads the list of.
+    const bool pdl = a.g.pdl != 0 && a.map.count != nullptr;
+    return launch_dependent(pdl, k, dim3(static_cast<unsigned>(a.g.grid)), dim3(kRowThreads),
+                            static_cast<size_t>(smem), s, a);
 }
 
 template <int ES, int MODE>

@@ -31,9 +31,16 @@ namespace {
 constexpr int kScanMaxThreads = 1024;  // a warp per row, up to 32 rows per round
 constexpr double kLn2 = 0.69314718055994530942;
 
-__device__ __forceinline__ int cta_of_tile(int64_t t, const Geometry& g)
+// CTAs pass 1 used: at most one per tile (every range non-empty).
+__device__ __forceinline__ int64_t used_grid(int64_t tiles, const Geometry& g)
 {
-    return static_cast<int>(((t + 1) * g.grid - 1) / g.tiles);
+    return tiles < g.grid ? tiles : g.grid;
+}
+
+// The pass-1 CTA whose tile range [c T / G, (c + 1) T / G) holds tile t.
+__device__ __forceinline__ int cta_of_tile(int64_t t, int64_t tiles, const Geometry& g)
+{
+    return static_cast<int>(((t + 1) * used_grid(tiles, g) - 1) / tiles);
 }
 
 // Merge the partials of one row, one warp per row: lane l takes partials
@@ -46,13 +53,13 @@ struct RowNorm {
     float l;
 };
 
-__device__ void merge_row(const ScanArgs& a, int64_t row, int lane, RowNorm* norm, int* argmax,
-                          int* flags)
+__device__ void merge_row(const ScanArgs& a, int64_t row, int64_t tiles, int lane, RowNorm* norm,
+                          int* argmax, int* flags)
 {
     const Geometry& g = a.g;
     const int64_t t0 = row * g.tiles_per_row;
-    const int c0 = cta_of_tile(t0, g);
-    const int c1 = cta_of_tile(t0 + g.tiles_per_row - 1, g);
+    const int c0 = cta_of_tile(t0, tiles, g);
+    const int c1 = cta_of_tile(t0 + g.tiles_per_row - 1, tiles, g);
     const int n = (c1 - c0 + 1) * kRowConsumerWarps;
     int fl = 0;
     float M = __uint_as_float(kF32NegInfBits), hi = 0.f, lo = 0.f;
@@ -61,7 +68,7 @@ __device__ void merge_row(const ScanArgs& a, int64_t row, int lane, RowNorm* nor
     for (int q = lane; q < n; q += 32) {
         const int c = c0 + q / kRowConsumerWarps;
         const int w = q % kRowConsumerWarps;
-        const int64_t first = (static_cast<int64_t>(c) * g.tiles / g.grid) / g.tiles_per_row;
+        const int64_t first = (static_cast<int64_t>(c) * tiles / used_grid(tiles, g)) / g.tiles_per_row;
         const Partial p =
             a.partials[(static_cast<int64_t>(c) * g.maxseg + (row - first)) * kRowConsumerWarps + w];
         fl |= p.flags;
@@ -112,51 +119,116 @@ __device__ __forceinline__ float load_logit(const uint8_t* p)
     return ES == 2 ? load_logit_bf16(p) : load_logit_f32(p);
 }
 
+// Compaction for early exit, run by the last CTA of the launch: the listed
+// sequences whose `still` flag is set, in list order (a block-wide prefix sum
+// in fixed order, so the next list is the same on every run).
+__device__ void compact_still(const ScanArgs& a, int64_t nseq)
+{
+    __shared__ int warp_tot[32];
+    __shared__ int s_carry;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    if (threadIdx.x == 0) s_carry = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < nseq; base += blockDim.x) {
+        const int64_t sq = base + threadIdx.x;
+        const int f = sq < nseq ? __ldcg(a.still + sq) : 0;
+        int incl = f;  // inclusive scan within the warp
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        if (lane == 31) warp_tot[warp] = incl;
+        __syncthreads();
+        int before = s_carry;
+        for (int w = 0; w < warp; ++w) before += warp_tot[w];
+        if (f) {
+            const int32_t id = a.map.active != nullptr ? a.map.active[sq] : static_cast<int32_t>(sq);
+            a.next_active[before + incl - 1] = id;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            int t = 0;
+            for (int w = 0; w < nwarps; ++w) t += warp_tot[w];
+            s_carry += t;
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) *a.next_count = s_carry;
+}
+
+// One CTA per listed sequence (the full pass lists every sequence). The phase
+// covers positions [p0, p0 + npos) that carry a draft token, npos =
+// min(nt, K - p0), and the bonus row K when p0 + nt = K + 1. The CTA merges
+// the phase's rows, takes the phase's decisions, and then either decides the
+// sequence (first rejection at j in the phase, or the bonus after K
+// acceptances) or leaves it undecided for the next phase.
 template <int ES>
 __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs a)
 {
-    // Dynamic shared memory: [2K+1] row normalisers (sampling) or argmaxes
-    // (greedy, in .m), then the K draft tokens and their target / draft logits.
+    // Dynamic shared memory: [nt + nd] row normalisers (sampling) or argmaxes
+    // (greedy, in .m), then the phase's draft tokens and their target / draft
+    // logits.
     extern __shared__ __align__(16) unsigned char smem_raw[];
     __shared__ int s_status;
     __shared__ int s_j;
+    __shared__ int s_last;
     const Geometry& g = a.g;
-    const int64_t b = blockIdx.x;
+    const RowMap& m = a.map;
+    const bool phased = m.count != nullptr;
+    int64_t nseq = g.B;
+    if (phased) {
+        pdl_wait();  // the previous scan's list, and this phase's pass 1, are complete
+        nseq = *m.count;
+    }
+    const int64_t sq = blockIdx.x;
+    if (sq >= nseq) return;
+    const int64_t b = m.active != nullptr ? m.active[sq] : sq;
     const int64_t K = g.K, V = g.V;
     const bool sampling = g.mode == 0;
-    const int64_t nrows = sampling ? 2 * K + 1 : K + 1;
+    const int p0 = m.p0;
+    const int npos = static_cast<int>(min(static_cast<int64_t>(m.nt), K - p0));
+    const bool has_bonus = p0 + m.nt == K + 1;
+    const int nrows = m.nt + m.nd;
     RowNorm* sh = reinterpret_cast<RowNorm*>(smem_raw);
-    int32_t* sx = reinterpret_cast<int32_t*>(sh + (2 * K + 1));
-    float* stx = reinterpret_cast<float*>(sx + K);
-    float* sdx = stx + K;
+    int32_t* sx = reinterpret_cast<int32_t*>(sh + nrows);
+    float* stx = reinterpret_cast<float*>(sx + npos);
+    float* sdx = stx + npos;
     if (threadIdx.x == 0) {
         s_status = 0;
-        s_j = static_cast<int>(K);
+        s_j = p0 + npos;  // no rejection among the phase's positions
     }
     __syncthreads();
 
     // Inputs only (complete before pass 1 started): the draft tokens and the
-    // logits they select. This overlaps the tail of pass 1.
-    for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+    // logits they select. In the full pass this overlaps the tail of pass 1.
+    // Every token is checked once, in the phase that starts at position 0.
+    if (p0 == 0)
+        for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
+            const int32_t x = a.tokens[b * K + i];
+            if (x < 0 || static_cast<int64_t>(x) >= V) atomicOr(&s_status, kFlagBadToken);
+        }
+    for (int q = threadIdx.x; q < npos; q += blockDim.x) {
+        const int64_t i = p0 + q;
         const int32_t x = a.tokens[b * K + i];
-        sx[i] = x;
-        if (x < 0 || static_cast<int64_t>(x) >= V) {
-            atomicOr(&s_status, kFlagBadToken);
-        } else if (sampling) {
-            stx[i] = load_logit<ES>(a.target + ((b * (K + 1) + i) * V + x) * ES);
-            sdx[i] = load_logit<ES>(a.draft + ((b * K + i) * V + x) * ES);
+        sx[q] = x;
+        if (x >= 0 && static_cast<int64_t>(x) < V && sampling) {
+            stx[q] = load_logit<ES>(a.target + ((b * (K + 1) + i) * V + x) * ES);
+            sdx[q] = load_logit<ES>(a.draft + ((b * K + i) * V + x) * ES);
         }
     }
-    pdl_trigger();  // the sampler's first kernel may start launching
-    pdl_wait();     // pass 1 has finished and its partials are visible
+    pdl_trigger();  // the next kernel may start launching
+    if (!phased) pdl_wait();  // pass 1 has finished and its partials are visible
     __syncthreads();
 
+    const int64_t tiles = map_rows(m, nseq) * g.tiles_per_row;
     const int lane = threadIdx.x & 31;
-    for (int64_t q = threadIdx.x >> 5; q < nrows; q += blockDim.x >> 5) {
-        const int64_t row = q <= K ? b * (K + 1) + q : g.rows_t + b * K + (q - K - 1);
+    for (int q = threadIdx.x >> 5; q < nrows; q += blockDim.x >> 5) {
+        const int64_t row = q < m.nt ? sq * m.nt + q : nseq * m.nt + sq * m.nd + (q - m.nt);
         RowNorm nm{0.f, 0.f};
         int am = 0, fl = 0;
-        merge_row(a, row, lane, &nm, &am, &fl);
+        merge_row(a, row, tiles, lane, &nm, &am, &fl);
         if (lane == 0) {
             if (!sampling) nm.m = __int_as_float(am);
             sh[q] = nm;
@@ -166,15 +238,16 @@ __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs
     __syncthreads();
 
     if (s_status == 0) {
-        for (int64_t i = threadIdx.x; i < K; i += blockDim.x) {
-            const int32_t x = sx[i];
+        for (int q = threadIdx.x; q < npos; q += blockDim.x) {
+            const int32_t x = sx[q];
+            const int64_t i = p0 + q;
             bool reject;
             if (sampling) {
-                const RowNorm nt = sh[i], nd = sh[K + 1 + i];
+                const RowNorm nt = sh[q], nd = sh[m.nt + q];
                 // log2 p_i(x) and log2 q_i(x): the fma is exact before its one
                 // rounding, and the normaliser's parts enter separately.
-                const float lp2 = fmaf(stx[i], a.c, -nt.m) - nt.l;
-                const float lq2 = fmaf(sdx[i], a.c, -nd.m) - nd.l;
+                const float lp2 = fmaf(stx[q], a.c, -nt.m) - nt.l;
+                const float lq2 = fmaf(sdx[q], a.c, -nd.m) - nd.l;
                 const float lr2 = lp2 - lq2;
                 if (a.log_ratio) a.log_ratio[b * K + i] = static_cast<double>(lr2) * kLn2;
                 const float r = lr2 >= 0.f ? 1.f : ex2(lr2);
@@ -182,7 +255,7 @@ __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs
                     verify_random_words(a.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i)).x);
                 reject = !(u < r);
             } else {
-                reject = __float_as_int(sh[i].m) != x;
+                reject = __float_as_int(sh[q].m) != x;
             }
             if (reject) atomicMin(&s_j, static_cast<int>(i));
         }
@@ -191,59 +264,75 @@ __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs
 
     const int status = s_status;
     const int j = s_j;
-    if (sampling) {
-        for (int64_t q = threadIdx.x; q <= K; q += blockDim.x)
+    const bool decided = status != 0 || j < p0 + npos || has_bonus;
+    if (sampling && !phased) {
+        for (int q = threadIdx.x; q < m.nt; q += blockDim.x)
             if (a.lse_t)
                 a.lse_t[b * (K + 1) + q] =
                     (static_cast<double>(sh[q].m) + static_cast<double>(sh[q].l)) * kLn2;
-        for (int64_t q = threadIdx.x; q < K; q += blockDim.x)
+        for (int q = threadIdx.x; q < m.nd; q += blockDim.x)
             if (a.lse_d)
-                a.lse_d[b * K + q] = (static_cast<double>(sh[K + 1 + q].m) +
-                                      static_cast<double>(sh[K + 1 + q].l)) *
+                a.lse_d[b * K + q] = (static_cast<double>(sh[m.nt + q].m) +
+                                      static_cast<double>(sh[m.nt + q].l)) *
                                      kLn2;
     }
     int32_t* out = a.out_tokens + b * (K + 1);
     if (status != 0) {
         for (int64_t i = threadIdx.x; i <= K; i += blockDim.x) out[i] = -1;
     } else {
-        for (int64_t i = threadIdx.x; i <= K; i += blockDim.x) {
-            if (i < j)
-                out[i] = sx[i];
-            else if (i > j)
+        // Positions of this phase up to j keep their drafts; after a
+        // decision every later position is padding.
+        for (int64_t i = p0 + threadIdx.x; i <= K; i += blockDim.x) {
+            if (i < j && i < p0 + npos)
+                out[i] = sx[i - p0];
+            else if (decided && i > j)
                 out[i] = -1;
-            else if (!sampling)
-                out[i] = __float_as_int(sh[i].m);
+            else if (decided && i == j && !sampling)
+                out[i] = __float_as_int(sh[j - p0].m);
         }
     }
     if (threadIdx.x == 0) {
-        a.num_accepted[b] = status != 0 ? -1 : j;
-        if (a.seq_status) a.seq_status[b] = status;
-        if (sampling) {
-            SeqRecord rec;
-            rec.j = j;
-            rec.status = status;
-            rec.mt = rec.lt = rec.md = rec.ld = 0.f;
-            rec.pad[0] = rec.pad[1] = 0;
-            if (status == 0) {
-                rec.mt = sh[j].m;
-                rec.lt = sh[j].l;
-                if (j < K) {
-                    rec.md = sh[K + 1 + j].m;
-                    rec.ld = sh[K + 1 + j].l;
+        if (decided) {
+            a.num_accepted[b] = status != 0 ? -1 : j;
+            if (a.seq_status) a.seq_status[b] = status;
+            if (sampling) {
+                SeqRecord rec;
+                rec.j = j;
+                rec.status = status;
+                rec.mt = rec.lt = rec.md = rec.ld = 0.f;
+                rec.pad[0] = rec.pad[1] = 0;
+                if (status == 0) {
+                    rec.mt = sh[j - p0].m;
+                    rec.lt = sh[j - p0].l;
+                    if (j < K) {
+                        rec.md = sh[m.nt + j - p0].m;
+                        rec.ld = sh[m.nt + j - p0].l;
+                    }
                 }
+                a.seqs[b] = rec;
             }
-            a.seqs[b] = rec;
+        }
+        if (a.next_active != nullptr) {
+            a.still[sq] = decided ? 0 : 1;
+            __threadfence();  // the flag before the ticket
+            s_last = atomicAdd(a.ticket, 1u) == static_cast<uint32_t>(nseq - 1);
         }
     }
+    if (a.next_active == nullptr) return;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();  // every other CTA's flag after the ticket
+    compact_still(a, nseq);
 }
 
 }  // namespace
 
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s)
 {
-    const size_t smem = sizeof(RowNorm) * static_cast<size_t>(2 * a.g.K + 1) + 12 * static_cast<size_t>(a.g.K);
-    const int64_t rows = a.g.mode == 0 ? 2 * a.g.K + 1 : a.g.K + 1;
-    const int warps = static_cast<int>(rows < 2 ? 2 : (rows > 32 ? 32 : rows));
+    const int64_t nrows = a.map.nt + a.map.nd;
+    const int64_t npos = a.map.nt < a.g.K - a.map.p0 ? a.map.nt : a.g.K - a.map.p0;
+    const size_t smem = sizeof(RowNorm) * static_cast<size_t>(nrows) + 12 * static_cast<size_t>(npos);
+    const int warps = static_cast<int>(nrows < 2 ? 2 : (nrows > 32 ? 32 : nrows));
     const dim3 grid(static_cast<unsigned>(a.g.B)), block(32 * warps);
     return a.g.es == 2 ? launch_dependent(a.g.pdl != 0, scan_kernel<2>, grid, block, smem, s, a)
                        : launch_dependent(a.g.pdl != 0, scan_kernel<4>, grid, block, smem, s, a);

@@ -55,7 +55,32 @@ int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
 
 struct Layout {
     size_t partials = 0, seqs = 0, block_sums = 0, total = 0;
+    // Early exit only.
+    size_t still = 0, lists = 0, counters = 0, counter_bytes = 0;
 };
+
+// Early exit: the positions 0 .. K are verified in phases of 1, 2, 4, ...
+// positions; phase k covers target rows [p0, p0 + nt) and draft rows
+// [p0, p0 + nd) of the sequences still undecided after phase k - 1.
+struct Phase {
+    int32_t p0, nt, nd;
+};
+constexpr int kMaxPhases = 16;  // K <= 1024 needs at most 11
+
+int plan_phases(int64_t K, bool sampling, Phase* ph)
+{
+    int n = 0;
+    int64_t p0 = 0, len = 1;
+    while (p0 <= K) {
+        const int64_t nt = len < K + 1 - p0 ? len : K + 1 - p0;
+        int64_t nd = 0;
+        if (sampling) nd = len < K - p0 ? len : (K - p0 > 0 ? K - p0 : 0);
+        ph[n++] = Phase{static_cast<int32_t>(p0), static_cast<int32_t>(nt), static_cast<int32_t>(nd)};
+        p0 += len;
+        len *= 2;
+    }
+    return n;
+}
 
 int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
 {
@@ -70,7 +95,8 @@ int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
     return SV_OK;
 }
 
-int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g, Layout* L)
+int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g, Layout* L,
+              bool early_exit = false)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -92,6 +118,16 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     g->tile_elems = (g->aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
     g->tiles_per_row = (V + g->tile_elems - 1) / g->tile_elems;
     g->tiles = g->rows * g->tiles_per_row;
+    if (early_exit) {
+        // The grid and the partials serve every phase: size them for the
+        // phase with the most rows per sequence, as if all B took part.
+        Phase ph[kMaxPhases];
+        const int nph = plan_phases(K, mode == SV_SAMPLE, ph);
+        int64_t most = 0;
+        for (int k = 0; k < nph; ++k)
+            most = ph[k].nt + ph[k].nd > most ? ph[k].nt + ph[k].nd : most;
+        g->tiles = B * most * g->tiles_per_row;
+    }
     const int64_t want = static_cast<int64_t>(sms) * blocks;
     g->grid = static_cast<int32_t>(g->tiles < want ? (g->tiles > 0 ? g->tiles : 1) : want);
     const int64_t per_cta = (g->tiles + g->grid - 1) / g->grid;
@@ -112,6 +148,15 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
     L->block_sums = off;
     if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nblocks) * sizeof(float));
+    if (early_exit) {
+        L->still = off;
+        off += round_up(static_cast<size_t>(B) * sizeof(int32_t));
+        L->lists = off;
+        off += round_up(2 * static_cast<size_t>(B) * sizeof(int32_t));
+        L->counters = off;  // per phase: the next count, then the ticket
+        L->counter_bytes = 2 * kMaxPhases * sizeof(int32_t);
+        off += round_up(L->counter_bytes);
+    }
     L->total = off > 0 ? off : kAlign;
     return SV_OK;
 }
@@ -122,7 +167,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         int64_t V, int dtype, float temperature, uint64_t seed, int mode, int32_t* out_tokens,
         int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
         double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
-        void* const* events, int n_events)
+        void* const* events, int n_events, bool early_exit = false)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -159,7 +204,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
 
     Geometry g;
     Layout L;
-    rc = make_plan(B, K, V, dtype, mode, &g, &L);
+    rc = make_plan(B, K, V, dtype, mode, &g, &L, early_exit);
     if (rc != SV_OK) return rc;
     if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
     // Events between the kernels would sit between programmatically chained
@@ -173,12 +218,44 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     auto* seqs = reinterpret_cast<sv::SeqRecord*>(ws + L.seqs);
     auto* block_sums = reinterpret_cast<float*>(ws + L.block_sums);
 
-    sv::RowStatsArgs ra{tp, dp, g, c, partials};
+    const sv::RowMap full{nullptr, nullptr, 0, static_cast<int32_t>(K + 1),
+                          static_cast<int32_t>(sampling ? K : 0)};
+    sv::RowStatsArgs ra{tp, dp, g, c, partials, full};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
-                    sampling ? log_ratio : nullptr, seq_status};
+                    sampling ? log_ratio : nullptr, seq_status, full,
+                    nullptr, nullptr, nullptr, nullptr};
     sv::SampleArgs pa{tp, dp, g, c, seed, seqs, block_sums,
                       out_tokens, num_accepted, seq_status};
+
+    if (early_exit) {
+        // Phases over the positions; each pass 1 reads only the rows of the
+        // sequences the previous scan left undecided.
+        auto* still = reinterpret_cast<int32_t*>(ws + L.still);
+        auto* lists = reinterpret_cast<int32_t*>(ws + L.lists);
+        auto* counters = reinterpret_cast<int32_t*>(ws + L.counters);
+        if (cudaMemsetAsync(counters, 0, L.counter_bytes, s) != cudaSuccess) return SV_ERR_CUDA;
+        Phase ph[kMaxPhases];
+        const int nph = plan_phases(K, sampling, ph);
+        for (int k = 0; k < nph; ++k) {
+            sv::RowMap mp{nullptr, nullptr, ph[k].p0, ph[k].nt, ph[k].nd};
+            if (k > 0) {
+                mp.active = lists + ((k - 1) & 1) * B;
+                mp.count = counters + (k - 1);
+            }
+            ra.map = mp;
+            sa.map = mp;
+            const bool last = k == nph - 1;
+            sa.still = last ? nullptr : still;
+            sa.next_active = last ? nullptr : lists + (k & 1) * B;
+            sa.next_count = last ? nullptr : counters + k;
+            sa.ticket = last ? nullptr : reinterpret_cast<uint32_t*>(counters + kMaxPhases + k);
+            if (sv::launch_row_stats(ra, s) != cudaSuccess) return SV_ERR_CUDA;
+            if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
+        }
+        if (sampling && sv::launch_sample(pa, s) != cudaSuccess) return SV_ERR_CUDA;
+        return SV_OK;
+    }
 
     if (!record(0)) return SV_ERR_CUDA;
     if (sv::launch_row_stats(ra, s) != cudaSuccess) return SV_ERR_CUDA;
@@ -250,6 +327,29 @@ SV_EXPORT int spec_verify(const void* target_logits, const void* draft_logits,
     return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
                out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
                nullptr, nullptr, nullptr, 0);
+}
+
+SV_EXPORT int sv_early_exit_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode,
+                                            size_t* bytes)
+{
+    if (bytes == nullptr) return SV_ERR_ARG;
+    Geometry g;
+    Layout L;
+    const int rc = make_plan(B, K, V, dtype, mode, &g, &L, true);
+    if (rc != SV_OK) return rc;
+    *bytes = L.total;
+    return SV_OK;
+}
+
+SV_EXPORT int spec_verify_early_exit(const void* target_logits, const void* draft_logits,
+                                     const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                                     int dtype, float temperature, uint64_t seed, int mode,
+                                     int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                     size_t workspace_bytes, void* stream)
+{
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr, nullptr, nullptr, 0, true);
 }
 
 SV_EXPORT int spec_verify_debug(const void* target_logits, const void* draft_logits,
@@ -345,4 +445,4 @@ SV_EXPORT const char* sv_error_string(int code)
     }
 }
 
-SV_EXPORT int sv_version(void) { return 101; }
+SV_EXPORT int sv_version(void) { return 102; }

@@ -84,12 +84,32 @@ struct Geometry {
     int32_t pdl;            // chain the kernels with programmatic dependent launch
 };
 
+// The rows one pass-1 launch and its scan cover. The full pass: every row of
+// every sequence (active == nullptr, count == nullptr, p0 = 0, nt = K + 1,
+// nd = K or 0 in greedy mode). Early exit: the rows of positions
+// [p0, p0 + nt) (target) and [p0, p0 + nd) (draft) of the sequences still
+// undecided, listed in ascending order by the previous scan. The row space is
+// [n * nt target rows | n * nd draft rows], sequence-major within each part.
+struct RowMap {
+    const int32_t* active;  // sequence ids of the phase; nullptr = 0 .. B - 1
+    const int32_t* count;   // how many (device memory); nullptr = B
+    int32_t p0;             // first position of the phase
+    int32_t nt;             // target rows per sequence in the phase
+    int32_t nd;             // draft rows per sequence in the phase
+};
+
+__host__ __device__ __forceinline__ int64_t map_rows(const RowMap& m, int64_t n)
+{
+    return n * (m.nt + m.nd);
+}
+
 struct RowStatsArgs {
     const uint8_t* target;
     const uint8_t* draft;
     Geometry g;
     float c;                // log2(e) / T
     Partial* partials;      // [grid][maxseg][kRowConsumerWarps]
+    RowMap map;
 };
 
 struct ScanArgs {
@@ -103,10 +123,17 @@ struct ScanArgs {
     int32_t* out_tokens;
     int32_t* num_accepted;
     SeqRecord* seqs;
-    double* lse_t;          // optional diagnostics
+    double* lse_t;          // optional diagnostics (full pass only)
     double* lse_d;
     double* log_ratio;
     int32_t* seq_status;
+    RowMap map;
+    // Early exit only (nullptr otherwise): the sequences still undecided after
+    // this phase, compacted in ascending order by the last CTA to finish.
+    int32_t* still;         // [B] per listed sequence: 1 if still undecided
+    int32_t* next_active;   // [B]
+    int32_t* next_count;    // [1]
+    uint32_t* ticket;       // [1], zero before the launch
 };
 
 struct SampleArgs {

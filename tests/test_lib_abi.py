@@ -34,7 +34,8 @@ def lib():
 def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "sv_workspace_bytes", "spec_verify", "spec_verify_debug", "spec_verify_timed",
-        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static", "sv_philox",
+        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static",
+        "sv_early_exit_workspace_bytes", "spec_verify_early_exit", "sv_philox",
         "sv_error_string",
         "sv_version"])
 
@@ -69,7 +70,7 @@ def test_error_strings_and_version(lib):
                  SV_ERR_SIZE, 12345):
         s = lib.sv_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
-    assert lib.sv_version() == 101
+    assert lib.sv_version() == 102
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails before any device work
@@ -112,6 +113,26 @@ def call(lib, B=2, K=3, V=64, dtype=1, T=1.0, mode=0, target=FAKE, draft=FAKE, t
 ])
 def test_host_side_validation(lib, kw, code):
     assert call(lib, **kw) == code
+
+
+def call_ee(lib, B=2, K=3, V=64, dtype=1, T=1.0, mode=0, target=FAKE, draft=FAKE, tokens=FAKE,
+            out=FAKE, nacc=FAKE, ws=FAKE, ws_bytes=1 << 20):
+    return lib.spec_verify_early_exit(target, draft, tokens, B, K, V, dtype, T, 7, mode, out, nacc,
+                                      ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(B=0), SV_OK),
+    (dict(dtype=7), SV_ERR_DTYPE),
+    (dict(T=0.0), SV_ERR_ARG),
+    (dict(K=1025), SV_ERR_SIZE),
+    (dict(target=None), SV_ERR_ARG),
+    (dict(draft=FAKE + 8), SV_ERR_ALIGN),
+    (dict(ws=None), SV_ERR_WORKSPACE),
+])
+def test_early_exit_host_side_validation(lib, kw, code):
+    """The early-exit entry shares spec_verify's checks, all before any CUDA call."""
+    assert call_ee(lib, **kw) == code
 
 
 def test_greedy_ignores_temperature_and_draft(lib):
