@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="wall-clock budget of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--early-exit-steps", type=int, default=1000,
+                   help="timed calls of spec_verify_early_exit reported beside the full pass "
+                        "(0: skip)")
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="threads for the CPU baseline (0: every core this process may use)")
     return p.parse_args()
@@ -205,6 +208,34 @@ def reference_arm(args, wl):
     print(json.dumps(line), flush=True)
 
 
+def early_exit_bytes(nacc, K: int, V: int, es: int, mode: str):
+    """Logit bytes spec_verify_early_exit reads for these outcomes, and the
+    ideal (rows up to each emitted position only). Its phases cover positions
+    [0, 1), [1, 3), [3, 7), ... (lengths 1, 2, 4, ...); a sequence decided at
+    position j takes part in every phase that starts at or before j. Sampling
+    adds the re-read of the emitted row pair."""
+    sampling = mode == "sample"
+    phases, p0, ln = [], 0, 1
+    while p0 <= K:
+        nt = min(ln, K + 1 - p0)
+        nd = max(0, min(ln, K - p0)) if sampling else 0
+        phases.append((p0, nt, nd))
+        p0 += ln
+        ln *= 2
+    read = ideal = 0
+    for j in nacc:
+        if j < 0:  # invalid: the first phase read its rows, then it stopped
+            read += phases[0][1] + phases[0][2]
+            continue
+        read += sum(nt + nd for p0, nt, nd in phases if p0 <= j)
+        ideal += (j + 1) + (min(j + 1, K) if sampling else 0)
+        if sampling:
+            again = 2 if j < K else 1
+            read += again
+            ideal += again
+    return read * V * es, ideal * V * es
+
+
 def max_over_ranks(x: float, dist=None) -> float:
     """The slowest rank's time: every rank's timed region is bracketed by
     barriers, and the job is done when the last rank is."""
@@ -327,6 +358,41 @@ def main():
     step_gbs = mean_bytes / (ms_per_step / 1e3) / 1e9
     pass1_gbs = pass1_bytes / (pass1_ms / 1e3) / 1e9
 
+    # The early-exit entry on the same inputs (a variant, reported beside the
+    # full pass): same outputs, fewer rows read.
+    early = None
+    if args.early_exit_steps > 0:
+        ws_ee = torch.empty(sv.sv_early_exit_workspace_bytes(B, K, V, copies[0]["target"].dtype,
+                                                             mode), dtype=torch.uint8, device=dev)
+
+        def ee_step(i):
+            c = i & 1
+            inp = copies[c]
+            sv.spec_verify_early_exit(inp["target"], inp["draft"], inp["tokens"], wl.temperature,
+                                      seeds[c], mode, out_tokens=out, num_accepted=nacc,
+                                      workspace=ws_ee, stream=stream)
+
+        ee_bytes = []
+        for c in range(2):
+            ee_step(c)
+            ee_bytes.append(early_exit_bytes(nacc.cpu().tolist(), K, V, es, mode))
+        for i in range(3):
+            ee_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.early_exit_steps):
+            ee_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ee_ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.early_exit_steps
+        read = sum(ee_bytes[i & 1][0] for i in range(2)) / 2
+        ideal = sum(ee_bytes[i & 1][1] for i in range(2)) / 2
+        early = {"value": job_throughput(world, B, 1, ee_ms / 1e3), "unit": "seqs/s",
+                 "ms_per_step": ee_ms, "steps": args.early_exit_steps,
+                 "bytes_read_per_step": read, "bytes_ideal_per_step": ideal,
+                 "hbm_gbs": read / (ee_ms / 1e3) / 1e9}
+
     # End to end through the host entry point: pinned host inputs, copies inside.
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
     h = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in c.items()}
@@ -376,6 +442,8 @@ def main():
         "clocks": clocks.summary(),
         "gpu_launches": sv.launches(mode, V, copies[0]["target"].dtype) * args.steps,
     }
+    if early is not None:
+        line["early_exit"] = early
     if world == 1 and not args.no_cpu_baseline:
         def host_fn(n):
             sub = {k: (v[:n] if v is not None else None) for k, v in copies[0].items()}
