@@ -251,6 +251,43 @@ int spec_verify_early_exit(const void* target_logits, const void* draft_logits,
                            void* stream);
 
 /*
+ * Workspace needed by spec_verify_sharded for these sizes on the CURRENT
+ * device (Vs = columns per shard, G shards). Writes the byte count to *bytes.
+ */
+int sv_sharded_workspace_bytes(int64_t B, int64_t K, int64_t Vs, int G, int dtype, int mode,
+                               size_t* bytes);
+
+/*
+ * spec_verify on logits split over the vocabulary, as a tensor-parallel LM
+ * head leaves them: shard g holds the columns [g Vs, (g + 1) Vs) of every
+ * row. The pages have no counterpart to this entry point; it computes what
+ * spec_verify computes on the concatenated logits (the same method, same
+ * tokens and counts, same random numbers), on one GPU, without the caller
+ * concatenating them. Pass 1 reduces each shard's part of every row, the scan
+ * merges the shards' partial normalisers (the exchange a multi-GPU version
+ * would make with an allreduce), and the emitted row pair of each sequence is
+ * gathered from the shards for the sampler.
+ *   target_shards  HOST array of G device pointers, shard g: [B, K+1, Vs] of
+ *                  `dtype`, 16-byte aligned.
+ *   draft_shards   HOST array of G device pointers, shard g: [B, K, Vs]; may
+ *                  be NULL when mode == SV_GREEDY or K == 0.
+ *   G              1 .. 16.
+ *   Vs             columns per shard; V = G Vs, with V < 2^31 (and, for
+ *                  G > 1, V at most 65535 * 2048 bf16 or 65535 * 1024 fp32
+ *                  columns).
+ * Other arguments, outputs and errors as spec_verify; the workspace is
+ * sv_sharded_workspace_bytes (for G > 1 in sampling mode it includes a
+ * [B][2][V] buffer for the gathered row pairs). The normalisers are merged
+ * shard by shard, in another order than spec_verify's, so the two can differ
+ * only on decisions the near-tie rule flags.
+ */
+int spec_verify_sharded(const void* const* target_shards, const void* const* draft_shards, int G,
+                        const int32_t* draft_tokens, int64_t B, int64_t K, int64_t Vs, int dtype,
+                        float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                        int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
  * The Philox4x32-10 generator the verification kernels draw from, evaluated on
  * the device for caller-chosen counters. The pages have no counterpart to this
  * entry point: it exists so that the device generator can be checked word for

@@ -21,10 +21,12 @@ from .api import (  # noqa: F401
     spec_verify_debug,
     spec_verify_early_exit,
     spec_verify_host,
+    spec_verify_sharded,
     spec_verify_static,
     spec_verify_timed,
     sv_early_exit_workspace_bytes,
     sv_host_staging_bytes,
+    sv_sharded_workspace_bytes,
     sv_philox,
     sv_workspace_bytes,
     version,

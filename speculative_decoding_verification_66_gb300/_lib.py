@@ -26,6 +26,10 @@ SIGNATURES = {
     "sv_early_exit_workspace_bytes": (_i32, [_i64, _i64, _i64, _i32, _i32, ctypes.POINTER(_sz)]),
     "spec_verify_early_exit": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _f32, _u64, _i32,
                                       _vp, _vp, _vp, _sz, _vp]),
+    "sv_sharded_workspace_bytes": (_i32, [_i64, _i64, _i64, _i32, _i32, _i32,
+                                          ctypes.POINTER(_sz)]),
+    "spec_verify_sharded": (_i32, [_vp, _vp, _i32, _vp, _i64, _i64, _i64, _i32, _f32, _u64, _i32,
+                                   _vp, _vp, _vp, _sz, _vp]),
     "sv_philox": (_i32, [_u64, _vp, _vp, _i64, _vp]),
     "sv_error_string": (ctypes.c_char_p, [_i32]),
     "sv_version": (_i32, []),

@@ -184,6 +184,68 @@ def spec_verify_early_exit(target_logits, draft_logits, draft_tokens, temperatur
     return out_tokens, num_accepted
 
 
+def sv_sharded_workspace_bytes(B: int, K: int, Vs: int, G: int, dtype, mode) -> int:
+    n = ctypes.c_size_t(0)
+    d = dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    _check(_lib.load().sv_sharded_workspace_bytes(B, K, Vs, G, d, mode_code(mode),
+                                                  ctypes.byref(n)), "sv_sharded_workspace_bytes")
+    return int(n.value)
+
+
+def spec_verify_sharded(target_shards, draft_shards, draft_tokens, temperature: float = 1.0,
+                        seed: int = 0, mode="sample", *, out_tokens=None, num_accepted=None,
+                        workspace=None, stream=None):
+    """spec_verify on logits split over the vocabulary: target_shards is a list
+    of G contiguous [B, K+1, Vs] tensors (shard g = columns [g Vs, (g+1) Vs)),
+    draft_shards G [B, K, Vs] tensors (None in greedy mode). Token ids are
+    global (0 .. G Vs - 1)."""
+    m = mode_code(mode)
+    G = len(target_shards)
+    if G < 1:
+        raise ValueError("need at least one shard")
+    t0 = target_shards[0]
+    if t0.dim() != 3 or not t0.is_cuda:
+        raise ValueError("target shards must be CUDA tensors [B, K+1, Vs]")
+    B, K1, Vs = t0.shape
+    K = K1 - 1
+    for t in target_shards:
+        if tuple(t.shape) != (B, K1, Vs) or t.dtype != t0.dtype or not t.is_contiguous() \
+                or t.device != t0.device:
+            raise ValueError("target shards must share shape, dtype and device, contiguous")
+    sampling = m == SV_SAMPLE and K > 0
+    if sampling:
+        if draft_shards is None or len(draft_shards) != G:
+            raise ValueError("draft_shards must hold G tensors in sampling mode")
+        for d in draft_shards:
+            if tuple(d.shape) != (B, K, Vs) or d.dtype != t0.dtype or not d.is_contiguous() \
+                    or d.device != t0.device:
+                raise ValueError("draft shards must be contiguous [B, K, Vs] like the targets")
+    if K > 0:
+        if draft_tokens is None or tuple(draft_tokens.shape) != (B, K) \
+                or draft_tokens.dtype != torch.int32 or not draft_tokens.is_contiguous():
+            raise ValueError("draft_tokens must be contiguous int32 [B, K]")
+    dev = t0.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    d = dtype_code(t0.dtype)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_sharded_workspace_bytes(B, K, Vs, G, d, m))
+    tp = (ctypes.c_void_p * G)(*[t.data_ptr() for t in target_shards])
+    dp = (ctypes.c_void_p * G)(*[x.data_ptr() for x in draft_shards]) if sampling else None
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_sharded(
+            ctypes.cast(tp, ctypes.c_void_p), ctypes.cast(dp, ctypes.c_void_p) if dp else None, G,
+            _ptr(draft_tokens if K > 0 else None), B, K, Vs, d, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream)),
+            "spec_verify_sharded")
+    return out_tokens, num_accepted
+
+
 def spec_verify_debug(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
                       seed: int = 0, mode="sample", *, workspace=None, stream=None) -> dict:
     """spec_verify plus the normalisers, log-ratios and per-sequence status."""

@@ -54,43 +54,50 @@ __device__ __forceinline__ const uint8_t* align_up16(const uint8_t* p)
 
 // Walks the tiles of a CTA's range in order, without divisions per tile.
 struct Cursor {
-    int64_t row;             // row in the launch's row space (see RowMap)
+    int64_t row;             // pass-1 row (a shard row) in the launch's row space
     int64_t k;               // tile index within the row
     int64_t n;               // sequences in the row space
+    int64_t goff;            // token index of the row's first element (the shard's offset)
     const uint8_t* rowp;     // first byte of the row
     const uint8_t* tend;     // 16-byte-aligned end of the row's tensor
 };
 
-// Row `row` of the row space [n * nt target rows | n * nd draft rows]: in each
-// part, sequence s of the map contributes its positions p0, p0 + 1, ... in
-// order. With the identity map of the full pass this is the plain
-// concatenation [target rows | draft rows].
+// Pass-1 row `row`: logical row R = row / G of the row space
+// [n * nt target rows | n * nd draft rows] (in each part sequence s of the map
+// contributes its positions p0, p0 + 1, ... in order), shard row % G of it.
+// With the identity map and G = 1 this is the plain concatenation
+// [target rows | draft rows].
 template <int ES>
 __device__ __forceinline__ void cursor_row(Cursor& c, const RowStatsArgs& a, int64_t row)
 {
     const Geometry& g = a.g;
     const RowMap& m = a.map;
+    const int64_t G = g.shards;
     c.row = row;
-    const int64_t row_bytes = g.V * ES;
-    const int64_t nt_rows = c.n * m.nt;
-    if (row >= c.n * (m.nt + m.nd)) {
+    const int64_t row_bytes = g.shard_len * ES;
+    if (row >= c.n * (m.nt + m.nd) * G) {
         // One past the last row (the cursor steps here after the last tile):
         // never copied from, and the map has no entry for it.
         c.rowp = a.target;
         c.tend = a.target;
+        c.goff = 0;
         return;
     }
-    if (row < nt_rows) {
-        const int64_t sq = row / m.nt, i = m.p0 + (row - sq * m.nt);
+    const int64_t lr = row / G;
+    const int gi = static_cast<int>(row - lr * G);
+    c.goff = gi * g.shard_len;
+    const int64_t nt_rows = c.n * m.nt;
+    if (lr < nt_rows) {
+        const int64_t sq = lr / m.nt, i = m.p0 + (lr - sq * m.nt);
         const int64_t b = m.active != nullptr ? m.active[sq] : sq;
-        c.rowp = a.target + (b * (g.K + 1) + i) * row_bytes;
-        c.tend = align_down16(a.target + g.rows_t * row_bytes);
+        c.rowp = a.sh.t[gi] + (b * (g.K + 1) + i) * row_bytes;
+        c.tend = align_down16(a.sh.t[gi] + g.rows_t * row_bytes);
     } else {
-        const int64_t r = row - nt_rows;
+        const int64_t r = lr - nt_rows;
         const int64_t sq = r / m.nd, i = m.p0 + (r - sq * m.nd);
         const int64_t b = m.active != nullptr ? m.active[sq] : sq;
-        c.rowp = a.draft + (b * g.K + i) * row_bytes;
-        c.tend = align_down16(a.draft + g.B * g.K * row_bytes);
+        c.rowp = a.sh.d[gi] + (b * g.K + i) * row_bytes;
+        c.tend = align_down16(a.sh.d[gi] + g.B * g.K * row_bytes);
     }
 }
 
@@ -132,10 +139,10 @@ __device__ __forceinline__ Span tile_span(const Cursor& c, const Geometry& g)
 {
     Span sp;
     const int64_t e0 = c.k * g.tile_elems;
-    const int64_t e1 = min(e0 + g.tile_elems, g.V);
+    const int64_t e1 = min(e0 + g.tile_elems, g.shard_len);
     const uint8_t* s = c.rowp + e0 * ES;
     const uint8_t* e = c.rowp + e1 * ES;
-    if (g.aligned) {
+    if (g.shard_aligned) {
         // Rows, tiles and tensor ends on 16-byte boundaries: no cover, no
         // masks, no element-wise tail.
         sp.a0 = s;
@@ -145,7 +152,7 @@ __device__ __forceinline__ Span tile_span(const Cursor& c, const Geometry& g)
         sp.nv = static_cast<int32_t>(sp.bulk >> 4);
         sp.head = 0;
         sp.last = 16 / ES;
-        sp.idx0 = e0;
+        sp.idx0 = c.goff + e0;
         return sp;
     }
     sp.a0 = align_down16(s);
@@ -157,7 +164,7 @@ __device__ __forceinline__ Span tile_span(const Cursor& c, const Geometry& g)
     sp.nv = static_cast<int32_t>((e - sp.a0 + 15) >> 4);
     sp.head = static_cast<int32_t>((s - sp.a0) / ES);
     sp.last = static_cast<int32_t>((e - (sp.a0 + 16 * (sp.nv - 1))) / ES);
-    sp.idx0 = e0 - sp.head;
+    sp.idx0 = c.goff + e0 - sp.head;
     return sp;
 }
 
@@ -390,7 +397,7 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
         pdl_wait();
         nseq = *a.map.count;
     }
-    const int64_t tiles = map_rows(a.map, nseq) * g.tiles_per_row;
+    const int64_t tiles = map_rows(a.map, nseq) * g.shards * g.tiles_per_row;
     // CTAs in use: at most one per tile, so every range below is non-empty
     // (an early-exit phase can have fewer tiles than the launch has CTAs).
     const int64_t grid = tiles < g.grid ? tiles : g.grid;
@@ -470,7 +477,7 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
 
     // ---------------- consumers ----------------
     const int tid = threadIdx.x;  // 0 .. kNC-1
-    const bool aligned = g.aligned != 0;
+    const bool aligned = g.shard_aligned != 0;
     Partial* my_partials =
         a.partials + static_cast<int64_t>(cta) * g.maxseg * kRowConsumerWarps + warp;
     SampleState ss;

@@ -149,8 +149,9 @@ __device__ __forceinline__ int load_seq(SeqJob& s, const SampleArgs& a, int64_t 
     s.b = b;
     s.ok = rec.status == 0;
     const int64_t K = g.K, row_bytes = g.V * es;
-    s.rp.trow = a.target + (b * (K + 1) + rec.j) * row_bytes;
-    s.rp.drow = rec.j < K ? a.draft + (b * K + rec.j) * row_bytes : nullptr;
+    const RowPairLayout& ly = a.lay;
+    s.rp.trow = a.target + (b * ly.t_seq + rec.j * ly.t_pos) * row_bytes;
+    s.rp.drow = rec.j < K ? a.draft + (b * ly.d_seq + rec.j * ly.d_pos) * row_bytes : nullptr;
     s.rp.c = a.c;
     s.rp.mt = rec.mt;
     s.rp.md = rec.md;
@@ -395,9 +396,8 @@ __global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const SampleArgs a
     auto tokens_at = [&](int64_t sl) { return static_cast<int>(lmin(G::kTok, g.V - sl * G::kTok)); };
     TensorEnds ends{nullptr, nullptr};
     if (!ALIGNED) {
-        const int64_t row_bytes = g.V * ES;
-        ends.t = down16(a.target + g.rows_t * row_bytes);
-        ends.d = a.draft != nullptr ? down16(a.draft + g.B * g.K * row_bytes) : nullptr;
+        ends.t = down16(a.lay.t_end);
+        ends.d = a.lay.d_end != nullptr ? down16(a.lay.d_end) : nullptr;
     }
     // Cursor of the next slice to issue: sequence nb, slice nsl of it.
     int64_t nb = i0 / per_seq, nsl = i0 - nb * per_seq;
@@ -594,7 +594,63 @@ cudaError_t launch_sampler(const SampleArgs& a, cudaStream_t s)
                             dim3(static_cast<unsigned>(a.g.B)), dim3(kRaceThreads), 0, s, a);
 }
 
+// Sharded verification: CTA (2 b + r, x) copies a chunk of the emitted target
+// (r = 0) or draft (r = 1) row of sequence b from the shards into row 2 b + r
+// of the pair buffer. Chunk x covers columns [x C, (x + 1) C) of the logical
+// row, C = kGatherThreads vectors; 16-byte copies when every shard row and
+// the buffer rows are 16-byte aligned, element copies otherwise.
+constexpr int kGatherThreads = 256;
+
+template <int ES>
+__global__ void __launch_bounds__(kGatherThreads) gather_pairs_kernel(const GatherArgs a)
+{
+    pdl_wait();  // the scan's sequence records are complete
+    const Geometry& g = a.g;
+    const int64_t b = blockIdx.x >> 1;
+    const int r = blockIdx.x & 1;
+    const SeqRecord rec = a.seqs[b];
+    if (rec.status != 0 || (r == 1 && rec.j >= g.K)) return;
+    const int64_t V = g.V, Vs = g.shard_len, K = g.K;
+    uint8_t* dst = a.pairs + (2 * b + r) * V * ES;
+    const int64_t row = r == 0 ? b * (K + 1) + rec.j : b * K + rec.j;
+    if (g.shard_aligned && g.aligned) {
+        constexpr int kEPV = 16 / ES;
+        const int64_t nvec = V / kEPV;  // whole vectors: V and Vs are multiples of kEPV
+        const int64_t v = static_cast<int64_t>(blockIdx.y) * kGatherThreads + threadIdx.x;
+        if (v >= nvec) return;
+        const int64_t col = v * kEPV;
+        const int gi = static_cast<int>(col / Vs);
+        const uint8_t* src = (r == 0 ? a.sh.t[gi] : a.sh.d[gi]) + (row * Vs + (col - gi * Vs)) * ES;
+        *reinterpret_cast<uint4*>(dst + col * ES) = __ldg(reinterpret_cast<const uint4*>(src));
+    } else {
+        const int64_t c0 = static_cast<int64_t>(blockIdx.y) * kGatherThreads * (16 / ES);
+        const int64_t c1 = c0 + kGatherThreads * (16 / ES) < V ? c0 + kGatherThreads * (16 / ES) : V;
+        for (int64_t col = c0 + threadIdx.x; col < c1; col += kGatherThreads) {
+            const int gi = static_cast<int>(col / Vs);
+            const uint8_t* src =
+                (r == 0 ? a.sh.t[gi] : a.sh.d[gi]) + (row * Vs + (col - gi * Vs)) * ES;
+            if (ES == 2)
+                *reinterpret_cast<uint16_t*>(dst + col * ES) =
+                    __ldg(reinterpret_cast<const unsigned short*>(src));
+            else
+                *reinterpret_cast<uint32_t*>(dst + col * ES) =
+                    __ldg(reinterpret_cast<const unsigned int*>(src));
+        }
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_gather_pairs(const GatherArgs& a, cudaStream_t s)
+{
+    const int64_t per_chunk = static_cast<int64_t>(kGatherThreads) * (16 / a.g.es);
+    const dim3 grid(static_cast<unsigned>(2 * a.g.B),
+                    static_cast<unsigned>((a.g.V + per_chunk - 1) / per_chunk));
+    return a.g.es == 2 ? launch_dependent(a.g.pdl != 0, gather_pairs_kernel<2>, grid,
+                                          dim3(kGatherThreads), 0, s, a)
+                       : launch_dependent(a.g.pdl != 0, gather_pairs_kernel<4>, grid,
+                                          dim3(kGatherThreads), 0, s, a);
+}
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s)
 {

@@ -53,32 +53,37 @@ struct RowNorm {
     float l;
 };
 
-__device__ void merge_row(const ScanArgs& a, int64_t row, int64_t tiles, int lane, RowNorm* norm,
+__device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int lane, RowNorm* norm,
                           int* argmax, int* flags)
 {
     const Geometry& g = a.g;
-    const int64_t t0 = row * g.tiles_per_row;
-    const int c0 = cta_of_tile(t0, tiles, g);
-    const int c1 = cta_of_tile(t0 + g.tiles_per_row - 1, tiles, g);
-    const int n = (c1 - c0 + 1) * kRowConsumerWarps;
     int fl = 0;
     float M = __uint_as_float(kF32NegInfBits), hi = 0.f, lo = 0.f;
     float best = __uint_as_float(kF32NegInfBits);
     int idx = INT_MAX;
-    for (int q = lane; q < n; q += 32) {
-        const int c = c0 + q / kRowConsumerWarps;
-        const int w = q % kRowConsumerWarps;
-        const int64_t first = (static_cast<int64_t>(c) * tiles / used_grid(tiles, g)) / g.tiles_per_row;
-        const Partial p =
-            a.partials[(static_cast<int64_t>(c) * g.maxseg + (row - first)) * kRowConsumerWarps + w];
-        fl |= p.flags;
-        if (g.mode == 0) {
-            merge_scaled(M, hi, lo, p.m, p.hi, p.lo);
-        } else {
-            const int pi = __float_as_int(p.hi);
-            if (p.m > best || (p.m == best && pi < idx)) {
-                best = p.m;
-                idx = pi;
+    // The logical row's shard rows, in shard order (one pass-1 row when not
+    // sharded); each one's partials in CTA, then warp order.
+    for (int64_t row = lrow * g.shards; row < (lrow + 1) * g.shards; ++row) {
+        const int64_t t0 = row * g.tiles_per_row;
+        const int c0 = cta_of_tile(t0, tiles, g);
+        const int c1 = cta_of_tile(t0 + g.tiles_per_row - 1, tiles, g);
+        const int n = (c1 - c0 + 1) * kRowConsumerWarps;
+        for (int q = lane; q < n; q += 32) {
+            const int c = c0 + q / kRowConsumerWarps;
+            const int w = q % kRowConsumerWarps;
+            const int64_t first =
+                (static_cast<int64_t>(c) * tiles / used_grid(tiles, g)) / g.tiles_per_row;
+            const Partial p =
+                a.partials[(static_cast<int64_t>(c) * g.maxseg + (row - first)) * kRowConsumerWarps + w];
+            fl |= p.flags;
+            if (g.mode == 0) {
+                merge_scaled(M, hi, lo, p.m, p.hi, p.lo);
+            } else {
+                const int pi = __float_as_int(p.hi);
+                if (p.m > best || (p.m == best && pi < idx)) {
+                    best = p.m;
+                    idx = pi;
+                }
             }
         }
     }
@@ -214,15 +219,19 @@ __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs
         const int32_t x = a.tokens[b * K + i];
         sx[q] = x;
         if (x >= 0 && static_cast<int64_t>(x) < V && sampling) {
-            stx[q] = load_logit<ES>(a.target + ((b * (K + 1) + i) * V + x) * ES);
-            sdx[q] = load_logit<ES>(a.draft + ((b * K + i) * V + x) * ES);
+            // Token x lives in shard x / Vs, at column x mod Vs.
+            const int64_t Vs = g.shard_len;
+            const int gi = static_cast<int>(x / Vs);
+            const int64_t col = x - gi * Vs;
+            stx[q] = load_logit<ES>(a.sh.t[gi] + ((b * (K + 1) + i) * Vs + col) * ES);
+            sdx[q] = load_logit<ES>(a.sh.d[gi] + ((b * K + i) * Vs + col) * ES);
         }
     }
     pdl_trigger();  // the next kernel may start launching
     if (!phased) pdl_wait();  // pass 1 has finished and its partials are visible
     __syncthreads();
 
-    const int64_t tiles = map_rows(m, nseq) * g.tiles_per_row;
+    const int64_t tiles = map_rows(m, nseq) * g.shards * g.tiles_per_row;
     const int lane = threadIdx.x & 31;
     for (int q = threadIdx.x >> 5; q < nrows; q += blockDim.x >> 5) {
         const int64_t row = q < m.nt ? sq * m.nt + q : nseq * m.nt + sq * m.nd + (q - m.nt);

@@ -57,6 +57,8 @@ struct Layout {
     size_t partials = 0, seqs = 0, block_sums = 0, total = 0;
     // Early exit only.
     size_t still = 0, lists = 0, counters = 0, counter_bytes = 0;
+    // Sharded only.
+    size_t pairs = 0;
 };
 
 // Early exit: the positions 0 .. K are verified in phases of 1, 2, 4, ...
@@ -96,7 +98,7 @@ int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
 }
 
 int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g, Layout* L,
-              bool early_exit = false)
+              bool early_exit = false, int shards = 1)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -114,10 +116,14 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     g->rows_t = B * (K + 1);
     g->rows = g->rows_t + (mode == SV_SAMPLE ? B * K : 0);
     g->aligned = (V * es) % 16 == 0;
+    // Pass 1 streams shard rows of V / G elements (the whole row when G = 1).
+    g->shards = shards;
+    g->shard_len = V / shards;
+    g->shard_aligned = (g->shard_len * es) % 16 == 0;
     // Misaligned rows need one extra 16-byte vector per tile in the buffer.
-    g->tile_elems = (g->aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
-    g->tiles_per_row = (V + g->tile_elems - 1) / g->tile_elems;
-    g->tiles = g->rows * g->tiles_per_row;
+    g->tile_elems = (g->shard_aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
+    g->tiles_per_row = (g->shard_len + g->tile_elems - 1) / g->tile_elems;
+    g->tiles = g->rows * shards * g->tiles_per_row;
     if (early_exit) {
         // The grid and the partials serve every phase: size them for the
         // phase with the most rows per sequence, as if all B took part.
@@ -126,7 +132,7 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
         int64_t most = 0;
         for (int k = 0; k < nph; ++k)
             most = ph[k].nt + ph[k].nd > most ? ph[k].nt + ph[k].nd : most;
-        g->tiles = B * most * g->tiles_per_row;
+        g->tiles = B * most * shards * g->tiles_per_row;
     }
     const int64_t want = static_cast<int64_t>(sms) * blocks;
     g->grid = static_cast<int32_t>(g->tiles < want ? (g->tiles > 0 ? g->tiles : 1) : want);
@@ -148,6 +154,11 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
     L->block_sums = off;
     if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nblocks) * sizeof(float));
+    if (shards > 1 && mode == SV_SAMPLE) {
+        // The emitted row pairs gathered from the shards, [B][2][V].
+        L->pairs = off;
+        off += round_up(static_cast<size_t>(2 * B) * static_cast<size_t>(V) * es);
+    }
     if (early_exit) {
         L->still = off;
         off += round_up(static_cast<size_t>(B) * sizeof(int32_t));
@@ -167,7 +178,8 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         int64_t V, int dtype, float temperature, uint64_t seed, int mode, int32_t* out_tokens,
         int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
         double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
-        void* const* events, int n_events, bool early_exit = false)
+        void* const* events, int n_events, bool early_exit = false,
+        const void* const* t_shards = nullptr, const void* const* d_shards = nullptr, int G = 1)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -189,6 +201,21 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         return SV_OK;
     }
     const bool sampling = mode == SV_SAMPLE;
+    if (t_shards != nullptr || G > 1) {
+        // Sharded: every shard must be given and 16-byte aligned; shard 0
+        // stands for the tensors in the checks below.
+        if (G < 1 || G > sv::kMaxShards || t_shards == nullptr ||
+            (sampling && K > 0 && d_shards == nullptr))
+            return SV_ERR_ARG;
+        for (int gi = 0; gi < G; ++gi) {
+            if (t_shards[gi] == nullptr || (sampling && K > 0 && d_shards[gi] == nullptr))
+                return SV_ERR_ARG;
+            if (!aligned_to(t_shards[gi], 16) || (sampling && K > 0 && !aligned_to(d_shards[gi], 16)))
+                return SV_ERR_ALIGN;
+        }
+        target = t_shards[0];
+        draft = sampling && K > 0 ? d_shards[0] : nullptr;
+    }
     if (target == nullptr || out_tokens == nullptr || num_accepted == nullptr) return SV_ERR_ARG;
     if (K > 0 && tokens == nullptr) return SV_ERR_ARG;
     if (sampling && K > 0 && draft == nullptr) return SV_ERR_ARG;
@@ -204,7 +231,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
 
     Geometry g;
     Layout L;
-    rc = make_plan(B, K, V, dtype, mode, &g, &L, early_exit);
+    rc = make_plan(B, K, V, dtype, mode, &g, &L, early_exit, G);
     if (rc != SV_OK) return rc;
     if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
     // Events between the kernels would sit between programmatically chained
@@ -220,13 +247,32 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
 
     const sv::RowMap full{nullptr, nullptr, 0, static_cast<int32_t>(K + 1),
                           static_cast<int32_t>(sampling ? K : 0)};
-    sv::RowStatsArgs ra{tp, dp, g, c, partials, full};
+    sv::Shards sh{};
+    for (int gi = 0; gi < G; ++gi) {
+        sh.t[gi] = static_cast<const uint8_t*>(t_shards != nullptr ? t_shards[gi] : target);
+        sh.d[gi] = dp == nullptr ? nullptr
+                                 : static_cast<const uint8_t*>(d_shards != nullptr ? d_shards[gi] : draft);
+    }
+    const int64_t row_bytes = V * g.es;
+    sv::RowPairLayout lay{K + 1, 1, K, 1, tp + g.rows_t * row_bytes,
+                          dp != nullptr ? dp + B * K * row_bytes : nullptr};
+    const uint8_t* sp_t = tp;
+    const uint8_t* sp_d = dp;
+    if (G > 1 && sampling) {
+        // The sampler reads the emitted pairs gathered from the shards.
+        uint8_t* pairs = ws + L.pairs;
+        sp_t = pairs;
+        sp_d = pairs + row_bytes;
+        lay = sv::RowPairLayout{2, 0, 2, 0, pairs + 2 * B * row_bytes, pairs + 2 * B * row_bytes};
+    }
+    sv::RowStatsArgs ra{tp, dp, g, c, partials, full, sh};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
                     sampling ? log_ratio : nullptr, seq_status, full,
-                    nullptr, nullptr, nullptr, nullptr};
-    sv::SampleArgs pa{tp, dp, g, c, seed, seqs, block_sums,
-                      out_tokens, num_accepted, seq_status};
+                    nullptr, nullptr, nullptr, nullptr, sh};
+    sv::SampleArgs pa{sp_t, sp_d, g, c, seed, seqs, block_sums,
+                      out_tokens, num_accepted, seq_status, lay};
+    sv::GatherArgs ga{g, sh, seqs, ws + L.pairs};
 
     if (early_exit) {
         // Phases over the positions; each pass 1 reads only the rows of the
@@ -262,6 +308,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     if (!record(1)) return SV_ERR_CUDA;
     if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
     if (!record(2)) return SV_ERR_CUDA;
+    if (sampling && G > 1 && sv::launch_gather_pairs(ga, s) != cudaSuccess) return SV_ERR_CUDA;
     if (sampling && sv::launch_sample(pa, s) != cudaSuccess) return SV_ERR_CUDA;
     if (!record(3)) return SV_ERR_CUDA;
     return SV_OK;
@@ -350,6 +397,37 @@ SV_EXPORT int spec_verify_early_exit(const void* target_logits, const void* draf
     return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
                out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
                nullptr, nullptr, nullptr, 0, true);
+}
+
+SV_EXPORT int sv_sharded_workspace_bytes(int64_t B, int64_t K, int64_t Vs, int G, int dtype, int mode,
+                                         size_t* bytes)
+{
+    if (bytes == nullptr || G < 1 || G > sv::kMaxShards || Vs < 1) return SV_ERR_ARG;
+    if (Vs >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+    Geometry g;
+    Layout L;
+    const int rc = make_plan(B, K, G * Vs, dtype, mode, &g, &L, false, G);
+    if (rc != SV_OK) return rc;
+    *bytes = L.total;
+    return SV_OK;
+}
+
+SV_EXPORT int spec_verify_sharded(const void* const* target_shards, const void* const* draft_shards,
+                                  int G, const int32_t* draft_tokens, int64_t B, int64_t K,
+                                  int64_t Vs, int dtype, float temperature, uint64_t seed, int mode,
+                                  int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                  size_t workspace_bytes, void* stream)
+{
+    if (G < 1 || G > sv::kMaxShards || Vs < 1) return SV_ERR_ARG;
+    if (Vs >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+    const int64_t V = G * Vs;
+    // The pair gather puts 256 vectors per CTA on grid y (at most 65535).
+    const int64_t per_chunk = 256 * (dtype == SV_BF16 ? 8 : 4);
+    if (G > 1 && (V + per_chunk - 1) / per_chunk > 65535) return SV_ERR_SIZE;
+    if (B > 0 && target_shards == nullptr) return SV_ERR_ARG;
+    return run(nullptr, nullptr, draft_tokens, B, K, V, dtype, temperature, seed, mode, out_tokens,
+               num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr,
+               nullptr, 0, false, target_shards, draft_shards, G);
 }
 
 SV_EXPORT int spec_verify_debug(const void* target_logits, const void* draft_logits,
@@ -445,4 +523,4 @@ SV_EXPORT const char* sv_error_string(int code)
     }
 }
 
-SV_EXPORT int sv_version(void) { return 102; }
+SV_EXPORT int sv_version(void) { return 103; }

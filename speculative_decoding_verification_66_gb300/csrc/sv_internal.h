@@ -78,7 +78,10 @@ struct Geometry {
     int64_t tiles;          // rows * tiles_per_row
     int32_t grid;           // pass-1 CTAs
     int32_t maxseg;         // most row segments one pass-1 CTA can touch
-    int32_t aligned;        // every row starts on a 16-byte boundary
+    int32_t aligned;        // every full row (V elements) starts on a 16-byte boundary
+    int64_t shard_len;      // pass-1 row length: V, or the shard width Vs when sharded
+    int32_t shards;         // G: pass-1 rows per logical row (1 when not sharded)
+    int32_t shard_aligned;  // every pass-1 row (shard_len elements) starts on a 16-byte boundary
     int64_t nblocks;        // race blocks per row
     int32_t sample_grid;    // CTAs of the sampler
     int32_t pdl;            // chain the kernels with programmatic dependent launch
@@ -103,6 +106,17 @@ __host__ __device__ __forceinline__ int64_t map_rows(const RowMap& m, int64_t n)
     return n * (m.nt + m.nd);
 }
 
+// The vocabulary split into G shards of Vs columns (a tensor-parallel LM
+// head's output): shard g of every row holds tokens [g Vs, (g + 1) Vs). Pass 1
+// streams each logical row as G shard rows (consecutive in its row space, so a
+// logical row's tiles stay contiguous); the scan merges them. Without sharding
+// G = 1 and shard 0 is the whole tensor.
+constexpr int kMaxShards = 16;
+struct Shards {
+    const uint8_t* t[kMaxShards];  // target shards [B, K+1, Vs]
+    const uint8_t* d[kMaxShards];  // draft shards [B, K, Vs] (unused in greedy mode)
+};
+
 struct RowStatsArgs {
     const uint8_t* target;
     const uint8_t* draft;
@@ -110,6 +124,7 @@ struct RowStatsArgs {
     float c;                // log2(e) / T
     Partial* partials;      // [grid][maxseg][kRowConsumerWarps]
     RowMap map;
+    Shards sh;
 };
 
 struct ScanArgs {
@@ -134,6 +149,17 @@ struct ScanArgs {
     int32_t* next_active;   // [B]
     int32_t* next_count;    // [1]
     uint32_t* ticket;       // [1], zero before the launch
+    Shards sh;
+};
+
+// Where the sampler finds the emitted row pair: target row j of sequence b is
+// row b * t_seq + j * t_pos of `target` (in rows of V elements), the draft row
+// likewise. The plain layout is (K + 1, 1) and (K, 1); a gathered pair buffer
+// [B][2][V] is (2, 0) with draft = buffer + one row.
+struct RowPairLayout {
+    int64_t t_seq, t_pos, d_seq, d_pos;
+    const uint8_t* t_end;  // end of the target / draft allocation (bulk copies stop
+    const uint8_t* d_end;  // at their 16-byte-aligned floor)
 };
 
 struct SampleArgs {
@@ -147,6 +173,16 @@ struct SampleArgs {
     int32_t* out_tokens;
     int32_t* num_accepted;
     int32_t* seq_status;    // optional
+    RowPairLayout lay;
+};
+
+// Sharded verification: copies each sequence's emitted row pair from the
+// shards into a contiguous buffer [B][2][V] (the pair the sampler reads).
+struct GatherArgs {
+    Geometry g;
+    Shards sh;
+    const SeqRecord* seqs;
+    uint8_t* pairs;
 };
 
 // Launch with programmatic stream serialization (the kernel must call
@@ -173,6 +209,7 @@ cudaError_t launch_dependent(bool pdl, void (*kernel)(KArgs...), dim3 grid, dim3
 cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
+cudaError_t launch_gather_pairs(const GatherArgs& a, cudaStream_t s);
 
 // Resident pass-1 CTAs per SM for this dtype / mode (occupancy query).
 cudaError_t row_stats_blocks_per_sm(int es, int mode, int* blocks);

@@ -35,7 +35,8 @@ def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "sv_workspace_bytes", "spec_verify", "spec_verify_debug", "spec_verify_timed",
         "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static",
-        "sv_early_exit_workspace_bytes", "spec_verify_early_exit", "sv_philox",
+        "sv_early_exit_workspace_bytes", "spec_verify_early_exit",
+        "sv_sharded_workspace_bytes", "spec_verify_sharded", "sv_philox",
         "sv_error_string",
         "sv_version"])
 
@@ -70,7 +71,7 @@ def test_error_strings_and_version(lib):
                  SV_ERR_SIZE, 12345):
         s = lib.sv_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
-    assert lib.sv_version() == 102
+    assert lib.sv_version() == 103
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails before any device work
@@ -119,6 +120,30 @@ def call_ee(lib, B=2, K=3, V=64, dtype=1, T=1.0, mode=0, target=FAKE, draft=FAKE
             out=FAKE, nacc=FAKE, ws=FAKE, ws_bytes=1 << 20):
     return lib.spec_verify_early_exit(target, draft, tokens, B, K, V, dtype, T, 7, mode, out, nacc,
                                       ws, ws_bytes, None)
+
+
+def test_sharded_host_side_validation(lib):
+    """spec_verify_sharded checks its shard arguments before any CUDA call."""
+    import ctypes
+    arr = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    bad = (ctypes.c_void_p * 2)(FAKE, FAKE + 2)
+    nul = (ctypes.c_void_p * 2)(FAKE, None)
+
+    def sh(G=2, t=arr, d=arr, B=2, K=3, Vs=32, dtype=1):
+        return lib.spec_verify_sharded(ctypes.cast(t, ctypes.c_void_p) if t is not None else None,
+                                       ctypes.cast(d, ctypes.c_void_p) if d is not None else None,
+                                       G, FAKE, B, K, Vs, dtype, 1.0, 7, 0, FAKE, FAKE, FAKE,
+                                       1 << 20, None)
+    assert sh(B=0) == SV_OK
+    assert sh(G=0) == SV_ERR_ARG
+    assert sh(G=17) == SV_ERR_ARG
+    assert sh(Vs=0) == SV_ERR_ARG
+    assert sh(t=None) == SV_ERR_ARG
+    assert sh(d=None) == SV_ERR_ARG
+    assert sh(t=nul) == SV_ERR_ARG
+    assert sh(t=bad) == SV_ERR_ALIGN
+    assert sh(d=bad) == SV_ERR_ALIGN
+    assert sh(dtype=9) == SV_ERR_DTYPE
 
 
 @pytest.mark.parametrize("kw,code", [
