@@ -53,6 +53,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="wall-clock budget of the CPU-baseline sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--sharded-steps", type=int, default=300,
+                   help="timed calls of spec_verify_sharded reported beside the full pass (0: skip)")
+    p.add_argument("--shards", type=int, default=8, help="vocabulary shards for that variant")
     p.add_argument("--early-exit-steps", type=int, default=1000,
                    help="timed calls of spec_verify_early_exit reported beside the full pass "
                         "(0: skip)")
@@ -393,6 +396,47 @@ def main():
                  "bytes_read_per_step": read, "bytes_ideal_per_step": ideal,
                  "hbm_gbs": read / (ee_ms / 1e3) / 1e9}
 
+    # The sharded entry on the same logits split into G vocabulary shards (a
+    # variant, reported beside the full pass).
+    sharded = None
+    G = args.shards
+    if args.sharded_steps > 0 and G > 1 and V % G == 0:
+        Vs = V // G
+        shard_sets = []
+        for inp in copies:
+            ts = [inp["target"][..., g * Vs:(g + 1) * Vs].contiguous() for g in range(G)]
+            ds = ([inp["draft"][..., g * Vs:(g + 1) * Vs].contiguous() for g in range(G)]
+                  if mode == "sample" else None)
+            shard_sets.append((ts, ds))
+        ws_sh = torch.empty(sv.sv_sharded_workspace_bytes(B, K, Vs, G, copies[0]["target"].dtype,
+                                                          mode), dtype=torch.uint8, device=dev)
+
+        def sh_step(i):
+            c = i & 1
+            ts, ds = shard_sets[c]
+            sv.spec_verify_sharded(ts, ds, copies[c]["tokens"], wl.temperature, seeds[c], mode,
+                                   out_tokens=out, num_accepted=nacc, workspace=ws_sh,
+                                   stream=stream)
+
+        for i in range(3):
+            sh_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.sharded_steps):
+            sh_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        sh_ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.sharded_steps
+        # With shard widths of whole 16-byte vectors the sampler reads the
+        # shards directly; otherwise a gather reads and writes the pairs once more.
+        gathered = mode == "sample" and (Vs * es) % 16 != 0
+        sh_bytes = mean_bytes + (2 * (mean_bytes - pass1_bytes) if gathered else 0)
+        sharded = {"shards": G, "value": job_throughput(world, B, 1, sh_ms / 1e3),
+                   "unit": "seqs/s", "ms_per_step": sh_ms, "steps": args.sharded_steps,
+                   "bytes_per_step": sh_bytes, "hbm_gbs": sh_bytes / (sh_ms / 1e3) / 1e9}
+        del shard_sets, ws_sh
+
     # End to end through the host entry point: pinned host inputs, copies inside.
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
     h = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in c.items()}
@@ -444,6 +488,8 @@ def main():
     }
     if early is not None:
         line["early_exit"] = early
+    if sharded is not None:
+        line["sharded"] = sharded
     if world == 1 and not args.no_cpu_baseline:
         def host_fn(n):
             sub = {k: (v[:n] if v is not None else None) for k, v in copies[0].items()}

@@ -265,8 +265,9 @@ int sv_sharded_workspace_bytes(int64_t B, int64_t K, int64_t Vs, int G, int dtyp
  * tokens and counts, same random numbers), on one GPU, without the caller
  * concatenating them. Pass 1 reduces each shard's part of every row, the scan
  * merges the shards' partial normalisers (the exchange a multi-GPU version
- * would make with an allreduce), and the emitted row pair of each sequence is
- * gathered from the shards for the sampler.
+ * would make with an allreduce), and the sampler reads each sequence's
+ * emitted row pair from the shards (when Vs * sizeof(element) is not a
+ * multiple of 16, the pair is first gathered into the workspace).
  *   target_shards  HOST array of G device pointers, shard g: [B, K+1, Vs] of
  *                  `dtype`, 16-byte aligned.
  *   draft_shards   HOST array of G device pointers, shard g: [B, K, Vs]; may
@@ -276,10 +277,10 @@ int sv_sharded_workspace_bytes(int64_t B, int64_t K, int64_t Vs, int G, int dtyp
  *                  G > 1, V at most 65535 * 2048 bf16 or 65535 * 1024 fp32
  *                  columns).
  * Other arguments, outputs and errors as spec_verify; the workspace is
- * sv_sharded_workspace_bytes (for G > 1 in sampling mode it includes a
- * [B][2][V] buffer for the gathered row pairs). The normalisers are merged
- * shard by shard, in another order than spec_verify's, so the two can differ
- * only on decisions the near-tie rule flags.
+ * sv_sharded_workspace_bytes (with unaligned shard widths in sampling mode it
+ * includes a [B][2][V] buffer for the gathered row pairs). The normalisers
+ * are merged in another order than spec_verify's, so the two can differ only
+ * on decisions the near-tie rule flags.
  */
 int spec_verify_sharded(const void* const* target_shards, const void* const* draft_shards, int G,
                         const int32_t* draft_tokens, int64_t B, int64_t K, int64_t Vs, int dtype,

@@ -54,49 +54,57 @@ __device__ __forceinline__ const uint8_t* align_up16(const uint8_t* p)
 
 // Walks the tiles of a CTA's range in order, without divisions per tile.
 struct Cursor {
-    int64_t row;             // pass-1 row (a shard row) in the launch's row space
+    int64_t row;             // pass-1 row in the launch's row space
     int64_t k;               // tile index within the row
     int64_t n;               // sequences in the row space
-    int64_t goff;            // token index of the row's first element (the shard's offset)
-    const uint8_t* rowp;     // first byte of the row
+    int64_t goff;            // token index of the row's first element (a shard row's offset)
+    int64_t ridx;            // row index within its tensor ([B, K+1] target or [B, K] draft)
+    int tensor;              // 0 target, 1 draft
+    const uint8_t* rowp;     // first byte of the row (one-tensor rows)
     const uint8_t* tend;     // 16-byte-aligned end of the row's tensor
 };
 
-// Pass-1 row `row`: logical row R = row / G of the row space
+// Pass-1 row `row`: logical row R = row / RS of the row space
 // [n * nt target rows | n * nd draft rows] (in each part sequence s of the map
-// contributes its positions p0, p0 + 1, ... in order), shard row % G of it.
-// With the identity map and G = 1 this is the plain concatenation
-// [target rows | draft rows].
+// contributes its positions p0, p0 + 1, ... in order), and with RS = G shard
+// rows per logical row, shard row % G of it. With the identity map and
+// RS = 1 this is the plain concatenation [target rows | draft rows].
 template <int ES>
 __device__ __forceinline__ void cursor_row(Cursor& c, const RowStatsArgs& a, int64_t row)
 {
     const Geometry& g = a.g;
     const RowMap& m = a.map;
-    const int64_t G = g.shards;
+    const int64_t RS = g.row_shards;
     c.row = row;
-    const int64_t row_bytes = g.shard_len * ES;
-    if (row >= c.n * (m.nt + m.nd) * G) {
+    const int64_t row_bytes = g.row_len * ES;
+    if (row >= c.n * (m.nt + m.nd) * RS) {
         // One past the last row (the cursor steps here after the last tile):
         // never copied from, and the map has no entry for it.
         c.rowp = a.target;
         c.tend = a.target;
         c.goff = 0;
+        c.ridx = 0;
+        c.tensor = 0;
         return;
     }
-    const int64_t lr = row / G;
-    const int gi = static_cast<int>(row - lr * G);
-    c.goff = gi * g.shard_len;
+    const int64_t lr = row / RS;
+    const int gi = static_cast<int>(row - lr * RS);
+    c.goff = gi * g.row_len;
     const int64_t nt_rows = c.n * m.nt;
     if (lr < nt_rows) {
         const int64_t sq = lr / m.nt, i = m.p0 + (lr - sq * m.nt);
         const int64_t b = m.active != nullptr ? m.active[sq] : sq;
-        c.rowp = a.sh.t[gi] + (b * (g.K + 1) + i) * row_bytes;
+        c.tensor = 0;
+        c.ridx = b * (g.K + 1) + i;
+        c.rowp = a.sh.t[gi] + c.ridx * row_bytes;
         c.tend = align_down16(a.sh.t[gi] + g.rows_t * row_bytes);
     } else {
         const int64_t r = lr - nt_rows;
         const int64_t sq = r / m.nd, i = m.p0 + (r - sq * m.nd);
         const int64_t b = m.active != nullptr ? m.active[sq] : sq;
-        c.rowp = a.sh.d[gi] + (b * g.K + i) * row_bytes;
+        c.tensor = 1;
+        c.ridx = b * g.K + i;
+        c.rowp = a.sh.d[gi] + c.ridx * row_bytes;
         c.tend = align_down16(a.sh.d[gi] + g.B * g.K * row_bytes);
     }
 }
@@ -139,10 +147,10 @@ __device__ __forceinline__ Span tile_span(const Cursor& c, const Geometry& g)
 {
     Span sp;
     const int64_t e0 = c.k * g.tile_elems;
-    const int64_t e1 = min(e0 + g.tile_elems, g.shard_len);
+    const int64_t e1 = min(e0 + g.tile_elems, g.row_len);
     const uint8_t* s = c.rowp + e0 * ES;
     const uint8_t* e = c.rowp + e1 * ES;
-    if (g.shard_aligned) {
+    if (g.row_aligned) {
         // Rows, tiles and tensor ends on 16-byte boundaries: no cover, no
         // masks, no element-wise tail.
         sp.a0 = s;
@@ -380,7 +388,7 @@ __device__ __forceinline__ void flush_greedy(const GreedyState& st, Partial* out
 }
 
 template <int ES, int MODE>
-__global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsArgs a)
+__global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const __grid_constant__ RowStatsArgs a)
 {
     extern __shared__ __align__(128) uint8_t ring[];
     __shared__ __align__(8) uint64_t full_bar[kRowStages];
@@ -397,7 +405,7 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
         pdl_wait();
         nseq = *a.map.count;
     }
-    const int64_t tiles = map_rows(a.map, nseq) * g.shards * g.tiles_per_row;
+    const int64_t tiles = map_rows(a.map, nseq) * g.row_shards * g.tiles_per_row;
     // CTAs in use: at most one per tile, so every range below is non-empty
     // (an early-exit phase can have fewer tiles than the launch has CTAs).
     const int64_t grid = tiles < g.grid ? tiles : g.grid;
@@ -458,7 +466,22 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
                     *reinterpret_cast<uint32_t*>(dst + (p - sp.a0)) =
                         __ldg(reinterpret_cast<const unsigned int*>(p));
             }
-            if (sp.bulk > 0) {
+            if (g.shards > 1 && g.row_shards == 1) {
+                // A logical-row tile [e0, e1) of sharded logits: one bulk copy
+                // per shard it overlaps, each landing at its place in the
+                // stage. Shard widths fill whole 16-byte vectors, so every
+                // piece starts and ends on a 16-byte boundary.
+                const int64_t e0 = cur.k * g.tile_elems;
+                const int64_t e1 = min(e0 + g.tile_elems, g.row_len);
+                const int64_t Vs = g.shard_len;
+                mbar_arrive_expect_tx(&full_bar[stage], static_cast<uint32_t>((e1 - e0) * ES));
+                for (int64_t gi = e0 / Vs; gi * Vs < e1; ++gi) {
+                    const int64_t p0 = max(e0, gi * Vs), p1 = min(e1, (gi + 1) * Vs);
+                    const uint8_t* base = cur.tensor == 0 ? a.sh.t[gi] : a.sh.d[gi];
+                    bulk_copy_g2s(dst + (p0 - e0) * ES, base + (cur.ridx * Vs + (p0 - gi * Vs)) * ES,
+                                  static_cast<uint32_t>((p1 - p0) * ES), &full_bar[stage]);
+                }
+            } else if (sp.bulk > 0) {
                 mbar_arrive_expect_tx(&full_bar[stage], sp.bulk);
                 bulk_copy_g2s(dst, sp.a0, sp.bulk, &full_bar[stage]);
             } else {
@@ -477,7 +500,7 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const RowStatsAr
 
     // ---------------- consumers ----------------
     const int tid = threadIdx.x;  // 0 .. kNC-1
-    const bool aligned = g.shard_aligned != 0;
+    const bool aligned = g.row_aligned != 0;
     Partial* my_partials =
         a.partials + static_cast<int64_t>(cta) * g.maxseg * kRowConsumerWarps + warp;
     SampleState ss;

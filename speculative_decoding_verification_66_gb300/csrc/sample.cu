@@ -75,6 +75,7 @@ struct Geo {
 struct RowPair {
     const uint8_t* trow;   // target row j
     const uint8_t* drow;   // draft row j, or nullptr for the bonus row
+    int32_t j;             // the emitted position (the row index within the sequence)
     float c, mt, md;       // c = log2(e) / T; mt, md: the rows' reference exponents
     float r;               // 2^(lt - ld): the draft term's scale relative to the target's
 };
@@ -152,6 +153,7 @@ __device__ __forceinline__ int load_seq(SeqJob& s, const SampleArgs& a, int64_t 
     const RowPairLayout& ly = a.lay;
     s.rp.trow = a.target + (b * ly.t_seq + rec.j * ly.t_pos) * row_bytes;
     s.rp.drow = rec.j < K ? a.draft + (b * ly.d_seq + rec.j * ly.d_pos) * row_bytes : nullptr;
+    s.rp.j = rec.j;
     s.rp.c = a.c;
     s.rp.mt = rec.mt;
     s.rp.md = rec.md;
@@ -169,27 +171,38 @@ struct TensorEnds {
 // The logits of the four tokens k0 .. k0 + 3 (k0 a multiple of 4) of both
 // rows, read from global memory (0 past the vocabulary, weighted to 0 below).
 template <int ES, bool ALIGNED>
-__device__ __forceinline__ void group_load(const RowPair& rp, int64_t k0, int64_t V, float (&xt)[4],
-                                           float (&xd)[4])
+__device__ __forceinline__ void group_load(const SampleArgs& a, const RowPair& rp, int64_t b,
+                                           int64_t k0, int64_t V, float (&xt)[4], float (&xd)[4])
 {
 #pragma unroll
     for (int q = 0; q < 4; ++q) xt[q] = xd[q] = 0.f;
     if (k0 >= V) return;
     if (ALIGNED) {
         // Aligned rows hold a multiple of 16 bytes, so a group that starts
-        // inside the row ends inside it.
+        // inside the row ends inside it (inside one shard: shard widths are
+        // multiples of 16 bytes too when the sampler reads shards directly).
+        const uint8_t* tb = rp.trow;
+        const uint8_t* db = rp.drow;
+        int64_t kk = k0;
+        if (a.direct) {
+            const int64_t Vs = a.g.shard_len;
+            const int gi = static_cast<int>(k0 / Vs);
+            kk = k0 - gi * Vs;
+            tb = a.sh.t[gi] + (b * (a.g.K + 1) + rp.j) * Vs * ES;
+            db = rp.drow != nullptr ? a.sh.d[gi] + (b * a.g.K + rp.j) * Vs * ES : nullptr;
+        }
         if (ES == 2) {
-            const uint2 v = __ldg(reinterpret_cast<const uint2*>(rp.trow + k0 * 2));
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(tb + kk * 2));
             xt[0] = bf16_lo(v.x); xt[1] = bf16_hi(v.x); xt[2] = bf16_lo(v.y); xt[3] = bf16_hi(v.y);
-            if (rp.drow) {
-                const uint2 u = __ldg(reinterpret_cast<const uint2*>(rp.drow + k0 * 2));
+            if (db) {
+                const uint2 u = __ldg(reinterpret_cast<const uint2*>(db + kk * 2));
                 xd[0] = bf16_lo(u.x); xd[1] = bf16_hi(u.x); xd[2] = bf16_lo(u.y); xd[3] = bf16_hi(u.y);
             }
         } else {
-            const float4 v = __ldg(reinterpret_cast<const float4*>(rp.trow + k0 * 4));
+            const float4 v = __ldg(reinterpret_cast<const float4*>(tb + kk * 4));
             xt[0] = v.x; xt[1] = v.y; xt[2] = v.z; xt[3] = v.w;
-            if (rp.drow) {
-                const float4 u = __ldg(reinterpret_cast<const float4*>(rp.drow + k0 * 4));
+            if (db) {
+                const float4 u = __ldg(reinterpret_cast<const float4*>(db + kk * 4));
                 xd[0] = u.x; xd[1] = u.y; xd[2] = u.z; xd[3] = u.w;
             }
         }
@@ -254,9 +267,35 @@ __device__ __forceinline__ int stage_offset(const uint8_t* row, int64_t e0, int 
 // element at a time. A slice with nothing to read completes the stage's phase
 // with a plain arrive.
 template <int ES, bool ALIGNED>
-__device__ __forceinline__ void issue_slice(const SeqJob& sj, const TensorEnds& ends, int64_t e0, int n,
+__device__ __forceinline__ void issue_slice(const SampleArgs& a, const SeqJob& sj,
+                                            const TensorEnds& ends, int64_t e0, int n,
                                             uint8_t* stage, uint64_t* bar, int lane)
 {
+    if (ALIGNED && a.direct) {
+        // Sharded logits: each row's slice [e0, e0 + n) comes from the shards
+        // it overlaps, one bulk copy per piece (16-byte aligned: shard widths
+        // fill whole vectors and slices start on 2 KB boundaries).
+        if (lane == 0) {
+            if (!sj.ok || n <= 0) {
+                mbar_arrive(bar);
+                return;
+            }
+            const int nrows = sj.rp.drow != nullptr ? 2 : 1;
+            mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nrows * n * ES));
+            const int64_t Vs = a.g.shard_len, e1 = e0 + n;
+            for (int r = 0; r < nrows; ++r)
+                for (int64_t gi = e0 / Vs; gi * Vs < e1; ++gi) {
+                    const int64_t p0 = e0 > gi * Vs ? e0 : gi * Vs;
+                    const int64_t p1 = e1 < (gi + 1) * Vs ? e1 : (gi + 1) * Vs;
+                    const uint8_t* base =
+                        r == 0 ? a.sh.t[gi] + (sj.b * (a.g.K + 1) + sj.rp.j) * Vs * ES
+                               : a.sh.d[gi] + (sj.b * a.g.K + sj.rp.j) * Vs * ES;
+                    bulk_copy_g2s(stage + r * kStageRow + (p0 - e0) * ES, base + (p0 - gi * Vs) * ES,
+                                  static_cast<uint32_t>((p1 - p0) * ES), bar);
+                }
+        }
+        return;
+    }
     const uint8_t* src[2] = {nullptr, nullptr};
     uint32_t bytes[2] = {0u, 0u};
     if (sj.ok && n > 0) {
@@ -365,7 +404,7 @@ __device__ __forceinline__ void store_sums(const SampleArgs& a, int64_t b, int64
 // slice i + 1 while the warp sums slice i from the other stage, and writes the
 // weight sum of each race block of the slice.
 template <int ES, bool ALIGNED>
-__global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const SampleArgs a)
+__global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const __grid_constant__ SampleArgs a)
 {
     using G = Geo<ES>;
     extern __shared__ __align__(128) uint8_t ring[];  // [warp][stage][target | draft]
@@ -408,7 +447,7 @@ __global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const SampleArgs a
     int64_t i = i0;
     if (i0 < i1) {
         load_seq(issued, a, nb, ES);
-        issue_slice<ES, ALIGNED>(issued, ends, nsl * G::kTok, tokens_at(nsl), stage(0), &bars[warp][0],
+        issue_slice<ES, ALIGNED>(a, issued, ends, nsl * G::kTok, tokens_at(nsl), stage(0), &bars[warp][0],
                                  lane);
         __syncwarp();  // element loads into the stage before any lane reads it
     }
@@ -424,7 +463,7 @@ __global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const SampleArgs a
         }
         if (i + 1 < i1) {
             if (nb != issued.b) load_seq(issued, a, nb, ES);
-            issue_slice<ES, ALIGNED>(issued, ends, nsl * G::kTok, tokens_at(nsl), stage(s ^ 1),
+            issue_slice<ES, ALIGNED>(a, issued, ends, nsl * G::kTok, tokens_at(nsl), stage(s ^ 1),
                                      &bars[warp][s ^ 1], lane);
         }
         const bool ok = mbar_wait_bounded(&bars[warp][s], (phases >> s) & 1u, nullptr);
@@ -504,7 +543,7 @@ __device__ __forceinline__ float cta_sum(float x, float* red)
 // block per group). Level 2: thread t takes four-token group t of the winning
 // block. Writes out_tokens[b, j].
 template <int ES, bool ALIGNED>
-__global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const SampleArgs a)
+__global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_constant__ SampleArgs a)
 {
     __shared__ Best red[kRaceWarps];
     __shared__ float redf[kRaceWarps];
@@ -545,7 +584,7 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const SampleA
         for (int64_t c = 0; c < nblk; ++c) {
             const int64_t k0 = c * kRaceBlock + 4 * t;
             float xt[4], xd[4], w[4];
-            group_load<ES, ALIGNED>(sj.rp, k0, g.V, xt, xd);
+            group_load<ES, ALIGNED>(a, sj.rp, b, k0, g.V, xt, xd);
             group_weights(sj.rp, k0, g.V, xt, xd, w);
             const float sc = cta_sum(((w[0] + w[1]) + w[2]) + w[3], redf);
             if (t == 0 && sc > 0.f) {
@@ -563,7 +602,7 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const SampleA
     if (!bad && blk.idx != INT_MAX) {
         const int64_t k0 = static_cast<int64_t>(blk.idx) * kRaceBlock + 4 * t;
         float xt[4], xd[4], w[4];
-        group_load<ES, ALIGNED>(sj.rp, k0, g.V, xt, xd);
+        group_load<ES, ALIGNED>(a, sj.rp, b, k0, g.V, xt, xd);
         group_weights(sj.rp, k0, g.V, xt, xd, w);
         race_group(tok, w, k0, make_uint4(pos, seq, 1u + static_cast<uint32_t>(k0 >> 2), 0u), key);
     }
@@ -602,7 +641,7 @@ cudaError_t launch_sampler(const SampleArgs& a, cudaStream_t s)
 constexpr int kGatherThreads = 256;
 
 template <int ES>
-__global__ void __launch_bounds__(kGatherThreads) gather_pairs_kernel(const GatherArgs a)
+__global__ void __launch_bounds__(kGatherThreads) gather_pairs_kernel(const __grid_constant__ GatherArgs a)
 {
     pdl_wait();  // the scan's sequence records are complete
     const Geometry& g = a.g;

@@ -28,7 +28,7 @@
 namespace sv {
 namespace {
 
-constexpr int kScanMaxThreads = 1024;  // a warp per row, up to 32 rows per round
+constexpr int kScanMaxThreads = 544;  // a warp per row, up to 17 rows per round
 constexpr double kLn2 = 0.69314718055994530942;
 
 // CTAs pass 1 used: at most one per tile (every range non-empty).
@@ -63,7 +63,7 @@ __device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int la
     int idx = INT_MAX;
     // The logical row's shard rows, in shard order (one pass-1 row when not
     // sharded); each one's partials in CTA, then warp order.
-    for (int64_t row = lrow * g.shards; row < (lrow + 1) * g.shards; ++row) {
+    for (int64_t row = lrow * g.row_shards; row < (lrow + 1) * g.row_shards; ++row) {
         const int64_t t0 = row * g.tiles_per_row;
         const int c0 = cta_of_tile(t0, tiles, g);
         const int c1 = cta_of_tile(t0 + g.tiles_per_row - 1, tiles, g);
@@ -170,7 +170,7 @@ __device__ void compact_still(const ScanArgs& a, int64_t nseq)
 // sequence (first rejection at j in the phase, or the bonus after K
 // acceptances) or leaves it undecided for the next phase.
 template <int ES>
-__global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs a)
+__global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_constant__ ScanArgs a)
 {
     // Dynamic shared memory: [nt + nd] row normalisers (sampling) or argmaxes
     // (greedy, in .m), then the phase's draft tokens and their target / draft
@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(kScanMaxThreads, 1) scan_kernel(const ScanArgs
     if (!phased) pdl_wait();  // pass 1 has finished and its partials are visible
     __syncthreads();
 
-    const int64_t tiles = map_rows(m, nseq) * g.shards * g.tiles_per_row;
+    const int64_t tiles = map_rows(m, nseq) * g.row_shards * g.tiles_per_row;
     const int lane = threadIdx.x & 31;
     for (int q = threadIdx.x >> 5; q < nrows; q += blockDim.x >> 5) {
         const int64_t row = q < m.nt ? sq * m.nt + q : nseq * m.nt + sq * m.nd + (q - m.nt);
@@ -341,7 +341,9 @@ cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s)
     const int64_t nrows = a.map.nt + a.map.nd;
     const int64_t npos = a.map.nt < a.g.K - a.map.p0 ? a.map.nt : a.g.K - a.map.p0;
     const size_t smem = sizeof(RowNorm) * static_cast<size_t>(nrows) + 12 * static_cast<size_t>(npos);
-    const int warps = static_cast<int>(nrows < 2 ? 2 : (nrows > 32 ? 32 : nrows));
+    // A warp per row, at most 17 (the headline's 2K + 1 rows; more take a
+    // second round): the launch bounds keep two such CTAs on an SM.
+    const int warps = static_cast<int>(nrows < 2 ? 2 : (nrows > 17 ? 17 : nrows));
     const dim3 grid(static_cast<unsigned>(a.g.B)), block(32 * warps);
     return a.g.es == 2 ? launch_dependent(a.g.pdl != 0, scan_kernel<2>, grid, block, smem, s, a)
                        : launch_dependent(a.g.pdl != 0, scan_kernel<4>, grid, block, smem, s, a);

@@ -116,14 +116,18 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     g->rows_t = B * (K + 1);
     g->rows = g->rows_t + (mode == SV_SAMPLE ? B * K : 0);
     g->aligned = (V * es) % 16 == 0;
-    // Pass 1 streams shard rows of V / G elements (the whole row when G = 1).
+    // Pass 1 streams logical rows (shard copies split at the boundaries), or
+    // each shard row when shard rows are not 16-byte aligned.
     g->shards = shards;
     g->shard_len = V / shards;
     g->shard_aligned = (g->shard_len * es) % 16 == 0;
+    g->row_shards = (g->shard_aligned && g->shard_len * es >= 4096) ? 1 : shards;
+    g->row_len = g->row_shards == 1 ? V : g->shard_len;
+    g->row_aligned = (g->row_len * es) % 16 == 0;
     // Misaligned rows need one extra 16-byte vector per tile in the buffer.
-    g->tile_elems = (g->shard_aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
-    g->tiles_per_row = (g->shard_len + g->tile_elems - 1) / g->tile_elems;
-    g->tiles = g->rows * shards * g->tiles_per_row;
+    g->tile_elems = (g->row_aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
+    g->tiles_per_row = (g->row_len + g->tile_elems - 1) / g->tile_elems;
+    g->tiles = g->rows * g->row_shards * g->tiles_per_row;
     if (early_exit) {
         // The grid and the partials serve every phase: size them for the
         // phase with the most rows per sequence, as if all B took part.
@@ -132,7 +136,7 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
         int64_t most = 0;
         for (int k = 0; k < nph; ++k)
             most = ph[k].nt + ph[k].nd > most ? ph[k].nt + ph[k].nd : most;
-        g->tiles = B * most * shards * g->tiles_per_row;
+        g->tiles = B * most * g->row_shards * g->tiles_per_row;
     }
     const int64_t want = static_cast<int64_t>(sms) * blocks;
     g->grid = static_cast<int32_t>(g->tiles < want ? (g->tiles > 0 ? g->tiles : 1) : want);
@@ -154,8 +158,9 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
     L->block_sums = off;
     if (mode == SV_SAMPLE) off += round_up(static_cast<size_t>(B * g->nblocks) * sizeof(float));
-    if (shards > 1 && mode == SV_SAMPLE) {
-        // The emitted row pairs gathered from the shards, [B][2][V].
+    if (shards > 1 && mode == SV_SAMPLE && !g->shard_aligned) {
+        // The emitted row pairs gathered from the shards, [B][2][V] (shard
+        // widths that are not whole 16-byte vectors only).
         L->pairs = off;
         off += round_up(static_cast<size_t>(2 * B) * static_cast<size_t>(V) * es);
     }
@@ -258,7 +263,8 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
                           dp != nullptr ? dp + B * K * row_bytes : nullptr};
     const uint8_t* sp_t = tp;
     const uint8_t* sp_d = dp;
-    if (G > 1 && sampling) {
+    const bool direct = G > 1 && g.shard_aligned;
+    if (G > 1 && sampling && !direct) {
         // The sampler reads the emitted pairs gathered from the shards.
         uint8_t* pairs = ws + L.pairs;
         sp_t = pairs;
@@ -271,7 +277,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
                     sampling ? log_ratio : nullptr, seq_status, full,
                     nullptr, nullptr, nullptr, nullptr, sh};
     sv::SampleArgs pa{sp_t, sp_d, g, c, seed, seqs, block_sums,
-                      out_tokens, num_accepted, seq_status, lay};
+                      out_tokens, num_accepted, seq_status, lay, direct ? 1 : 0, sh};
     sv::GatherArgs ga{g, sh, seqs, ws + L.pairs};
 
     if (early_exit) {
@@ -308,7 +314,8 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     if (!record(1)) return SV_ERR_CUDA;
     if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
     if (!record(2)) return SV_ERR_CUDA;
-    if (sampling && G > 1 && sv::launch_gather_pairs(ga, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (sampling && G > 1 && !direct && sv::launch_gather_pairs(ga, s) != cudaSuccess)
+        return SV_ERR_CUDA;
     if (sampling && sv::launch_sample(pa, s) != cudaSuccess) return SV_ERR_CUDA;
     if (!record(3)) return SV_ERR_CUDA;
     return SV_OK;

@@ -79,9 +79,14 @@ struct Geometry {
     int32_t grid;           // pass-1 CTAs
     int32_t maxseg;         // most row segments one pass-1 CTA can touch
     int32_t aligned;        // every full row (V elements) starts on a 16-byte boundary
-    int64_t shard_len;      // pass-1 row length: V, or the shard width Vs when sharded
-    int32_t shards;         // G: pass-1 rows per logical row (1 when not sharded)
-    int32_t shard_aligned;  // every pass-1 row (shard_len elements) starts on a 16-byte boundary
+    int64_t shard_len;      // Vs, the shard width (V when not sharded)
+    int32_t shards;         // G (1 when not sharded)
+    int32_t shard_aligned;  // Vs elements fill whole 16-byte vectors
+    int32_t row_shards;     // pass-1 rows per logical row: 1, or G when shard rows are
+                            // not 16-byte aligned or shorter than 4 KB (then pass 1
+                            // streams each shard row)
+    int64_t row_len;        // pass-1 row length: V, or Vs when row_shards == G
+    int32_t row_aligned;    // pass-1 rows fill whole 16-byte vectors
     int64_t nblocks;        // race blocks per row
     int32_t sample_grid;    // CTAs of the sampler
     int32_t pdl;            // chain the kernels with programmatic dependent launch
@@ -107,10 +112,11 @@ __host__ __device__ __forceinline__ int64_t map_rows(const RowMap& m, int64_t n)
 }
 
 // The vocabulary split into G shards of Vs columns (a tensor-parallel LM
-// head's output): shard g of every row holds tokens [g Vs, (g + 1) Vs). Pass 1
-// streams each logical row as G shard rows (consecutive in its row space, so a
-// logical row's tiles stay contiguous); the scan merges them. Without sharding
-// G = 1 and shard 0 is the whole tensor.
+// head's output): shard g of every row holds tokens [g Vs, (g + 1) Vs).
+// Without sharding G = 1 and shard 0 is the whole tensor. When Vs fills whole
+// 16-byte vectors, pass 1 tiles the logical rows and splits a tile's bulk copy
+// at the shard boundaries; otherwise it streams each logical row as G shard
+// rows (consecutive in its row space) and the scan merges them.
 constexpr int kMaxShards = 16;
 struct Shards {
     const uint8_t* t[kMaxShards];  // target shards [B, K+1, Vs]
@@ -174,6 +180,11 @@ struct SampleArgs {
     int32_t* num_accepted;
     int32_t* seq_status;    // optional
     RowPairLayout lay;
+    // Sharded logits with 16-byte-aligned shard widths: the sampler reads
+    // the emitted pair from the shards themselves (target row b (K+1) + j of
+    // every shard, draft row b K + j), splitting copies at shard boundaries.
+    int32_t direct;
+    Shards sh;
 };
 
 // Sharded verification: copies each sequence's emitted row pair from the
