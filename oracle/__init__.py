@@ -96,6 +96,12 @@ def lib() -> ctypes.CDLL:
             L.svo_verify.argtypes = [vp, vp, vp, i64, i64, i64, i32, dbl, u64, i32, i64, i64,
                                      vp, vp, vp, vp, vp, vp, vp, vp]
             L.svo_verify.restype = i32
+            L.svo_verify_filtered.argtypes = [vp, vp, vp, i64, i64, i64, i32, dbl, u64, i32, i64,
+                                              dbl, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp]
+            L.svo_verify_filtered.restype = i32
+            L.svo_filter_row.argtypes = [vp, i64, i32, dbl, dbl, i64, dbl, vp, vp, vp]
+            L.svo_filter_row.restype = i32
             _lib = L
     return _lib
 
@@ -193,8 +199,17 @@ def row_argmax(row: np.ndarray):
     return int(k), bool(flag[0])
 
 
+def filter_row(row: np.ndarray, T: float, lse: float, top_k: int, top_p: float):
+    """Top-k / top-p cut of one row: (threshold logit, log kept mass, top-p margin)."""
+    row = np.ascontiguousarray(row)
+    out = np.zeros(3)
+    lib().svo_filter_row(_ptr(row), row.shape[-1], _dtype_code(row), T, lse, int(top_k),
+                         float(top_p), _ptr(out[0:1]), _ptr(out[1:2]), _ptr(out[2:3]))
+    return float(out[0]), float(out[1]), float(out[2])
+
+
 def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mode: int = SAMPLE,
-           threads: int = 1, seq_range=None) -> dict:
+           threads: int = 1, seq_range=None, top_k: int = 0, top_p: float = 1.0) -> dict:
     """Run the oracle over a batch.
 
     target: [B, K+1, V] float32 or uint16 (bf16 bits); draft: [B, K, V] or None
@@ -202,7 +217,8 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
     value the CUDA path receives. ``threads`` > 1 splits the sequences into
     contiguous ranges run on a thread pool (the C code is unchanged and holds no
     shared state). ``seq_range=(b0, b1)`` restricts the work; outputs outside it
-    are left at their fill values.
+    are left at their fill values. ``top_k`` / ``top_p`` filter both rows of
+    every position (0 and 1.0: off); ``top_p`` is widened from float32 like T.
     """
     target = np.ascontiguousarray(target)
     if target.ndim != 3:
@@ -224,17 +240,22 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
         "log_ratio": np.full((B, K), np.nan),
         "accept_margin": np.full((B, K), np.nan),
         "sample_margin": np.full(B, np.nan),
+        "filter_margin_t": np.full((B, K + 1), np.inf),
+        "filter_margin_d": np.full((B, K), np.inf),
         "seq_status": np.full(B, -7, dtype=np.int32),
     }
+    P = float(np.float32(top_p))
     b0, b1 = (0, B) if seq_range is None else seq_range
     L = lib()
 
     def run(lo, hi):
-        rc = L.svo_verify(_ptr(target), _ptr(draft), _ptr(tokens), B, K, V, dt, T, seed, mode,
-                          lo, hi, _ptr(out["out_tokens"]), _ptr(out["num_accepted"]),
-                          _ptr(out["lse_t"]), _ptr(out["lse_d"]), _ptr(out["log_ratio"]),
-                          _ptr(out["accept_margin"]), _ptr(out["sample_margin"]),
-                          _ptr(out["seq_status"]))
+        rc = L.svo_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), B, K, V, dt, T,
+                                   seed, mode, int(top_k), P, lo, hi, _ptr(out["out_tokens"]),
+                                   _ptr(out["num_accepted"]), _ptr(out["lse_t"]),
+                                   _ptr(out["lse_d"]), _ptr(out["log_ratio"]),
+                                   _ptr(out["accept_margin"]), _ptr(out["sample_margin"]),
+                                   _ptr(out["filter_margin_t"]), _ptr(out["filter_margin_d"]),
+                                   _ptr(out["seq_status"]))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")
 

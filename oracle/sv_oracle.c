@@ -170,22 +170,92 @@ double svo_accept_prob(double log_p, double log_q)
     return exp(log_p - log_q);
 }
 
+/* log p'(x) of a filtered row: -inf below the threshold. */
+static double filtered_log_prob(const void* row, int64_t k, int dtype, double T, double lse,
+                                double thr, double log_mass)
+{
+    if (!(svo_elem(row, k, dtype) >= thr)) return -INFINITY;
+    return svo_log_prob(row, k, dtype, T, lse) - log_mass;
+}
+
 /* [RU] §5 step 3 / §6 and [VN]: after a rejection the next token comes from    */
 /* max(0, p - q)/Z; [ZH] §4 item 4: after K acceptances it comes from the       */
-/* bonus row's own distribution p.                                              */
-void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
-                        double T, double lse_t, double lse_d, double* w)
+/* bonus row's own distribution p. Written for the filtered rows p' and q'    */
+/* (threshold -inf and log mass 0: no filter); draft_row NULL gives p'.        */
+static void filtered_weights(const void* trow, const void* drow, int64_t V, int dtype, double T,
+                             double lse_t, double thr_t, double lm_t, double lse_d, double thr_d,
+                             double lm_d, double* w)
 {
     int64_t k;
     for (k = 0; k < V; ++k) {
-        double p = exp(svo_log_prob(target_row, k, dtype, T, lse_t));
-        if (draft_row != NULL) {
-            double q = exp(svo_log_prob(draft_row, k, dtype, T, lse_d));
+        double p = exp(filtered_log_prob(trow, k, dtype, T, lse_t, thr_t, lm_t));
+        if (drow != NULL) {
+            double q = exp(filtered_log_prob(drow, k, dtype, T, lse_d, thr_d, lm_d));
             w[k] = (p > q) ? (p - q) : 0.0;
         } else {
             w[k] = p;
         }
     }
+}
+
+void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
+                        double T, double lse_t, double lse_d, double* w)
+{
+    filtered_weights(target_row, draft_row, V, dtype, T, lse_t, -INFINITY, 0.0, lse_d, -INFINITY,
+                     0.0, w);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Top-k / top-p ([VN], paragraph on temperature, top-k and top-p: whatever    */
+/* transform the draft's distribution gets, the target's gets the same). Read  */
+/* here, for one row, as: keep the tokens whose logit is >= the k-th largest   */
+/* logit (every tie at the boundary kept); among those, with their softmax     */
+/* renormalised over them, keep the tokens whose logit is >= the largest value */
+/* v such that the kept tokens with logit >= v hold at least top_p of the      */
+/* mass. Both cuts are a threshold on the logit value, so equal logits are     */
+/* kept or dropped together. top_k <= 0 or >= V and top_p >= 1 switch a cut   */
+/* off. The filtered distribution is p' = p [logit >= thr] / M.               */
+/* ------------------------------------------------------------------------- */
+static int cmp_desc(const void* a, const void* b)
+{
+    double x = *(const double*)a, y = *(const double*)b;
+    return (x < y) - (x > y);
+}
+
+int svo_filter_row(const void* row, int64_t V, int dtype, double T, double lse, int64_t top_k,
+                   double top_p, double* thr, double* log_mass, double* margin)
+{
+    double* v = (double*)malloc(sizeof(double) * (size_t)V);
+    double thr_k = -INFINITY, mass_k = 0.0, kept = 0.0;
+    int64_t k, g;
+    if (v == NULL) return -1;
+    for (k = 0; k < V; ++k) v[k] = svo_elem(row, k, dtype);
+    qsort(v, (size_t)V, sizeof(double), cmp_desc);
+    if (top_k > 0 && top_k < V) thr_k = v[top_k - 1];
+    for (k = 0; k < V && v[k] >= thr_k; ++k) mass_k += exp(v[k] / T - lse);
+    *thr = thr_k;
+    *margin = INFINITY;
+    if (top_p < 1.0) {
+        /* Walk the groups of equal logits from the largest down. */
+        const double target = top_p * mass_k;
+        double before = 0.0;
+        for (k = 0; k < V && v[k] >= thr_k; k = g) {
+            double group = 0.0, after;
+            for (g = k; g < V && v[g] == v[k]; ++g) group += exp(v[g] / T - lse);
+            after = before + group;
+            if (after >= target) {
+                double m1 = (after - target) / mass_k, m2 = (target - before) / mass_k;
+                *thr = v[k] > thr_k ? v[k] : thr_k;
+                *margin = m1 < m2 ? m1 : m2;
+                break;
+            }
+            before = after;
+        }
+    }
+    for (k = 0; k < V && v[k] >= *thr; ++k) kept += exp(v[k] / T - lse);
+    *log_mass = log(kept);
+    free(v);
+    return 0;
 }
 
 double svo_race_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t k)
@@ -284,10 +354,12 @@ static void fail_sequence(int64_t b, int64_t K, int32_t status, int32_t* out_tok
 
 static void verify_sampling(const void* target, const void* draft, const int32_t* tokens,
                             int64_t b, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
-                            int32_t* out_tokens, int32_t* num_accepted, double* lse_t_out,
-                            double* lse_d_out, double* log_ratio_out, double* accept_margin,
-                            double* sample_margin, int32_t* seq_status)
+                            int64_t top_k, double top_p, int32_t* out_tokens,
+                            int32_t* num_accepted, double* lse_t_out, double* lse_d_out,
+                            double* log_ratio_out, double* accept_margin, double* sample_margin,
+                            double* fm_t, double* fm_d, int32_t* seq_status)
 {
+    const int filtering = (top_k > 0 && top_k < V) || top_p < 1.0;
     const size_t esz = (dtype == SVO_F32) ? 4 : 2;
     const unsigned char* trow0 = (const unsigned char*)target + (size_t)(b * (K + 1)) * V * esz;
     const unsigned char* drow0 =
@@ -295,6 +367,10 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
     double* lse_t = (double*)malloc(sizeof(double) * (size_t)(K + 1));
     double* lse_d = (double*)malloc(sizeof(double) * (size_t)(K > 0 ? K : 1));
     double* w = (double*)malloc(sizeof(double) * (size_t)V);
+    /* Thresholds and log kept masses of the filtered rows: [0, K] target, then
+     * [K + 1, 2K] draft (no filtering: -inf and 0). */
+    double* thr = (double*)malloc(sizeof(double) * (size_t)(2 * K + 1));
+    double* lm = (double*)malloc(sizeof(double) * (size_t)(2 * K + 1));
     int32_t status = 0;
     int64_t i, j;
     double margin;
@@ -318,16 +394,39 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
     if (accept_margin)
         for (i = 0; i < K; ++i) accept_margin[b * K + i] = NAN;
     if (sample_margin) sample_margin[b] = NAN;
+    for (i = 0; i <= 2 * K; ++i) {
+        thr[i] = -INFINITY;
+        lm[i] = 0.0;
+    }
+    if (fm_t)
+        for (i = 0; i <= K; ++i) fm_t[b * (K + 1) + i] = INFINITY;
+    if (fm_d)
+        for (i = 0; i < K; ++i) fm_d[b * K + i] = INFINITY;
     if (status != 0) {
         fail_sequence(b, K, status, out_tokens, num_accepted, seq_status);
         goto done;
+    }
+    if (filtering) {
+        double mg;
+        for (i = 0; i <= K; ++i) {
+            svo_filter_row(trow0 + (size_t)i * V * esz, V, dtype, T, lse_t[i], top_k, top_p,
+                           &thr[i], &lm[i], &mg);
+            if (fm_t) fm_t[b * (K + 1) + i] = mg;
+        }
+        for (i = 0; i < K; ++i) {
+            svo_filter_row(drow0 + (size_t)i * V * esz, V, dtype, T, lse_d[i], top_k, top_p,
+                           &thr[K + 1 + i], &lm[K + 1 + i], &mg);
+            if (fm_d) fm_d[b * K + i] = mg;
+        }
     }
 
     /* Log ratio log p_i(x_i) - log q_i(x_i) at every position (diagnostic). */
     for (i = 0; i < K; ++i) {
         int32_t x = tokens[b * K + i];
-        double lp = svo_log_prob(trow0 + (size_t)i * V * esz, x, dtype, T, lse_t[i]);
-        double lq = svo_log_prob(drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i]);
+        double lp = filtered_log_prob(trow0 + (size_t)i * V * esz, x, dtype, T, lse_t[i], thr[i],
+                                      lm[i]);
+        double lq = filtered_log_prob(drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i],
+                                      thr[K + 1 + i], lm[K + 1 + i]);
         if (log_ratio_out) log_ratio_out[b * K + i] = lp - lq;
     }
 
@@ -336,9 +435,13 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
     j = K;
     for (i = 0; i < K; ++i) {
         int32_t x = tokens[b * K + i];
-        double lp = svo_log_prob(trow0 + (size_t)i * V * esz, x, dtype, T, lse_t[i]);
-        double lq = svo_log_prob(drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i]);
-        double r = svo_accept_prob(lp, lq);
+        double lp = filtered_log_prob(trow0 + (size_t)i * V * esz, x, dtype, T, lse_t[i], thr[i],
+                                      lm[i]);
+        double lq = filtered_log_prob(drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i],
+                                      thr[K + 1 + i], lm[K + 1 + i]);
+        /* A token the filtered target cannot produce is rejected (even when */
+        /* the filtered draft cannot produce it either).                      */
+        double r = lp == -INFINITY ? 0.0 : svo_accept_prob(lp, lq);
         double u = svo_uniform(seed, (uint32_t)b, (uint32_t)i, 0);
         if (accept_margin) accept_margin[b * K + i] = fabs(u - r);
         if (!(u < r)) {
@@ -350,15 +453,17 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
     /* Step 3: the token at position j -- the residual after a rejection, the   */
     /* bonus row after K acceptances.                                           */
     if (j < K) {
-        svo_sample_weights(trow0 + (size_t)j * V * esz, drow0 + (size_t)j * V * esz, V, dtype, T,
-                           lse_t[j], lse_d[j], w);
+        filtered_weights(trow0 + (size_t)j * V * esz, drow0 + (size_t)j * V * esz, V, dtype, T,
+                         lse_t[j], thr[j], lm[j], lse_d[j], thr[K + 1 + j], lm[K + 1 + j], w);
     } else {
-        svo_sample_weights(trow0 + (size_t)K * V * esz, NULL, V, dtype, T, lse_t[K], 0.0, w);
+        filtered_weights(trow0 + (size_t)K * V * esz, NULL, V, dtype, T, lse_t[K], thr[K], lm[K],
+                         0.0, 0.0, 0.0, w);
     }
     token = svo_race_sample(w, V, seed, (uint32_t)b, (uint32_t)j, &margin);
     if (token < 0) {
-        /* Every residual weight rounded to zero: race p_j instead. */
-        svo_sample_weights(trow0 + (size_t)j * V * esz, NULL, V, dtype, T, lse_t[j], 0.0, w);
+        /* Every residual weight rounded to zero: race p'_j instead. */
+        filtered_weights(trow0 + (size_t)j * V * esz, NULL, V, dtype, T, lse_t[j], thr[j], lm[j],
+                         0.0, 0.0, 0.0, w);
         token = svo_race_sample(w, V, seed, (uint32_t)b, (uint32_t)j, &margin);
         margin = 0.0;
     }
@@ -374,6 +479,8 @@ done:
     free(lse_t);
     free(lse_d);
     free(w);
+    free(thr);
+    free(lm);
 }
 
 static void verify_greedy(const void* target, const int32_t* tokens, int64_t b, int64_t K,
@@ -424,7 +531,21 @@ int svo_verify(const void* target, const void* draft, const int32_t* tokens,
                double* lse_t, double* lse_d, double* log_ratio,
                double* accept_margin, double* sample_margin, int32_t* seq_status)
 {
+    return svo_verify_filtered(target, draft, tokens, B, K, V, dtype, T, seed, mode, 0, 1.0, b0,
+                               b1, out_tokens, num_accepted, lse_t, lse_d, log_ratio,
+                               accept_margin, sample_margin, NULL, NULL, seq_status);
+}
+
+int svo_verify_filtered(const void* target, const void* draft, const int32_t* tokens,
+                        int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
+                        int mode, int64_t top_k, double top_p, int64_t b0, int64_t b1,
+                        int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
+                        double* lse_d, double* log_ratio, double* accept_margin,
+                        double* sample_margin, double* filter_margin_t, double* filter_margin_d,
+                        int32_t* seq_status)
+{
     int64_t b;
+    if (!(top_p > 0.0 && top_p <= 1.0)) return -1;
     if (B < 0 || K < 0 || V < 1 || b0 < 0 || b1 > B || b0 > b1) return -1;
     if (dtype != SVO_F32 && dtype != SVO_BF16) return -1;
     if (mode != SVO_SAMPLE && mode != SVO_GREEDY) return -1;
@@ -434,9 +555,9 @@ int svo_verify(const void* target, const void* draft, const int32_t* tokens,
     if (mode == SVO_SAMPLE && !(T > 0.0 && isfinite(T))) return -1;
     for (b = b0; b < b1; ++b) {
         if (mode == SVO_SAMPLE)
-            verify_sampling(target, draft, tokens, b, K, V, dtype, T, seed, out_tokens,
-                            num_accepted, lse_t, lse_d, log_ratio, accept_margin, sample_margin,
-                            seq_status);
+            verify_sampling(target, draft, tokens, b, K, V, dtype, T, seed, top_k, top_p,
+                            out_tokens, num_accepted, lse_t, lse_d, log_ratio, accept_margin,
+                            sample_margin, filter_margin_t, filter_margin_d, seq_status);
         else
             verify_greedy(target, tokens, b, K, V, dtype, out_tokens, num_accepted,
                           accept_margin, sample_margin, seq_status);

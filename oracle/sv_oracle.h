@@ -103,6 +103,33 @@ int svo_verify(const void* target, const void* draft, const int32_t* tokens,
                double* lse_t, double* lse_d, double* log_ratio,
                double* accept_margin, double* sample_margin, int32_t* seq_status);
 
+/*
+ * Top-k / top-p cut of one row (logits of `row` over T, natural-log normaliser
+ * lse): *thr = the smallest logit value kept (every token with logit >= *thr
+ * is kept), *log_mass = log of the kept softmax mass, *margin = the top-p
+ * boundary's distance, relative to the top-k set's mass, between top_p and the
+ * masses just above and just including the boundary value (+inf when top-p is
+ * off). top_k <= 0 or >= V, and top_p >= 1, switch a cut off. Returns 0.
+ */
+int svo_filter_row(const void* row, int64_t V, int dtype, double T, double lse, int64_t top_k,
+                   double top_p, double* thr, double* log_mass, double* margin);
+
+/*
+ * svo_verify with both rows of every position filtered by top-k then top-p
+ * before the acceptance test and the residual / bonus draw (greedy mode
+ * ignores the filters: they never remove a row's maximum). filter_margin_t
+ * [B, K+1] and filter_margin_d [B, K] (optional) get each row's top-p boundary
+ * margin. top_p must lie in (0, 1]. A draft token the filtered target gives
+ * probability 0 is rejected.
+ */
+int svo_verify_filtered(const void* target, const void* draft, const int32_t* tokens,
+                        int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
+                        int mode, int64_t top_k, double top_p, int64_t b0, int64_t b1,
+                        int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
+                        double* lse_d, double* log_ratio, double* accept_margin,
+                        double* sample_margin, double* filter_margin_t, double* filter_margin_d,
+                        int32_t* seq_status);
+
 #ifdef __cplusplus
 }
 #endif

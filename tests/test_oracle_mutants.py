@@ -21,8 +21,8 @@ MUTANTS = {
     "accept_test_inverted": ("if (!(u < r)) {", "if (u < r) {"),
     "no_truncation": ("            j = i;\n            break;\n        }\n    }\n\n    /* Step 3",
                       "            j = i;\n        }\n    }\n\n    /* Step 3"),
-    "bonus_row_off_by_one": ("svo_sample_weights(trow0 + (size_t)K * V * esz, NULL",
-                             "svo_sample_weights(trow0 + (size_t)(K - 1) * V * esz, NULL"),
+    "bonus_row_off_by_one": ("filtered_weights(trow0 + (size_t)K * V * esz, NULL",
+                             "filtered_weights(trow0 + (size_t)(K - 1) * V * esz, NULL"),
     "race_score_inverted": ("double score = w / (-log(v));", "double score = w * (-log(v));"),
     "race_clock_sign": ("double score = w / (-log(v));", "double score = w / log(v);"),
     "race_lane_fixed": ("(2u * (r[k & 3u] >> 9) + 1u)", "(2u * (r[0] >> 9) + 1u)"),
@@ -39,9 +39,22 @@ MUTANTS = {
     "argmax_last_occurrence": ("else if (v > best) {", "else if (v >= best) {"),
     "philox_words_swapped": ("uint32_t y1 = lo1;", "uint32_t y1 = lo0;"),
     "philox_key_schedule_dropped": ("k1 += PHILOX_W1;", ""),
-    "draft_row_index": ("drow0 + (size_t)i * V * esz, x, dtype, T, lse_d[i]);\n        double r",
-                        "drow0 + (size_t)0 * V * esz, x, dtype, T, lse_d[i]);\n        double r"),
+    "draft_row_index": ("thr[K + 1 + i], lm[K + 1 + i]);\n        /* A token",
+                        "thr[K + 1 + i], lm[K + 1 + i]);\n        lq = filtered_log_prob(drow0, x, dtype, T, lse_d[0], thr[K + 1], lm[K + 1]);\n        /* A token"),
     "uniform_shift": ("(r[lane & 3] >> 8)", "(r[lane & 3] >> 9)"),
+    "topk_rank_off_by_one": ("thr_k = v[top_k - 1];", "thr_k = v[top_k];"),
+    "topp_target_ignores_topk_mass": ("const double target = top_p * mass_k;",
+                                      "const double target = top_p;"),
+    "topp_ties_split": ("g < V && v[g] == v[k]; ++g)", "g < V && g == k; ++g)"),
+    "topp_keeps_one_group_less": ("*thr = v[k] > thr_k ? v[k] : thr_k;",
+                                  "*thr = (k > 0 ? v[k - 1] : v[k]) > thr_k ? (k > 0 ? v[k - 1] : v[k]) : thr_k;"),
+    "filtered_mass_not_renormalised": ("return svo_log_prob(row, k, dtype, T, lse) - log_mass;",
+                                       "return svo_log_prob(row, k, dtype, T, lse);"),
+    "draft_left_unfiltered": ("&thr[K + 1 + i], &lm[K + 1 + i], &mg);",
+                              "&mg, &mg, &mg);"),
+    "zero_target_mass_accepted": ("double r = lp == -INFINITY ? 0.0 : svo_accept_prob(lp, lq);",
+                                  "double r = svo_accept_prob(lp, lq);"),
+    "bonus_row_unfiltered": ("lse_t[K], thr[K], lm[K],", "lse_t[K], -INFINITY, 0.0,"),
 }
 
 

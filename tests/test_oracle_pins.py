@@ -572,3 +572,199 @@ def test_philox_many_is_philox_per_counter(oracle_mod):
     many = oracle_mod.philox_many(ctr, key)
     for r in range(ctr.shape[0]):
         assert np.array_equal(many[r], oracle_mod.philox(ctr[r], key))
+
+
+# --------------------------------------------------------------------------
+# Top-k / top-p applied to both rows ([VN], paragraph on temperature, top-k
+# and top-p). The filtered rows are p' and q'; every law above must hold with
+# p' in place of p.
+# --------------------------------------------------------------------------
+def brute_filter(row, T, top_k, top_p):
+    """The cut straight from its definition, by trying every value of the row
+    as a threshold: top-k keeps the largest value v with #{x >= v} >= k;
+    top-p, inside that set, the largest v whose upper set holds >= top_p of
+    the set's mass. Returns (threshold, kept mask, p' over the row, margin)."""
+    x = np.asarray(row, dtype=np.float64)
+    V = x.size
+    p = softmax64(x, T)
+    cands = sorted(set(x.tolist()))
+    tk = -math.inf
+    if 0 < top_k < V:
+        tk = max(v for v in cands if (x >= v).sum() >= top_k)
+    mass_k = p[x >= tk].sum()
+    thr, margin = tk, math.inf
+    if top_p < 1.0:
+        target = top_p * mass_k
+        thr = max(v for v in cands if v >= tk and p[x >= v].sum() >= target)
+        after, before = p[x >= thr].sum(), p[x > thr].sum()
+        margin = min(after - target, target - before) / mass_k
+    kept = x >= thr
+    pf = np.where(kept, p, 0.0)
+    return thr, kept, pf / pf.sum(), margin
+
+
+def _tied_row(rng, V, T):
+    """Logits on a coarse grid, so that ties are common."""
+    return (rng.integers(-8, 8, size=V) / 2).astype(np.float32)
+
+
+@pytest.mark.parametrize("top_k,top_p", [(0, 1.0), (1, 1.0), (3, 1.0), (5, 1.0), (0, 0.3),
+                                         (0, 0.9), (4, 0.5), (6, 0.95), (2, 0.01), (11, 0.7)])
+@pytest.mark.parametrize("T", [1.0, 0.6])
+def test_filter_row_against_brute_force(oracle_mod, top_k, top_p, T):
+    rng = np.random.default_rng(17 + top_k)
+    for trial in range(40):
+        V = int(rng.integers(1, 14))
+        row = _tied_row(rng, V, T) if trial % 2 else rng.normal(size=V).astype(np.float32)
+        lse = np.log(np.exp(row.astype(np.float64) / T).sum())
+        thr, log_mass, margin = oracle_mod.filter_row(row, T, lse, top_k, top_p)
+        bthr, kept, pf, bmargin = brute_filter(row, T, top_k, top_p)
+        assert thr == bthr, (row, top_k, top_p)
+        p = softmax64(row, T)
+        assert math.isclose(log_mass, math.log(p[kept].sum()), rel_tol=1e-12, abs_tol=1e-12)
+        if math.isinf(bmargin):
+            assert math.isinf(margin)
+        else:
+            assert math.isclose(margin, bmargin, rel_tol=1e-9, abs_tol=1e-12)
+
+
+def test_filter_row_closed_forms(oracle_mod):
+    """p proportional to [4, 2, 1, 1]: top-p walks the groups 1/2, 3/4, 1 (the
+    two 1s are one group, kept or dropped together)."""
+    row = np.log(np.array([4.0, 2.0, 1.0, 1.0])).astype(np.float32)
+    lse = float(np.log(np.exp(row.astype(np.float64)).sum()))
+    r = {}
+    for top_k, top_p in [(0, 0.45), (0, 0.6), (0, 0.85), (1, 1.0), (3, 1.0), (3, 0.4), (0, 1.0)]:
+        r[(top_k, top_p)] = oracle_mod.filter_row(row, 1.0, lse, top_k, top_p)
+    p = softmax64(row)
+    assert r[(0, 0.45)][0] == row[0] and math.isclose(r[(0, 0.45)][2], 0.05 / 1.0, rel_tol=1e-6)
+    assert r[(0, 0.6)][0] == row[1] and math.isclose(r[(0, 0.6)][2], 0.1, rel_tol=1e-6)
+    # the boundary group holds both 1s: margin = min(1 - 0.85, 0.85 - 0.75)
+    assert r[(0, 0.85)][0] == row[2] and math.isclose(r[(0, 0.85)][2], 0.1, rel_tol=1e-6)
+    assert r[(1, 1.0)][0] == row[0] and math.isclose(r[(1, 1.0)][1], math.log(p[0]))
+    # third-largest value is a tie: top-3 keeps all four tokens
+    assert r[(3, 1.0)][0] == row[2] and abs(r[(3, 1.0)][1]) < 1e-12
+    # top-p inside the top-3 set (all of it here): 0.4 of it is reached by {4}
+    assert r[(3, 0.4)][0] == row[0]
+    assert r[(0, 1.0)][0] == -math.inf and math.isinf(r[(0, 1.0)][2])
+
+
+def test_filters_off_change_nothing(oracle_mod):
+    rng = np.random.default_rng(8)
+    B, K, V = 40, 3, 30
+    t = rng.normal(size=(B, K + 1, V)).astype(np.float32)
+    d = rng.normal(size=(B, K, V)).astype(np.float32)
+    tok = draw_tokens(rng, softmax64(d))
+    a = oracle_mod.verify(t, d, tok, 1.0, seed=6)
+    for top_k, top_p in [(0, 1.0), (V, 1.0), (V + 5, 1.0), (-1, 1.0)]:
+        b = oracle_mod.verify(t, d, tok, 1.0, seed=6, top_k=top_k, top_p=top_p)
+        for k in a:
+            np.testing.assert_array_equal(a[k], b[k])
+
+
+def _draw_filtered(rng, rows, T, top_k, top_p, n):
+    """n draws per position from the brute-force filtered rows [K, V]."""
+    q = np.stack([brute_filter(r, T, top_k, top_p)[2] for r in rows])
+    return draw_tokens(rng, np.broadcast_to(q, (n,) + q.shape))
+
+
+@pytest.mark.parametrize("V,K,top_k,top_p", [(8, 2, 4, 1.0), (8, 3, 0, 0.8), (10, 2, 6, 0.75),
+                                             (6, 2, 2, 1.0)])
+def test_filtered_output_marginal_chisquare(oracle_mod, V, K, top_k, top_p):
+    """With both rows filtered and drafts drawn from q', the token emitted at
+    every reached position follows the filtered target p'."""
+    from scipy import stats
+    n, T = 300_000, 0.8
+    Tw = float(np.float32(T))
+    rng = np.random.default_rng(V * 1000 + K * 10 + top_k)
+    t, d = _random_rows(rng, K, V)
+    d = (0.7 * t[:K] + 0.5 * d).astype(np.float32)  # a draft that overlaps the target
+    tokens = _draw_filtered(rng, d, Tw, top_k, top_p, n)
+    res = oracle_mod.verify(np.broadcast_to(t, (n, K + 1, V)).copy(),
+                            np.broadcast_to(d, (n, K, V)).copy(), tokens, T, seed=77,
+                            threads=8, top_k=top_k, top_p=top_p)
+    assert (res["seq_status"] == 0).all()
+    na = res["num_accepted"]
+    for i in range(K + 1):
+        pf = brute_filter(t[i], Tw, top_k, top_p)[2]
+        sel = na >= i
+        assert sel.sum() > n // 50, (i, sel.sum())
+        counts = np.bincount(res["out_tokens"][sel, i], minlength=V)
+        assert counts[pf == 0].sum() == 0, (i, counts, pf)
+        keep = pf > 0
+        if keep.sum() > 1:
+            pv = stats.chisquare(counts[keep], pf[keep] * sel.sum()).pvalue
+            assert pv > 1e-3 / (K + 1), (i, counts, pf)
+
+
+def test_filtered_acceptance_rate(oracle_mod):
+    """P(accept at 0) = sum_x min(p'(x), q'(x)) with x ~ q'."""
+    n, V, K, T, top_k, top_p = 400_000, 9, 1, 1.0, 5, 0.85
+    rng = np.random.default_rng(31)
+    t, d = _random_rows(rng, K, V)
+    tokens = _draw_filtered(rng, d, T, top_k, top_p, n)
+    res = oracle_mod.verify(np.broadcast_to(t, (n, K + 1, V)).copy(),
+                            np.broadcast_to(d, (n, K, V)).copy(), tokens, T, seed=5, threads=8,
+                            top_k=top_k, top_p=top_p)
+    beta = np.minimum(brute_filter(t[0], T, top_k, top_p)[2],
+                      brute_filter(d[0], T, top_k, top_p)[2]).sum()
+    f = np.mean(res["num_accepted"] >= 1)
+    assert abs(f - beta) < 5 * math.sqrt(beta * (1 - beta) / n)
+
+
+def test_token_outside_filtered_rows_is_rejected(oracle_mod):
+    """top-k = 1 on rows that share their maximum: p' = q' = one-hot at it. A
+    draft token anywhere else has p'(x) = q'(x) = 0 and is rejected; the
+    residual is empty, so the emitted token is the draw from p': the maximum."""
+    V, K, B = 12, 3, 64
+    rng = np.random.default_rng(2)
+    t = rng.normal(size=(B, K + 1, V)).astype(np.float32)
+    d = rng.normal(size=(B, K, V)).astype(np.float32)
+    t[:, :, 5] = 10.0
+    d[:, :, 5] = 9.0
+    tok = np.full((B, K), 5, dtype=np.int32)
+    pos = rng.integers(0, K, size=B)
+    other = rng.integers(0, V - 1, size=B)
+    other = other + (other >= 5)
+    tok[np.arange(B), pos] = other
+    r = oracle_mod.verify(t, d, tok, 1.0, seed=3, top_k=1)
+    np.testing.assert_array_equal(r["num_accepted"], pos)
+    np.testing.assert_array_equal(r["out_tokens"][np.arange(B), pos], 5)
+    # unfiltered, the same tokens have p, q > 0 and some survive
+    u = oracle_mod.verify(t, d, tok, 1.0, seed=3)
+    assert (u["num_accepted"] > pos).any()
+
+
+def test_filtered_p_equals_q_accepts_everything(oracle_mod):
+    from scipy import stats
+    V, K, n, top_k, top_p = 9, 2, 200_000, 6, 0.9
+    rng = np.random.default_rng(12)
+    t, _ = _random_rows(rng, K, V)
+    tokens = _draw_filtered(rng, t[:K], 1.0, top_k, top_p, n)
+    res = oracle_mod.verify(np.broadcast_to(t, (n, K + 1, V)).copy(),
+                            np.broadcast_to(t[:K], (n, K, V)).copy(), tokens, 1.0, seed=9,
+                            threads=8, top_k=top_k, top_p=top_p)
+    assert (res["num_accepted"] == K).all()
+    pf = brute_filter(t[K], 1.0, top_k, top_p)[2]
+    counts = np.bincount(res["out_tokens"][:, K], minlength=V)
+    keep = pf > 0
+    assert counts[~keep].sum() == 0
+    assert stats.chisquare(counts[keep], pf[keep] * n).pvalue > 1e-3
+
+
+def test_filter_margins_reported(oracle_mod):
+    rng = np.random.default_rng(4)
+    B, K, V, top_p = 20, 2, 15, 0.7
+    t = rng.normal(size=(B, K + 1, V)).astype(np.float32)
+    d = rng.normal(size=(B, K, V)).astype(np.float32)
+    tok = draw_tokens(rng, softmax64(d))
+    r = oracle_mod.verify(t, d, tok, 1.0, seed=1, top_k=8, top_p=top_p)
+    for b in range(B):
+        for i in range(K + 1):
+            assert math.isclose(r["filter_margin_t"][b, i],
+                                brute_filter(t[b, i], 1.0, 8, float(np.float32(top_p)))[3],
+                                rel_tol=1e-9, abs_tol=1e-12)
+        for i in range(K):
+            assert math.isclose(r["filter_margin_d"][b, i],
+                                brute_filter(d[b, i], 1.0, 8, float(np.float32(top_p)))[3],
+                                rel_tol=1e-9, abs_tol=1e-12)
