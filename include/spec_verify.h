@@ -289,6 +289,76 @@ int spec_verify_sharded(const void* const* target_shards, const void* const* dra
                         void* stream);
 
 /*
+ * Workspace needed by spec_verify_filtered for these sizes on the CURRENT
+ * device. Writes the byte count to *bytes.
+ */
+int sv_filtered_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode,
+                                size_t* bytes);
+
+/*
+ * spec_verify with top-k / top-p applied to both distributions of every
+ * position ("Speculative decoding" (aihero.vn), the paragraph on
+ * temperature, top-k and top-p: the draft and the target get the same
+ * transform). Each row's softmax at `temperature` is cut to the tokens whose
+ * logit is >= a threshold and renormalised over them:
+ *   top-k  keep the logits >= the top_k-th largest (ties at the boundary are
+ *          kept); top_k = 0 or top_k >= V: no top-k cut;
+ *   top-p  inside the top-k set, keep the logits >= the largest value v whose
+ *          upper set {x >= v} holds at least top_p of the set's mass;
+ *          top_p = 1: no top-p cut.
+ * The filtered rows p' and q' then replace p and q everywhere: acceptance
+ * min(1, p'(x)/q'(x)) (a draft token with p'(x) = 0 is rejected), the
+ * residual max(0, p' - q'), the bonus draw from p'_K. Draft tokens should be
+ * drawn from q' for the output to follow p'.
+ *   top_k   >= 0 (SV_ERR_ARG otherwise).
+ *   top_p   in (0, 1] (SV_ERR_ARG otherwise, NaN included).
+ * Other arguments, outputs and errors as spec_verify; the workspace is
+ * sv_filtered_workspace_bytes. Greedy mode ignores both cuts (they never
+ * remove a row's maximum), and with both cuts off the call is spec_verify.
+ * Thresholds are exact (integer work on the logits' order); the top-p
+ * boundary's masses are 64-bit fixed point, so a boundary that the exact
+ * masses put within 1e-5 of top_p (relative to the top-k mass) may fall on
+ * the other side. Not combined with early exit or sharded logits. Calls make
+ * 4 launches: thresholds, scan, and the two sampler launches.
+ */
+int spec_verify_filtered(const void* target_logits, const void* draft_logits,
+                         const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
+                         float temperature, int64_t top_k, float top_p, uint64_t seed, int mode,
+                         int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify_filtered plus per-row diagnostics (each output optional, NULL
+ * to skip; device memory):
+ *   lse_t [B, K+1], lse_d [B, K]  float64, natural-log normaliser of the KEPT
+ *                                 tokens: log sum over x >= thr of exp(x / T);
+ *   thr_t [B, K+1], thr_d [B, K]  float32, each row's threshold: a token is
+ *                                 kept when its logit is >= it (-inf: no cut);
+ *   seq_status [B]                int32, SV_SEQ_* bits (0 = valid).
+ * Rows of invalid sequences hold unspecified values. lse_* must be 8-byte
+ * aligned, the others 4-byte aligned (SV_ERR_ALIGN).
+ */
+int spec_verify_filtered_debug(const void* target_logits, const void* draft_logits,
+                               const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                               int dtype, float temperature, int64_t top_k, float top_p,
+                               uint64_t seed, int mode, int32_t* out_tokens,
+                               int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                               void* stream, double* lse_t, double* lse_d, float* thr_t,
+                               float* thr_d, int32_t* seq_status);
+
+/*
+ * spec_verify_filtered with n_events >= 4 cudaEvent_t handles recorded on
+ * `stream` before the thresholds launch, after it, after the scan and after
+ * the sampler (launches are then not chained programmatically).
+ */
+int spec_verify_filtered_timed(const void* target_logits, const void* draft_logits,
+                               const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                               int dtype, float temperature, int64_t top_k, float top_p,
+                               uint64_t seed, int mode, int32_t* out_tokens,
+                               int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                               void* stream, void* const* events, int n_events);
+
+/*
  * The Philox4x32-10 generator the verification kernels draw from, evaluated on
  * the device for caller-chosen counters. The pages have no counterpart to this
  * entry point: it exists so that the device generator can be checked word for

@@ -98,7 +98,7 @@ def lib() -> ctypes.CDLL:
             L.svo_verify.restype = i32
             L.svo_verify_filtered.argtypes = [vp, vp, vp, i64, i64, i64, i32, dbl, u64, i32, i64,
                                               dbl, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                              vp]
+                                              vp, vp, vp]
             L.svo_verify_filtered.restype = i32
             L.svo_filter_row.argtypes = [vp, i64, i32, dbl, dbl, i64, dbl, vp, vp, vp]
             L.svo_filter_row.restype = i32
@@ -242,6 +242,8 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
         "sample_margin": np.full(B, np.nan),
         "filter_margin_t": np.full((B, K + 1), np.inf),
         "filter_margin_d": np.full((B, K), np.inf),
+        "filter_thr": np.full((B, 2 * K + 1), np.nan),
+        "filter_log_mass": np.full((B, 2 * K + 1), np.nan),
         "seq_status": np.full(B, -7, dtype=np.int32),
     }
     P = float(np.float32(top_p))
@@ -255,6 +257,7 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
                                    _ptr(out["lse_d"]), _ptr(out["log_ratio"]),
                                    _ptr(out["accept_margin"]), _ptr(out["sample_margin"]),
                                    _ptr(out["filter_margin_t"]), _ptr(out["filter_margin_d"]),
+                                   _ptr(out["filter_thr"]), _ptr(out["filter_log_mass"]),
                                    _ptr(out["seq_status"]))
         if rc != 0:
             raise ValueError("oracle rejected its arguments")

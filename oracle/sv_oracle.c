@@ -357,7 +357,8 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
                             int64_t top_k, double top_p, int32_t* out_tokens,
                             int32_t* num_accepted, double* lse_t_out, double* lse_d_out,
                             double* log_ratio_out, double* accept_margin, double* sample_margin,
-                            double* fm_t, double* fm_d, int32_t* seq_status)
+                            double* fm_t, double* fm_d, double* thr_out, double* lm_out,
+                            int32_t* seq_status)
 {
     const int filtering = (top_k > 0 && top_k < V) || top_p < 1.0;
     const size_t esz = (dtype == SVO_F32) ? 4 : 2;
@@ -419,6 +420,11 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
             if (fm_d) fm_d[b * K + i] = mg;
         }
     }
+    /* Thresholds and log kept masses, [B][2K + 1] (target rows, then draft). */
+    if (thr_out)
+        for (i = 0; i <= 2 * K; ++i) thr_out[b * (2 * K + 1) + i] = thr[i];
+    if (lm_out)
+        for (i = 0; i <= 2 * K; ++i) lm_out[b * (2 * K + 1) + i] = lm[i];
 
     /* Log ratio log p_i(x_i) - log q_i(x_i) at every position (diagnostic). */
     for (i = 0; i < K; ++i) {
@@ -533,7 +539,7 @@ int svo_verify(const void* target, const void* draft, const int32_t* tokens,
 {
     return svo_verify_filtered(target, draft, tokens, B, K, V, dtype, T, seed, mode, 0, 1.0, b0,
                                b1, out_tokens, num_accepted, lse_t, lse_d, log_ratio,
-                               accept_margin, sample_margin, NULL, NULL, seq_status);
+                               accept_margin, sample_margin, NULL, NULL, NULL, NULL, seq_status);
 }
 
 int svo_verify_filtered(const void* target, const void* draft, const int32_t* tokens,
@@ -542,7 +548,7 @@ int svo_verify_filtered(const void* target, const void* draft, const int32_t* to
                         int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
                         double* lse_d, double* log_ratio, double* accept_margin,
                         double* sample_margin, double* filter_margin_t, double* filter_margin_d,
-                        int32_t* seq_status)
+                        double* filter_thr, double* filter_log_mass, int32_t* seq_status)
 {
     int64_t b;
     if (!(top_p > 0.0 && top_p <= 1.0)) return -1;
@@ -557,7 +563,8 @@ int svo_verify_filtered(const void* target, const void* draft, const int32_t* to
         if (mode == SVO_SAMPLE)
             verify_sampling(target, draft, tokens, b, K, V, dtype, T, seed, top_k, top_p,
                             out_tokens, num_accepted, lse_t, lse_d, log_ratio, accept_margin,
-                            sample_margin, filter_margin_t, filter_margin_d, seq_status);
+                            sample_margin, filter_margin_t, filter_margin_d, filter_thr,
+                            filter_log_mass, seq_status);
         else
             verify_greedy(target, tokens, b, K, V, dtype, out_tokens, num_accepted,
                           accept_margin, sample_margin, seq_status);

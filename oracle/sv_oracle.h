@@ -119,8 +119,10 @@ int svo_filter_row(const void* row, int64_t V, int dtype, double T, double lse, 
  * before the acceptance test and the residual / bonus draw (greedy mode
  * ignores the filters: they never remove a row's maximum). filter_margin_t
  * [B, K+1] and filter_margin_d [B, K] (optional) get each row's top-p boundary
- * margin. top_p must lie in (0, 1]. A draft token the filtered target gives
- * probability 0 is rejected.
+ * margin; filter_thr and filter_log_mass [B, 2K+1] (optional: target rows 0..K,
+ * then draft rows 0..K-1) each row's threshold and log kept mass (-inf and 0
+ * without filtering). top_p must lie in (0, 1]. A draft token the filtered
+ * target gives probability 0 is rejected.
  */
 int svo_verify_filtered(const void* target, const void* draft, const int32_t* tokens,
                         int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
@@ -128,7 +130,7 @@ int svo_verify_filtered(const void* target, const void* draft, const int32_t* to
                         int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
                         double* lse_d, double* log_ratio, double* accept_margin,
                         double* sample_margin, double* filter_margin_t, double* filter_margin_d,
-                        int32_t* seq_status);
+                        double* filter_thr, double* filter_log_mass, int32_t* seq_status);
 
 #ifdef __cplusplus
 }

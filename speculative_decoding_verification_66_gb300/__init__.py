@@ -20,11 +20,15 @@ from .api import (  # noqa: F401
     spec_verify,
     spec_verify_debug,
     spec_verify_early_exit,
+    spec_verify_filtered,
+    spec_verify_filtered_debug,
+    spec_verify_filtered_timed,
     spec_verify_host,
     spec_verify_sharded,
     spec_verify_static,
     spec_verify_timed,
     sv_early_exit_workspace_bytes,
+    sv_filtered_workspace_bytes,
     sv_host_staging_bytes,
     sv_sharded_workspace_bytes,
     sv_philox,

@@ -246,6 +246,91 @@ def spec_verify_sharded(target_shards, draft_shards, draft_tokens, temperature: 
     return out_tokens, num_accepted
 
 
+def sv_filtered_workspace_bytes(B: int, K: int, V: int, dtype, mode) -> int:
+    n = ctypes.c_size_t(0)
+    d = dtype_code(dtype) if isinstance(dtype, torch.dtype) else int(dtype)
+    _check(_lib.load().sv_filtered_workspace_bytes(B, K, V, d, mode_code(mode), ctypes.byref(n)),
+           "sv_filtered_workspace_bytes")
+    return int(n.value)
+
+
+def spec_verify_filtered(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
+                         top_k: int = 0, top_p: float = 1.0, seed: int = 0, mode="sample", *,
+                         out_tokens=None, num_accepted=None, workspace=None, stream=None,
+                         events=None):
+    """spec_verify with top-k / top-p applied to both rows of every position
+    (top_k = 0 and top_p = 1.0: off). ``events``: 4 torch.cuda.Event(enable_timing=True)
+    recorded before the thresholds launch, after it, after the scan and after the
+    sampler."""
+    m = mode_code(mode)
+    B, K, V = _shapes(target_logits, draft_logits, draft_tokens, m)
+    dev = target_logits.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    d = dtype_code(target_logits.dtype)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_filtered_workspace_bytes(B, K, V, d, m))
+    args = [_ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature), int(top_k),
+            float(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream)]
+    with torch.cuda.device(dev):
+        if events is None:
+            _check(_lib.load().spec_verify_filtered(*args), "spec_verify_filtered")
+        else:
+            for e in events:
+                if not e.cuda_event:  # created lazily by torch on the first record
+                    e.record(stream)
+            handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+            _check(_lib.load().spec_verify_filtered_timed(*args, handles, len(events)),
+                   "spec_verify_filtered_timed")
+    return out_tokens, num_accepted
+
+
+def spec_verify_filtered_debug(target_logits, draft_logits, draft_tokens,
+                               temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+                               seed: int = 0, mode="sample", *, workspace=None,
+                               stream=None) -> dict:
+    """spec_verify_filtered plus each row's kept-token normaliser and threshold."""
+    m = mode_code(mode)
+    B, K, V = _shapes(target_logits, draft_logits, draft_tokens, m)
+    dev = target_logits.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    d = dtype_code(target_logits.dtype)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_filtered_workspace_bytes(B, K, V, d, m))
+    out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+           "num_accepted": torch.empty((B,), dtype=torch.int32, device=dev),
+           "lse_t": torch.full((B, K + 1), float("nan"), dtype=torch.float64, device=dev),
+           "lse_d": torch.full((B, K), float("nan"), dtype=torch.float64, device=dev),
+           "thr_t": torch.full((B, K + 1), float("nan"), dtype=torch.float32, device=dev),
+           "thr_d": torch.full((B, K), float("nan"), dtype=torch.float32, device=dev),
+           "seq_status": torch.full((B,), -7, dtype=torch.int32, device=dev)}
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_filtered_debug(
+            _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature), int(top_k),
+            float(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out["out_tokens"]),
+            _ptr(out["num_accepted"]), _ptr(workspace), workspace.numel(),
+            ctypes.c_void_p(stream.cuda_stream), _ptr(out["lse_t"]), _ptr(out["lse_d"]),
+            _ptr(out["thr_t"]), _ptr(out["thr_d"]), _ptr(out["seq_status"])),
+            "spec_verify_filtered_debug")
+    return out
+
+
+def spec_verify_filtered_timed(target_logits, draft_logits, draft_tokens, events,
+                               temperature: float = 1.0, top_k: int = 0, top_p: float = 1.0,
+                               seed: int = 0, mode="sample", **kw):
+    """spec_verify_filtered with its 4 timing events (see there)."""
+    return spec_verify_filtered(target_logits, draft_logits, draft_tokens, temperature, top_k,
+                                top_p, seed, mode, events=events, **kw)
+
+
 def spec_verify_debug(target_logits, draft_logits, draft_tokens, temperature: float = 1.0,
                       seed: int = 0, mode="sample", *, workspace=None, stream=None) -> dict:
     """spec_verify plus the normalisers, log-ratios and per-sequence status."""

@@ -78,18 +78,23 @@ struct RowPair {
     int32_t j;             // the emitted position (the row index within the sequence)
     float c, mt, md;       // c = log2(e) / T; mt, md: the rows' reference exponents
     float r;               // 2^(lt - ld): the draft term's scale relative to the target's
+    float tt, td;          // top-k / top-p thresholds of the two rows (filtered runs)
 };
 
 // Sampling weight of one token from its logits, up to a factor common to the
 // whole row pair: max(0, p - q) 2^lt after a rejection, p 2^lt for the bonus
 // (log2 p = x c - mt - lt, see SeqRecord). Both race levels compare weights of
 // one row pair only, so the common factor changes no decision; it saves the
-// per-token subtraction of lt and ld.
+// per-token subtraction of lt and ld. Filtered (F): p and q are the filtered
+// rows, 0 below each row's threshold.
+template <bool F>
 __device__ __forceinline__ float weight_of(const RowPair& rp, float xt, float xd)
 {
-    const float p = ex2(fmaf(xt, rp.c, -rp.mt));
+    float p = ex2(fmaf(xt, rp.c, -rp.mt));
+    if (F && !(xt >= rp.tt)) p = 0.f;
     if (rp.drow == nullptr) return p;
-    const float q = ex2(fmaf(xd, rp.c, -rp.md));
+    float q = ex2(fmaf(xd, rp.c, -rp.md));
+    if (F && !(xd >= rp.td)) q = 0.f;
     return fmaxf(fmaf(-q, rp.r, p), 0.0f);
 }
 
@@ -158,6 +163,8 @@ __device__ __forceinline__ int load_seq(SeqJob& s, const SampleArgs& a, int64_t 
     s.rp.mt = rec.mt;
     s.rp.md = rec.md;
     s.rp.r = rec.j < K ? exp2f(rec.lt - rec.ld) : 1.0f;
+    s.rp.tt = rec.tt;
+    s.rp.td = rec.td;
     return rec.j;
 }
 
@@ -218,11 +225,12 @@ __device__ __forceinline__ void group_load(const SampleArgs& a, const RowPair& r
 }
 
 // Weights of a loaded group (0 for tokens past the vocabulary).
+template <bool F>
 __device__ __forceinline__ void group_weights(const RowPair& rp, int64_t k0, int64_t V,
                                               const float (&xt)[4], const float (&xd)[4], float (&w)[4])
 {
 #pragma unroll
-    for (int q = 0; q < 4; ++q) w[q] = k0 + q < V ? weight_of(rp, xt[q], xd[q]) : 0.f;
+    for (int q = 0; q < 4; ++q) w[q] = k0 + q < V ? weight_of<F>(rp, xt[q], xd[q]) : 0.f;
 }
 
 // Race step over one group of four candidates with weights w (indices
@@ -344,7 +352,7 @@ __device__ __forceinline__ void issue_slice(const SampleArgs& a, const SeqJob& s
 // Per-lane weight sums of the race blocks of one staged slice of n tokens
 // (acc[k]: block k of the slice). Aligned rows: lane l reads vectors
 // l, l + 32, ... of each row; other rows: elements l, l + 32, ....
-template <int ES, bool ALIGNED>
+template <int ES, bool ALIGNED, bool F>
 __device__ __forceinline__ void sum_slice(const RowPair& rp, const uint8_t* st, int off_t, int off_d,
                                           int n, int lane, float (&acc)[Geo<ES>::kBlocks])
 {
@@ -365,7 +373,7 @@ __device__ __forceinline__ void sum_slice(const RowPair& rp, const uint8_t* st, 
 #pragma unroll
                 for (int e = 0; e < G::kEPV; ++e) xd[e] = 0.f;
 #pragma unroll
-            for (int e = 0; e < G::kEPV; ++e) acc[q / G::kQPB] += weight_of(rp, xt[e], xd[e]);
+            for (int e = 0; e < G::kEPV; ++e) acc[q / G::kQPB] += weight_of<F>(rp, xt[e], xd[e]);
         }
     } else {
 #pragma unroll
@@ -376,7 +384,7 @@ __device__ __forceinline__ void sum_slice(const RowPair& rp, const uint8_t* st, 
                 if (e >= n) break;
                 const float xt = elem<ES>(bt + e * ES);
                 const float xd = rp.drow ? elem<ES>(bd + e * ES) : 0.f;
-                acc[k] += weight_of(rp, xt, xd);
+                acc[k] += weight_of<F>(rp, xt, xd);
             }
         }
     }
@@ -403,7 +411,7 @@ __device__ __forceinline__ void store_sums(const SampleArgs& a, int64_t b, int64
 // warp takes a contiguous run of slices with a two-stage ring: lane 0 copies
 // slice i + 1 while the warp sums slice i from the other stage, and writes the
 // weight sum of each race block of the slice.
-template <int ES, bool ALIGNED>
+template <int ES, bool ALIGNED, bool F>
 __global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const __grid_constant__ SampleArgs a)
 {
     using G = Geo<ES>;
@@ -476,7 +484,7 @@ __global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const __grid_const
             float acc[G::kBlocks];
 #pragma unroll
             for (int q = 0; q < G::kBlocks; ++q) acc[q] = 0.f;
-            sum_slice<ES, ALIGNED>(cur.rp, stage(s), stage_offset<ALIGNED>(cur.rp.trow, e0, ES),
+            sum_slice<ES, ALIGNED, F>(cur.rp, stage(s), stage_offset<ALIGNED>(cur.rp.trow, e0, ES),
                                    cur.rp.drow ? stage_offset<ALIGNED>(cur.rp.drow, e0, ES) : 0, n,
                                    lane, acc);
 #pragma unroll
@@ -542,7 +550,7 @@ __device__ __forceinline__ float cta_sum(float x, float* red)
 // groups of four blocks t, t + kRaceThreads, ... of the block sums (one Philox
 // block per group). Level 2: thread t takes four-token group t of the winning
 // block. Writes out_tokens[b, j].
-template <int ES, bool ALIGNED>
+template <int ES, bool ALIGNED, bool F>
 __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_constant__ SampleArgs a)
 {
     __shared__ Best red[kRaceWarps];
@@ -585,7 +593,7 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_
             const int64_t k0 = c * kRaceBlock + 4 * t;
             float xt[4], xd[4], w[4];
             group_load<ES, ALIGNED>(a, sj.rp, b, k0, g.V, xt, xd);
-            group_weights(sj.rp, k0, g.V, xt, xd, w);
+            group_weights<F>(sj.rp, k0, g.V, xt, xd, w);
             const float sc = cta_sum(((w[0] + w[1]) + w[2]) + w[3], redf);
             if (t == 0 && sc > 0.f) {
                 const uint4 r = philox4x32_10(
@@ -603,7 +611,7 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_
         const int64_t k0 = static_cast<int64_t>(blk.idx) * kRaceBlock + 4 * t;
         float xt[4], xd[4], w[4];
         group_load<ES, ALIGNED>(a, sj.rp, b, k0, g.V, xt, xd);
-        group_weights(sj.rp, k0, g.V, xt, xd, w);
+        group_weights<F>(sj.rp, k0, g.V, xt, xd, w);
         race_group(tok, w, k0, make_uint4(pos, seq, 1u + static_cast<uint32_t>(k0 >> 2), 0u), key);
     }
     tok = cta_best(tok, red);
@@ -619,18 +627,26 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_
     }
 }
 
-template <int ES, bool ALIGNED>
+template <int ES, bool ALIGNED, bool F>
 cudaError_t launch_sampler(const SampleArgs& a, cudaStream_t s)
 {
     const int smem = kWarps * kWarpRing;
-    cudaError_t e = cudaFuncSetAttribute(sample_stream_kernel<ES, ALIGNED>,
+    cudaError_t e = cudaFuncSetAttribute(sample_stream_kernel<ES, ALIGNED, F>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    e = launch_dependent(a.g.pdl != 0, sample_stream_kernel<ES, ALIGNED>, dim3(a.g.sample_grid),
+    e = launch_dependent(a.g.pdl != 0, sample_stream_kernel<ES, ALIGNED, F>, dim3(a.g.sample_grid),
                          dim3(kT), static_cast<size_t>(smem), s, a);
     if (e != cudaSuccess) return e;
-    return launch_dependent(a.g.pdl != 0, sample_race_kernel<ES, ALIGNED>,
+    return launch_dependent(a.g.pdl != 0, sample_race_kernel<ES, ALIGNED, F>,
                             dim3(static_cast<unsigned>(a.g.B)), dim3(kRaceThreads), 0, s, a);
+}
+
+template <bool F>
+cudaError_t launch_sampler_f(const SampleArgs& a, cudaStream_t s)
+{
+    if (a.g.aligned)
+        return a.g.es == 2 ? launch_sampler<2, true, F>(a, s) : launch_sampler<4, true, F>(a, s);
+    return a.g.es == 2 ? launch_sampler<2, false, F>(a, s) : launch_sampler<4, false, F>(a, s);
 }
 
 // Sharded verification: CTA (2 b + r, x) copies a chunk of the emitted target
@@ -693,8 +709,7 @@ cudaError_t launch_gather_pairs(const GatherArgs& a, cudaStream_t s)
 
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s)
 {
-    if (a.g.aligned) return a.g.es == 2 ? launch_sampler<2, true>(a, s) : launch_sampler<4, true>(a, s);
-    return a.g.es == 2 ? launch_sampler<2, false>(a, s) : launch_sampler<4, false>(a, s);
+    return a.filtered ? launch_sampler_f<true>(a, s) : launch_sampler_f<false>(a, s);
 }
 
 int sample_tokens_per_slice(int es) { return es == 2 ? Geo<2>::kTok : Geo<4>::kTok; }
@@ -702,13 +717,13 @@ int sample_tokens_per_slice(int es) { return es == 2 ? Geo<2>::kTok : Geo<4>::kT
 cudaError_t sample_blocks_per_sm(int es, int* blocks)
 {
     const int smem = kWarps * kWarpRing;
-    auto* k = es == 2 ? sample_stream_kernel<2, false> : sample_stream_kernel<4, false>;
+    auto* k = es == 2 ? sample_stream_kernel<2, false, false> : sample_stream_kernel<4, false, false>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int b1 = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b1, k, kT, smem);
     if (e != cudaSuccess) return e;
-    auto* ka = es == 2 ? sample_stream_kernel<2, true> : sample_stream_kernel<4, true>;
+    auto* ka = es == 2 ? sample_stream_kernel<2, true, false> : sample_stream_kernel<4, true, false>;
     e = cudaFuncSetAttribute(ka, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     int b2 = 0;

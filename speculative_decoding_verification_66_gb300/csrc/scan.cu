@@ -47,10 +47,11 @@ __device__ __forceinline__ int cta_of_tile(int64_t t, int64_t tiles, const Geome
 // l, l + 32, ... (online), then the lanes combine over a fixed butterfly.
 // Sampling -> the row's log2 normaliser as (m, l): integer-valued exponent m
 // and l = log2 of the float-pair sum; greedy -> argmax. Every lane returns the
-// same values.
+// same values. thr: the row's top-k / top-p threshold (-inf: unfiltered).
 struct RowNorm {
     float m;
     float l;
+    float thr;
 };
 
 __device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int lane, RowNorm* norm,
@@ -112,6 +113,7 @@ __device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int la
         if (!ok) fl |= kFlagNonFinite;  // all -inf, or a sum that is not finite
         norm->m = M;
         norm->l = l;
+        norm->thr = __uint_as_float(kF32NegInfBits);
     } else {
         *argmax = (idx == INT_MAX) ? 0 : idx;  // a row of -inf only: index 0
     }
@@ -235,9 +237,15 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
     const int lane = threadIdx.x & 31;
     for (int q = threadIdx.x >> 5; q < nrows; q += blockDim.x >> 5) {
         const int64_t row = q < m.nt ? sq * m.nt + q : nseq * m.nt + sq * m.nd + (q - m.nt);
-        RowNorm nm{0.f, 0.f};
+        RowNorm nm{0.f, 0.f, 0.f};
         int am = 0, fl = 0;
-        merge_row(a, row, tiles, lane, &nm, &am, &fl);
+        if (a.filt != nullptr) {
+            const FiltRow fr = a.filt[row];
+            nm = RowNorm{fr.m, fr.l, fr.thr};
+            fl = fr.flags;
+        } else {
+            merge_row(a, row, tiles, lane, &nm, &am, &fl);
+        }
         if (lane == 0) {
             if (!sampling) nm.m = __int_as_float(am);
             sh[q] = nm;
@@ -254,12 +262,16 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
             if (sampling) {
                 const RowNorm nt = sh[q], nd = sh[m.nt + q];
                 // log2 p_i(x) and log2 q_i(x): the fma is exact before its one
-                // rounding, and the normaliser's parts enter separately.
-                const float lp2 = fmaf(stx[q], a.c, -nt.m) - nt.l;
-                const float lq2 = fmaf(sdx[q], a.c, -nd.m) - nd.l;
+                // rounding, and the normaliser's parts enter separately. A
+                // token below a row's threshold has probability 0 there; one
+                // the (filtered) target gives 0 is rejected.
+                const bool in_t = stx[q] >= nt.thr, in_d = sdx[q] >= nd.thr;
+                const float ninf = __uint_as_float(kF32NegInfBits);
+                const float lp2 = in_t ? fmaf(stx[q], a.c, -nt.m) - nt.l : ninf;
+                const float lq2 = in_d ? fmaf(sdx[q], a.c, -nd.m) - nd.l : ninf;
                 const float lr2 = lp2 - lq2;
                 if (a.log_ratio) a.log_ratio[b * K + i] = static_cast<double>(lr2) * kLn2;
-                const float r = lr2 >= 0.f ? 1.f : ex2(lr2);
+                const float r = !in_t ? 0.f : (lr2 >= 0.f ? 1.f : ex2(lr2));
                 const float u = word_to_uniform(
                     verify_random_words(a.seed, static_cast<uint32_t>(b), static_cast<uint32_t>(i)).x);
                 reject = !(u < r);
@@ -275,6 +287,10 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
     const int j = s_j;
     const bool decided = status != 0 || j < p0 + npos || has_bonus;
     if (sampling && !phased) {
+        for (int q = threadIdx.x; q < m.nt; q += blockDim.x)
+            if (a.thr_t) a.thr_t[b * (K + 1) + q] = sh[q].thr;
+        for (int q = threadIdx.x; q < m.nd; q += blockDim.x)
+            if (a.thr_d) a.thr_d[b * K + q] = sh[m.nt + q].thr;
         for (int q = threadIdx.x; q < m.nt; q += blockDim.x)
             if (a.lse_t)
                 a.lse_t[b * (K + 1) + q] =
@@ -309,13 +325,15 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
                 rec.j = j;
                 rec.status = status;
                 rec.mt = rec.lt = rec.md = rec.ld = 0.f;
-                rec.pad[0] = rec.pad[1] = 0;
+                rec.tt = rec.td = __uint_as_float(kF32NegInfBits);
                 if (status == 0) {
                     rec.mt = sh[j - p0].m;
                     rec.lt = sh[j - p0].l;
+                    rec.tt = sh[j - p0].thr;
                     if (j < K) {
                         rec.md = sh[m.nt + j - p0].m;
                         rec.ld = sh[m.nt + j - p0].l;
+                        rec.td = sh[m.nt + j - p0].thr;
                     }
                 }
                 a.seqs[b] = rec;

@@ -23,6 +23,7 @@ struct DeviceCache {
     int sms = 0;
     int blocks[2][2] = {{0, 0}, {0, 0}};  // pass-1 CTAs per SM, [es == 2][mode]
     int sample_blocks[2] = {0, 0};        // sampler CTAs per SM, [es == 2]
+    int filter_blocks[2] = {0, 0};        // filter CTAs per SM, [es == 2]
 };
 std::mutex g_mu;
 DeviceCache g_cache[kMaxDevices];
@@ -45,12 +46,26 @@ int device_limits(int es, int mode, int* sms, int* blocks, int* sample_blocks)
         for (int e = 0; e < 2; ++e)
             if (sv::sample_blocks_per_sm(e ? 2 : 4, &c.sample_blocks[e]) != cudaSuccess)
                 return SV_ERR_CUDA;
+        for (int e = 0; e < 2; ++e)
+            if (sv::filter_blocks_per_sm(e ? 2 : 4, &c.filter_blocks[e]) != cudaSuccess)
+                return SV_ERR_CUDA;
         c.ready = true;
     }
     *sms = c.sms;
     *blocks = c.blocks[es == 2][mode];
     *sample_blocks = c.sample_blocks[es == 2];
-    return (*sms > 0 && *blocks > 0 && *sample_blocks > 0) ? SV_OK : SV_ERR_CUDA;
+    return (*sms > 0 && *blocks > 0 && *sample_blocks > 0 && c.filter_blocks[es == 2] > 0)
+               ? SV_OK
+               : SV_ERR_CUDA;
+}
+
+// Resident filter CTAs per SM on the current device (after device_limits).
+int filter_blocks(int es)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+    std::lock_guard<std::mutex> lock(g_mu);
+    return g_cache[dev].ready ? g_cache[dev].sms * g_cache[dev].filter_blocks[es == 2] : 0;
 }
 
 struct Layout {
@@ -59,6 +74,8 @@ struct Layout {
     size_t still = 0, lists = 0, counters = 0, counter_bytes = 0;
     // Sharded only.
     size_t pairs = 0;
+    // Filtered only: one FiltRow per row.
+    size_t filt = 0;
 };
 
 // Early exit: the positions 0 .. K are verified in phases of 1, 2, 4, ...
@@ -98,7 +115,7 @@ int check_sizes(int64_t B, int64_t K, int64_t V, int dtype, int mode)
 }
 
 int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g, Layout* L,
-              bool early_exit = false, int shards = 1)
+              bool early_exit = false, int shards = 1, bool filtered = false)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -164,6 +181,10 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
         L->pairs = off;
         off += round_up(static_cast<size_t>(2 * B) * static_cast<size_t>(V) * es);
     }
+    if (filtered && mode == SV_SAMPLE) {
+        L->filt = off;
+        off += round_up(static_cast<size_t>(g->rows) * sizeof(sv::FiltRow));
+    }
     if (early_exit) {
         L->still = off;
         off += round_up(static_cast<size_t>(B) * sizeof(int32_t));
@@ -184,10 +205,14 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
         double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
         void* const* events, int n_events, bool early_exit = false,
-        const void* const* t_shards = nullptr, const void* const* d_shards = nullptr, int G = 1)
+        const void* const* t_shards = nullptr, const void* const* d_shards = nullptr, int G = 1,
+        int64_t top_k = 0, float top_p = 1.0f, float* thr_t = nullptr, float* thr_d = nullptr)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
+    if (top_k < 0 || !(top_p > 0.f && top_p <= 1.f)) return SV_ERR_ARG;
+    // Filtering changes sampling only (the cuts keep every row's maximum).
+    const bool filtered = mode == SV_SAMPLE && ((top_k > 0 && top_k < V) || top_p < 1.f);
     float c = 0.f;
     if (mode == SV_SAMPLE) {
         if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_ARG;
@@ -230,15 +255,17 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         !aligned_to(num_accepted, 4) || (seq_status && !aligned_to(seq_status, 4)))
         return SV_ERR_ALIGN;
     if ((lse_t && !aligned_to(lse_t, 8)) || (lse_d && !aligned_to(lse_d, 8)) ||
-        (log_ratio && !aligned_to(log_ratio, 8)))
+        (log_ratio && !aligned_to(log_ratio, 8)) || (thr_t && !aligned_to(thr_t, 4)) ||
+        (thr_d && !aligned_to(thr_d, 4)))
         return SV_ERR_ALIGN;
     if (!aligned_to(workspace, kAlign)) return SV_ERR_WORKSPACE;
 
     Geometry g;
     Layout L;
-    rc = make_plan(B, K, V, dtype, mode, &g, &L, early_exit, G);
+    rc = make_plan(B, K, V, dtype, mode, &g, &L, early_exit, G, filtered);
     if (rc != SV_OK) return rc;
     if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+    if (filtered && (early_exit || G > 1)) return SV_ERR_ARG;
     // Events between the kernels would sit between programmatically chained
     // launches; the timed variant launches them one after the other instead.
     g.pdl = events == nullptr ? 1 : 0;
@@ -274,11 +301,31 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     sv::RowStatsArgs ra{tp, dp, g, c, partials, full, sh};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
-                    sampling ? log_ratio : nullptr, seq_status, full,
+                    sampling ? log_ratio : nullptr, seq_status, full, nullptr,
+                    sampling ? thr_t : nullptr, sampling ? thr_d : nullptr,
                     nullptr, nullptr, nullptr, nullptr, sh};
     sv::SampleArgs pa{sp_t, sp_d, g, c, seed, seqs, block_sums,
-                      out_tokens, num_accepted, seq_status, lay, direct ? 1 : 0, sh};
+                      out_tokens, num_accepted, seq_status, lay, direct ? 1 : 0, sh, 0};
     sv::GatherArgs ga{g, sh, seqs, ws + L.pairs};
+
+    if (filtered) {
+        // Thresholds and kept-mass normalisers of every row replace pass 1.
+        auto* filt = reinterpret_cast<sv::FiltRow*>(ws + L.filt);
+        const int64_t cap = filter_blocks(g.es);
+        if (cap <= 0) return SV_ERR_CUDA;
+        const int grid = static_cast<int>(g.rows < cap ? g.rows : cap);
+        sv::FilterArgs fa{tp, dp, g, c, top_k, top_p, filt};
+        sa.filt = filt;
+        pa.filtered = 1;
+        if (!record(0)) return SV_ERR_CUDA;
+        if (sv::launch_filter(fa, grid, s) != cudaSuccess) return SV_ERR_CUDA;
+        if (!record(1)) return SV_ERR_CUDA;
+        if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
+        if (!record(2)) return SV_ERR_CUDA;
+        if (sv::launch_sample(pa, s) != cudaSuccess) return SV_ERR_CUDA;
+        if (!record(3)) return SV_ERR_CUDA;
+        return SV_OK;
+    }
 
     if (early_exit) {
         // Phases over the positions; each pass 1 reads only the rows of the
@@ -437,6 +484,58 @@ SV_EXPORT int spec_verify_sharded(const void* const* target_shards, const void* 
                nullptr, 0, false, target_shards, draft_shards, G);
 }
 
+SV_EXPORT int sv_filtered_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int mode,
+                                         size_t* bytes)
+{
+    if (bytes == nullptr) return SV_ERR_ARG;
+    Geometry g;
+    Layout L;
+    const int rc = make_plan(B, K, V, dtype, mode, &g, &L, false, 1, true);
+    if (rc != SV_OK) return rc;
+    *bytes = L.total;
+    return SV_OK;
+}
+
+SV_EXPORT int spec_verify_filtered(const void* target_logits, const void* draft_logits,
+                                   const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                                   int dtype, float temperature, int64_t top_k, float top_p,
+                                   uint64_t seed, int mode, int32_t* out_tokens,
+                                   int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                                   void* stream)
+{
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr, nullptr, nullptr, 0, false, nullptr, nullptr, 1, top_k, top_p);
+}
+
+SV_EXPORT int spec_verify_filtered_debug(const void* target_logits, const void* draft_logits,
+                                         const int32_t* draft_tokens, int64_t B, int64_t K,
+                                         int64_t V, int dtype, float temperature, int64_t top_k,
+                                         float top_p, uint64_t seed, int mode,
+                                         int32_t* out_tokens, int32_t* num_accepted,
+                                         void* workspace, size_t workspace_bytes, void* stream,
+                                         double* lse_t, double* lse_d, float* thr_t, float* thr_d,
+                                         int32_t* seq_status)
+{
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, lse_t, lse_d, nullptr,
+               seq_status, nullptr, 0, false, nullptr, nullptr, 1, top_k, top_p, thr_t, thr_d);
+}
+
+SV_EXPORT int spec_verify_filtered_timed(const void* target_logits, const void* draft_logits,
+                                         const int32_t* draft_tokens, int64_t B, int64_t K,
+                                         int64_t V, int dtype, float temperature, int64_t top_k,
+                                         float top_p, uint64_t seed, int mode,
+                                         int32_t* out_tokens, int32_t* num_accepted,
+                                         void* workspace, size_t workspace_bytes, void* stream,
+                                         void* const* events, int n_events)
+{
+    if (events == nullptr) return SV_ERR_ARG;
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr, nullptr, events, n_events, false, nullptr, nullptr, 1, top_k, top_p);
+}
+
 SV_EXPORT int spec_verify_debug(const void* target_logits, const void* draft_logits,
                                 const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
                                 int dtype, float temperature, uint64_t seed, int mode,
@@ -530,4 +629,4 @@ SV_EXPORT const char* sv_error_string(int code)
     }
 }
 
-SV_EXPORT int sv_version(void) { return 103; }
+SV_EXPORT int sv_version(void) { return 104; }

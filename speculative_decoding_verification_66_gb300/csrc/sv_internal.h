@@ -58,12 +58,16 @@ static_assert(sizeof(Partial) == 16, "Partial layout");
 // Per-sequence record written by the acceptance scan, read by the sampler.
 // A row's log2 normaliser log2 sum_k 2^(x_k c) is m + l: m the integer-valued
 // reference exponent, l = log2 of the scaled sum.
+//
+// With top-k / top-p filtering the normalisers are those of the kept tokens,
+// and tt / td are the rows' thresholds: token k keeps its probability when
+// its logit is >= the threshold, else gets 0 (-inf: no filtering).
 struct SeqRecord {
     int32_t j;         // emitted position (0..K)
     int32_t status;    // SV_SEQ_* bits; 0 = valid
     float mt, lt;      // normaliser of target row j
     float md, ld;      // normaliser of draft row j (unused when j == K)
-    int32_t pad[2];
+    float tt, td;      // thresholds of target / draft row j
 };
 static_assert(sizeof(SeqRecord) == 32, "SeqRecord layout");
 
@@ -123,6 +127,29 @@ struct Shards {
     const uint8_t* d[kMaxShards];  // draft shards [B, K, Vs] (unused in greedy mode)
 };
 
+// Top-k / top-p filtering: one record per row of the row space [target rows
+// b (K+1) + i | draft rows B (K+1) + b K + i]. The filtered row keeps the
+// tokens whose logit is >= thr and renormalises over them: log2 p'(x) =
+// x c - m - l for those, with m an integer-valued reference exponent and l
+// = log2 of the kept mass scaled by 2^-m.
+struct FiltRow {
+    float m;
+    float l;
+    float thr;
+    int32_t flags;  // kFlagNonFinite: NaN or +inf in the row, or no finite logit
+};
+static_assert(sizeof(FiltRow) == 16, "FiltRow layout");
+
+struct FilterArgs {
+    const uint8_t* target;
+    const uint8_t* draft;
+    Geometry g;
+    float c;            // log2(e) / T
+    int64_t top_k;      // 0 < top_k < V, else off
+    float top_p;        // in (0, 1); 1 = off
+    FiltRow* rows;      // [B (2K + 1)]
+};
+
 struct RowStatsArgs {
     const uint8_t* target;
     const uint8_t* draft;
@@ -149,6 +176,11 @@ struct ScanArgs {
     double* log_ratio;
     int32_t* seq_status;
     RowMap map;
+    // Filtering only (nullptr otherwise): the rows' normalisers and
+    // thresholds come from here instead of pass 1's partials.
+    const FiltRow* filt;
+    float* thr_t;           // optional: thresholds of the target rows [B, K+1]
+    float* thr_d;           // and of the draft rows [B, K] (full pass only)
     // Early exit only (nullptr otherwise): the sequences still undecided after
     // this phase, compacted in ascending order by the last CTA to finish.
     int32_t* still;         // [B] per listed sequence: 1 if still undecided
@@ -185,6 +217,7 @@ struct SampleArgs {
     // every shard, draft row b K + j), splitting copies at shard boundaries.
     int32_t direct;
     Shards sh;
+    int32_t filtered;       // weights are masked by the records' thresholds
 };
 
 // Sharded verification: copies each sequence's emitted row pair from the
@@ -221,6 +254,9 @@ cudaError_t launch_row_stats(const RowStatsArgs& a, cudaStream_t s);
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 cudaError_t launch_gather_pairs(const GatherArgs& a, cudaStream_t s);
+cudaError_t launch_filter(const FilterArgs& a, int grid, cudaStream_t s);
+// Resident filter CTAs per SM.
+cudaError_t filter_blocks_per_sm(int es, int* blocks);
 
 // Resident pass-1 CTAs per SM for this dtype / mode (occupancy query).
 cudaError_t row_stats_blocks_per_sm(int es, int mode, int* blocks);

@@ -64,14 +64,15 @@ def torch_dtype(name: str) -> torch.dtype:
     return {"f32": torch.float32, "bf16": torch.bfloat16}[name]
 
 
-def make_inputs(wl: Workload, seed: int, device="cpu") -> dict:
+def make_inputs(wl: Workload, seed: int, device="cpu", top_k: int = 0, top_p: float = 1.0) -> dict:
     """Draw one batch for ``wl``.
 
     Returns dict(target [B, K+1, V], draft [B, K, V] or None, tokens [B, K] int32),
     all on ``device``. Noise is drawn in float32 from a generator seeded with
     ``seed`` on ``device``, then stored in the workload's dtype. Draft tokens are
     drawn from the *stored* draft logits, so they follow the draft distribution
-    the verifier sees.
+    the verifier sees; with ``top_k`` / ``top_p`` (0 / 1.0: no cut) from that
+    distribution cut the same way.
     """
     dev = torch.device(device)
     g = torch.Generator(device=dev)
@@ -94,20 +95,45 @@ def make_inputs(wl: Workload, seed: int, device="cpu") -> dict:
     drf.add_(wl.draft_noise * torch.randn((B, K, V), generator=g, device=dev))
     draft = drf.to(dt)
     del tgt, drf
-    tokens = draw_from_logits(draft, wl.temperature, g)
+    tokens = draw_from_logits(draft, wl.temperature, g, top_k, top_p)
     return {"target": target, "draft": draft, "tokens": tokens}
 
 
-def draw_from_logits(logits: torch.Tensor, temperature: float, g: torch.Generator) -> torch.Tensor:
-    """One token per row from softmax(logits / T): what a draft model's sampler does."""
+def _draft_sampler_probs(x: torch.Tensor, temperature: float, top_k: int, top_p: float):
+    """The draft model's own sampling distribution over rows x [n, V] (float32):
+    softmax(x / T), cut to the top_k largest logits and then to the smallest
+    upper set of logit values holding top_p of the rest, as a serving stack's
+    sampler does before it draws. Input generation only."""
+    probs = torch.softmax(x / temperature, dim=-1)
+    V = x.shape[-1]
+    if 0 < top_k < V:
+        kth = torch.topk(x, top_k, dim=-1).values[:, -1:]
+        probs = probs * (x >= kth)
+    if top_p < 1.0:
+        xs, order = torch.sort(x, dim=-1, descending=True)
+        ps = torch.gather(probs, -1, order)
+        csum = torch.cumsum(ps, dim=-1)
+        need = top_p * csum[:, -1:]
+        first = torch.searchsorted(csum.contiguous(), need.contiguous()).clamp_(max=V - 1)
+        thr = torch.gather(xs, -1, first)
+        probs = probs * (x >= thr)
+    return probs / probs.sum(dim=-1, keepdim=True)
+
+
+def draw_from_logits(logits: torch.Tensor, temperature: float, g: torch.Generator,
+                     top_k: int = 0, top_p: float = 1.0) -> torch.Tensor:
+    """One token per row from softmax(logits / T) (optionally top-k / top-p cut):
+    what a draft model's sampler does."""
     B, K, V = logits.shape
     if B * K == 0:
         return torch.zeros((B, K), dtype=torch.int32, device=logits.device)
     out = torch.empty((B * K,), dtype=torch.int64, device=logits.device)
     flat = logits.reshape(B * K, V)
     step = max(1, (1 << 28) // max(V, 1))
+    if top_k > 0 or top_p < 1.0:
+        step = max(1, step // 4)
     for s in range(0, B * K, step):
-        probs = torch.softmax(flat[s:s + step].float() / temperature, dim=-1)
+        probs = _draft_sampler_probs(flat[s:s + step].float(), temperature, top_k, top_p)
         out[s:s + step] = torch.multinomial(probs, 1, generator=g).squeeze(1)
     return out.view(B, K).to(torch.int32)
 

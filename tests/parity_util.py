@@ -63,11 +63,19 @@ def compare(gpu: dict, orc: dict, tokens: np.ndarray, K: int, V: int, rows=None,
             n_dec += min(no + 1, K) + 1
             assert ng == no and np.array_equal(og, oo), f"seq {b}: greedy gpu {og} oracle {oo}"
             continue
-        am = orc["accept_margin"][b]
+        am = orc["accept_margin"][b].copy()
+        s_flag = orc["sample_margin"][b] < FLAG
+        if "filter_margin_t" in orc:
+            # Top-p boundaries: a row whose boundary lies within FLAG of top_p
+            # may keep one more or one fewer group of tokens on either side;
+            # that flags every decision that uses the row.
+            fm_t, fm_d = orc["filter_margin_t"][b], orc["filter_margin_d"][b]
+            if K > 0:
+                am = np.minimum(am, np.minimum(fm_t[:K], fm_d))
+            s_flag = s_flag or fm_t[no] < FLAG or (no < K and fm_d[no] < FLAG)
         decisions = list(range(min(no + 1, K)))
         n_dec += len(decisions) + 1
         first_flag = next((i for i in decisions if am[i] < FLAG), None)
-        s_flag = orc["sample_margin"][b] < FLAG
         if first_flag is not None:
             n_flag_seq += 1
             n_flag_dec += 1

@@ -1,0 +1,256 @@
+"""Parity of spec_verify_filtered (top-k / top-p applied to the target and the
+draft row of every position) with the float64 oracle's filtered verification.
+
+Thresholds are integer work on the logits' order, so they must match exactly;
+a top-p boundary that the oracle puts within 1e-5 (relative) of top_p flags
+the decisions that use its row, like a near-tie of the acceptance draw.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_66_gb300 as sv
+from parity_util import compare
+from speculative_decoding_verification_66_gb300.workloads import (WORKLOADS, make_inputs,
+                                                                   to_host_arrays)
+
+pytestmark = pytest.mark.gpu
+THREADS = max(1, min(16, os.cpu_count() or 1))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sv.load()
+    torch.cuda.set_device(0)
+
+
+def f_run(inputs, wl, seed, top_k, top_p):
+    out, nacc = sv.spec_verify_filtered(inputs["target"], inputs["draft"], inputs["tokens"],
+                                        wl.temperature, top_k, top_p, seed, wl.mode)
+    torch.cuda.synchronize()
+    return {"out_tokens": out.cpu().numpy(), "num_accepted": nacc.cpu().numpy()}
+
+
+def f_debug(inputs, wl, seed, top_k, top_p):
+    r = sv.spec_verify_filtered_debug(inputs["target"], inputs["draft"], inputs["tokens"],
+                                      wl.temperature, top_k, top_p, seed, wl.mode)
+    torch.cuda.synchronize()
+    return {k: v.cpu().numpy() for k, v in r.items()}
+
+
+def check_rows(g, orc, idx, K):
+    """Per-row thresholds: equal to the oracle's, or the oracle's top-p
+    boundary lies within the near-tie band. Where they are equal the kept
+    normalisers agree to 1e-5 and the row needs no flag; the returned oracle
+    dict keeps the filter flags of the other rows only."""
+    orc = dict(orc)
+    fm_t = orc["filter_margin_t"].copy()
+    fm_d = orc["filter_margin_d"].copy()
+    n_rows = n_diff = 0
+    for b in idx:
+        if orc["seq_status"][b] != 0:
+            continue
+        for i in range(2 * K + 1):
+            tgt = i <= K
+            gi = i if tgt else i - K - 1
+            gthr = float((g["thr_t"] if tgt else g["thr_d"])[b, gi])
+            othr = float(orc["filter_thr"][b, i])
+            margin = (fm_t if tgt else fm_d)[b, gi]
+            n_rows += 1
+            if gthr == othr:
+                glse = (g["lse_t"] if tgt else g["lse_d"])[b, gi]
+                olse = (orc["lse_t"] if tgt else orc["lse_d"])[b, gi] + orc["filter_log_mass"][b, i]
+                assert abs(glse - olse) <= 1e-5 * max(1.0, abs(olse)), (b, i, glse, olse)
+                (fm_t if tgt else fm_d)[b, gi] = np.inf
+            else:
+                n_diff += 1
+                assert margin < 1e-5, (b, i, gthr, othr, margin)
+    orc["filter_margin_t"], orc["filter_margin_d"] = fm_t, fm_d
+    return orc, n_rows, n_diff
+
+
+def oracle_run(host, wl, seed, top_k, top_p, seq_range=None):
+    t, d, x = host
+    mode = oracle.SAMPLE if wl.mode == "sample" else oracle.GREEDY
+    kw = {} if seq_range is None else {"seq_range": seq_range}
+    return oracle.verify(t, d, x, wl.temperature, seed, mode, threads=THREADS, top_k=top_k,
+                         top_p=top_p, **kw)
+
+
+def check(wl, seed, top_k, top_p, device_inputs=None, rows=None):
+    inputs = device_inputs if device_inputs is not None else \
+        make_inputs(wl, seed, "cuda", top_k=top_k, top_p=top_p)
+    host = to_host_arrays(inputs)
+    s = 0xF117E000 + seed
+    g = f_debug(inputs, wl, s, top_k, top_p) if wl.mode == "sample" else \
+        f_run(inputs, wl, s, top_k, top_p)
+    if rows is None:
+        orc = oracle_run(host, wl, s, top_k, top_p)
+        idx = list(range(wl.B))
+    else:
+        orc = None
+        for lo, hi in rows:
+            r = oracle_run(host, wl, s, top_k, top_p, (lo, hi))
+            if orc is None:
+                orc = r
+            else:
+                for k in orc:
+                    orc[k][lo:hi] = r[k][lo:hi]
+        idx = [b for lo, hi in rows for b in range(lo, hi)]
+    bad_g = g["num_accepted"][idx] < 0
+    bad_o = orc["seq_status"][idx] != 0
+    assert np.array_equal(bad_g, bad_o), "invalid sequences differ"
+    if wl.mode == "sample":
+        assert np.array_equal(g["seq_status"][idx], orc["seq_status"][idx])
+        orc, n_rows, n_diff = check_rows(g, orc, idx, wl.K)
+        assert n_diff <= max(2, 0.05 * n_rows), (n_diff, n_rows)
+    else:
+        g["seq_status"] = np.where(g["num_accepted"] < 0, orc["seq_status"], 0)
+    return compare(g, orc, host[2], wl.K, wl.V, rows=idx, greedy=wl.mode == "greedy",
+                   check_stats=False), g, orc
+
+
+CASES = [
+    ("small_f32", {}, 50, 1.0),        # fp32: three-level top-k descent
+    ("small_f32", {}, 0, 0.9),         # fp32 top-p alone
+    ("small_f32", {}, 300, 0.7),       # top-p inside a top-k set
+    ("spiky_bf16", {}, 20, 1.0),
+    ("spiky_bf16", {}, 0, 0.95),
+    ("spiky_bf16", {}, 1, 1.0),        # top-1: p' one-hot at the maximum
+    ("spiky_bf16", {}, 64, 0.5),
+    ("llama3_bf16", {"B": 12}, 50, 0.9),
+    ("llama3_bf16", {"B": 12}, 0, 0.8),
+    ("qwen_long_bf16", {"B": 4}, 100, 0.95),
+]
+
+
+@pytest.mark.parametrize("name,size,top_k,top_p", CASES)
+@pytest.mark.parametrize("seed", [0, 1])
+def test_filtered_parity(name, size, top_k, top_p, seed):
+    wl = WORKLOADS[name].resized(**size)
+    st, _, _ = check(wl, seed, top_k, top_p)
+    assert st["flagged_decisions"] <= max(2, 1e-2 * st["decisions"]), st
+
+
+def test_filtered_full_size_sampled_rows():
+    wl = WORKLOADS["llama3_bf16"]
+    B = wl.B
+    st, _, _ = check(wl, 7, 50, 0.9, rows=[(0, 3), (B // 2 - 1, B // 2 + 1), (B - 3, B)])
+    assert st["decisions"] > 0
+
+
+@pytest.mark.parametrize("V,dtype", [(1, "bf16"), (7, "bf16"), (33, "f32"), (50257, "bf16"),
+                                     (8191, "f32"), (151936, "bf16")])
+@pytest.mark.parametrize("top_k,top_p", [(5, 1.0), (0, 0.6), (3, 0.9)])
+def test_filtered_ragged_vocab(V, dtype, top_k, top_p):
+    """Rows that do not start on 16-byte boundaries (head and tail elements),
+    vocabularies shorter than k, and single-token rows."""
+    wl = WORKLOADS["small_f32"].resized(B=5, K=3, V=V, dtype=dtype, temperature=0.9)
+    check(wl, 3, top_k, top_p)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("top_k,top_p", [(7, 1.0), (0, 0.75), (12, 0.6), (2, 1.0)])
+def test_filtered_ties_at_the_boundary(dtype, top_k, top_p):
+    """Logits on a coarse grid: most boundaries fall inside a run of equal
+    values, all of which stay, including -0 next to +0."""
+    wl = WORKLOADS["small_f32"].resized(B=24, K=4, V=2000, dtype=dtype)
+    inputs = make_inputs(wl, 17, "cuda", top_k=top_k, top_p=top_p)
+    for key in ("target", "draft"):
+        t = inputs[key].float()
+        t = torch.round(t * 2) / 2
+        t[t == 0] = torch.where(torch.rand_like(t[t == 0]) < 0.5, -0.0, 0.0)
+        inputs[key] = t.to(inputs[key].dtype)
+    check(wl, 17, top_k, top_p, device_inputs=inputs)
+
+
+def test_filtered_masked_vocabulary():
+    """-inf logits (a masked vocabulary): top-k larger than the number of
+    finite logits keeps them all, and masked tokens never come out."""
+    wl = WORKLOADS["spiky_bf16"].resized(B=16, K=3, V=3000)
+    inputs = make_inputs(wl, 5, "cuda", top_k=40)
+    for key in ("target", "draft"):
+        inputs[key][:, :, 100:] = float("-inf")
+    inputs["tokens"] = torch.randint(0, 100, inputs["tokens"].shape, device="cuda",
+                                     dtype=torch.int32)
+    for top_k, top_p in [(40, 1.0), (150, 1.0), (0, 0.9)]:
+        _, g, _ = check(wl, 5, top_k, top_p, device_inputs=inputs)
+        assert (g["out_tokens"][g["out_tokens"] >= 0] < 100).all()
+
+
+def test_filtered_off_is_spec_verify():
+    wl = WORKLOADS["spiky_bf16"].resized(B=32)
+    inputs = make_inputs(wl, 2, "cuda")
+    a = sv.spec_verify(inputs["target"], inputs["draft"], inputs["tokens"], wl.temperature, 99)
+    for top_k, top_p in [(0, 1.0), (wl.V, 1.0), (wl.V + 10, 1.0)]:
+        b = sv.spec_verify_filtered(inputs["target"], inputs["draft"], inputs["tokens"],
+                                    wl.temperature, top_k, top_p, 99)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_filtered_greedy_ignores_the_cuts():
+    wl = WORKLOADS["greedy_bf16"].resized(B=16)
+    inputs = make_inputs(wl, 3, "cuda")
+    a = sv.spec_verify(inputs["target"], None, inputs["tokens"], 1.0, 5, "greedy")
+    b = sv.spec_verify_filtered(inputs["target"], None, inputs["tokens"], 1.0, 3, 0.5, 5,
+                                "greedy")
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_filtered_p_equals_q_accepts_everything():
+    wl = WORKLOADS["llama3_bf16"].resized(B=16, K=5)
+    inputs = make_inputs(wl, 8, "cuda", top_k=30, top_p=0.9)
+    inputs["draft"] = inputs["target"][:, :wl.K].contiguous()
+    # redraw the drafts from the (now identical) filtered target rows
+    from speculative_decoding_verification_66_gb300.workloads import draw_from_logits
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(8)
+    inputs["tokens"] = draw_from_logits(inputs["draft"], wl.temperature, gen, 30, 0.9)
+    st, g, _ = check(wl, 8, 30, 0.9, device_inputs=inputs)
+    # tokens are drawn by the input generator's own cut; only where it agrees
+    # with the verifier's do all drafts pass
+    assert (g["num_accepted"] == wl.K).mean() > 0.9
+
+
+def test_filtered_invalid_rows():
+    wl = WORKLOADS["small_f32"].resized(B=8, K=3, V=700)
+    inputs = make_inputs(wl, 21, "cuda", top_k=10)
+    t, d, x = inputs["target"], inputs["draft"], inputs["tokens"]
+    t[2, 1, 17] = float("nan")
+    d[3, 0, 5] = float("inf")
+    t[4, :, :] = float("-inf")
+    x[5, 2] = wl.V
+    _, g, _ = check(wl, 21, 10, 0.9, device_inputs=inputs)
+    assert list(g["num_accepted"][[2, 3, 4, 5]]) == [-1, -1, -1, -1]
+
+
+def test_filtered_repeatable_and_empty():
+    wl = WORKLOADS["llama3_bf16"].resized(B=8)
+    inputs = make_inputs(wl, 4, "cuda", top_k=50, top_p=0.9)
+    a = f_run(inputs, wl, 5, 50, 0.9)
+    b = f_run(inputs, wl, 5, 50, 0.9)
+    assert np.array_equal(a["out_tokens"], b["out_tokens"])
+    assert np.array_equal(a["num_accepted"], b["num_accepted"])
+    wl0 = wl.resized(B=0)
+    i0 = make_inputs(wl0, 0, "cuda")
+    out, nacc = sv.spec_verify_filtered(i0["target"], i0["draft"], i0["tokens"], 1.0, 5, 0.9, 1)
+    torch.cuda.synchronize()
+    assert out.shape == (0, wl.K + 1) and nacc.shape == (0,)
+
+
+def test_filtered_timed_events():
+    wl = WORKLOADS["spiky_bf16"].resized(B=16)
+    inputs = make_inputs(wl, 6, "cuda", top_k=20, top_p=0.9)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    a = sv.spec_verify_filtered_timed(inputs["target"], inputs["draft"], inputs["tokens"], ev,
+                                      wl.temperature, 20, 0.9, 3)
+    torch.cuda.synchronize()
+    assert all(ev[i].elapsed_time(ev[i + 1]) >= 0 for i in range(3))
+    b = sv.spec_verify_filtered(inputs["target"], inputs["draft"], inputs["tokens"],
+                                wl.temperature, 20, 0.9, 3)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])

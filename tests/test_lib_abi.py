@@ -37,6 +37,8 @@ def test_header_declares_the_api():
         "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static",
         "sv_early_exit_workspace_bytes", "spec_verify_early_exit",
         "sv_sharded_workspace_bytes", "spec_verify_sharded", "sv_philox",
+        "sv_filtered_workspace_bytes", "spec_verify_filtered", "spec_verify_filtered_timed",
+        "spec_verify_filtered_debug",
         "sv_error_string",
         "sv_version"])
 
@@ -71,7 +73,7 @@ def test_error_strings_and_version(lib):
                  SV_ERR_SIZE, 12345):
         s = lib.sv_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
-    assert lib.sv_version() == 103
+    assert lib.sv_version() == 104
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails before any device work
@@ -158,6 +160,36 @@ def test_sharded_host_side_validation(lib):
 def test_early_exit_host_side_validation(lib, kw, code):
     """The early-exit entry shares spec_verify's checks, all before any CUDA call."""
     assert call_ee(lib, **kw) == code
+
+
+def test_filtered_host_side_validation(lib):
+    """spec_verify_filtered checks top_k / top_p with the other arguments,
+    before any CUDA call."""
+    def f(B=2, K=3, V=64, dtype=1, T=1.0, top_k=5, top_p=0.9, mode=0, target=FAKE, events=None,
+          n_events=0):
+        args = (target, FAKE, FAKE, B, K, V, dtype, T, top_k, top_p, 7, mode, FAKE, FAKE, FAKE,
+                1 << 20, None)
+        if events is None and n_events == 0:
+            return lib.spec_verify_filtered(*args)
+        return lib.spec_verify_filtered_timed(*args, events, n_events)
+    assert f(B=0) == SV_OK
+    assert f(B=0, top_k=0, top_p=1.0) == SV_OK
+    assert f(top_k=-1) == SV_ERR_ARG
+    assert f(top_p=0.0) == SV_ERR_ARG
+    assert f(top_p=1.5) == SV_ERR_ARG
+    assert f(top_p=float("nan")) == SV_ERR_ARG
+    assert f(B=0, top_p=-0.5) == SV_ERR_ARG
+    assert f(T=0.0) == SV_ERR_ARG
+    assert f(target=FAKE + 2) == SV_ERR_ALIGN
+    assert f(dtype=9) == SV_ERR_DTYPE
+    assert f(K=2000) == SV_ERR_SIZE
+    assert f(events=(ctypes.c_void_p * 2)(), n_events=2) == SV_ERR_ARG
+    assert f(events=None, n_events=4) == SV_ERR_ARG
+    dbg = lib.spec_verify_filtered_debug
+    args = (FAKE, FAKE, FAKE, 2, 3, 64, 1, 1.0, 5, 0.9, 7, 0, FAKE, FAKE, FAKE, 1 << 20, None)
+    assert dbg(*args, FAKE, FAKE, FAKE + 2, FAKE, FAKE) == SV_ERR_ALIGN
+    assert dbg(*args, FAKE, FAKE, FAKE, FAKE + 1, FAKE) == SV_ERR_ALIGN
+    assert dbg(*args, FAKE + 4, FAKE, FAKE, FAKE, FAKE) == SV_ERR_ALIGN
 
 
 def test_greedy_ignores_temperature_and_draft(lib):

@@ -768,3 +768,12 @@ def test_filter_margins_reported(oracle_mod):
             assert math.isclose(r["filter_margin_d"][b, i],
                                 brute_filter(d[b, i], 1.0, 8, float(np.float32(top_p)))[3],
                                 rel_tol=1e-9, abs_tol=1e-12)
+        # per-row thresholds and log kept masses, target rows then draft rows
+        rows = list(t[b]) + list(d[b])
+        for i, row in enumerate(rows):
+            thr, kept, _, _ = brute_filter(row, 1.0, 8, float(np.float32(top_p)))
+            assert r["filter_thr"][b, i] == thr
+            assert math.isclose(r["filter_log_mass"][b, i],
+                                math.log(softmax64(row)[kept].sum()), rel_tol=1e-9, abs_tol=1e-12)
+    u = oracle_mod.verify(t, d, tok, 1.0, seed=1)
+    assert np.all(u["filter_thr"] == -np.inf) and np.all(u["filter_log_mass"] == 0.0)
