@@ -59,6 +59,11 @@ def parse():
     p.add_argument("--early-exit-steps", type=int, default=1000,
                    help="timed calls of spec_verify_early_exit reported beside the full pass "
                         "(0: skip)")
+    p.add_argument("--filtered-steps", type=int, default=300,
+                   help="timed calls of spec_verify_filtered reported beside the full pass "
+                        "(0: skip)")
+    p.add_argument("--top-k", type=int, default=50, help="top-k of the filtered variant")
+    p.add_argument("--top-p", type=float, default=0.9, help="top-p of the filtered variant")
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="threads for the CPU baseline (0: every core this process may use)")
     return p.parse_args()
@@ -437,6 +442,60 @@ def main():
                    "bytes_per_step": sh_bytes, "hbm_gbs": sh_bytes / (sh_ms / 1e3) / 1e9}
         del shard_sets, ws_sh
 
+    # Top-k / top-p on both rows (a variant, reported beside the full pass):
+    # the same logits, drafts redrawn from the filtered draft rows.
+    filtered = None
+    if args.filtered_steps > 0 and mode == "sample":
+        from speculative_decoding_verification_66_gb300.workloads import draw_from_logits
+        tk, tp = args.top_k, args.top_p
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(4321 + rank)
+        f_tokens = [draw_from_logits(c["draft"], wl.temperature, gen, tk, tp) for c in copies]
+        ws_f = torch.empty(sv.sv_filtered_workspace_bytes(B, K, V, copies[0]["target"].dtype,
+                                                          mode), dtype=torch.uint8, device=dev)
+
+        def f_step(i, ev=None):
+            c = i & 1
+            inp = copies[c]
+            sv.spec_verify_filtered(inp["target"], inp["draft"], f_tokens[c], wl.temperature, tk,
+                                    tp, seeds[c], mode, out_tokens=out, num_accepted=nacc,
+                                    workspace=ws_f, stream=stream, events=ev)
+
+        f_acc = []
+        for c in range(2):
+            f_step(c)
+            f_acc.append(nacc.float().mean().item())
+        for i in range(3):
+            f_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.filtered_steps):
+            f_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        f_ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.filtered_steps
+        n_f = max(3, min(args.filtered_steps, 100))
+        fev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_f)]
+        for i in range(n_f):
+            f_step(i, fev[i])
+        torch.cuda.synchronize()
+        thr_ms = sum(e[0].elapsed_time(e[1]) for e in fev) / n_f
+        f_scan_ms = sum(e[1].elapsed_time(e[2]) for e in fev) / n_f
+        f_sample_ms = sum(e[2].elapsed_time(e[3]) for e in fev) / n_f
+        # The thresholds pass must read every row once (further sweeps of a
+        # row are meant to hit L2): the same algorithmic bytes as pass 1.
+        thr_gbs = pass1_bytes / (thr_ms / 1e3) / 1e9
+        filtered = {"top_k": tk, "top_p": tp, "value": job_throughput(world, B, 1, f_ms / 1e3),
+                    "unit": "seqs/s", "ms_per_step": f_ms, "steps": args.filtered_steps,
+                    "mean_accepted": sum(f_acc) / len(f_acc),
+                    "stage_ms": {"thresholds": thr_ms, "scan": f_scan_ms, "sample": f_sample_ms,
+                                 "steps_timed": n_f},
+                    "thresholds_kernel": {"bound": "hbm", "achieved": thr_gbs, "peak": peak,
+                                          "unit": "GB/s", "frac": thr_gbs / peak,
+                                          "algorithmic_bytes": pass1_bytes}}
+        del ws_f, f_tokens
+
     # End to end through the host entry point: pinned host inputs, copies inside.
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
     h = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in c.items()}
@@ -490,6 +549,8 @@ def main():
         line["early_exit"] = early
     if sharded is not None:
         line["sharded"] = sharded
+    if filtered is not None:
+        line["filtered"] = filtered
     if world == 1 and not args.no_cpu_baseline:
         def host_fn(n):
             sub = {k: (v[:n] if v is not None else None) for k, v in copies[0].items()}

@@ -126,6 +126,9 @@ CASES = [
     ("llama3_bf16", {"B": 12}, 50, 0.9),
     ("llama3_bf16", {"B": 12}, 0, 0.8),
     ("qwen_long_bf16", {"B": 4}, 100, 0.95),
+    ("qwen_long_bf16", {"B": 4}, 0, 0.9),    # flat rows: top-p bins refined twice
+    ("spiky_bf16", {"B": 16}, 3000, 1.0),    # k beyond the candidate list: whole-row select
+    ("small_f32", {"B": 4}, 4000, 0.8),
 ]
 
 
@@ -181,6 +184,19 @@ def test_filtered_masked_vocabulary():
     for top_k, top_p in [(40, 1.0), (150, 1.0), (0, 0.9)]:
         _, g, _ = check(wl, 5, top_k, top_p, device_inputs=inputs)
         assert (g["out_tokens"][g["out_tokens"] >= 0] < 100).all()
+
+
+@pytest.mark.parametrize("top_k,top_p", [(5, 1.0), (5, 0.5), (0, 0.9)])
+def test_filtered_many_ties_at_the_top(top_k, top_p):
+    """10000 tokens share the maximum: the top-k candidate list overflows and
+    the whole-row select takes over; top-p keeps the whole tied group."""
+    wl = WORKLOADS["spiky_bf16"].resized(B=6, K=3, V=32000)
+    inputs = make_inputs(wl, 23, "cuda", top_k=top_k, top_p=top_p)
+    for key in ("target", "draft"):
+        inputs[key][:, :, 1000:11000] = inputs[key].float().amax(dim=-1, keepdim=True).to(
+            inputs[key].dtype)
+    st, g, orc = check(wl, 23, top_k, top_p, device_inputs=inputs)
+    assert (g["num_accepted"] >= 0).all()
 
 
 def test_filtered_off_is_spec_verify():
