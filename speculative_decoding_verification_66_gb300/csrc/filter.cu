@@ -54,30 +54,27 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kFilterThreads = 512;
+constexpr int kFilterThreads = 256;
 constexpr int kWarpsF = kFilterThreads / 32;
-constexpr int kListCap = 6144;                       // list entries (keys)
+constexpr int kCand = 8;                             // group maxima per thread (bf16; fp32: 4)
+constexpr int kListCap = 4096;                       // list entries (keys)
 constexpr int kDBins = 32;                           // log2-distance bins per level
 constexpr int kRefine = 3;                           // sub-bin levels after the first
 constexpr int kRadixBins = 256;                      // 8-bit digits
+constexpr int kMaxShares = 8;                        // thread shares read again one at a time
 constexpr float kFix = 1099511627776.0f;             // 2^40
 
-// Group maxima per thread: one per lane position of a 16-byte vector.
-template <int ES>
-constexpr int groups() { return 16 / ES; }
-
-// Dynamic shared memory: the per-thread bins [kDBins][kFilterThreads]; on the
-// top-k path and in every select, the same 64 KB hold the candidate keys
-// (first 16 KB), the per-warp counts (next 16 KB) and the per-warp masses
-// (last 32 KB). Then the list.
+// Dynamic shared memory: the per-thread bins [kDBins][kFilterThreads]; during
+// the reads that use it, the same 32 KB hold the bulk-copy ring, and in every
+// select the candidate keys (first 4 KB), the per-warp counts (next 8 KB) and
+// the per-warp masses (16 KB). Then the list.
 constexpr size_t kBinsBytes = sizeof(uint32_t) * kDBins * kFilterThreads;
-constexpr size_t kCandBytes = 16384;
+constexpr size_t kCandBytes = sizeof(uint32_t) * kCand * kFilterThreads;
 constexpr size_t kCountBytes = sizeof(uint32_t) * kWarpsF * kRadixBins;
 constexpr size_t kMassBytes = sizeof(uint64_t) * kWarpsF * kRadixBins;
 constexpr size_t kListBytes = sizeof(uint32_t) * kListCap;
 constexpr size_t kFilterSmem = kBinsBytes + kListBytes;
 static_assert(kCandBytes + kCountBytes + kMassBytes <= kBinsBytes, "select scratch fits the bins");
-static_assert(sizeof(uint32_t) * kFilterThreads * 8 <= kCandBytes, "candidates fit");
 
 // Order-preserving key: x < y  <=>  key(x) < key(y) for non-NaN floats, with
 // -0 and +0 one value (they compare equal as logits). Every real logit,
@@ -171,6 +168,7 @@ struct Scratch {
     int e;
     int lo;
     int list_n;
+    int inc_n;
 };
 
 template <typename H>
@@ -202,6 +200,71 @@ __device__ __forceinline__ void append(uint32_t key, uint32_t* list, int* count)
     base = grp.shfl(base, 0);
     const int pos = base + static_cast<int>(grp.thread_rank());
     if (pos < kListCap) list[pos] = key;
+}
+
+// Rows whose length is a whole number of 16-byte vectors stream through a
+// two-stage ring of bulk copies (the 64 KB of the bins region, free during
+// the reads that use it): thread 0 issues the copies, every thread waits on
+// the stage's mbarrier, reads its vectors from shared memory, and the CTA
+// barrier after each tile frees the stage for the copy two tiles ahead.
+constexpr int kTileBytes = 16384;
+constexpr int kStages = 2;
+static_assert(kStages * kTileBytes <= static_cast<int>(kBinsBytes), "ring fits the bins");
+
+struct Ring {
+    uint64_t* bar;   // [kStages] mbarriers
+    uint8_t* buf;    // kStages tiles
+    uint32_t phase;  // bit s: parity of the next wait on stage s
+};
+
+__device__ __forceinline__ void fence_proxy_async()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// fv(v) for every 16-byte vector of a row of `bytes` bytes (a multiple of 16,
+// 16-byte aligned). False if a copy did not land within the wait limit; the
+// copies still pending have then been waited for (bounded) and the ring must
+// not be used again.
+template <typename FV>
+__device__ bool ring_sweep(Ring& rg, const uint8_t* row, int64_t bytes, FV&& fv)
+{
+    const int t = threadIdx.x, T = blockDim.x;
+    const int64_t ntiles = (bytes + kTileBytes - 1) / kTileBytes;
+    auto tile_bytes = [&](int64_t i) {
+        const int64_t n = bytes - i * kTileBytes;
+        return static_cast<uint32_t>(n < kTileBytes ? n : kTileBytes);
+    };
+    auto issue = [&](int64_t i) {
+        const int st = static_cast<int>(i % kStages);
+        mbar_arrive_expect_tx(&rg.bar[st], tile_bytes(i));
+        bulk_copy_g2s(rg.buf + st * kTileBytes, row + i * kTileBytes, tile_bytes(i), &rg.bar[st]);
+    };
+    if (t == 0) {
+        fence_proxy_async();  // earlier generic accesses to the buffer come first
+        for (int64_t i = 0; i < ntiles && i < kStages; ++i) issue(i);
+    }
+    for (int64_t i = 0; i < ntiles; ++i) {
+        const int st = static_cast<int>(i % kStages);
+        bool ok = mbar_wait_bounded(&rg.bar[st], (rg.phase >> st) & 1u, nullptr);
+        rg.phase ^= 1u << st;
+        if (ok) {
+            const uint8_t* base = rg.buf + st * kTileBytes;
+            const int nvec = static_cast<int>(tile_bytes(i) / 16);
+            for (int v = t; v < nvec; v += T) fv(ld_shared_v4(base + 16 * v));
+        }
+        if (!__syncthreads_and(ok)) {
+            // Let the copies still in flight land before giving up.
+            if (!ok) mbar_wait_bounded(&rg.bar[st], ((rg.phase >> st) & 1u) ^ 1u, nullptr);
+            if (i + 1 < ntiles) {
+                const int sn = static_cast<int>((i + 1) % kStages);
+                mbar_wait_bounded(&rg.bar[sn], (rg.phase >> sn) & 1u, nullptr);
+            }
+            return false;
+        }
+        if (t == 0 && i + kStages < ntiles) issue(i + kStages);
+    }
+    return true;
 }
 
 // Largest digit e of h[0, nb) with base + sum_{d >= e} h[d] >= target. Leaves e
@@ -340,6 +403,179 @@ __device__ __noinline__ uint32_t select_kth(const Src& src, uint64_t k, int leve
         prefix |= static_cast<uint32_t>(d) << shift;
     }
     return prefix;
+}
+
+// Warp-aggregated histogram updates for a warp whose 32 lanes all call them
+// (digit -1: nothing to add). Lanes with the same digit form one group; its
+// lowest lane adds the group's count or mass to the warp's private row, so no
+// two lanes ever update one word at once (same-address shared atomics replay
+// once per conflicting lane, and list keys crowd into few digits).
+__device__ __forceinline__ void warp_add_count(uint32_t* mine, int digit)
+{
+    const unsigned m = __match_any_sync(0xFFFFFFFFu, digit);
+    if (digit >= 0 && static_cast<int>(threadIdx.x & 31) == __ffs(m) - 1) mine[digit] += __popc(m);
+}
+
+// Masses below 2^55: the low 23 and the high bits are summed separately as
+// 32-bit words (32 lanes cannot overflow either), then recombined exactly.
+__device__ __forceinline__ void warp_add_mass(uint64_t* mine, int digit, uint64_t w)
+{
+    const unsigned m = __match_any_sync(0xFFFFFFFFu, digit);
+    const uint32_t lo = __reduce_add_sync(m, static_cast<uint32_t>(w & 0x7FFFFFu));
+    const uint32_t hi = __reduce_add_sync(m, static_cast<uint32_t>(w >> 23));
+    if (digit >= 0 && static_cast<int>(threadIdx.x & 31) == __ffs(m) - 1)
+        mine[digit] += (static_cast<uint64_t>(hi) << 23) + lo;
+}
+
+// The k-th largest of n keys in shared memory (1 <= k <= n), to its top
+// 8 * levels bits: radix select with warp-aggregated histograms.
+__device__ __noinline__ uint32_t list_select_kth(const uint32_t* keys, int n, uint64_t k, int levels,
+                                                 uint32_t* hc, Scratch& s)
+{
+    uint32_t* mine = hc + (threadIdx.x >> 5) * kRadixBins;
+    uint32_t prefix = 0;
+    uint64_t base = 0;
+    for (int l = 0; l < levels; ++l) {
+        const int shift = 24 - 8 * l;
+        const uint32_t hi = above_mask(shift);
+        __syncthreads();
+        zero(hc, kWarpsF * kRadixBins);
+        __syncthreads();
+        for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+            const int i = i0 + static_cast<int>(threadIdx.x);
+            const uint32_t key = i < n ? keys[i] : 0u;
+            const bool in = i < n && (key & hi) == prefix;
+            warp_add_count(mine, in ? static_cast<int>((key >> shift) & 0xFFu) : -1);
+        }
+        fold_warps(hc);
+        crossing(hc, kRadixBins, base, k, s);
+        const int d = s.e < 0 ? 0 : s.e;
+        base = s.above;
+        prefix |= static_cast<uint32_t>(d) << shift;
+    }
+    return prefix;
+}
+
+// select_mass over n keys in shared memory, with warp-aggregated histograms.
+__device__ __noinline__ uint32_t list_select_mass(const uint32_t* keys, int n, uint64_t base,
+                                                  uint64_t target, float c, float mref,
+                                                  uint64_t* hm, Scratch& s, uint64_t* kept)
+{
+    uint64_t* mine = hm + (threadIdx.x >> 5) * kRadixBins;
+    uint32_t prefix = 0;
+    int d = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+        const uint32_t hi = above_mask(shift);
+        __syncthreads();
+        zero(hm, kWarpsF * kRadixBins);
+        __syncthreads();
+        for (int i0 = 0; i0 < n; i0 += blockDim.x) {
+            const int i = i0 + static_cast<int>(threadIdx.x);
+            const uint32_t key = i < n ? keys[i] : 0u;
+            const bool in = i < n && (key & hi) == prefix;
+            const uint64_t w = in ? mass_of(key_value(key), c, mref) : 0u;
+            warp_add_mass(mine, in ? static_cast<int>((key >> shift) & 0xFFu) : -1, w);
+        }
+        fold_warps(hm);
+        crossing(hm, kRadixBins, base, target, s);
+        d = s.e < 0 ? 0 : s.e;
+        base = s.above;
+        prefix |= static_cast<uint32_t>(d) << shift;
+    }
+    *kept = base + hm[d];
+    return prefix;
+}
+
+// Top-k then top-p on a list of n <= kSmallList keys by one warp, without
+// block barriers: for each element its rank (keys above it, keys at or above
+// it) and its upper-set mass, by a pass over the whole list. The k-th largest
+// key tau_k is the one with fewer than k keys above it and at least k at or
+// above it; the top-p threshold is the largest key whose upper-set mass
+// reaches ceil(top_p * mass(tau_k)). w: scratch for the n masses. Lane 0's
+// results are the answer.
+constexpr int kSmallList = 128;
+
+__device__ __noinline__ void small_select(const uint32_t* keys, int n, bool tk, uint64_t k, bool tp,
+                                          float top_p, float c, float mref, uint64_t* w,
+                                          uint32_t* tau_out, uint64_t* kept_out)
+{
+    const int lane = threadIdx.x & 31;
+    constexpr int kPer = kSmallList / 32;
+    for (int i = lane; i < n; i += 32) w[i] = mass_of(key_value(keys[i]), c, mref);
+    __syncwarp();
+    uint32_t kk[kPer];
+    int gt[kPer], ge[kPer];
+    uint64_t up[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const int i = lane + 32 * q;
+        kk[q] = i < n ? keys[i] : 0u;
+        gt[q] = ge[q] = 0;
+        up[q] = 0;
+    }
+    for (int j = 0; j < n; ++j) {
+        const uint32_t kj = keys[j];
+        const uint64_t wj = w[j];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            gt[q] += kj > kk[q];
+            ge[q] += kj >= kk[q];
+            up[q] += kj >= kk[q] ? wj : 0u;
+        }
+    }
+    // tau_k: the largest key with rank window containing k (all such keys are equal).
+    uint32_t tau = 0u;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        const bool real = lane + 32 * q < n;
+        if (real && (!tk || (static_cast<uint64_t>(gt[q]) < k && static_cast<uint64_t>(ge[q]) >= k)))
+            tau = tk ? kk[q] : 0u;
+    }
+    if (!tk) {
+        // No top-k cut: every key counts; tau_k is the smallest key.
+        uint32_t mn = 0xFFFFFFFFu;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+            if (lane + 32 * q < n) mn = kk[q] < mn ? kk[q] : mn;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
+        tau = mn;
+    } else {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) tau = max(tau, __shfl_xor_sync(0xFFFFFFFFu, tau, off));
+    }
+    uint64_t mass_k = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+        if (lane + 32 * q < n && kk[q] >= tau) mass_k += w[lane + 32 * q];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mass_k += __shfl_xor_sync(0xFFFFFFFFu, mass_k, off);
+    uint64_t kept = mass_k;
+    if (tp) {
+        const uint64_t target =
+            static_cast<uint64_t>(ceil(static_cast<double>(top_p) * static_cast<double>(mass_k)));
+        uint32_t best = 0u;
+        uint64_t best_up = 0u;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+            if (lane + 32 * q < n && up[q] >= target && kk[q] > best) {
+                best = kk[q];
+                best_up = up[q];
+            }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const uint32_t ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
+            const uint64_t ou = __shfl_xor_sync(0xFFFFFFFFu, best_up, off);
+            if (ob > best) {
+                best = ob;
+                best_up = ou;
+            }
+        }
+        tau = best;
+        kept = best_up;
+    }
+    *tau_out = tau;
+    *kept_out = kept;
 }
 
 // Sum of the masses of src's keys >= tau.
@@ -488,7 +724,7 @@ __device__ __noinline__ bool topp_bins(const uint8_t* row, int64_t V, float c, f
         const int n = s.list_n;
         if (n <= kListCap) {
             __syncthreads();  // every thread has read n before the bins are reused
-            *tau = select_mass(ListSrc{list, n}, above, target, c, mref, hm, s, kept);
+            *tau = list_select_mass(list, n, above, target, c, mref, hm, s, kept);
             return true;
         }
         if (L == kRefine) break;
@@ -526,12 +762,13 @@ __device__ __noinline__ void row_select(const uint8_t* row, int64_t V, bool tk, 
     *kept = m;
 }
 
-// bf16 bits (as a float, widened) of the bf16 value whose 16-bit key is p.
+// The 16 bits of the bf16 value whose 16-bit key is p.
 __device__ __forceinline__ uint32_t bf16_bits_of_key16(uint32_t p)
 {
     return (p & 0x8000u) ? (p & 0x7FFFu) : (~p & 0xFFFFu);
 }
 
+// Packed x >= y on both bf16 halves: 0xFFFF per half where it holds.
 __device__ __forceinline__ unsigned ge2_mask(uint32_t a, uint32_t b)
 {
     __nv_bfloat162 x, y;
@@ -540,10 +777,60 @@ __device__ __forceinline__ unsigned ge2_mask(uint32_t a, uint32_t b)
     return __hge2_mask(x, y);
 }
 
-template <int ES>
-__global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const __grid_constant__ FilterArgs a)
+// Lane-wise minimum of two packed bfloat16 pairs.
+__device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
 {
-    constexpr int G = groups<ES>();
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Appends every element >= lk (by key) of thread tt's share of the row: the
+// head / tail indices and 16-byte vectors congruent to tt modulo the block
+// size, as the reads give them out. The whole CTA reads the share, one vector
+// per thread.
+template <int ES>
+__device__ void reread_share(const uint8_t* row, int64_t V, int tt, uint32_t lk, uint32_t* list,
+                             int* count)
+{
+    constexpr int kEPV = 16 / ES;
+    const uintptr_t p = reinterpret_cast<uintptr_t>(row);
+    int64_t head = static_cast<int64_t>(((16u - static_cast<uint32_t>(p & 15u)) & 15u) / ES);
+    if (head > V) head = V;
+    const int64_t nvec = (V - head) / kEPV;
+    const int64_t tail = head + nvec * kEPV;
+    const int64_t T = blockDim.x;
+    if (threadIdx.x == 0) {
+        if (tt < head) {
+            const uint32_t key = fkey(load_elem<ES>(row + tt * ES));
+            if (key >= lk) append(key, list, count);
+        }
+        if (tail + tt < V) {
+            const uint32_t key = fkey(load_elem<ES>(row + (tail + tt) * ES));
+            if (key >= lk) append(key, list, count);
+        }
+    }
+    const uint4* vp = reinterpret_cast<const uint4*>(row + head * ES);
+    for (int64_t v = tt + threadIdx.x * T; v < nvec; v += T * T) {
+        float x[kEPV];
+        unpack_vec<ES>(__ldg(vp + v), x);
+#pragma unroll
+        for (int e = 0; e < kEPV; ++e) {
+            const uint32_t key = fkey(x[e]);
+            if (key >= lk) append(key, list, count);
+        }
+    }
+}
+
+__device__ __forceinline__ void fail_rows(const FilterArgs& a, int64_t r)
+{
+    if (threadIdx.x == 0)
+        for (int64_t q = r; q < a.g.rows; q += gridDim.x) a.rows[q] = FiltRow{0.f, 0.f, 0.f, kFlagTimeout};
+}
+
+template <int ES>
+__global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_constant__ FilterArgs a)
+{
     extern __shared__ __align__(16) uint8_t smem[];
     uint32_t* bins = reinterpret_cast<uint32_t*>(smem);
     uint32_t* cand = bins;
@@ -551,12 +838,22 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const __grid_
     uint64_t* hm = reinterpret_cast<uint64_t*>(smem + kCandBytes + kCountBytes);
     uint32_t* list = reinterpret_cast<uint32_t*>(smem + kBinsBytes);
     __shared__ Scratch s;
+    __shared__ __align__(8) uint64_t ring_bar[kStages];
     const Geometry& g = a.g;
     const int64_t V = g.V;
     const int T = blockDim.x, t = threadIdx.x;
+    // Whole 16-byte vectors per row: every row starts 16-byte aligned.
+    const bool use_ring = (V * ES) % 16 == 0;
+    Ring rg{ring_bar, smem, 0u};
+    if (t == 0) {
+        for (int i = 0; i < kStages; ++i) mbar_init(&ring_bar[i], 1);
+        fence_barrier_init();
+    }
+    __syncthreads();
     const bool tk = a.top_k > 0 && a.top_k < V;
     const bool tp = a.top_p < 1.0f;
     const uint64_t k = tk ? static_cast<uint64_t>(a.top_k) : 0;
+    constexpr int G = 16 / ES;  // groups per thread: the lane positions of a 16-byte vector
     const bool fast_k = tk && a.top_k <= static_cast<int64_t>(G) * T;
     const float c = a.c;
     const float ninf = __uint_as_float(kF32NegInfBits);
@@ -571,45 +868,67 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const __grid_
             r < g.rows_t ? a.target + r * V * ES : a.draft + (r - g.rows_t) * V * ES;
         __syncthreads();  // the previous row is done with shared memory
 
-        // First read (HBM): the NaN-propagating maximum of each lane position
-        // of this thread's vectors (scalar head / tail elements join group 0).
-        float gm[G];
-        {
-            float hs = ninf;
-            if constexpr (ES == 2) {
-                uint32_t acc[4] = {kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair};
-                sweep_vec<ES>(
-                    row, V,
-                    [&](const uint4& u) {
-                        acc[0] = bf16x2_max_nan(acc[0], u.x);
-                        acc[1] = bf16x2_max_nan(acc[1], u.y);
-                        acc[2] = bf16x2_max_nan(acc[2], u.z);
-                        acc[3] = bf16x2_max_nan(acc[3], u.w);
-                    },
-                    [&](float x) { hs = fmax_nan(hs, x); });
+        // First read (HBM): per lane position of this thread's vectors (a
+        // group), the NaN-propagating maximum and the second largest value
+        // (packed min / max, no branches). Scalar head / tail elements form
+        // one more group, folded into group 0 afterwards.
+        float m1[G], m2[G];
+        bool landed = true;
+        float h1 = ninf, h2 = ninf;
+        auto fs = [&](float x) {
+            h2 = fmaxf(h2, fminf(h1, x));
+            h1 = fmax_nan(h1, x);
+        };
+        if constexpr (ES == 2) {
+            uint32_t a1[4] = {kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair};
+            uint32_t a2[4] = {kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair, kBf16NegInfPair};
+            auto fv = [&](const uint4& u) {
+                const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    gm[2 * q] = bf16_lo(acc[q]);
-                    gm[2 * q + 1] = bf16_hi(acc[q]);
+                    a2[q] = bf16x2_max_nan(a2[q], bf16x2_min(a1[q], w[q]));
+                    a1[q] = bf16x2_max_nan(a1[q], w[q]);
                 }
-            } else {
+            };
+            if (use_ring)
+                landed = ring_sweep(rg, row, V * ES, fv);
+            else
+                sweep_vec<ES>(row, V, fv, fs);
 #pragma unroll
-                for (int q = 0; q < G; ++q) gm[q] = ninf;
-                sweep_vec<ES>(
-                    row, V,
-                    [&](const uint4& u) {
-                        gm[0] = fmax_nan(gm[0], __uint_as_float(u.x));
-                        gm[1] = fmax_nan(gm[1], __uint_as_float(u.y));
-                        gm[2] = fmax_nan(gm[2], __uint_as_float(u.z));
-                        gm[3] = fmax_nan(gm[3], __uint_as_float(u.w));
-                    },
-                    [&](float x) { hs = fmax_nan(hs, x); });
+            for (int q = 0; q < 4; ++q) {
+                m1[2 * q] = bf16_lo(a1[q]);
+                m1[2 * q + 1] = bf16_hi(a1[q]);
+                m2[2 * q] = bf16_lo(a2[q]);
+                m2[2 * q + 1] = bf16_hi(a2[q]);
             }
-            gm[0] = fmax_nan(gm[0], hs);
-        }
-        float mx = gm[0];
+        } else {
 #pragma unroll
-        for (int q = 1; q < G; ++q) mx = fmax_nan(mx, gm[q]);
+            for (int q = 0; q < G; ++q) m1[q] = m2[q] = ninf;
+            auto fv = [&](const uint4& u) {
+                const float x[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                                    __uint_as_float(u.w)};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    m2[q] = fmaxf(m2[q], fminf(m1[q], x[q]));
+                    m1[q] = fmax_nan(m1[q], x[q]);
+                }
+            };
+            if (use_ring)
+                landed = ring_sweep(rg, row, V * ES, fv);
+            else
+                sweep_vec<ES>(row, V, fv, fs);
+        }
+        m2[0] = fmaxf(fmaxf(m2[0], h2), fminf(m1[0], h1));
+        m1[0] = fmax_nan(m1[0], h1);
+        float mx = m1[0];
+#pragma unroll
+        for (int q = 1; q < G; ++q) mx = fmax_nan(mx, m1[q]);
+        if (!landed) {
+            // A bulk copy did not arrive in time: this row and the CTA's
+            // remaining rows report a timeout.
+            fail_rows(a, r);
+            return;
+        }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) mx = fmax_nan(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, off));
         if ((t & 31) == 0) s.wmax[t >> 5] = mx;
@@ -626,24 +945,45 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const __grid_
         uint64_t kept = 0;
         bool done = false;
         if (fast_k) {
-            // The group maxima are G T disjoint elements (an empty group's -inf
-            // only lowers the bound), so at least k elements are >= the k-th
-            // largest of them; to 16 bits it is a lower bound on the k-th
-            // largest logit.
+            // The group maxima are distinct elements (an empty group's -inf
+            // only lowers the bound), so at least k elements have keys >= the
+            // k-th largest of them: to 16 bits it bounds the k-th largest
+            // logit from below. A group whose second value is below the
+            // bound has at most one element above it, its maximum; a thread
+            // with a group that has two or more reads its share again.
 #pragma unroll
-            for (int q = 0; q < G; ++q) cand[G * t + q] = fkey(gm[q]);
+            for (int q = 0; q < G; ++q) cand[G * t + q] = fkey(m1[q]);
             if (t == 0) s.list_n = 0;
             __syncthreads();
-            const uint32_t p16 = select_kth(ListSrc{cand, G * T}, k, 2, hc, s) >> 16;
-            // The 16-bit prefix of -inf's key (0x007FFFFF) or below: no bound.
-            const bool open = p16 <= 0x007Fu;
-            const float bound = open ? ninf : key_value(p16 << 16);
-            const uint32_t b16 = open ? 0xFF80u : bf16_bits_of_key16(p16);
-            const uint32_t b2 = b16 | (b16 << 16);
-            // Second read: every element >= the bound joins the list.
-            sweep_vec<ES>(
-                row, V,
-                [&](const uint4& u) {
+            const uint32_t lk = (list_select_kth(cand, G * T, k, 2, hc, s) >> 16) << 16;
+            bool complete = true;
+#pragma unroll
+            for (int q = 0; q < G; ++q) complete = complete && fkey(m2[q]) < lk;
+            int* inc = reinterpret_cast<int*>(cand);  // the candidates are no longer needed
+            if (t == 0) s.inc_n = 0;
+            if (__syncthreads_count(!complete) <= kMaxShares) {
+                if (complete) {
+#pragma unroll
+                    for (int q = 0; q < G; ++q) {
+                        const uint32_t key = fkey(m1[q]);
+                        if (key >= lk) append(key, list, &s.list_n);
+                    }
+                } else {
+                    inc[atomicAdd(&s.inc_n, 1)] = t;
+                }
+                __syncthreads();
+                for (int q = 0; q < s.inc_n; ++q)
+                    reread_share<ES>(row, V, inc[q], lk, list, &s.list_n);
+            } else {
+                // Many groups hold two or more elements above the bound (k in the
+                // hundreds): one more read of the whole row, a packed compare
+                // per 16-byte vector.
+                const uint32_t p16 = lk >> 16;
+                const bool open = p16 <= 0x007Fu;  // the bound is -inf's prefix or lower
+                const float bound = open ? ninf : key_value(lk);
+                const uint32_t b16 = open ? 0xFF80u : bf16_bits_of_key16(p16);
+                const uint32_t b2 = b16 | (b16 << 16);
+                auto fv = [&](const uint4& u) {
                     bool any;
                     if constexpr (ES == 2) {
                         any = (ge2_mask(u.x, b2) | ge2_mask(u.y, b2) | ge2_mask(u.z, b2) |
@@ -659,20 +999,44 @@ __global__ void __launch_bounds__(kFilterThreads, 2) filter_kernel(const __grid_
                         for (int e = 0; e < 16 / ES; ++e)
                             if (x[e] >= bound) append(fkey(x[e]), list, &s.list_n);
                     }
-                },
-                [&](float x) {
-                    if (x >= bound) append(fkey(x), list, &s.list_n);
-                });
+                };
+                if (use_ring) {
+                    __syncthreads();  // the select is done with the bins region
+                    if (!ring_sweep(rg, row, V * ES, fv)) {
+                        fail_rows(a, r);
+                        return;
+                    }
+                } else {
+                    sweep_vec<ES>(row, V, fv, [&](float x) {
+                        if (x >= bound) append(fkey(x), list, &s.list_n);
+                    });
+                }
+            }
             __syncthreads();
             const int n = s.list_n;
-            if (n <= kListCap) {
+            if (n <= kSmallList) {
+                // One warp selects; the others wait at the barrier below.
+                if (t < 32) {
+                    uint32_t tw;
+                    uint64_t kw;
+                    small_select(list, n, tk, k, tp, a.top_p, c, mref, hm, &tw, &kw);
+                    if (t == 0) {
+                        s.above = kw;
+                        s.e = static_cast<int>(tw);
+                    }
+                }
+                __syncthreads();
+                tau = static_cast<uint32_t>(s.e);
+                kept = s.above;
+                done = true;
+            } else if (n <= kListCap) {
                 const ListSrc L{list, n};
-                tau = select_kth(L, k, 4, hc, s);
+                tau = list_select_kth(list, n, k, 4, hc, s);
                 kept = mass_ge(L, tau, c, mref, s);
                 if (tp) {
                     const uint64_t target = static_cast<uint64_t>(
                         ceil(static_cast<double>(a.top_p) * static_cast<double>(kept)));
-                    tau = select_mass(L, 0, target, c, mref, hm, s, &kept);
+                    tau = list_select_mass(list, n, 0, target, c, mref, hm, s, &kept);
                 }
                 done = true;
             }
