@@ -61,7 +61,8 @@ constexpr int kListCap = 4096;                       // list entries (keys)
 constexpr int kDBins = 32;                           // log2-distance bins per level
 constexpr int kRefine = 3;                           // sub-bin levels after the first
 constexpr int kRadixBins = 256;                      // 8-bit digits
-constexpr int kMaxShares = 8;                        // thread shares read again one at a time
+constexpr int kMaxShares = 16;                       // thread shares read again (else the whole row)
+constexpr int kSortK = 64;                           // k up to which the thread maxima give the bound
 constexpr float kFix = 1099511627776.0f;             // 2^40
 
 // Dynamic shared memory: the per-thread bins [kDBins][kFilterThreads]; during
@@ -578,6 +579,75 @@ __device__ __noinline__ void small_select(const uint32_t* keys, int n, bool tk, 
     *kept_out = kept;
 }
 
+// small_select for lists of up to kMidList keys by the whole CTA: each thread
+// ranks its elements (i = t + j blockDim) against the whole list; the k-th
+// largest key, the top-k mass and the top-p threshold then take a few block
+// reductions. Every thread returns the results.
+constexpr int kMidList = 512;
+
+__device__ __noinline__ void mid_select(const uint32_t* keys, int n, uint64_t k, bool tp, float top_p,
+                                        float c, float mref, uint64_t* w, Scratch& s,
+                                        uint32_t* tau_out, uint64_t* kept_out)
+{
+    constexpr int kPer = kMidList / kFilterThreads;
+    const int t = threadIdx.x, T = blockDim.x;
+    for (int i = t; i < n; i += T) w[i] = mass_of(key_value(keys[i]), c, mref);
+    if (t == 0) {
+        s.lo = 0;
+        s.e = 0;
+    }
+    __syncthreads();
+    uint32_t kk[kPer];
+    int gt[kPer], ge[kPer];
+    uint64_t up[kPer];
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+        kk[q] = t + q * T < n ? keys[t + q * T] : 0u;
+        gt[q] = ge[q] = 0;
+        up[q] = 0;
+    }
+    for (int j = 0; j < n; ++j) {
+        const uint32_t kj = keys[j];
+        const uint64_t wj = w[j];
+#pragma unroll
+        for (int q = 0; q < kPer; ++q) {
+            gt[q] += kj > kk[q];
+            ge[q] += kj >= kk[q];
+            up[q] += kj >= kk[q] ? wj : 0u;
+        }
+    }
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+        if (t + q * T < n && static_cast<uint64_t>(gt[q]) < k && static_cast<uint64_t>(ge[q]) >= k)
+            s.lo = static_cast<int>(kk[q]);  // every such element holds the same key
+    __syncthreads();
+    uint32_t tau = static_cast<uint32_t>(s.lo);
+    uint64_t mk = 0;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+        if (t + q * T < n && kk[q] >= tau) mk += w[t + q * T];
+    const uint64_t mass_k = block_sum(mk, s);
+    uint64_t kept = mass_k;
+    if (tp) {
+        const uint64_t target =
+            static_cast<uint64_t>(ceil(static_cast<double>(top_p) * static_cast<double>(mass_k)));
+        uint32_t best = 0u;
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+            if (t + q * T < n && up[q] >= target && kk[q] > best) best = kk[q];
+        atomicMax(reinterpret_cast<unsigned int*>(&s.e), best);
+        __syncthreads();
+        tau = static_cast<uint32_t>(s.e);
+#pragma unroll
+        for (int q = 0; q < kPer; ++q)
+            if (t + q * T < n && kk[q] == tau) s.above = up[q];  // equal keys, equal sums
+        __syncthreads();
+        kept = s.above;
+    }
+    *tau_out = tau;
+    *kept_out = kept;
+}
+
 // Sum of the masses of src's keys >= tau.
 template <typename Src>
 __device__ __noinline__ uint64_t mass_ge(const Src& src, uint32_t tau, float c, float mref,
@@ -768,6 +838,41 @@ __device__ __forceinline__ uint32_t bf16_bits_of_key16(uint32_t p)
     return (p & 0x8000u) ? (p & 0x7FFFu) : (~p & 0xFFFFu);
 }
 
+// Sorts 256 keys held 8 per lane (key j of lane l is element 8 l + j) into
+// descending order across the warp: a bitonic network, compare-exchanges in
+// registers for partners in the same lane and by shuffles otherwise.
+__device__ __forceinline__ void warp_sort256_desc(uint32_t (&v)[8])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int size = 2; size <= 256; size <<= 1) {
+#pragma unroll
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride >= 8) {
+                const int ls = stride >> 3;
+                const bool lower = (lane & ls) == 0;
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v[j], ls);
+                    const bool desc = ((lane * 8 + j) & size) == 0;
+                    v[j] = (lower == desc) ? max(v[j], o) : min(v[j], o);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int pj = j ^ stride;
+                    if (pj > j) {
+                        const bool desc = ((lane * 8 + j) & size) == 0;
+                        const uint32_t x = v[j], y = v[pj];
+                        v[j] = desc ? max(x, y) : min(x, y);
+                        v[pj] = desc ? min(x, y) : max(x, y);
+                    }
+                }
+            }
+        }
+    }
+}
+
 // Packed x >= y on both bf16 halves: 0xFFFF per half where it holds.
 __device__ __forceinline__ unsigned ge2_mask(uint32_t a, uint32_t b)
 {
@@ -785,22 +890,25 @@ __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
     return r;
 }
 
-// Appends every element >= lk (by key) of thread tt's share of the row: the
-// head / tail indices and 16-byte vectors congruent to tt modulo the block
-// size, as the reads give them out. The whole CTA reads the share, one vector
-// per thread.
+// Appends every element >= lk (by key) of the shares of threads inc[0 .. ninc)
+// of the row: a share is the head / tail indices and 16-byte vectors
+// congruent to its thread index modulo the block size, as the reads give them
+// out. The CTA reads the shares' vectors together, one vector per thread per
+// round, the loads of a round issued before any is used.
 template <int ES>
-__device__ void reread_share(const uint8_t* row, int64_t V, int tt, uint32_t lk, uint32_t* list,
-                             int* count)
+__device__ __noinline__ void reread_shares(const uint8_t* row, int64_t V, const int* inc, int ninc,
+                                           uint32_t lk, uint32_t* list, int* count)
 {
     constexpr int kEPV = 16 / ES;
+    constexpr int kU = 4;
     const uintptr_t p = reinterpret_cast<uintptr_t>(row);
     int64_t head = static_cast<int64_t>(((16u - static_cast<uint32_t>(p & 15u)) & 15u) / ES);
     if (head > V) head = V;
     const int64_t nvec = (V - head) / kEPV;
     const int64_t tail = head + nvec * kEPV;
     const int64_t T = blockDim.x;
-    if (threadIdx.x == 0) {
+    if (threadIdx.x < ninc) {
+        const int tt = inc[threadIdx.x];
         if (tt < head) {
             const uint32_t key = fkey(load_elem<ES>(row + tt * ES));
             if (key >= lk) append(key, list, count);
@@ -811,13 +919,28 @@ __device__ void reread_share(const uint8_t* row, int64_t V, int tt, uint32_t lk,
         }
     }
     const uint4* vp = reinterpret_cast<const uint4*>(row + head * ES);
-    for (int64_t v = tt + threadIdx.x * T; v < nvec; v += T * T) {
-        float x[kEPV];
-        unpack_vec<ES>(__ldg(vp + v), x);
+    const int64_t per = (nvec + T - 1) / T;  // vectors in a share (at most)
+    const int64_t items = per * ninc;
+    for (int64_t i0 = threadIdx.x; i0 < items; i0 += kU * T) {
+        uint4 u[kU];
+        bool ok[kU];
 #pragma unroll
-        for (int e = 0; e < kEPV; ++e) {
-            const uint32_t key = fkey(x[e]);
-            if (key >= lk) append(key, list, count);
+        for (int q = 0; q < kU; ++q) {
+            const int64_t i = i0 + q * T;
+            const int64_t g = i < items ? inc[i / per] + (i % per) * T : nvec;
+            ok[q] = g < nvec;
+            if (ok[q]) u[q] = __ldg(vp + g);
+        }
+#pragma unroll
+        for (int q = 0; q < kU; ++q) {
+            if (!ok[q]) continue;
+            float x[kEPV];
+            unpack_vec<ES>(u[q], x);
+#pragma unroll
+            for (int e = 0; e < kEPV; ++e) {
+                const uint32_t key = fkey(x[e]);
+                if (key >= lk) append(key, list, count);
+            }
         }
     }
 }
@@ -951,11 +1074,37 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
             // logit from below. A group whose second value is below the
             // bound has at most one element above it, its maximum; a thread
             // with a group that has two or more reads its share again.
-#pragma unroll
-            for (int q = 0; q < G; ++q) cand[G * t + q] = fkey(m1[q]);
             if (t == 0) s.list_n = 0;
-            __syncthreads();
-            const uint32_t lk = (list_select_kth(cand, G * T, k, 2, hc, s) >> 16) << 16;
+            uint32_t lk;
+            if (k <= static_cast<uint64_t>(kSortK) && T == 256) {
+                // For small k the thread maxima (distinct elements as well)
+                // give a bound almost as tight: one warp sorts them and
+                // takes the k-th.
+                uint32_t tm = fkey(m1[0]);
+#pragma unroll
+                for (int q = 1; q < G; ++q) tm = max(tm, fkey(m1[q]));
+                cand[t] = tm;
+                __syncthreads();
+                if (t < 32) {
+                    uint32_t v[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) v[j] = cand[8 * t + j];
+                    warp_sort256_desc(v);
+                    const int kk = static_cast<int>(k) - 1;
+                    if (t == (kk >> 3)) {
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            if (j == (kk & 7)) s.lo = static_cast<int>(v[j]);
+                    }
+                }
+                __syncthreads();
+                lk = static_cast<uint32_t>(s.lo);
+            } else {
+#pragma unroll
+                for (int q = 0; q < G; ++q) cand[G * t + q] = fkey(m1[q]);
+                __syncthreads();
+                lk = (list_select_kth(cand, G * T, k, 2, hc, s) >> 16) << 16;
+            }
             bool complete = true;
 #pragma unroll
             for (int q = 0; q < G; ++q) complete = complete && fkey(m2[q]) < lk;
@@ -972,14 +1121,13 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                     inc[atomicAdd(&s.inc_n, 1)] = t;
                 }
                 __syncthreads();
-                for (int q = 0; q < s.inc_n; ++q)
-                    reread_share<ES>(row, V, inc[q], lk, list, &s.list_n);
+                reread_shares<ES>(row, V, inc, s.inc_n, lk, list, &s.list_n);
             } else {
                 // Many groups hold two or more elements above the bound (k in the
                 // hundreds): one more read of the whole row, a packed compare
                 // per 16-byte vector.
                 const uint32_t p16 = lk >> 16;
-                const bool open = p16 <= 0x007Fu;  // the bound is -inf's prefix or lower
+                const bool open = lk <= 0x007FFFFFu;  // the bound is -inf or lower
                 const float bound = open ? ninf : key_value(lk);
                 const uint32_t b16 = open ? 0xFF80u : bf16_bits_of_key16(p16);
                 const uint32_t b2 = b16 | (b16 << 16);
@@ -1028,6 +1176,9 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                 __syncthreads();
                 tau = static_cast<uint32_t>(s.e);
                 kept = s.above;
+                done = true;
+            } else if (n <= kMidList) {
+                mid_select(list, n, k, tp, a.top_p, c, mref, hm, s, &tau, &kept);
                 done = true;
             } else if (n <= kListCap) {
                 const ListSrc L{list, n};

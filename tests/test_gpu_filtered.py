@@ -127,6 +127,10 @@ CASES = [
     ("llama3_bf16", {"B": 12}, 0, 0.8),
     ("qwen_long_bf16", {"B": 4}, 100, 0.95),
     ("qwen_long_bf16", {"B": 4}, 0, 0.9),    # flat rows: top-p bins refined twice
+    ("spiky_bf16", {"B": 16}, 200, 1.0),     # lists of 129..512 keys: block-wide select
+    ("spiky_bf16", {"B": 16}, 500, 0.8),
+    ("llama3_bf16", {"B": 8}, 1000, 0.9),    # longer lists: radix select on the list
+    ("small_f32", {"B": 4}, 1000, 1.0),
     ("spiky_bf16", {"B": 16}, 3000, 1.0),    # k beyond the candidate list: whole-row select
     ("small_f32", {"B": 4}, 4000, 0.8),
 ]
