@@ -38,8 +38,9 @@
 // Masses are integers, so every sum -- and every decision -- is the same on
 // every run: a list element's mass is its 2^(x c - m) (m the ceiling of
 // max x c) scaled by 2^40 and rounded; a bin adds per-thread 32-bit sums of
-// its elements' masses relative to the bin's upper edge, scaled by 2^SC with
-// SC chosen so that a thread's sum cannot overflow, and rescaled by a shift.
+// its elements' masses relative to the bin's reference power of two, scaled by
+// 2^SC with SC chosen so that a thread's sum cannot overflow, and rescaled by
+// a shift.
 // The roundings (below 2^-22 of each element's mass) and the SFU exponential
 // (a few ulp per term) move a top-p boundary by well under 1e-5 of the mass.
 #include <cooperative_groups.h>
@@ -216,6 +217,7 @@ struct Ring {
     uint64_t* bar;   // [kStages] mbarriers
     uint8_t* buf;    // kStages tiles
     uint32_t phase;  // bit s: parity of the next wait on stage s
+    int tile;        // bytes per stage (a multiple of 16)
 };
 
 __device__ __forceinline__ void fence_proxy_async()
@@ -231,15 +233,16 @@ template <typename FV>
 __device__ bool ring_sweep(Ring& rg, const uint8_t* row, int64_t bytes, FV&& fv)
 {
     const int t = threadIdx.x, T = blockDim.x;
-    const int64_t ntiles = (bytes + kTileBytes - 1) / kTileBytes;
+    const int64_t tb = rg.tile;
+    const int64_t ntiles = (bytes + tb - 1) / tb;
     auto tile_bytes = [&](int64_t i) {
-        const int64_t n = bytes - i * kTileBytes;
-        return static_cast<uint32_t>(n < kTileBytes ? n : kTileBytes);
+        const int64_t n = bytes - i * tb;
+        return static_cast<uint32_t>(n < tb ? n : tb);
     };
     auto issue = [&](int64_t i) {
         const int st = static_cast<int>(i % kStages);
         mbar_arrive_expect_tx(&rg.bar[st], tile_bytes(i));
-        bulk_copy_g2s(rg.buf + st * kTileBytes, row + i * kTileBytes, tile_bytes(i), &rg.bar[st]);
+        bulk_copy_g2s(rg.buf + st * tb, row + i * tb, tile_bytes(i), &rg.bar[st]);
     };
     if (t == 0) {
         fence_proxy_async();  // earlier generic accesses to the buffer come first
@@ -250,7 +253,7 @@ __device__ bool ring_sweep(Ring& rg, const uint8_t* row, int64_t bytes, FV&& fv)
         bool ok = mbar_wait_bounded(&rg.bar[st], (rg.phase >> st) & 1u, nullptr);
         rg.phase ^= 1u << st;
         if (ok) {
-            const uint8_t* base = rg.buf + st * kTileBytes;
+            const uint8_t* base = rg.buf + st * tb;
             const int nvec = static_cast<int>(tile_bytes(i) / 16);
             for (int v = t; v < nvec; v += T) fv(ld_shared_v4(base + 16 * v));
         }
@@ -692,6 +695,33 @@ __device__ __noinline__ uint32_t select_mass(const Src& src, uint64_t base, uint
     return prefix;
 }
 
+// Conversions by float addition instead of float <-> integer conversions
+// (those issue at a quarter of the rate; these are one add and one integer
+// subtract): adding 1.5 * 2^23 to a float of magnitude below 2^22 rounds it to
+// an integer held in the low mantissa bits.
+constexpr float kMagic = 12582912.0f;  // 1.5 * 2^23
+constexpr uint32_t kMagicBits = 0x4B400000u;
+
+// First-level bin of a log2 mass e (e <= 0 up to rounding): j = round(-e),
+// r = j as a float. The bin's masses 2^e lie within a factor 2^(1/2) of 2^-j.
+struct DBin {
+    int j;
+    float r;
+};
+__device__ __forceinline__ DBin dbin(float e)
+{
+    const float y = kMagic - e;
+    int j = static_cast<int>(__float_as_uint(y) - kMagicBits);
+    j = j < 0 ? 0 : (j > kDBins - 1 ? kDBins - 1 : j);
+    return DBin{j, static_cast<float>(y - kMagic)};
+}
+
+// round(m * scale) for 0 <= m * scale < 2^22.
+__device__ __forceinline__ uint32_t to_fixed(float m, float scale)
+{
+    return __float_as_uint(fmaf(m, scale, 8388608.0f)) - 0x4B000000u;
+}
+
 // Totals of the per-thread bins (column j of bins[kDBins][T]) in 2^40 units:
 // a bin's words hold masses 2^(x c - m + edge) 2^sc, so the total is shifted
 // by 40 - sc - edge (edge = j at the first level, J0 below it). Written to
@@ -713,30 +743,50 @@ __device__ void bin_totals(const uint32_t* bins, int sc, int J0, bool first, Scr
     }
 }
 
-// Top-p alone on one row (see the file comment). Returns false when the row
-// needs the radix select over the whole row instead.
+// Top-p alone on one row (see the file comment). Returns 1 when done, 0 when
+// the row needs the radix select over the whole row instead, -1 when a bulk
+// copy did not arrive in time. Rows of whole 16-byte vectors stream through
+// the ring, placed in whichever region the sweep leaves free: the list while
+// per-thread bins are being filled, the bins while the list is.
 template <int ES>
-__device__ __noinline__ bool topp_bins(const uint8_t* row, int64_t V, float c, float mref,
-                                       float top_p, int sc, uint32_t* bins, uint32_t* list,
-                                       Scratch& s, uint32_t* tau, uint64_t* kept)
+__device__ __noinline__ int topp_bins(const uint8_t* row, int64_t V, float c, float mref,
+                                      float top_p, int sc, uint32_t* bins, uint32_t* list,
+                                      Scratch& s, Ring& rg, bool use_ring, uint32_t* tau,
+                                      uint64_t* kept)
 {
     const int T = blockDim.x, t = threadIdx.x;
     const float scale = __int_as_float((127 + sc) << 23);  // 2^sc
     uint64_t* hm = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(bins) + kCandBytes +
                                                kCountBytes);
-    // First level: bin j = floor(log2 distance from 2^m), j < 32.
+    // f(x) for every element; false if a copy did not land.
+    auto each = [&](bool ring_in_list, auto&& f) -> bool {
+        if (!use_ring) {
+            sweep<ES>(row, V, f);
+            return true;
+        }
+        rg.buf = ring_in_list ? reinterpret_cast<uint8_t*>(list) : reinterpret_cast<uint8_t*>(bins);
+        rg.tile = ring_in_list ? static_cast<int>(kListBytes / kStages) : kTileBytes;
+        return ring_sweep(rg, row, V * ES, [&](const uint4& u) {
+            float x[16 / ES];
+            unpack_vec<ES>(u, x);
+#pragma unroll
+            for (int e = 0; e < 16 / ES; ++e) f(x[e]);
+        });
+    };
+    // First level: bin j = round(log2 distance from 2^m), j < 32.
     for (int j = 0; j < kDBins; ++j) bins[j * T + t] = 0u;
     float tail = 0.f;
-    sweep<ES>(row, V, [&](float x) {
+    __syncthreads();  // the list region is free for the ring
+    if (!each(true, [&](float x) {
         const float e = fmaf(x, c, -mref);  // log2 of the mass relative to 2^m
-        if (e > -32.f) {
-            int j = static_cast<int>(-e);
-            j = j < 0 ? 0 : j;
-            bins[j * T + t] += __float2uint_rn(ex2(e + static_cast<float>(j)) * scale);
+        if (e > -31.5f) {
+            const DBin b = dbin(e);
+            bins[b.j * T + t] += to_fixed(ex2(e + b.r), scale);
         } else {
             tail += ex2(e);
         }
-    });
+    }))
+        return -1;
     // The tail beyond 32 units: a float sum per thread, added in a fixed order.
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) tail += __shfl_xor_sync(0xFFFFFFFFu, tail, off);
@@ -755,57 +805,71 @@ __device__ __noinline__ bool topp_bins(const uint8_t* row, int64_t V, float c, f
     const uint64_t target =
         static_cast<uint64_t>(ceil(static_cast<double>(top_p) * static_cast<double>(M)));
     crossing(s.tot, kDBins + 1, 0, target, s);
-    if (s.e <= 0) return false;  // the crossing lies in the tail
+    if (s.e <= 0) return 0;  // the crossing lies in the tail
     const int J0 = kDBins - s.e;
     uint64_t above = s.above;
+    // The window (bin J0, then sub-bins of it) spans log2 distances
+    // [J0 - 1/2 + off, J0 - 1/2 + off + width); each of its elements has a
+    // mass of at least 2^(40 - (far edge)) in 2^40 units, so the window's mass
+    // bounds its count.
+    uint64_t wmass = s.tot[s.e];
+    double off = 0.0, width = 1.0;
     int chosen[kRefine];
-    for (int L = 1; L <= kRefine; ++L) {
-        // Read the window (bin J0, then the chosen sub-bins) into the list and,
-        // in case it does not fit, into the next level's sub-bins.
+    for (int L = 0; L <= kRefine; ++L) {
+        const double ub =
+            static_cast<double>(wmass) / exp2(40.0 - (J0 - 0.5 + off + width)) * 1.001 + 16.0;
+        const bool collect = ub <= kListCap || L == kRefine;
+        // Read the window: into the list when it fits, else into the next
+        // level's 32 sub-bins.
         __syncthreads();
-        for (int j = 0; j < kDBins; ++j) bins[j * T + t] = 0u;
+        if (!collect)
+            for (int j = 0; j < kDBins; ++j) bins[j * T + t] = 0u;
         if (t == 0) s.list_n = 0;
         __syncthreads();
-        sweep<ES>(row, V, [&](float x) {
+        if (!each(!collect, [&](float x) {
             const float e = fmaf(x, c, -mref);
-            if (!(e > -32.f)) return;
-            int j = static_cast<int>(-e);
-            j = j < 0 ? 0 : j;
-            if (j != J0) return;
-            // Base-32 digits of the distance's fraction u = -e - J0 (exact
-            // float steps: scalings by 32 and subtractions of integers).
-            float y = -e - static_cast<float>(J0);
-            int idx = 0;
-            for (int l = 1; l <= L; ++l) {
+            if (!(e > -31.5f)) return;
+            const DBin b = dbin(e);
+            if (b.j != J0) return;
+            // Base-32 digits of the distance's offset in the bin, y = -e - J0
+            // + 1/2 in [0, 1] (monotone float steps: scalings by 32 and
+            // subtractions of integers).
+            float y = (-e - b.r) + 0.5f;
+            for (int l = 0; l < L; ++l) {
                 y *= 32.f;
                 int dl = static_cast<int>(y);
                 dl = dl < 0 ? 0 : (dl > kDBins - 1 ? kDBins - 1 : dl);
-                if (l == L) {
-                    idx = dl;
-                } else {
-                    if (dl != chosen[l - 1]) return;
-                    y -= static_cast<float>(dl);
-                }
+                if (dl != chosen[l]) return;
+                y -= static_cast<float>(dl);
             }
-            append(fkey(x), list, &s.list_n);
-            bins[idx * T + t] += __float2uint_rn(ex2(e + static_cast<float>(J0)) * scale);
-        });
+            if (collect) {
+                append(fkey(x), list, &s.list_n);
+            } else {
+                int idx = static_cast<int>(y * 32.f);
+                idx = idx < 0 ? 0 : (idx > kDBins - 1 ? kDBins - 1 : idx);
+                bins[idx * T + t] += to_fixed(ex2(e + b.r), scale);
+            }
+        }))
+            return -1;
         __syncthreads();
-        const int n = s.list_n;
-        if (n <= kListCap) {
+        if (collect) {
+            const int n = s.list_n;
+            if (n > kListCap) return 0;
             __syncthreads();  // every thread has read n before the bins are reused
             *tau = list_select_mass(list, n, above, target, c, mref, hm, s, kept);
-            return true;
+            return 1;
         }
-        if (L == kRefine) break;
         bin_totals(bins, sc, J0, false, s);
         __syncthreads();
         crossing(s.tot, kDBins, above, target, s);
-        if (s.e < 0) return false;
-        chosen[L - 1] = kDBins - 1 - s.e;
+        if (s.e < 0) return 0;
+        chosen[L] = kDBins - 1 - s.e;
         above = s.above;
+        wmass = s.tot[s.e];
+        off += chosen[L] * (width / kDBins);
+        width /= kDBins;
     }
-    return false;
+    return 0;
 }
 
 // The radix select over the whole row (rare: see the file comment).
@@ -967,7 +1031,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
     const int T = blockDim.x, t = threadIdx.x;
     // Whole 16-byte vectors per row: every row starts 16-byte aligned.
     const bool use_ring = (V * ES) % 16 == 0;
-    Ring rg{ring_bar, smem, 0u};
+    Ring rg{ring_bar, smem, 0u, kTileBytes};
     if (t == 0) {
         for (int i = 0; i < kStages; ++i) mbar_init(&ring_bar[i], 1);
         fence_barrier_init();
@@ -980,10 +1044,13 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
     const bool fast_k = tk && a.top_k <= static_cast<int64_t>(G) * T;
     const float c = a.c;
     const float ninf = __uint_as_float(kF32NegInfBits);
-    // Per-thread bin words add at most V / T + 16 masses of at most 2^sc (+1).
+    // Per-thread bin words add at most V / T + 16 masses of at most
+    // 2^(sc + 1/2) (+1/2).
     int lg = 0;
     while ((int64_t(1) << lg) < V / T + 16) ++lg;
-    const int sc = 31 - lg;
+    // One bit of headroom for masses up to 2^(1/2) of a bin's reference, and
+    // at most 22 bits so that to_fixed stays exact.
+    const int sc = 30 - lg < 22 ? 30 - lg : 22;
     pdl_trigger();  // the scan may launch; it waits for this grid before reading
 
     for (int64_t r = blockIdx.x; r < g.rows; r += gridDim.x) {
@@ -1192,7 +1259,15 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                 done = true;
             }
         } else if (tp && !tk) {
-            done = topp_bins<ES>(row, V, c, mref, a.top_p, sc, bins, list, s, &tau, &kept);
+            const int got = topp_bins<ES>(row, V, c, mref, a.top_p, sc, bins, list, s, rg, use_ring,
+                                          &tau, &kept);
+            rg.buf = smem;  // the ring's usual place
+            rg.tile = kTileBytes;
+            if (got < 0) {
+                fail_rows(a, r);
+                return;
+            }
+            done = got > 0;
         }
         if (!done) row_select<ES>(row, V, tk, k, tp, a.top_p, c, mref, hc, hm, s, &tau, &kept);
         if (t == 0) {
