@@ -274,3 +274,18 @@ def test_filtered_timed_events():
     b = sv.spec_verify_filtered(inputs["target"], inputs["draft"], inputs["tokens"],
                                 wl.temperature, 20, 0.9, 3)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("K", [0, 1, 16])
+@pytest.mark.parametrize("top_k,top_p", [(20, 1.0), (0, 0.8), (50, 0.9)])
+def test_filtered_draft_counts(K, top_k, top_p):
+    """K = 0 (only the bonus row, drawn from the filtered p'_0), one draft, and
+    long runs."""
+    wl = WORKLOADS["spiky_bf16"].resized(B=6, K=K, V=3000)
+    check(wl, 31, top_k, top_p)
+
+
+def test_filtered_single_sequence_full_vocab():
+    wl = WORKLOADS["llama3_bf16"].resized(B=1)
+    st, _, _ = check(wl, 41, 50, 0.9)
+    assert st["decisions"] > 0
