@@ -19,8 +19,15 @@ Parity status of each function (how it is pinned, see ``tests/test_oracle_*.py``
   near-tie law, and closed-form acceptance rates.
 * ``row_argmax`` -- pinned against ``torch.argmax`` (first occurrence).
 
+* ``lm_head_logits`` / ``verify_lmhead`` -- the LM head h W^T (the pages take
+  each model's logits as given; this is the product a language model's output
+  layer computes), pinned by brute-force sums on tiny inputs, one-hot hidden
+  states that pick out one column of W, and linearity; then ``verify`` on the
+  float64 logits.
+
 Arrays: float32 logits are passed as ``np.float32``; bfloat16 logits as their
-raw 16-bit patterns in ``np.uint16``.
+raw 16-bit patterns in ``np.uint16``; float64 logits (the LM head's exact
+products) as ``np.float64``.
 """
 from __future__ import annotations
 
@@ -37,7 +44,7 @@ _SRC = os.path.join(_HERE, "sv_oracle.c")
 _HDR = os.path.join(_HERE, "sv_oracle.h")
 _LIB = os.path.join(_HERE, "libsvoracle.so")
 
-F32, BF16 = 0, 1
+F32, BF16, F64 = 0, 1, 2
 SAMPLE, GREEDY = 0, 1
 BAD_TOKEN, NONFINITE = 1, 2
 
@@ -115,7 +122,9 @@ def _dtype_code(a: np.ndarray) -> int:
         return F32
     if a.dtype == np.uint16:
         return BF16
-    raise TypeError(f"logits must be float32 or uint16 (bfloat16 bits), got {a.dtype}")
+    if a.dtype == np.float64:
+        return F64
+    raise TypeError(f"logits must be float32, uint16 (bfloat16 bits) or float64, got {a.dtype}")
 
 
 def philox(ctr, key) -> np.ndarray:
@@ -271,3 +280,49 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
         with ThreadPoolExecutor(max_workers=threads) as ex:
             list(ex.map(lambda t: run(bounds[t], bounds[t + 1]), range(threads)))
     return out
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bfloat16 bit patterns (uint16) to float64, exactly: the 16 bits are the
+    high half of a binary32."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def lm_head_logits(hidden_bits: np.ndarray, weight_bits: np.ndarray) -> np.ndarray:
+    """logits[..., v] = sum_d h[..., d] W[v, d] in float64.
+
+    hidden_bits [..., D] and weight_bits [V, D] are bfloat16 bit patterns.
+    Every product of two bfloat16 values is exact in float64 (8 + 8
+    significant bits), and the float64 sum over D terms is within D 2^-53 of
+    the exact dot product, far below the float32 accumulation the GPU does.
+    The matrix product is the library's; no blocking or reordering here.
+    """
+    h = bf16_bits_to_f64(hidden_bits)
+    w = bf16_bits_to_f64(weight_bits)
+    if h.shape[-1] != w.shape[1]:
+        raise ValueError("hidden [..., D] and weight [V, D] disagree on D")
+    return h @ w.T
+
+
+def verify_lmhead(hidden_t, weight_t, hidden_d, weight_d, tokens, temperature: float, seed: int,
+                  mode: int = SAMPLE, seq_range=None, threads: int = 1) -> dict:
+    """``verify`` on the logits the two LM heads produce: target logits
+    hidden_t [B, K+1, Dt] x weight_t [V, Dt]^T, draft logits hidden_d [B, K, Dd]
+    x weight_d [V, Dd]^T (None in greedy mode), all bfloat16 bit patterns.
+    ``seq_range=(b0, b1)`` computes the logits of those sequences only (the
+    other rows stay zero pages that are never touched) and verifies them; the
+    other sequences' outputs keep their fill values."""
+    hidden_t = np.ascontiguousarray(hidden_t, dtype=np.uint16)
+    B, K1, _ = hidden_t.shape
+    K = K1 - 1
+    V = weight_t.shape[0]
+    b0, b1 = (0, B) if seq_range is None else seq_range
+    lt = np.zeros((B, K1, V), dtype=np.float64)
+    lt[b0:b1] = lm_head_logits(hidden_t[b0:b1], weight_t)
+    ld = None
+    if mode == SAMPLE and hidden_d is not None:
+        hidden_d = np.ascontiguousarray(hidden_d, dtype=np.uint16)
+        ld = np.zeros((B, K, V), dtype=np.float64)
+        ld[b0:b1] = lm_head_logits(hidden_d[b0:b1], weight_d)
+    return verify(lt, ld, tokens, temperature, seed, mode, threads=threads, seq_range=(b0, b1))

@@ -119,6 +119,11 @@ double svo_uniform(uint64_t seed, uint32_t seq, uint32_t pos, int lane)
 double svo_elem(const void* row, int64_t k, int dtype)
 {
     float f;
+    if (dtype == SVO_F64) {
+        double d;
+        memcpy(&d, (const unsigned char*)row + 8 * k, 8);
+        return d;
+    }
     if (dtype == SVO_F32) {
         memcpy(&f, (const unsigned char*)row + 4 * k, 4);
     } else {
@@ -361,7 +366,7 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
                             int32_t* seq_status)
 {
     const int filtering = (top_k > 0 && top_k < V) || top_p < 1.0;
-    const size_t esz = (dtype == SVO_F32) ? 4 : 2;
+    const size_t esz = (dtype == SVO_F64) ? 8 : (dtype == SVO_F32) ? 4 : 2;
     const unsigned char* trow0 = (const unsigned char*)target + (size_t)(b * (K + 1)) * V * esz;
     const unsigned char* drow0 =
         draft ? (const unsigned char*)draft + (size_t)(b * K) * V * esz : NULL;
@@ -493,7 +498,7 @@ static void verify_greedy(const void* target, const int32_t* tokens, int64_t b, 
                           int64_t V, int dtype, int32_t* out_tokens, int32_t* num_accepted,
                           double* accept_margin, double* sample_margin, int32_t* seq_status)
 {
-    const size_t esz = (dtype == SVO_F32) ? 4 : 2;
+    const size_t esz = (dtype == SVO_F64) ? 8 : (dtype == SVO_F32) ? 4 : 2;
     const unsigned char* trow0 = (const unsigned char*)target + (size_t)(b * (K + 1)) * V * esz;
     int64_t* a = (int64_t*)malloc(sizeof(int64_t) * (size_t)(K + 1));
     int32_t status = 0;
@@ -553,7 +558,7 @@ int svo_verify_filtered(const void* target, const void* draft, const int32_t* to
     int64_t b;
     if (!(top_p > 0.0 && top_p <= 1.0)) return -1;
     if (B < 0 || K < 0 || V < 1 || b0 < 0 || b1 > B || b0 > b1) return -1;
-    if (dtype != SVO_F32 && dtype != SVO_BF16) return -1;
+    if (dtype != SVO_F32 && dtype != SVO_BF16 && dtype != SVO_F64) return -1;
     if (mode != SVO_SAMPLE && mode != SVO_GREEDY) return -1;
     if (target == NULL || out_tokens == NULL || num_accepted == NULL) return -1;
     if (K > 0 && tokens == NULL) return -1;

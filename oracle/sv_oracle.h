@@ -12,7 +12,9 @@
  *   p = target distribution, q = draft distribution, both softmax(logits / T).
  *   target rows: [B, K+1, V]; row i < K verifies draft token x_i, row K is the
  *   bonus row. draft rows: [B, K, V]. Row-major, contiguous.
- *   dtype 0 = IEEE binary32, dtype 1 = bfloat16 (raw 16-bit patterns).
+ *   dtype 0 = IEEE binary32, dtype 1 = bfloat16 (raw 16-bit patterns),
+ *   dtype 2 = IEEE binary64 (logits an LM head computed exactly, e.g. from
+ *   bfloat16 hidden states and weights).
  */
 #ifndef SV_ORACLE_H
 #define SV_ORACLE_H
@@ -23,7 +25,7 @@
 extern "C" {
 #endif
 
-enum { SVO_F32 = 0, SVO_BF16 = 1 };
+enum { SVO_F32 = 0, SVO_BF16 = 1, SVO_F64 = 2 };
 enum { SVO_SAMPLE = 0, SVO_GREEDY = 1 };
 
 /* Per-sequence status bits written by svo_verify. */

@@ -157,3 +157,108 @@ def to_host_arrays(inputs: dict):
 
     return conv(inputs["target"]), conv(inputs["draft"]), \
         inputs["tokens"].detach().cpu().numpy().astype(np.int32)
+
+
+@dataclasses.dataclass(frozen=True)
+class LmWorkload:
+    """Hidden states and output matrices for verification from the models'
+    last layer (the LM head computes the logits). Synthetic: no trained
+    weights exist here. Target: h ~ N(0, 1) per coordinate, W ~ N(0,
+    target_std^2 / d_target), so every target logit is ~ N(0, target_std^2).
+    Draft: the first m = min(d_draft, d_target) coordinates of the target's
+    hidden state plus N(0, draft_noise^2), and the first m columns of W scaled
+    by sqrt(d_target / m), so a draft logit has about the same spread and a
+    correlation of about sqrt(m / d_target) with the target's (a wider draft
+    gets fresh coordinates with small weights)."""
+    name: str
+    B: int
+    K: int
+    V: int
+    d_target: int
+    d_draft: int
+    mode: str
+    temperature: float
+    target_std: float
+    draft_noise: float
+
+    @property
+    def label(self) -> str:
+        t = f" T={self.temperature:g}" if self.mode == "sample" else ""
+        return (f"B={self.B} K={self.K} V={self.V} D={self.d_target}/{self.d_draft} "
+                f"{self.mode}{t}")
+
+    def resized(self, **kw) -> "LmWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+LM_WORKLOADS = {
+    # Small: several row blocks, vocabulary tiles and k-blocks, ragged at every edge.
+    "lm_small": LmWorkload("lm_small", 64, 4, 1000, 200, 136, "sample", 1.0, 2.0, 0.3),
+    # Llama-3-8B target (hidden 4096) with a Llama-3.2-1B-sized draft (hidden
+    # 2048), vocabulary 128256, B=256, K=8, T=0.7.
+    "lm_llama3_bf16": LmWorkload("lm_llama3_bf16", 256, 8, 128256, 4096, 2048, "sample", 0.7,
+                                 2.5, 0.3),
+    # Greedy on the same target head.
+    "lm_greedy_bf16": LmWorkload("lm_greedy_bf16", 256, 8, 128256, 4096, 2048, "greedy", 1.0,
+                                 2.5, 0.3),
+}
+
+
+def make_lmhead_inputs(lw: LmWorkload, seed: int, device="cpu") -> dict:
+    """One batch for ``lw``: hidden_t [B, K+1, Dt], weight_t [V, Dt], hidden_d
+    [B, K, Dd], weight_d [V, Dd] (bfloat16; the draft pair None in greedy mode)
+    and tokens [B, K] int32. Draft tokens are drawn from the draft head's own
+    softmax at the workload's temperature (greedy: the argmax of a noisy copy
+    of the target logits), computed here in float32 from the stored bfloat16
+    operands. Input generation only."""
+    dev = torch.device(device)
+    g = torch.Generator(device=dev)
+    g.manual_seed(int(seed))
+    B, K, V, Dt, Dd = lw.B, lw.K, lw.V, lw.d_target, lw.d_draft
+    ht = torch.randn((B, K + 1, Dt), generator=g, device=dev).to(torch.bfloat16)
+    wt = (torch.randn((V, Dt), generator=g, device=dev) * (lw.target_std / Dt ** 0.5)).to(
+        torch.bfloat16)
+    if lw.mode == "greedy":
+        tokens = torch.zeros((B, K), dtype=torch.int32, device=dev)
+        wtf = wt.float()
+        step = max(1, (1 << 26) // max(V * max(K, 1), 1))
+        for s in range(0, B if K > 0 else 0, step):
+            e = min(B, s + step)
+            lg = ht[s:e, :K].float() @ wtf.T
+            lg += lw.draft_noise * lw.target_std * torch.randn(lg.shape, generator=g, device=dev)
+            tokens[s:e] = lg.argmax(dim=-1).to(torch.int32)
+        return {"hidden_t": ht.contiguous(), "weight_t": wt.contiguous(), "hidden_d": None,
+                "weight_d": None, "tokens": tokens}
+    m = min(Dd, Dt)
+    hd = lw.draft_noise * torch.randn((B, K, Dd), generator=g, device=dev)
+    hd[..., :m] += ht[:, :K, :m].float()
+    if Dd > m:  # a wider draft: its extra coordinates are fresh N(0, 1)
+        hd[..., m:] = torch.randn((B, K, Dd - m), generator=g, device=dev)
+    hd = hd.to(torch.bfloat16).contiguous()
+    wd = torch.empty((V, Dd), device=dev)
+    wd[:, :m] = wt[:, :m].float() * (Dt / m) ** 0.5
+    if Dd > m:  # small weights on the extra coordinates
+        wd[:, m:] = torch.randn((V, Dd - m), generator=g, device=dev) * (
+            0.3 * lw.target_std / Dd ** 0.5)
+    wd = wd.to(torch.bfloat16).contiguous()
+    tokens = torch.zeros((B, K), dtype=torch.int32, device=dev)
+    step = max(1, (1 << 26) // max(V * max(K, 1), 1))
+    wdf = wd.float()
+    for s in range(0, B, step):
+        e = min(B, s + step)
+        if K == 0:
+            break
+        lg = (hd[s:e].float() @ wdf.T).contiguous()
+        tokens[s:e] = draw_from_logits(lg, lw.temperature, g)
+    return {"hidden_t": ht.contiguous(), "weight_t": wt.contiguous(), "hidden_d": hd,
+            "weight_d": wd, "tokens": tokens}
+
+
+def lm_host_arrays(inputs: dict):
+    """(hidden_t, weight_t, hidden_d, weight_d, tokens) as the oracle reads
+    them: bfloat16 bit patterns (uint16) and int32."""
+    def conv(t):
+        return None if t is None else bf16_bits(t)
+
+    return (conv(inputs["hidden_t"]), conv(inputs["weight_t"]), conv(inputs["hidden_d"]),
+            conv(inputs["weight_d"]), inputs["tokens"].detach().cpu().numpy().astype("int32"))
