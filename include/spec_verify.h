@@ -359,6 +359,100 @@ int spec_verify_filtered_timed(const void* target_logits, const void* draft_logi
                                void* stream, void* const* events, int n_events);
 
 /*
+ * Workspace needed by spec_verify_lmhead for these sizes on the CURRENT
+ * device (d_target / d_draft: hidden sizes). Writes the byte count to *bytes.
+ */
+int sv_lmhead_workspace_bytes(int64_t B, int64_t K, int64_t V, int64_t d_target,
+                              int64_t d_draft, int mode, size_t* bytes);
+
+/*
+ * spec_verify from the models' last hidden states instead of their logits.
+ * The pages take each model's logits as given: one vector of V logits per
+ * position ("Как работает speculative decoding на уровне логитов..."
+ * (aivaro.ru) §4 and §5 step 1). A language model makes them with its output
+ * layer, logits = h W^T for a hidden state h and an output matrix W [V, D];
+ * this entry point computes that product on the tensor cores and folds the
+ * row statistics into it, so the [B, 2K+1, V] logits are never written:
+ *   1. one GEMM over every target and draft row yields, per 256-column
+ *      vocabulary tile, the row's partial softmax normaliser at `temperature`
+ *      (greedy: the tile's maximum and its lowest column) and the draft
+ *      token's logit;
+ *   2. the scan merges the partials and takes the acceptance decisions
+ *      exactly as spec_verify does;
+ *   3. (sampling) the hidden states of each sequence's emitted position are
+ *      gathered and a second GEMM writes that position's target and draft
+ *      logits ([B][2][V] float32, in the workspace), from which the sampler
+ *      draws the residual or bonus token as spec_verify does.
+ *   hidden_target  device, [B, K+1, d_target] bfloat16, row-major, 16-byte
+ *                  aligned: the target model's hidden state at every verified
+ *                  position (position i < K scores draft token x_i, position
+ *                  K is the bonus position).
+ *   weight_target  device, [V, d_target] bfloat16, row-major, 16-byte
+ *                  aligned: the target's output matrix.
+ *   hidden_draft   device, [B, K, d_draft] bfloat16 (NULL in greedy mode or
+ *                  when K == 0): the draft model's hidden state at the
+ *                  position that drew x_i.
+ *   weight_draft   device, [V, d_draft] bfloat16 (NULL likewise).
+ *   d_target, d_draft  hidden sizes, multiples of 8 (the rows' 16-byte
+ *                  alignment), >= 8, < 2^31.
+ * Products are exact in float32 and accumulated in float32 over the hidden
+ * dimension, so the logits differ from exact ones by float32 accumulation
+ * rounding; decisions within the near-tie rule's band may differ from
+ * spec_verify run on exactly rounded logits. Other arguments, outputs and
+ * errors as spec_verify; the workspace is sv_lmhead_workspace_bytes. A
+ * bounded wait inside the GEMM that runs out reports every sequence as
+ * SV_SEQ_TIMEOUT. Calls make 3 launches in greedy mode (GEMM, scan, timeout
+ * check) and 7 when sampling (GEMM, scan, gather, pair GEMM, two sampler
+ * launches, timeout check), plus one memset.
+ */
+int spec_verify_lmhead(const void* hidden_target, const void* weight_target,
+                       const void* hidden_draft, const void* weight_draft,
+                       const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                       int64_t d_target, int64_t d_draft, float temperature, uint64_t seed,
+                       int mode, int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
+/*
+ * spec_verify_lmhead plus the per-row diagnostics of spec_verify_debug (each
+ * optional, NULL to skip; sampling mode only, except seq_status).
+ */
+int spec_verify_lmhead_debug(const void* hidden_target, const void* weight_target,
+                             const void* hidden_draft, const void* weight_draft,
+                             const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                             int64_t d_target, int64_t d_draft, float temperature, uint64_t seed,
+                             int mode, int32_t* out_tokens, int32_t* num_accepted,
+                             void* workspace, size_t workspace_bytes, void* stream, double* lse_t,
+                             double* lse_d, double* log_ratio, int32_t* seq_status);
+
+/*
+ * spec_verify_lmhead with n_events >= 5 cudaEvent_t handles recorded on
+ * `stream` before the statistics GEMM, after it, after the scan, after the
+ * emitted pairs' GEMM (greedy: after the scan again) and at the end.
+ */
+int spec_verify_lmhead_timed(const void* hidden_target, const void* weight_target,
+                             const void* hidden_draft, const void* weight_draft,
+                             const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                             int64_t d_target, int64_t d_draft, float temperature, uint64_t seed,
+                             int mode, int32_t* out_tokens, int32_t* num_accepted,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             void* const* events, int n_events);
+
+/*
+ * The LM head alone: out = hidden W^T as float32, the GEMM spec_verify_lmhead
+ * runs, exposed so that it can be checked against a plain matrix product.
+ *   hidden  device, [R, D] bfloat16, row-major, 16-byte aligned.
+ *   weight  device, [V, D] bfloat16, row-major, 16-byte aligned.
+ *   D       a multiple of 8, >= 8.
+ *   out     device, [R, V] float32, written.
+ *   err     device int32, 4-byte aligned: set to 1 (never cleared) when a
+ *           bounded wait inside the kernel runs out; out is then incomplete.
+ * Stream-ordered; allocates nothing. Returns SV_OK, SV_ERR_ARG, SV_ERR_SIZE
+ * (R, V or D >= 2^31), SV_ERR_ALIGN or SV_ERR_CUDA.
+ */
+int sv_lmhead_logits(const void* hidden, const void* weight, int64_t R, int64_t D, int64_t V,
+                     float* out, int32_t* err, void* stream);
+
+/*
  * The Philox4x32-10 generator the verification kernels draw from, evaluated on
  * the device for caller-chosen counters. The pages have no counterpart to this
  * entry point: it exists so that the device generator can be checked word for

@@ -24,12 +24,17 @@ from .api import (  # noqa: F401
     spec_verify_filtered_debug,
     spec_verify_filtered_timed,
     spec_verify_host,
+    spec_verify_lmhead,
+    spec_verify_lmhead_debug,
+    spec_verify_lmhead_timed,
     spec_verify_sharded,
     spec_verify_static,
     spec_verify_timed,
     sv_early_exit_workspace_bytes,
     sv_filtered_workspace_bytes,
     sv_host_staging_bytes,
+    sv_lmhead_logits,
+    sv_lmhead_workspace_bytes,
     sv_sharded_workspace_bytes,
     sv_philox,
     sv_workspace_bytes,

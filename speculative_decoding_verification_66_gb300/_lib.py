@@ -38,6 +38,16 @@ SIGNATURES = {
                                           _vp]),
     "spec_verify_filtered_timed": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _f32, _i64, _f32,
                                           _u64, _i32, _vp, _vp, _vp, _sz, _vp, _vp, _i32]),
+    "sv_lmhead_workspace_bytes": (_i32, [_i64, _i64, _i64, _i64, _i64, _i32,
+                                         ctypes.POINTER(_sz)]),
+    "spec_verify_lmhead": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64, _f32,
+                                  _u64, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_lmhead_debug": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                        _f32, _u64, _i32, _vp, _vp, _vp, _sz, _vp, _vp, _vp, _vp,
+                                        _vp]),
+    "spec_verify_lmhead_timed": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
+                                        _f32, _u64, _i32, _vp, _vp, _vp, _sz, _vp, _vp, _i32]),
+    "sv_lmhead_logits": (_i32, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp]),
     "sv_philox": (_i32, [_u64, _vp, _vp, _i64, _vp]),
     "sv_error_string": (ctypes.c_char_p, [_i32]),
     "sv_version": (_i32, []),

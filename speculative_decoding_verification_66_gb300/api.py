@@ -439,6 +439,138 @@ def spec_verify_static(target_logits, draft_logits, draft_tokens, temperature: f
     return out_tokens, num_accepted
 
 
+def sv_lmhead_workspace_bytes(B: int, K: int, V: int, d_target: int, d_draft: int,
+                              mode) -> int:
+    n = ctypes.c_size_t(0)
+    _check(_lib.load().sv_lmhead_workspace_bytes(B, K, V, d_target, d_draft, mode_code(mode),
+                                                 ctypes.byref(n)), "sv_lmhead_workspace_bytes")
+    return n.value
+
+
+def _lm_shapes(hidden_target, weight_target, hidden_draft, weight_draft, draft_tokens, m):
+    for name, t in (("hidden_target", hidden_target), ("weight_target", weight_target)):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+    if hidden_target.dim() != 3 or weight_target.dim() != 2:
+        raise ValueError("hidden_target must be [B, K+1, D] and weight_target [V, D]")
+    B, K1, Dt = hidden_target.shape
+    K = K1 - 1
+    V = weight_target.shape[0]
+    if weight_target.shape[1] != Dt:
+        raise ValueError("weight_target must be [V, d_target]")
+    Dd = Dt
+    if m == SV_SAMPLE and K > 0:
+        for name, t in (("hidden_draft", hidden_draft), ("weight_draft", weight_draft)):
+            if t is None or t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+        Dd = hidden_draft.shape[-1]
+        if tuple(hidden_draft.shape) != (B, K, Dd) or tuple(weight_draft.shape) != (V, Dd):
+            raise ValueError("hidden_draft must be [B, K, d_draft] and weight_draft [V, d_draft]")
+    if K > 0 and (draft_tokens is None or tuple(draft_tokens.shape) != (B, K)
+                  or draft_tokens.dtype != torch.int32 or not draft_tokens.is_contiguous()):
+        raise ValueError("draft_tokens must be a contiguous [B, K] int32 tensor")
+    return B, K, V, Dt, Dd
+
+
+def spec_verify_lmhead(hidden_target, weight_target, hidden_draft, weight_draft, draft_tokens,
+                       temperature: float = 1.0, seed: int = 0, mode="sample", *,
+                       out_tokens=None, num_accepted=None, workspace=None, stream=None,
+                       events=None, diagnostics=False):
+    """Verification from the models' last hidden states: the LM head (h W^T)
+    runs on the tensor cores with the row statistics folded in, so the logits
+    are never written. ``events``: 5 torch.cuda.Event(enable_timing=True)
+    (before the statistics GEMM, after it, after the scan, after the emitted
+    pairs' GEMM, at the end). ``diagnostics=True`` returns a dict with the
+    per-row normalisers, log-ratios and per-sequence status as well."""
+    m = mode_code(mode)
+    B, K, V, Dt, Dd = _lm_shapes(hidden_target, weight_target, hidden_draft, weight_draft,
+                                 draft_tokens, m)
+    dev = hidden_target.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if out_tokens is None:
+        out_tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    if num_accepted is None:
+        num_accepted = torch.empty((B,), dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_lmhead_workspace_bytes(B, K, V, Dt, Dd, m))
+    with_draft = m == SV_SAMPLE and K > 0
+    args = [_ptr(hidden_target), _ptr(weight_target),
+            _ptr(hidden_draft if with_draft else None), _ptr(weight_draft if with_draft else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, Dt, Dd, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream)]
+    L = _lib.load()
+    with torch.cuda.device(dev):
+        if diagnostics:
+            out = {"out_tokens": out_tokens, "num_accepted": num_accepted,
+                   "lse_t": torch.full((B, K + 1), float("nan"), dtype=torch.float64, device=dev),
+                   "lse_d": torch.full((B, K), float("nan"), dtype=torch.float64, device=dev),
+                   "log_ratio": torch.full((B, K), float("nan"), dtype=torch.float64,
+                                           device=dev),
+                   "seq_status": torch.full((B,), -7, dtype=torch.int32, device=dev)}
+            _check(L.spec_verify_lmhead_debug(*args, _ptr(out["lse_t"]), _ptr(out["lse_d"]),
+                                              _ptr(out["log_ratio"]), _ptr(out["seq_status"])),
+                   "spec_verify_lmhead_debug")
+            return out
+        if events is None:
+            _check(L.spec_verify_lmhead(*args), "spec_verify_lmhead")
+        else:
+            for e in events:
+                if not e.cuda_event:  # created lazily by torch on the first record
+                    e.record(stream)
+            handles = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+            _check(L.spec_verify_lmhead_timed(*args, handles, len(events)),
+                   "spec_verify_lmhead_timed")
+    return out_tokens, num_accepted
+
+
+def spec_verify_lmhead_debug(hidden_target, weight_target, hidden_draft, weight_draft,
+                             draft_tokens, temperature: float = 1.0, seed: int = 0,
+                             mode="sample", **kw) -> dict:
+    """spec_verify_lmhead plus the per-row normalisers, log-ratios and status."""
+    return spec_verify_lmhead(hidden_target, weight_target, hidden_draft, weight_draft,
+                              draft_tokens, temperature, seed, mode, diagnostics=True, **kw)
+
+
+def spec_verify_lmhead_timed(hidden_target, weight_target, hidden_draft, weight_draft,
+                             draft_tokens, events, temperature: float = 1.0, seed: int = 0,
+                             mode="sample", **kw):
+    """spec_verify_lmhead with its 5 timing events (see there)."""
+    return spec_verify_lmhead(hidden_target, weight_target, hidden_draft, weight_draft,
+                              draft_tokens, temperature, seed, mode, events=events, **kw)
+
+
+def sv_lmhead_logits(hidden, weight, out=None, err=None, stream=None) -> torch.Tensor:
+    """The LM head alone: hidden [R, D] x weight [V, D]^T as float32 [R, V]
+    (bfloat16 operands). ``err``: a device int32 tensor of one element that the
+    kernel sets to 1 if a bounded wait runs out; checked here when given None."""
+    if hidden.dtype != torch.bfloat16 or weight.dtype != torch.bfloat16:
+        raise ValueError("hidden and weight must be bfloat16")
+    if hidden.dim() != 2 or weight.dim() != 2 or hidden.shape[1] != weight.shape[1]:
+        raise ValueError("hidden must be [R, D] and weight [V, D]")
+    if not (hidden.is_cuda and weight.is_cuda and hidden.is_contiguous()
+            and weight.is_contiguous()):
+        raise ValueError("hidden and weight must be contiguous CUDA tensors")
+    R, D = hidden.shape
+    V = weight.shape[0]
+    dev = hidden.device
+    if out is None:
+        out = torch.empty((R, V), dtype=torch.float32, device=dev)
+    check = err is None
+    if err is None:
+        err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    with torch.cuda.device(dev):
+        _check(_lib.load().sv_lmhead_logits(_ptr(hidden), _ptr(weight), R, D, V, _ptr(out),
+                                            _ptr(err), ctypes.c_void_p(stream.cuda_stream)),
+               "sv_lmhead_logits")
+    if check and int(err.item()) != 0:
+        raise RuntimeError("sv_lmhead_logits: a bounded wait inside the kernel ran out")
+    return out
+
+
 def sv_philox(seed: int, counters: torch.Tensor, out=None, stream=None) -> torch.Tensor:
     """The device Philox4x32-10 words of each counter: counters is an [n, 4]
     int32 CUDA tensor (the words' bit patterns), the result the same shape."""

@@ -62,9 +62,24 @@ __device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int la
     float M = __uint_as_float(kF32NegInfBits), hi = 0.f, lo = 0.f;
     float best = __uint_as_float(kF32NegInfBits);
     int idx = INT_MAX;
-    // The logical row's shard rows, in shard order (one pass-1 row when not
-    // sharded); each one's partials in CTA, then warp order.
-    for (int64_t row = lrow * g.row_shards; row < (lrow + 1) * g.row_shards; ++row) {
+    auto take = [&](const Partial& p) {
+        fl |= p.flags;
+        if (g.mode == 0) {
+            merge_scaled(M, hi, lo, p.m, p.hi, p.lo);
+        } else {
+            const int pi = __float_as_int(p.hi);
+            if (p.m > best || (p.m == best && pi < idx)) {
+                best = p.m;
+                idx = pi;
+            }
+        }
+    };
+    // LM-head statistics: one partial per vocabulary tile, in tile order.
+    for (int64_t q = lane; q < a.lm_tiles; q += 32) take(a.partials[lrow * a.lm_tiles + q]);
+    // Pass 1: the logical row's shard rows, in shard order (one pass-1 row
+    // when not sharded); each one's partials in CTA, then warp order.
+    for (int64_t row = lrow * g.row_shards; a.lm_tiles == 0 && row < (lrow + 1) * g.row_shards;
+         ++row) {
         const int64_t t0 = row * g.tiles_per_row;
         const int c0 = cta_of_tile(t0, tiles, g);
         const int c1 = cta_of_tile(t0 + g.tiles_per_row - 1, tiles, g);
@@ -74,18 +89,8 @@ __device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int la
             const int w = q % kRowConsumerWarps;
             const int64_t first =
                 (static_cast<int64_t>(c) * tiles / used_grid(tiles, g)) / g.tiles_per_row;
-            const Partial p =
-                a.partials[(static_cast<int64_t>(c) * g.maxseg + (row - first)) * kRowConsumerWarps + w];
-            fl |= p.flags;
-            if (g.mode == 0) {
-                merge_scaled(M, hi, lo, p.m, p.hi, p.lo);
-            } else {
-                const int pi = __float_as_int(p.hi);
-                if (p.m > best || (p.m == best && pi < idx)) {
-                    best = p.m;
-                    idx = pi;
-                }
-            }
+            take(a.partials[(static_cast<int64_t>(c) * g.maxseg + (row - first)) * kRowConsumerWarps +
+                            w]);
         }
     }
 #pragma unroll
@@ -220,7 +225,10 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
         const int64_t i = p0 + q;
         const int32_t x = a.tokens[b * K + i];
         sx[q] = x;
-        if (x >= 0 && static_cast<int64_t>(x) < V && sampling) {
+        if (x >= 0 && static_cast<int64_t>(x) < V && sampling && a.tok != nullptr) {
+            stx[q] = a.tok[b * (K + 1) + i];
+            sdx[q] = a.tok[g.B * (K + 1) + b * K + i];
+        } else if (x >= 0 && static_cast<int64_t>(x) < V && sampling) {
             // Token x lives in shard x / Vs, at column x mod Vs.
             const int64_t Vs = g.shard_len;
             const int gi = static_cast<int>(x / Vs);

@@ -615,6 +615,289 @@ SV_EXPORT int spec_verify_host(const void* h_target_logits, const void* h_draft_
     return SV_OK;
 }
 
+// ---------------------------------------------------------------------------
+// LM head fused with the row statistics.
+// ---------------------------------------------------------------------------
+namespace {
+
+struct LmLayout {
+    size_t part = 0, tok = 0, seqs = 0, block_sums = 0, err = 0, ht = 0, hd = 0, pairs = 0;
+    size_t total = 0;
+    int64_t rows = 0, n_vt = 0;
+};
+
+int lm_check_sizes(int64_t B, int64_t K, int64_t V, int64_t Dt, int64_t Dd, int mode)
+{
+    int rc = check_sizes(B, K, V, SV_F32, mode);
+    if (rc != SV_OK) return rc;
+    const bool draft = mode == SV_SAMPLE && K > 0;
+    if (Dt < 8 || Dt % 8 != 0 || (draft && (Dd < 8 || Dd % 8 != 0))) return SV_ERR_ARG;
+    // Tensor-map limits: extents below 2^32, row strides (2 D bytes) below 2^40.
+    if (Dt >= (int64_t(1) << 31) || Dd >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+    if (B * (K + 1) >= (int64_t(1) << 31)) return SV_ERR_SIZE;
+    return SV_OK;
+}
+
+int lm_plan(int64_t B, int64_t K, int64_t V, int64_t Dt, int64_t Dd, int mode, Geometry* g,
+            LmLayout* L)
+{
+    int rc = lm_check_sizes(B, K, V, Dt, Dd, mode);
+    if (rc != SV_OK) return rc;
+    Layout base;
+    rc = make_plan(B, K, V, SV_F32, mode, g, &base);
+    if (rc != SV_OK) return rc;
+    const bool sampling = mode == SV_SAMPLE;
+    L->n_vt = sv::lmhead_vocab_tiles(V);
+    L->rows = B * (K + 1) + (sampling ? B * K : 0);
+    size_t off = 0;
+    L->part = off;
+    off += round_up(static_cast<size_t>(L->rows) * static_cast<size_t>(L->n_vt) * sizeof(sv::Partial));
+    L->tok = off;
+    off += round_up(static_cast<size_t>(L->rows) * sizeof(float));
+    L->seqs = off;
+    off += round_up(static_cast<size_t>(B) * sizeof(sv::SeqRecord));
+    L->err = off;
+    off += round_up(sizeof(int32_t));
+    if (sampling) {
+        L->block_sums = off;
+        off += round_up(static_cast<size_t>(B * g->nblocks) * sizeof(float));
+        L->ht = off;
+        off += round_up(static_cast<size_t>(B * Dt) * 2);
+        L->hd = off;
+        off += round_up(static_cast<size_t>(B * (K > 0 ? Dd : 8)) * 2);
+        L->pairs = off;
+        off += round_up(static_cast<size_t>(2 * B) * static_cast<size_t>(V) * sizeof(float));
+    }
+    L->total = off;
+    return SV_OK;
+}
+
+// Stats GEMM -> scan -> (sampling) emitted hidden states -> logits of the
+// emitted row pairs -> sampler; the LM head's timeout check last. Events
+// (5): before the stats GEMM, after it, after the scan, after the emitted
+// pairs' GEMM, at the end.
+int run_lmhead(const void* hidden_t, const void* w_t, const void* hidden_d, const void* w_d,
+               const int32_t* tokens, int64_t B, int64_t K, int64_t V, int64_t Dt, int64_t Dd,
+               float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+               int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
+               double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
+               void* const* events, int n_events)
+{
+    int rc = lm_check_sizes(B, K, V, Dt, Dd, mode);
+    if (rc != SV_OK) return rc;
+    const bool sampling = mode == SV_SAMPLE;
+    float c = 0.f;
+    if (sampling) {
+        if (!(temperature > 0.f) || !std::isfinite(temperature)) return SV_ERR_ARG;
+        c = static_cast<float>(1.4426950408889634 / static_cast<double>(temperature));
+        if (!std::isfinite(c) || !(c > 0.f)) return SV_ERR_ARG;
+    }
+    if (events != nullptr && n_events < 5) return SV_ERR_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    auto record = [&](int i) -> bool {
+        return events == nullptr ||
+               cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) == cudaSuccess;
+    };
+    if (B == 0) {
+        for (int i = 0; i < 5; ++i)
+            if (!record(i)) return SV_ERR_CUDA;
+        return SV_OK;
+    }
+    const bool with_draft = sampling && K > 0;
+    if (hidden_t == nullptr || w_t == nullptr || out_tokens == nullptr || num_accepted == nullptr)
+        return SV_ERR_ARG;
+    if (K > 0 && tokens == nullptr) return SV_ERR_ARG;
+    if (with_draft && (hidden_d == nullptr || w_d == nullptr)) return SV_ERR_ARG;
+    if (workspace == nullptr) return SV_ERR_WORKSPACE;
+    if (!aligned_to(hidden_t, 16) || !aligned_to(w_t, 16) ||
+        (with_draft && (!aligned_to(hidden_d, 16) || !aligned_to(w_d, 16))))
+        return SV_ERR_ALIGN;
+    if ((tokens && !aligned_to(tokens, 4)) || !aligned_to(out_tokens, 4) ||
+        !aligned_to(num_accepted, 4) || (seq_status && !aligned_to(seq_status, 4)))
+        return SV_ERR_ALIGN;
+    if ((lse_t && !aligned_to(lse_t, 8)) || (lse_d && !aligned_to(lse_d, 8)) ||
+        (log_ratio && !aligned_to(log_ratio, 8)))
+        return SV_ERR_ALIGN;
+    if (!aligned_to(workspace, kAlign)) return SV_ERR_WORKSPACE;
+    Geometry g;
+    LmLayout L;
+    rc = lm_plan(B, K, V, Dt, Dd, mode, &g, &L);
+    if (rc != SV_OK) return rc;
+    if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
+    g.pdl = 0;  // the scan reads the token logits as soon as it starts
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    auto* part = reinterpret_cast<sv::Partial*>(ws + L.part);
+    auto* tok = reinterpret_cast<float*>(ws + L.tok);
+    auto* seqs = reinterpret_cast<sv::SeqRecord*>(ws + L.seqs);
+    auto* err = reinterpret_cast<int32_t*>(ws + L.err);
+
+    if (cudaMemsetAsync(err, 0, sizeof(int32_t), s) != cudaSuccess) return SV_ERR_CUDA;
+    sv::LmArgs la{};
+    la.p[0] = sv::LmProblem{hidden_t, w_t, B * (K + 1), Dt, 0, static_cast<int32_t>(K + 1),
+                            nullptr, 0, 0, 0, 0};
+    la.nprob = 1;
+    if (with_draft) {
+        la.p[1] = sv::LmProblem{hidden_d, w_d, B * K, Dd, B * (K + 1), static_cast<int32_t>(K),
+                                nullptr, 0, 0, 0, 0};
+        la.nprob = 2;
+    }
+    la.V = V;
+    la.K = static_cast<int32_t>(K);
+    la.tokens = tokens;
+    la.c = c;
+    la.greedy = sampling ? 0 : 1;
+    la.part = part;
+    la.tok = tok;
+    la.err = err;
+    bool mapped = false;
+    if (!record(0)) return SV_ERR_CUDA;
+    if (sv::launch_lmhead(sv::kLmStats, la, s, &mapped) != cudaSuccess || !mapped)
+        return SV_ERR_CUDA;
+    if (!record(1)) return SV_ERR_CUDA;
+
+    const sv::RowMap full{nullptr, nullptr, 0, static_cast<int32_t>(K + 1),
+                          static_cast<int32_t>(sampling ? K : 0)};
+    sv::ScanArgs sa{};
+    sa.tokens = tokens;
+    sa.g = g;
+    sa.c = c;
+    sa.seed = seed;
+    sa.partials = part;
+    sa.out_tokens = out_tokens;
+    sa.num_accepted = num_accepted;
+    sa.seqs = seqs;
+    sa.lse_t = sampling ? lse_t : nullptr;
+    sa.lse_d = sampling ? lse_d : nullptr;
+    sa.log_ratio = sampling ? log_ratio : nullptr;
+    sa.seq_status = seq_status;
+    sa.map = full;
+    sa.lm_tiles = L.n_vt;
+    sa.tok = sampling ? tok : nullptr;
+    if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
+    if (!record(2)) return SV_ERR_CUDA;
+
+    if (sampling) {
+        // The emitted pair of every sequence: hidden states gathered, then
+        // their logits [B][2][V] (target row, draft row) as float32.
+        uint8_t* ht = ws + L.ht;
+        uint8_t* hd = ws + L.hd;
+        float* pairs = reinterpret_cast<float*>(ws + L.pairs);
+        if (sv::launch_gather_hidden(hidden_t, with_draft ? hidden_d : nullptr, seqs, B, K, Dt,
+                                     with_draft ? Dd : 0, ht, hd, s) != cudaSuccess)
+            return SV_ERR_CUDA;
+        sv::LmArgs le{};
+        le.p[0] = sv::LmProblem{ht, w_t, B, Dt, 0, 0, pairs, 2 * V, 0, 0, 0};
+        le.nprob = 1;
+        if (with_draft) {
+            le.p[1] = sv::LmProblem{hd, w_d, B, Dd, 0, 0, pairs + V, 2 * V, 0, 0, 0};
+            le.nprob = 2;
+        }
+        le.V = V;
+        le.err = err;
+        if (sv::launch_lmhead(sv::kLmLogits, le, s, &mapped) != cudaSuccess || !mapped)
+            return SV_ERR_CUDA;
+        if (!record(3)) return SV_ERR_CUDA;
+        const int64_t row_bytes = V * 4;
+        const uint8_t* pb = reinterpret_cast<const uint8_t*>(pairs);
+        sv::RowPairLayout lay{2, 0, 2, 0, pb + 2 * B * row_bytes, pb + 2 * B * row_bytes};
+        sv::SampleArgs pa{pb, pb + row_bytes, g, c, seed, seqs,
+                          reinterpret_cast<float*>(ws + L.block_sums), out_tokens, num_accepted,
+                          seq_status, lay, 0, sv::Shards{}, 0};
+        if (sv::launch_sample(pa, s) != cudaSuccess) return SV_ERR_CUDA;
+    } else if (!record(3)) {
+        return SV_ERR_CUDA;
+    }
+    if (sv::launch_lm_fail(err, B, K, out_tokens, num_accepted, seq_status, s) != cudaSuccess)
+        return SV_ERR_CUDA;
+    if (!record(4)) return SV_ERR_CUDA;
+    return SV_OK;
+}
+
+}  // namespace
+
+SV_EXPORT int sv_lmhead_workspace_bytes(int64_t B, int64_t K, int64_t V, int64_t d_target,
+                                        int64_t d_draft, int mode, size_t* bytes)
+{
+    if (bytes == nullptr) return SV_ERR_ARG;
+    Geometry g;
+    LmLayout L;
+    const int rc = lm_plan(B, K, V, d_target, d_draft, mode, &g, &L);
+    if (rc != SV_OK) return rc;
+    *bytes = L.total;
+    return SV_OK;
+}
+
+SV_EXPORT int spec_verify_lmhead(const void* hidden_target, const void* weight_target,
+                                 const void* hidden_draft, const void* weight_draft,
+                                 const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                                 int64_t d_target, int64_t d_draft, float temperature,
+                                 uint64_t seed, int mode, int32_t* out_tokens,
+                                 int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                                 void* stream)
+{
+    return run_lmhead(hidden_target, weight_target, hidden_draft, weight_draft, draft_tokens, B, K,
+                      V, d_target, d_draft, temperature, seed, mode, out_tokens, num_accepted,
+                      workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, 0);
+}
+
+SV_EXPORT int spec_verify_lmhead_debug(const void* hidden_target, const void* weight_target,
+                                       const void* hidden_draft, const void* weight_draft,
+                                       const int32_t* draft_tokens, int64_t B, int64_t K,
+                                       int64_t V, int64_t d_target, int64_t d_draft,
+                                       float temperature, uint64_t seed, int mode,
+                                       int32_t* out_tokens, int32_t* num_accepted,
+                                       void* workspace, size_t workspace_bytes, void* stream,
+                                       double* lse_t, double* lse_d, double* log_ratio,
+                                       int32_t* seq_status)
+{
+    return run_lmhead(hidden_target, weight_target, hidden_draft, weight_draft, draft_tokens, B, K,
+                      V, d_target, d_draft, temperature, seed, mode, out_tokens, num_accepted,
+                      workspace, workspace_bytes, stream, lse_t, lse_d, log_ratio, seq_status,
+                      nullptr, 0);
+}
+
+SV_EXPORT int spec_verify_lmhead_timed(const void* hidden_target, const void* weight_target,
+                                       const void* hidden_draft, const void* weight_draft,
+                                       const int32_t* draft_tokens, int64_t B, int64_t K,
+                                       int64_t V, int64_t d_target, int64_t d_draft,
+                                       float temperature, uint64_t seed, int mode,
+                                       int32_t* out_tokens, int32_t* num_accepted,
+                                       void* workspace, size_t workspace_bytes, void* stream,
+                                       void* const* events, int n_events)
+{
+    if (events == nullptr) return SV_ERR_ARG;
+    return run_lmhead(hidden_target, weight_target, hidden_draft, weight_draft, draft_tokens, B, K,
+                      V, d_target, d_draft, temperature, seed, mode, out_tokens, num_accepted,
+                      workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr,
+                      events, n_events);
+}
+
+SV_EXPORT int sv_lmhead_logits(const void* hidden, const void* weight, int64_t R, int64_t D,
+                               int64_t V, float* out, int32_t* err, void* stream)
+{
+    if (R < 0 || V < 1 || D < 8 || D % 8 != 0) return SV_ERR_ARG;
+    if (R >= (int64_t(1) << 31) || V >= (int64_t(1) << 31) || D >= (int64_t(1) << 31))
+        return SV_ERR_SIZE;
+    if (R == 0) return SV_OK;
+    if (hidden == nullptr || weight == nullptr || out == nullptr || err == nullptr)
+        return SV_ERR_ARG;
+    if (!aligned_to(hidden, 16) || !aligned_to(weight, 16) || !aligned_to(out, 4) ||
+        !aligned_to(err, 4))
+        return SV_ERR_ALIGN;
+    sv::LmArgs la{};
+    la.p[0] = sv::LmProblem{hidden, weight, R, D, 0, 0, out, V, 0, 0, 0};
+    la.nprob = 1;
+    la.V = V;
+    la.err = err;
+    bool mapped = false;
+    if (sv::launch_lmhead(sv::kLmLogits, la, static_cast<cudaStream_t>(stream), &mapped) !=
+            cudaSuccess ||
+        !mapped)
+        return SV_ERR_CUDA;
+    return SV_OK;
+}
+
 SV_EXPORT const char* sv_error_string(int code)
 {
     switch (code) {
@@ -629,4 +912,4 @@ SV_EXPORT const char* sv_error_string(int code)
     }
 }
 
-SV_EXPORT int sv_version(void) { return 104; }
+SV_EXPORT int sv_version(void) { return 105; }

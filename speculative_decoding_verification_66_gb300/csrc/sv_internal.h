@@ -188,6 +188,11 @@ struct ScanArgs {
     int32_t* next_count;    // [1]
     uint32_t* ticket;       // [1], zero before the launch
     Shards sh;
+    // LM-head statistics only (0 / nullptr otherwise): the partials are
+    // [rows][lm_tiles], one per vocabulary tile, and the draft tokens' raw
+    // logits come from tok (row space order) instead of the logits tensors.
+    int64_t lm_tiles;
+    const float* tok;
 };
 
 // Where the sampler finds the emitted row pair: target row j of sequence b is
@@ -229,6 +234,45 @@ struct GatherArgs {
     uint8_t* pairs;
 };
 
+// LM head on the tensor cores: logits = hidden [R, D] x weights [V, D]^T,
+// bfloat16 operands, float32 accumulation, 128 x 256 output tiles. One launch
+// covers one or two problems (target and draft heads) over one vocabulary.
+//  kLmLogits: float32 logits to out[r * ldo + col].
+//  kLmStats:  no logits leave the chip. Sampling: one Partial per (row,
+//             vocabulary tile) -- m = ceil(max x c), (hi + lo) 2^m = the tile's
+//             sum of 2^(x c) -- and the raw logit of the row's draft token;
+//             greedy: the tile's largest logit and its lowest column.
+// Rows of problem p are rows row0 + r of the partial / token-logit row space,
+// the same space the scan uses: [B (K+1) target rows | B K draft rows].
+constexpr int kLmLogits = 0;
+constexpr int kLmStats = 1;
+struct LmProblem {
+    const void* hidden;   // [R, D] bfloat16, 16-byte aligned, D a multiple of 8
+    const void* weights;  // [V, D] bfloat16, likewise
+    int64_t R;
+    int64_t D;
+    int64_t row0;         // stats: first row in the row space
+    int32_t per;          // stats: rows per sequence (K + 1 target, K draft)
+    float* out;           // logits: [R, ldo] float32
+    int64_t ldo;
+    // Set by launch_lmhead.
+    int32_t n_rb, n_kb;
+    int64_t tiles;
+};
+struct LmArgs {
+    LmProblem p[2];
+    int32_t nprob;
+    int64_t V;
+    int32_t n_vt;            // set by launch_lmhead
+    int32_t K;
+    const int32_t* tokens;   // [B, K] (stats, sampling)
+    float c;                 // log2(e) / T
+    int32_t greedy;
+    Partial* part;           // [rows][n_vt] (stats)
+    float* tok;              // [rows] token logits (stats, sampling)
+    int32_t* err;            // set to 1 when a bounded wait runs out
+};
+
 // Launch with programmatic stream serialization (the kernel must call
 // pdl_wait() before it reads what the previous kernel in the stream wrote).
 // With pdl == false it is an ordinary launch (the wait then returns at once).
@@ -257,6 +301,15 @@ cudaError_t launch_gather_pairs(const GatherArgs& a, cudaStream_t s);
 cudaError_t launch_filter(const FilterArgs& a, int grid, cudaStream_t s);
 // Resident filter CTAs per SM.
 cudaError_t filter_blocks_per_sm(int es, int* blocks);
+// The LM head; *mapped = false when a tensor map could not be made (nothing
+// launched). Vocabulary tiles per row, and the emitted rows' hidden states.
+cudaError_t launch_lmhead(int mode, LmArgs a, cudaStream_t s, bool* mapped);
+int64_t lmhead_vocab_tiles(int64_t V);
+cudaError_t launch_gather_hidden(const void* ht, const void* hd, const SeqRecord* seqs, int64_t B,
+                                 int64_t K, int64_t Dt, int64_t Dd, void* out_t, void* out_d,
+                                 cudaStream_t s);
+cudaError_t launch_lm_fail(const int32_t* err, int64_t B, int64_t K, int32_t* out_tokens,
+                           int32_t* num_accepted, int32_t* seq_status, cudaStream_t s);
 
 // Resident pass-1 CTAs per SM for this dtype / mode (occupancy query).
 cudaError_t row_stats_blocks_per_sm(int es, int mode, int* blocks);

@@ -1,0 +1,148 @@
+"""The LM head on the tensor cores, and verification from hidden states.
+
+Two levels, each against the float64 oracle:
+
+* ``sv_lmhead_logits`` (the GEMM alone) against the exact products h W^T of
+  the same bfloat16 values: every element within the float32 accumulation
+  bound D 2^-21 sum_d |h_d W_vd| (recursive summation in float32 is within
+  (D - 1) 2^-24 of that sum; the factor 8 leaves room for the tensor core's
+  own order of additions). A wrong operand layout, swizzle, descriptor or
+  tile index gives errors of the size of the logits themselves.
+* ``spec_verify_lmhead`` against ``oracle.verify_lmhead`` (the oracle's
+  verification run on the exact float64 logits). The GPU's logits carry
+  float32 accumulation error, about 1e-5 on a logit at D = 4096, which moves
+  an acceptance ratio by a few 1e-5: the near-tie band is therefore 1e-3
+  here (instead of 1e-5) and the normaliser tolerance 1e-4 relative.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import speculative_decoding_verification_66_gb300 as sv
+from speculative_decoding_verification_66_gb300.workloads import (LM_WORKLOADS, lm_host_arrays,
+                                                                   make_lmhead_inputs)
+from parity_util import compare
+
+pytestmark = pytest.mark.gpu
+
+FLAG_LM = 1e-3
+RTOL_LM = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sv.load()
+    torch.cuda.set_device(0)
+
+
+def _bf16(shape, g, scale=1.0):
+    return (torch.randn(shape, generator=g, device="cuda") * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("R,D,V", [(128, 64, 256), (1, 8, 1), (300, 200, 1000), (129, 520, 513),
+                                   (77, 136, 131), (256, 4096, 768), (640, 64, 2000)])
+def test_lmhead_logits_match_exact_products(R, D, V):
+    g = torch.Generator(device="cuda")
+    g.manual_seed(R * 1000003 + D * 1009 + V)
+    h = _bf16((R, D), g)
+    w = _bf16((V, D), g, 1.0 / D ** 0.5)
+    out = sv.sv_lmhead_logits(h, w)
+    torch.cuda.synchronize()
+    hb, wb = oracle.bf16_bits_to_f64(sv.workloads.bf16_bits(h)), \
+        oracle.bf16_bits_to_f64(sv.workloads.bf16_bits(w))
+    exact = oracle.lm_head_logits(sv.workloads.bf16_bits(h), sv.workloads.bf16_bits(w))
+    bound = D * 2.0 ** -21 * (np.abs(hb) @ np.abs(wb).T) + 1e-30
+    err = np.abs(out.cpu().numpy().astype(np.float64) - exact)
+    worst = float((err / bound).max())
+    assert worst <= 1.0, f"R={R} D={D} V={V}: error {err.max():.3g}, {worst:.3g} x the bound"
+
+
+def test_lmhead_logits_one_hot_rows_pick_columns():
+    """h = e_d selects column d of W exactly (no rounding at all)."""
+    R, D, V = 200, 192, 700
+    g = torch.Generator(device="cuda")
+    g.manual_seed(7)
+    w = _bf16((V, D), g)
+    h = torch.zeros((R, D), dtype=torch.bfloat16, device="cuda")
+    cols = torch.arange(R, device="cuda") % D
+    h[torch.arange(R, device="cuda"), cols] = 1.0
+    out = sv.sv_lmhead_logits(h, w)
+    assert torch.equal(out, w.float()[:, cols].T.contiguous())
+
+
+def _lm_call(inp, lw, seed, **kw):
+    return sv.spec_verify_lmhead(inp["hidden_t"], inp["weight_t"], inp["hidden_d"],
+                                 inp["weight_d"], inp["tokens"], lw.temperature, seed, lw.mode,
+                                 **kw)
+
+
+def _check(lw, seed, seq_ranges=None, inp=None):
+    if inp is None:
+        inp = make_lmhead_inputs(lw, seed, "cuda")
+    s = 0x1A4EAD00 + seed
+    greedy = lw.mode == "greedy"
+    gpu = _lm_call(inp, lw, s, diagnostics=True)
+    torch.cuda.synchronize()
+    gpu = {k: v.cpu().numpy() for k, v in gpu.items()}
+    host = lm_host_arrays(inp)
+    st = None
+    for rng in (seq_ranges or [None]):
+        orc = oracle.verify_lmhead(*host[:4], host[4], lw.temperature, s,
+                                   oracle.GREEDY if greedy else oracle.SAMPLE, seq_range=rng,
+                                   threads=8)
+        rows = None if rng is None else range(*rng)
+        st = compare(gpu, orc, host[4], lw.K, lw.V, rows=rows, greedy=greedy, flag=FLAG_LM,
+                     rtol=RTOL_LM)
+    # The plain call gives the same tokens as the diagnostic one.
+    out, nacc = _lm_call(inp, lw, s)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), gpu["out_tokens"])
+    assert np.array_equal(nacc.cpu().numpy(), gpu["num_accepted"])
+    return st
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_lmhead_verify_small(seed):
+    st = _check(LM_WORKLOADS["lm_small"], seed)
+    assert st["flagged_sequences"] <= 3
+
+
+@pytest.mark.parametrize("kw", [dict(K=0), dict(K=1), dict(B=1, K=7), dict(V=7, d_target=8,
+                                                                         d_draft=8),
+                                dict(V=257, d_target=64, d_draft=1024),
+                                dict(mode="greedy"), dict(mode="greedy", K=0),
+                                dict(temperature=0.3), dict(B=130, K=2, V=3000)])
+def test_lmhead_verify_edges(kw):
+    _check(LM_WORKLOADS["lm_small"].resized(**kw), 5)
+
+
+def test_lmhead_verify_empty_batch():
+    lw = LM_WORKLOADS["lm_small"].resized(B=0)
+    inp = make_lmhead_inputs(lw, 0, "cuda")
+    out, nacc = _lm_call(inp, lw, 1)
+    assert out.shape == (0, lw.K + 1) and nacc.shape == (0,)
+
+
+def test_lmhead_nonfinite_hidden_state_flags_sequence():
+    lw = LM_WORKLOADS["lm_small"]
+    inp = make_lmhead_inputs(lw, 3, "cuda")
+    inp["hidden_t"][5, 2, 17] = float("nan")
+    inp["hidden_d"][9, 1, 3] = float("inf")
+    gpu = _lm_call(inp, lw, 9, diagnostics=True)
+    torch.cuda.synchronize()
+    st = gpu["seq_status"].cpu().numpy()
+    assert st[5] == sv.SV_SEQ_NONFINITE and st[9] == sv.SV_SEQ_NONFINITE
+    assert (np.delete(st, [5, 9]) == 0).all()
+    assert (gpu["out_tokens"][5].cpu() == -1).all() and int(gpu["num_accepted"][9]) == -1
+
+
+@pytest.mark.parametrize("name", ["lm_llama3_bf16", "lm_greedy_bf16"])
+def test_lmhead_verify_full_size_sampled(name):
+    """The full-size configuration the benchmark times; the oracle checks
+    every output of 6 sequences spread over the batch (their logits in
+    float64: 17 rows x 128256 x 4096 products each)."""
+    lw = LM_WORKLOADS[name]
+    _check(lw, 11, seq_ranges=[(0, 2), (127, 129), (254, 256)])

@@ -39,6 +39,8 @@ def test_header_declares_the_api():
         "sv_sharded_workspace_bytes", "spec_verify_sharded", "sv_philox",
         "sv_filtered_workspace_bytes", "spec_verify_filtered", "spec_verify_filtered_timed",
         "spec_verify_filtered_debug",
+        "sv_lmhead_workspace_bytes", "spec_verify_lmhead", "spec_verify_lmhead_debug",
+        "spec_verify_lmhead_timed", "sv_lmhead_logits",
         "sv_error_string",
         "sv_version"])
 
@@ -73,7 +75,7 @@ def test_error_strings_and_version(lib):
                  SV_ERR_SIZE, 12345):
         s = lib.sv_error_string(code)
         assert isinstance(s, bytes) and len(s) > 0
-    assert lib.sv_version() == 104
+    assert lib.sv_version() == 105
 
 
 FAKE = 0x10000  # never dereferenced: every case below fails before any device work
@@ -190,6 +192,66 @@ def test_filtered_host_side_validation(lib):
     assert dbg(*args, FAKE, FAKE, FAKE + 2, FAKE, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE, FAKE, FAKE, FAKE + 1, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE + 4, FAKE, FAKE, FAKE, FAKE) == SV_ERR_ALIGN
+
+
+def test_lmhead_host_side_validation(lib):
+    """spec_verify_lmhead and sv_lmhead_logits check sizes, pointers and
+    alignment before any CUDA call."""
+    def f(B=2, K=3, V=64, Dt=64, Dd=32, T=1.0, mode=0, ht=FAKE, wt=FAKE, hd=FAKE, wd=FAKE,
+          tokens=FAKE, out=FAKE, ws=FAKE, events=None, n_events=0):
+        args = (ht, wt, hd, wd, tokens, B, K, V, Dt, Dd, T, 7, mode, out, FAKE, ws, 1 << 20,
+                None)
+        if events is None and n_events == 0:
+            return lib.spec_verify_lmhead(*args)
+        return lib.spec_verify_lmhead_timed(*args, events, n_events)
+    assert f(B=0) == SV_OK
+    assert f(B=0, ht=None, wt=None, hd=None, wd=None, tokens=None, out=None, ws=None) == SV_OK
+    assert f(Dt=12) == SV_ERR_ARG            # rows must be whole 16-byte vectors
+    assert f(Dt=0) == SV_ERR_ARG
+    assert f(Dd=4) == SV_ERR_ARG
+    assert f(mode=1, Dd=4, hd=None, wd=None, ht=FAKE + 2) == SV_ERR_ALIGN  # Dd unused
+    assert f(K=0, Dd=0, hd=None, wd=None, tokens=None, ws=None) == SV_ERR_WORKSPACE
+    assert f(T=0.0) == SV_ERR_ARG
+    assert f(T=float("nan")) == SV_ERR_ARG
+    assert f(mode=3) == SV_ERR_ARG
+    assert f(K=1025) == SV_ERR_SIZE
+    assert f(V=0) == SV_ERR_ARG
+    assert f(Dt=1 << 31) == SV_ERR_SIZE
+    assert f(ht=None) == SV_ERR_ARG
+    assert f(wt=None) == SV_ERR_ARG
+    assert f(hd=None) == SV_ERR_ARG
+    assert f(wd=None) == SV_ERR_ARG
+    assert f(tokens=None) == SV_ERR_ARG
+    assert f(out=None) == SV_ERR_ARG
+    assert f(ws=None) == SV_ERR_WORKSPACE
+    assert f(ws=FAKE + 64) == SV_ERR_WORKSPACE
+    assert f(ht=FAKE + 2) == SV_ERR_ALIGN
+    assert f(wt=FAKE + 8) == SV_ERR_ALIGN
+    assert f(hd=FAKE + 4) == SV_ERR_ALIGN
+    assert f(wd=FAKE + 12) == SV_ERR_ALIGN
+    assert f(tokens=FAKE + 2) == SV_ERR_ALIGN
+    assert f(out=FAKE + 1) == SV_ERR_ALIGN
+    assert f(events=(ctypes.c_void_p * 4)(), n_events=4) == SV_ERR_ARG
+    assert f(events=None, n_events=5) == SV_ERR_ARG
+    # Greedy needs neither the draft head nor a temperature.
+    assert f(mode=1, T=-1.0, hd=None, wd=None, Dd=0, ht=FAKE + 2) == SV_ERR_ALIGN
+    dbg = lib.spec_verify_lmhead_debug
+    args = (FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 64, 64, 32, 1.0, 7, 0, FAKE, FAKE, FAKE, 1 << 20,
+            None)
+    assert dbg(*args, FAKE + 4, FAKE, FAKE, FAKE) == SV_ERR_ALIGN
+    assert dbg(*args, FAKE, FAKE, FAKE + 2, FAKE) == SV_ERR_ALIGN
+    assert dbg(*args, FAKE, FAKE, FAKE, FAKE + 1) == SV_ERR_ALIGN
+    g = lib.sv_lmhead_logits
+    assert g(FAKE, FAKE, 0, 64, 100, FAKE, FAKE, None) == SV_OK
+    assert g(FAKE, FAKE, 4, 60, 100, FAKE, FAKE, None) == SV_ERR_ARG
+    assert g(FAKE, FAKE, 4, 64, 0, FAKE, FAKE, None) == SV_ERR_ARG
+    assert g(FAKE, FAKE, -1, 64, 10, FAKE, FAKE, None) == SV_ERR_ARG
+    assert g(FAKE, FAKE, 1 << 31, 64, 10, FAKE, FAKE, None) == SV_ERR_SIZE
+    assert g(None, FAKE, 4, 64, 10, FAKE, FAKE, None) == SV_ERR_ARG
+    assert g(FAKE, FAKE, 4, 64, 10, FAKE, None, None) == SV_ERR_ARG
+    assert g(FAKE + 2, FAKE, 4, 64, 10, FAKE, FAKE, None) == SV_ERR_ALIGN
+    assert g(FAKE, FAKE + 8, 4, 64, 10, FAKE, FAKE, None) == SV_ERR_ALIGN
+    assert g(FAKE, FAKE, 4, 64, 10, FAKE + 2, FAKE, None) == SV_ERR_ALIGN
 
 
 def test_greedy_ignores_temperature_and_draft(lib):
