@@ -36,6 +36,8 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verified seqs/s and logits HBM GB/s (fraction of GB300 peak) per B×(K+1)×V"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0            # dense bf16, burst (profiling recipe fallback)
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0  # the same, sustained under the power cap
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 KERNEL_SOURCES = ["row_stats.cu", "sv_device.cuh", "sv_internal.h"]
 
@@ -64,9 +66,22 @@ def parse():
                         "(0: skip)")
     p.add_argument("--top-k", type=int, default=50, help="top-k of the filtered variant")
     p.add_argument("--top-p", type=float, default=0.9, help="top-p of the filtered variant")
+    p.add_argument("--lmhead-steps", type=int, default=100,
+                   help="timed calls of spec_verify_lmhead (verification from hidden states, "
+                        "the LM head fused with the row statistics) reported beside the full "
+                        "pass; 0 = skip")
     p.add_argument("--cpu-threads", type=int, default=0,
                    help="threads for the CPU baseline (0: every core this process may use)")
     return p.parse_args()
+
+
+def tensor_peaks():
+    """(burst, sustained) dense bf16 TFLOP/s and their source."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["bf16_tflops"]), float(d["bf16_tflops_sustained"]), "measured"
+    return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
 def peaks():
@@ -496,6 +511,69 @@ def main():
                                           "algorithmic_bytes": pass1_bytes}}
         del ws_f, f_tokens
 
+    # Verification from the models' last hidden states (a variant, reported
+    # beside the full pass): the LM heads run on the tensor cores with the row
+    # statistics fused, so no logits are written; only the emitted pairs'
+    # logits are made, by a second GEMM. Output matrices of 1.05 GB (target)
+    # and 0.5 GB (draft) stream from HBM every step, larger than L2.
+    lmhead = None
+    if args.lmhead_steps > 0:
+        from speculative_decoding_verification_66_gb300.workloads import (LM_WORKLOADS,
+                                                                           make_lmhead_inputs)
+        lw = LM_WORKLOADS["lm_llama3_bf16" if mode == "sample" else "lm_greedy_bf16"].resized(
+            B=B, K=K, V=V, temperature=wl.temperature)
+        lin = make_lmhead_inputs(lw, 77 + rank, dev)
+        ws_l = torch.empty(sv.sv_lmhead_workspace_bytes(B, K, V, lw.d_target, lw.d_draft, mode),
+                           dtype=torch.uint8, device=dev)
+
+        def l_step(i, ev=None):
+            sv.spec_verify_lmhead(lin["hidden_t"], lin["weight_t"], lin["hidden_d"],
+                                  lin["weight_d"], lin["tokens"], lw.temperature, seeds[i & 1],
+                                  mode, out_tokens=out, num_accepted=nacc, workspace=ws_l,
+                                  stream=stream, events=ev)
+
+        l_step(0)
+        l_acc = nacc.float().mean().item()
+        for i in range(3):
+            l_step(i)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.lmhead_steps):
+            l_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        l_ms = max_over_ranks(e0.elapsed_time(e1), dist) / args.lmhead_steps
+        n_l = max(3, min(args.lmhead_steps, 50))
+        lev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(n_l)]
+        for i in range(n_l):
+            l_step(i, lev[i])
+        torch.cuda.synchronize()
+        st = [sum(e[k].elapsed_time(e[k + 1]) for e in lev) / n_l for k in range(4)]
+        Dt, Dd = lw.d_target, lw.d_draft
+        rows_d = B * K if mode == "sample" else 0
+        stats_flops = 2 * V * (B * (K + 1) * Dt + rows_d * Dd)
+        pair_flops = 2 * V * B * (Dt + (Dd if rows_d else 0)) if mode == "sample" else 0
+        tpk, tpk_sus, tsrc = tensor_peaks()
+        stats_tf = stats_flops / (st[0] / 1e3) / 1e12
+        lmhead = {"workload": lw.label, "value": job_throughput(world, B, 1, l_ms / 1e3),
+                  "unit": "seqs/s", "ms_per_step": l_ms, "steps": args.lmhead_steps,
+                  "mean_accepted": l_acc,
+                  "stage_ms": {"stats_gemm": st[0], "scan": st[1], "pair_gemm": st[2],
+                               "sample": st[3], "steps_timed": n_l},
+                  "stats_kernel": {"bound": "tensor", "achieved": stats_tf, "peak": tpk,
+                                   "unit": "TFLOP/s", "frac": stats_tf / tpk,
+                                   "frac_of_sustained": stats_tf / tpk_sus, "flops": stats_flops,
+                                   "peak_source": f"{tsrc} bf16_tflops (burst)"}}
+        if pair_flops:
+            pair_tf = pair_flops / (st[2] / 1e3) / 1e12
+            lmhead["pair_kernel"] = {"bound": "tensor", "achieved": pair_tf, "peak": tpk,
+                                     "unit": "TFLOP/s", "frac": pair_tf / tpk,
+                                     "flops": pair_flops,
+                                     "weight_bytes": V * 2 * (Dt + Dd),
+                                     "weight_gbs": V * 2 * (Dt + Dd) / (st[2] / 1e3) / 1e9}
+        del lin, ws_l
+
     # End to end through the host entry point: pinned host inputs, copies inside.
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))
     h = [{k: (v.cpu().pin_memory() if v is not None else None) for k, v in c.items()}
@@ -561,6 +639,8 @@ def main():
         line["sharded"] = sharded
     if filtered is not None:
         line["filtered"] = filtered
+    if lmhead is not None:
+        line["lmhead"] = lmhead
     if world == 1 and not args.no_cpu_baseline:
         def host_fn(n):
             sub = {k: (v[:n] if v is not None else None) for k, v in copies[0].items()}
