@@ -116,6 +116,33 @@ def profiled_traffic(wl):
     return None
 
 
+LM_SOURCES = ["lmhead.cu", "sv_device.cuh", "sv_internal.h"]
+
+
+def lm_kernel_sha():
+    h = hashlib.sha256()
+    for f in LM_SOURCES:
+        h.update(open(os.path.join(ROOT, "speculative_decoding_verification_66_gb300", "csrc", f),
+                      "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_lm_traffic(lw):
+    """DRAM bytes per statistics-GEMM launch for this LM-head workload, from a
+    committed ncu summary (profiles/lmhead_*.md) taken at this batch on the
+    current kernel source; None otherwise."""
+    want = f"{lw.name} B={lw.B}"
+    sha = lm_kernel_sha()
+    for path in sorted(glob.glob(os.path.join(PROFILE_DIR, "lmhead_*.md"))):
+        text = open(path).read()
+        m_wl = re.search(r"traffic_workload:\s*(.+)", text)
+        m_sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", text)
+        m_tr = re.search(r"traffic_bytes_per_launch:\s*([0-9.e+]+)", text)
+        if m_wl and m_sha and m_tr and m_wl.group(1).strip() == want and m_sha.group(1) == sha:
+            return float(m_tr.group(1))
+    return None
+
+
 class ClockSampler:
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -564,6 +591,9 @@ def main():
                   "stats_kernel": {"bound": "tensor", "achieved": stats_tf, "peak": tpk,
                                    "unit": "TFLOP/s", "frac": stats_tf / tpk,
                                    "frac_of_sustained": stats_tf / tpk_sus, "flops": stats_flops,
+                                   "algorithmic_bytes": V * 2 * (Dt + (Dd if rows_d else 0)) +
+                                   2 * (B * (K + 1) * Dt + rows_d * Dd),
+                                   "traffic": profiled_lm_traffic(lw),
                                    "peak_source": f"{tsrc} bf16_tflops (burst)"}}
         if pair_flops:
             pair_tf = pair_flops / (st[2] / 1e3) / 1e12

@@ -34,6 +34,45 @@ def _call(entry, inp, wl, seed, **kw):
                                    40, 0.9, seed, wl.mode, **kw)
 
 
+def test_lmhead_capture_and_replay():
+    """spec_verify_lmhead in a graph: tensor maps are kernel parameters, so the
+    captured launches replay on whatever the captured buffers hold."""
+    from speculative_decoding_verification_66_gb300.workloads import (LM_WORKLOADS,
+                                                                       make_lmhead_inputs)
+    lw = LM_WORKLOADS["lm_small"]
+    static = make_lmhead_inputs(lw, 0, "cuda")
+    out = torch.empty((lw.B, lw.K + 1), dtype=torch.int32, device="cuda")
+    nacc = torch.empty((lw.B,), dtype=torch.int32, device="cuda")
+    ws = torch.empty(sv.sv_lmhead_workspace_bytes(lw.B, lw.K, lw.V, lw.d_target, lw.d_draft,
+                                                  lw.mode), dtype=torch.uint8, device="cuda")
+
+    def call(inp, **kw):
+        return sv.spec_verify_lmhead(inp["hidden_t"], inp["weight_t"], inp["hidden_d"],
+                                     inp["weight_d"], inp["tokens"], lw.temperature, 21, lw.mode,
+                                     **kw)
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            call(static, out_tokens=out, num_accepted=nacc, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call(static, out_tokens=out, num_accepted=nacc, workspace=ws)
+    for seed in (1, 2):
+        fresh = make_lmhead_inputs(lw, seed, "cuda")
+        for k in static:
+            static[k].copy_(fresh[k])
+        g.replay()
+        torch.cuda.synchronize()
+        ref_out, ref_n = call(fresh)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out), seed
+        assert torch.equal(nacc, ref_n), seed
+
+
 @pytest.mark.parametrize("entry", ["full", "early_exit", "filtered"])
 @pytest.mark.parametrize("name", ["small_f32", "spiky_bf16", "greedy_bf16"])
 def test_capture_and_replay(entry, name):
