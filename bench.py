@@ -116,7 +116,7 @@ def profiled_traffic(wl):
     return None
 
 
-LM_SOURCES = ["lmhead.cu", "sv_device.cuh", "sv_internal.h"]
+LM_SOURCES = ["lmhead.cu", "sv_device.cuh", "sv_internal.h", "sv_stages.h"]
 
 
 def lm_kernel_sha():

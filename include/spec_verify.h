@@ -438,6 +438,26 @@ int spec_verify_lmhead_timed(const void* hidden_target, const void* weight_targe
                              void* const* events, int n_events);
 
 /*
+ * Test hook for the timeout path (no counterpart on the pages): spec_verify_lmhead
+ * with the statistics GEMM's producer holding every load until the device
+ * int32 *gate becomes nonzero. That wait is bounded like every other wait in
+ * the kernels (about 2 s); when it runs out the kernel drains, releases its
+ * tensor memory and returns, and every sequence is reported as
+ * SV_SEQ_TIMEOUT (num_accepted -1, tokens -1, seq_status if given), with the
+ * context still usable. A caller that sets *gate before the wait runs out
+ * gets spec_verify_lmhead's results.
+ *   gate  device int32, 4-byte aligned (SV_ERR_ARG if NULL, SV_ERR_ALIGN).
+ * Other arguments as spec_verify_lmhead_debug (seq_status optional).
+ */
+int spec_verify_lmhead_gated(const void* hidden_target, const void* weight_target,
+                             const void* hidden_draft, const void* weight_draft,
+                             const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                             int64_t d_target, int64_t d_draft, float temperature, uint64_t seed,
+                             int mode, int32_t* out_tokens, int32_t* num_accepted,
+                             void* workspace, size_t workspace_bytes, void* stream,
+                             int32_t* seq_status, const int32_t* gate);
+
+/*
  * The LM head alone: out = hidden W^T as float32, the GEMM spec_verify_lmhead
  * runs, exposed so that it can be checked against a plain matrix product.
  *   hidden  device, [R, D] bfloat16, row-major, 16-byte aligned.

@@ -26,6 +26,7 @@ from .api import (  # noqa: F401
     spec_verify_host,
     spec_verify_lmhead,
     spec_verify_lmhead_debug,
+    spec_verify_lmhead_gated,
     spec_verify_lmhead_timed,
     spec_verify_sharded,
     spec_verify_static,

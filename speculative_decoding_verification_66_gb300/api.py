@@ -541,6 +541,37 @@ def spec_verify_lmhead_timed(hidden_target, weight_target, hidden_draft, weight_
                               draft_tokens, temperature, seed, mode, events=events, **kw)
 
 
+def spec_verify_lmhead_gated(hidden_target, weight_target, hidden_draft, weight_draft,
+                             draft_tokens, gate, temperature: float = 1.0, seed: int = 0,
+                             mode="sample", *, workspace=None, stream=None) -> dict:
+    """Test hook for the timeout path: spec_verify_lmhead with the statistics
+    GEMM's loads held until the device int32 ``gate`` (one element) is nonzero.
+    Returns out_tokens, num_accepted and seq_status."""
+    m = mode_code(mode)
+    B, K, V, Dt, Dd = _lm_shapes(hidden_target, weight_target, hidden_draft, weight_draft,
+                                 draft_tokens, m)
+    if gate.dtype != torch.int32 or not gate.is_cuda or gate.numel() < 1:
+        raise ValueError("gate must be an int32 CUDA tensor")
+    dev = hidden_target.device
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_lmhead_workspace_bytes(B, K, V, Dt, Dd, m))
+    out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+           "num_accepted": torch.empty((B,), dtype=torch.int32, device=dev),
+           "seq_status": torch.full((B,), -7, dtype=torch.int32, device=dev)}
+    with_draft = m == SV_SAMPLE and K > 0
+    with torch.cuda.device(dev):
+        _check(_lib.load().spec_verify_lmhead_gated(
+            _ptr(hidden_target), _ptr(weight_target),
+            _ptr(hidden_draft if with_draft else None), _ptr(weight_draft if with_draft else None),
+            _ptr(draft_tokens if K > 0 else None), B, K, V, Dt, Dd, float(temperature),
+            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out["out_tokens"]), _ptr(out["num_accepted"]),
+            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream),
+            _ptr(out["seq_status"]), _ptr(gate)), "spec_verify_lmhead_gated")
+    return out
+
+
 def sv_lmhead_logits(hidden, weight, out=None, err=None, stream=None) -> torch.Tensor:
     """The LM head alone: hidden [R, D] x weight [V, D]^T as float32 [R, V]
     (bfloat16 operands). ``err``: a device int32 tensor of one element that the

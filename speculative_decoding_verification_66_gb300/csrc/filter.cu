@@ -48,7 +48,7 @@
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
-#include "sv_internal.h"
+#include "sv_stages.h"
 
 namespace sv {
 namespace {

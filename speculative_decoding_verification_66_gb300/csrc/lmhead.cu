@@ -19,7 +19,7 @@
 #include <cuda.h>
 
 #include "sv_device.cuh"
-#include "sv_internal.h"
+#include "sv_stages.h"
 
 namespace sv {
 namespace {
@@ -294,6 +294,20 @@ __global__ void __launch_bounds__(kLmThreads, 1)
         // Producer: one k-block of both operands per ring stage.
         int64_t it = 0;
         bool ok = true;
+        if (a.gate != nullptr) {
+            // Test hook: hold every load until *gate != 0, with the same bound
+            // as every other wait. Nothing sets it in the tests that use it, so
+            // the wait runs out and the kernel takes its timeout path.
+            const volatile int32_t* gate = a.gate;
+            const long long t0 = clock64();
+            while (*gate == 0) {
+                if (clock64() - t0 > kWaitLimitCycles) {
+                    ok = false;
+                    break;
+                }
+                __nanosleep(1000);
+            }
+        }
         for (int64_t t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
             const TileAt ti = tile_at(a, t);
             const CUtensorMap* ma = ti.p ? &ta1 : &ta0;

@@ -23,7 +23,7 @@
 #include <climits>
 
 #include "sv_device.cuh"
-#include "sv_internal.h"
+#include "sv_stages.h"
 
 namespace sv {
 namespace {

@@ -5,7 +5,7 @@
 #include <mutex>
 
 #include "spec_verify.h"
-#include "sv_internal.h"
+#include "sv_stages.h"
 
 #define SV_EXPORT extern "C" __attribute__((visibility("default")))
 
@@ -681,7 +681,7 @@ int run_lmhead(const void* hidden_t, const void* w_t, const void* hidden_d, cons
                float temperature, uint64_t seed, int mode, int32_t* out_tokens,
                int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
                double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
-               void* const* events, int n_events)
+               void* const* events, int n_events, const int32_t* gate = nullptr)
 {
     int rc = lm_check_sizes(B, K, V, Dt, Dd, mode);
     if (rc != SV_OK) return rc;
@@ -749,6 +749,7 @@ int run_lmhead(const void* hidden_t, const void* w_t, const void* hidden_d, cons
     la.part = part;
     la.tok = tok;
     la.err = err;
+    la.gate = gate;
     bool mapped = false;
     if (!record(0)) return SV_ERR_CUDA;
     if (sv::launch_lmhead(sv::kLmStats, la, s, &mapped) != cudaSuccess || !mapped)
@@ -871,6 +872,23 @@ SV_EXPORT int spec_verify_lmhead_timed(const void* hidden_target, const void* we
                       V, d_target, d_draft, temperature, seed, mode, out_tokens, num_accepted,
                       workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, nullptr,
                       events, n_events);
+}
+
+SV_EXPORT int spec_verify_lmhead_gated(const void* hidden_target, const void* weight_target,
+                                       const void* hidden_draft, const void* weight_draft,
+                                       const int32_t* draft_tokens, int64_t B, int64_t K,
+                                       int64_t V, int64_t d_target, int64_t d_draft,
+                                       float temperature, uint64_t seed, int mode,
+                                       int32_t* out_tokens, int32_t* num_accepted,
+                                       void* workspace, size_t workspace_bytes, void* stream,
+                                       int32_t* seq_status, const int32_t* gate)
+{
+    if (gate == nullptr) return SV_ERR_ARG;
+    if (!aligned_to(gate, 4)) return SV_ERR_ALIGN;
+    return run_lmhead(hidden_target, weight_target, hidden_draft, weight_draft, draft_tokens, B, K,
+                      V, d_target, d_draft, temperature, seed, mode, out_tokens, num_accepted,
+                      workspace, workspace_bytes, stream, nullptr, nullptr, nullptr, seq_status,
+                      nullptr, 0, gate);
 }
 
 SV_EXPORT int sv_lmhead_logits(const void* hidden, const void* weight, int64_t R, int64_t D,

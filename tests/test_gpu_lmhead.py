@@ -146,3 +146,29 @@ def test_lmhead_verify_full_size_sampled(name):
     float64: 17 rows x 128256 x 4096 products each)."""
     lw = LM_WORKLOADS[name]
     _check(lw, 11, seq_ranges=[(0, 2), (127, 129), (254, 256)])
+
+
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_lmhead_timeout_path(mode):
+    """The bounded waits' timeout path, without a fault: the statistics GEMM's
+    producer waits on a device flag that nothing sets. The wait runs out
+    (about 2 s), the kernel drains and releases its tensor memory, and every
+    sequence comes back as SV_SEQ_TIMEOUT. The context stays usable: an
+    ordinary call afterwards still matches the oracle, and a gated call whose
+    flag is already set matches the ordinary call."""
+    lw = LM_WORKLOADS["lm_small"].resized(B=8, mode=mode)
+    inp = make_lmhead_inputs(lw, 2, "cuda")
+    gate = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = sv.spec_verify_lmhead_gated(inp["hidden_t"], inp["weight_t"], inp["hidden_d"],
+                                    inp["weight_d"], inp["tokens"], gate, lw.temperature, 3, mode)
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == sv.SV_SEQ_TIMEOUT).all()
+    assert (r["num_accepted"].cpu() == -1).all() and (r["out_tokens"].cpu() == -1).all()
+    _check(lw, 2, inp=inp)
+    gate.fill_(1)
+    r = sv.spec_verify_lmhead_gated(inp["hidden_t"], inp["weight_t"], inp["hidden_d"],
+                                    inp["weight_d"], inp["tokens"], gate, lw.temperature, 3, mode)
+    out, nacc = _lm_call(inp, lw, 3)
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == 0).all()
+    assert torch.equal(r["out_tokens"], out) and torch.equal(r["num_accepted"], nacc)

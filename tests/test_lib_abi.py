@@ -40,7 +40,7 @@ def test_header_declares_the_api():
         "sv_filtered_workspace_bytes", "spec_verify_filtered", "spec_verify_filtered_timed",
         "spec_verify_filtered_debug",
         "sv_lmhead_workspace_bytes", "spec_verify_lmhead", "spec_verify_lmhead_debug",
-        "spec_verify_lmhead_timed", "sv_lmhead_logits",
+        "spec_verify_lmhead_timed", "spec_verify_lmhead_gated", "sv_lmhead_logits",
         "sv_error_string",
         "sv_version"])
 
@@ -241,6 +241,11 @@ def test_lmhead_host_side_validation(lib):
     assert dbg(*args, FAKE + 4, FAKE, FAKE, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE, FAKE, FAKE + 2, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE, FAKE, FAKE, FAKE + 1) == SV_ERR_ALIGN
+    gated = lib.spec_verify_lmhead_gated
+    gargs = (FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 64, 64, 32, 1.0, 7, 0, FAKE, FAKE, FAKE, 1 << 20,
+             None, FAKE)
+    assert gated(*gargs, None) == SV_ERR_ARG
+    assert gated(*gargs, FAKE + 2) == SV_ERR_ALIGN
     g = lib.sv_lmhead_logits
     assert g(FAKE, FAKE, 0, 64, 100, FAKE, FAKE, None) == SV_OK
     assert g(FAKE, FAKE, 4, 60, 100, FAKE, FAKE, None) == SV_ERR_ARG
