@@ -92,11 +92,19 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_of(name: str) -> bytes:
+    """A source file without its comments and blank space, so that the sha
+    below changes with the code a capture measured, not with its comments."""
+    text = open(os.path.join(ROOT, "speculative_decoding_verification_66_gb300", "csrc", name)).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split()).encode()
+
+
 def kernel_sha():
     h = hashlib.sha256()
     for f in KERNEL_SOURCES:
-        h.update(open(os.path.join(ROOT, "speculative_decoding_verification_66_gb300", "csrc", f),
-                      "rb").read())
+        h.update(_code_of(f))
     return h.hexdigest()[:16]
 
 
@@ -122,8 +130,7 @@ LM_SOURCES = ["lmhead.cu", "sv_device.cuh", "sv_internal.h", "sv_stages.h"]
 def lm_kernel_sha():
     h = hashlib.sha256()
     for f in LM_SOURCES:
-        h.update(open(os.path.join(ROOT, "speculative_decoding_verification_66_gb300", "csrc", f),
-                      "rb").read())
+        h.update(_code_of(f))
     return h.hexdigest()[:16]
 
 

@@ -1,6 +1,15 @@
 // lmhead.cu -- the LM head on the 5th-generation tensor cores: logits =
 // hidden [R, D] x W[V, D]^T in bfloat16 with float32 accumulation.
 //
+// What it computes: the per-position logit vectors that "Как работает
+// speculative decoding на уровне логитов..." (aivaro.ru) §4 and §5 step 1 take
+// as given, made the way a language model's output layer makes them (h W^T).
+// In the statistics mode the epilogue reduces each 256-column tile of a row
+// to its part of the row's softmax normaliser at temperature T (§9 of the same
+// page, "Speculative decoding" (aihero.vn) temperature paragraph), or, greedy,
+// to the tile's maximum and lowest arg-max column, and keeps the draft token's
+// logit; the logits themselves never reach HBM.
+//
 // Design (one CTA per SM, persistent over 128 x 256 output tiles):
 //  * warp 0 (one lane): TMA producer. Each k-block is a 128 x 64 tile of the
 //    hidden states and a 256 x 64 tile of the weights (64 bf16 = 128 bytes of
