@@ -609,7 +609,40 @@ def main():
                                      "flops": pair_flops,
                                      "weight_bytes": V * 2 * (Dt + Dd),
                                      "weight_gbs": V * 2 * (Dt + Dd) / (st[2] / 1e3) / 1e9}
-        del lin, ws_l
+        # End to end from host memory: the output matrices stay resident on the
+        # device (model parameters); every step copies its hidden states and
+        # draft tokens in from pinned host buffers and its results back out.
+        hin = {k: lin[k].cpu().pin_memory() for k in ("hidden_t", "hidden_d", "tokens")
+               if lin[k] is not None}
+        din = {k: torch.empty_like(lin[k]) for k in hin}
+        h_lo = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        h_ln = torch.empty((B,), dtype=torch.int32).pin_memory()
+
+        def l_e2e(i):
+            for k in hin:
+                din[k].copy_(hin[k], non_blocking=True)
+            sv.spec_verify_lmhead(din["hidden_t"], lin["weight_t"], din.get("hidden_d"),
+                                  lin["weight_d"], din["tokens"], lw.temperature, seeds[i & 1],
+                                  mode, out_tokens=out, num_accepted=nacc, workspace=ws_l,
+                                  stream=stream)
+            h_lo.copy_(out, non_blocking=True)
+            h_ln.copy_(nacc, non_blocking=True)
+
+        n_le = max(3, min(args.lmhead_steps, 20))
+        for i in range(2):
+            l_e2e(i)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(n_le):
+            l_e2e(i)
+        torch.cuda.synchronize()
+        le_s = max_over_ranks(time.perf_counter() - t0, dist)
+        lmhead["e2e"] = {"value": job_throughput(world, B, n_le, le_s), "unit": "seqs/s",
+                         "h2d_bytes_per_step": sum(t.numel() * t.element_size()
+                                                   for t in hin.values()),
+                         "d2h_bytes_per_step": h_lo.numel() * 4 + h_ln.numel() * 4,
+                         "steps": n_le, "resident": "output matrices (model parameters)"}
+        del lin, ws_l, din, hin
 
     # End to end through the host entry point: pinned host inputs, copies inside.
     e2e_steps = args.e2e_steps if args.e2e_steps is not None else max(3, min(args.steps, 20))

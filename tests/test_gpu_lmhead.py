@@ -172,3 +172,33 @@ def test_lmhead_timeout_path(mode):
     torch.cuda.synchronize()
     assert (r["seq_status"].cpu() == 0).all()
     assert torch.equal(r["out_tokens"], out) and torch.equal(r["num_accepted"], nacc)
+
+
+@pytest.mark.parametrize("v1,v2", [(100, 300), (10, 20), (255, 256), (0, 999)])
+def test_lmhead_greedy_ties_take_the_lowest_index(v1, v2):
+    """Greedy ties across and within 256-column tiles: one-hot hidden states
+    make every logit an exact copy of one weight, and two vocabulary entries
+    share the largest weight of every column, so each row's maximum is tied
+    between v1 and v2 exactly. The lowest index must win, as the oracle's."""
+    B, K, V, D = 6, 3, 1000, 64
+    g = torch.Generator(device="cuda")
+    g.manual_seed(v1 * 7 + v2)
+    w = (torch.rand((V, D), generator=g, device="cuda") * 2 - 1).to(torch.bfloat16)
+    w[v1] = 4.0
+    w[v2] = 4.0
+    cols = torch.randint(0, D, (B, K + 1), generator=g, device="cuda")
+    h = torch.zeros((B, K + 1, D), dtype=torch.bfloat16, device="cuda")
+    h.scatter_(2, cols.unsqueeze(-1), 1.0)
+    # Drafts: the tie winner for the first b mod K positions of sequence b,
+    # then the loser, so sequences stop at different positions (b mod K).
+    tok = torch.full((B, K), v1, dtype=torch.int32, device="cuda")
+    for b in range(B):
+        tok[b, b % K:] = v2
+    r = sv.spec_verify_lmhead(h, w, None, None, tok, 1.0, 5, "greedy", diagnostics=True)
+    torch.cuda.synchronize()
+    host = (sv.workloads.bf16_bits(h), sv.workloads.bf16_bits(w), None, None,
+            tok.cpu().numpy())
+    orc = oracle.verify_lmhead(*host[:4], host[4], 1.0, 5, oracle.GREEDY)
+    assert np.array_equal(r["num_accepted"].cpu().numpy(), orc["num_accepted"])
+    assert np.array_equal(r["out_tokens"].cpu().numpy(), orc["out_tokens"])
+    assert (r["out_tokens"].cpu().numpy() != v2).all()
