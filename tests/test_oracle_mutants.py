@@ -55,6 +55,10 @@ MUTANTS = {
     "zero_target_mass_accepted": ("double r = lp == -INFINITY ? 0.0 : svo_accept_prob(lp, lq);",
                                   "double r = svo_accept_prob(lp, lq);"),
     "bonus_row_unfiltered": ("lse_t[K], thr[K], lm[K],", "lse_t[K], -INFINITY, 0.0,"),
+    "f64_reader_stride": ("memcpy(&d, (const unsigned char*)row + 8 * k, 8);",
+                          "memcpy(&d, (const unsigned char*)row + 4 * k, 8);"),
+    "f64_read_as_f32": ("    if (dtype == SVO_F64) {\n        double d;",
+                        "    if (dtype == -1) {\n        double d;"),
 }
 
 
@@ -72,7 +76,8 @@ def test_pins_catch_planted_mistake(tmp_path, name):
                     "-lm"], check=True)
     env = dict(os.environ, SVO_LIB_PATH=str(so))
     p = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py"),
+                        os.path.join(ROOT, "tests", "test_oracle_lmhead.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert p.returncode != 0, f"mutant {name} passed every pin:\n{p.stdout[-2000:]}"
     assert "failed" in p.stdout, p.stdout[-2000:]
