@@ -603,12 +603,16 @@ def main():
                                    "traffic": profiled_lm_traffic(lw),
                                    "peak_source": f"{tsrc} bf16_tflops (burst)"}}
         if pair_flops:
+            # Near the ridge: its floor is the larger of the tensor time and the
+            # time to stream both output matrices once more.
             pair_tf = pair_flops / (st[2] / 1e3) / 1e12
-            lmhead["pair_kernel"] = {"bound": "tensor", "achieved": pair_tf, "peak": tpk,
-                                     "unit": "TFLOP/s", "frac": pair_tf / tpk,
-                                     "flops": pair_flops,
-                                     "weight_bytes": V * 2 * (Dt + Dd),
-                                     "weight_gbs": V * 2 * (Dt + Dd) / (st[2] / 1e3) / 1e9}
+            wbytes = V * 2 * (Dt + Dd)
+            floor_ms = max(pair_flops / (tpk * 1e12), wbytes / (peak * 1e9)) * 1e3
+            lmhead["pair_kernel"] = {"bound": "tensor+hbm (ridge)", "achieved": pair_tf,
+                                     "peak": tpk, "unit": "TFLOP/s", "frac": pair_tf / tpk,
+                                     "flops": pair_flops, "weight_bytes": wbytes,
+                                     "weight_gbs": wbytes / (st[2] / 1e3) / 1e9,
+                                     "floor_ms": floor_ms, "frac_of_floor": floor_ms / st[2]}
         # End to end from host memory: the output matrices stay resident on the
         # device (model parameters); every step copies its hidden states and
         # draft tokens in from pinned host buffers and its results back out.
