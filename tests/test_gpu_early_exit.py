@@ -99,7 +99,7 @@ def test_early_exit_ragged_vocab(V, dtype, mode):
     check(base.resized(B=5, K=3, V=V, dtype=dtype, mode=mode, temperature=0.9), 3)
 
 
-@pytest.mark.parametrize("K", [0, 1, 2, 3, 7, 16, 40])
+@pytest.mark.parametrize("K", [0, 1, 2, 3, 7, 16, 40, 1024])
 @pytest.mark.parametrize("mode", ["sample", "greedy"])
 def test_early_exit_draft_counts(K, mode):
     """Phases of 1, 2, 4, ... positions: K = 0 (bonus only), phase ends that

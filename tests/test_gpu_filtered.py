@@ -276,7 +276,7 @@ def test_filtered_timed_events():
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
-@pytest.mark.parametrize("K", [0, 1, 16])
+@pytest.mark.parametrize("K", [0, 1, 16, 1024])
 @pytest.mark.parametrize("top_k,top_p", [(20, 1.0), (0, 0.8), (50, 0.9)])
 def test_filtered_draft_counts(K, top_k, top_p):
     """K = 0 (only the bonus row, drawn from the filtered p'_0), one draft, and

@@ -114,7 +114,8 @@ def test_lmhead_verify_small(seed):
                                                                          d_draft=8),
                                 dict(V=257, d_target=64, d_draft=1024),
                                 dict(mode="greedy"), dict(mode="greedy", K=0),
-                                dict(temperature=0.3), dict(B=130, K=2, V=3000)])
+                                dict(temperature=0.3), dict(B=130, K=2, V=3000),
+                                dict(B=2, K=1024, V=1000)])
 def test_lmhead_verify_edges(kw):
     _check(LM_WORKLOADS["lm_small"].resized(**kw), 5)
 

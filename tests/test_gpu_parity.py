@@ -106,7 +106,7 @@ def test_ragged_vocab(V, dtype, mode):
     check(wl, 3)
 
 
-@pytest.mark.parametrize("K", [0, 1, 2, 16, 40])
+@pytest.mark.parametrize("K", [0, 1, 2, 16, 40, 1024])
 @pytest.mark.parametrize("mode", ["sample", "greedy"])
 def test_draft_counts(K, mode):
     base = WORKLOADS["small_f32"] if mode == "sample" else WORKLOADS["greedy_bf16"]

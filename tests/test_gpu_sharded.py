@@ -77,6 +77,13 @@ def test_sharded_ragged(V, G, dtype, mode):
     check(base.resized(B=5, K=3, V=V, dtype=dtype, mode=mode, temperature=0.8), G, 9)
 
 
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_sharded_maximum_draft_count(mode):
+    """K = 1024, the largest supported, over 4 shards."""
+    base = WORKLOADS["small_f32"] if mode == "sample" else WORKLOADS["greedy_bf16"]
+    check(base.resized(B=3, K=1024, V=3000, dtype="bf16", mode=mode), 4, 13)
+
+
 def test_sharded_matches_unsharded_entry():
     wl = WORKLOADS["spiky_bf16"]
     inputs = make_inputs(wl, 12, "cuda")
