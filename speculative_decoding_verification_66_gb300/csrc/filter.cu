@@ -205,19 +205,24 @@ __device__ __forceinline__ void append(uint32_t key, uint32_t* list, int* count)
 }
 
 // Rows whose length is a whole number of 16-byte vectors stream through a
-// two-stage ring of bulk copies (the 64 KB of the bins region, free during
-// the reads that use it): thread 0 issues the copies, every thread waits on
-// the stage's mbarrier, reads its vectors from shared memory, and the CTA
-// barrier after each tile frees the stage for the copy two tiles ahead.
+// ring of bulk copies: thread 0 issues the copies, every thread waits on the
+// stage's mbarrier, reads its vectors from shared memory, and the CTA barrier
+// after each tile frees the stage for the copy nst tiles ahead. The first read
+// of a row has all 48 KB of shared memory free and runs three stages; later
+// reads run two, in whichever region they leave free.
 constexpr int kTileBytes = 16384;
 constexpr int kStages = 2;
+constexpr int kFirstStages = 3;
 static_assert(kStages * kTileBytes <= static_cast<int>(kBinsBytes), "ring fits the bins");
+static_assert(kFirstStages * kTileBytes <= static_cast<int>(kBinsBytes + kListBytes),
+              "first-read ring fits shared memory");
 
 struct Ring {
-    uint64_t* bar;   // [kStages] mbarriers
-    uint8_t* buf;    // kStages tiles
+    uint64_t* bar;   // [kFirstStages] mbarriers
+    uint8_t* buf;    // nst tiles
     uint32_t phase;  // bit s: parity of the next wait on stage s
     int tile;        // bytes per stage (a multiple of 16)
+    int nst;         // stages in use (kStages, or kFirstStages for a row's first read)
 };
 
 __device__ __forceinline__ void fence_proxy_async()
@@ -239,17 +244,18 @@ __device__ bool ring_sweep(Ring& rg, const uint8_t* row, int64_t bytes, FV&& fv)
         const int64_t n = bytes - i * tb;
         return static_cast<uint32_t>(n < tb ? n : tb);
     };
+    const int nst = rg.nst;
     auto issue = [&](int64_t i) {
-        const int st = static_cast<int>(i % kStages);
+        const int st = static_cast<int>(i % nst);
         mbar_arrive_expect_tx(&rg.bar[st], tile_bytes(i));
         bulk_copy_g2s(rg.buf + st * tb, row + i * tb, tile_bytes(i), &rg.bar[st]);
     };
     if (t == 0) {
         fence_proxy_async();  // earlier generic accesses to the buffer come first
-        for (int64_t i = 0; i < ntiles && i < kStages; ++i) issue(i);
+        for (int64_t i = 0; i < ntiles && i < nst; ++i) issue(i);
     }
     for (int64_t i = 0; i < ntiles; ++i) {
-        const int st = static_cast<int>(i % kStages);
+        const int st = static_cast<int>(i % nst);
         bool ok = mbar_wait_bounded(&rg.bar[st], (rg.phase >> st) & 1u, nullptr);
         rg.phase ^= 1u << st;
         if (ok) {
@@ -260,13 +266,13 @@ __device__ bool ring_sweep(Ring& rg, const uint8_t* row, int64_t bytes, FV&& fv)
         if (!__syncthreads_and(ok)) {
             // Let the copies still in flight land before giving up.
             if (!ok) mbar_wait_bounded(&rg.bar[st], ((rg.phase >> st) & 1u) ^ 1u, nullptr);
-            if (i + 1 < ntiles) {
-                const int sn = static_cast<int>((i + 1) % kStages);
+            for (int j = 1; j < nst && i + j < ntiles; ++j) {
+                const int sn = static_cast<int>((i + j) % nst);
                 mbar_wait_bounded(&rg.bar[sn], (rg.phase >> sn) & 1u, nullptr);
             }
             return false;
         }
-        if (t == 0 && i + kStages < ntiles) issue(i + kStages);
+        if (t == 0 && i + nst < ntiles) issue(i + nst);
     }
     return true;
 }
@@ -766,6 +772,7 @@ __device__ __noinline__ int topp_bins(const uint8_t* row, int64_t V, float c, fl
         }
         rg.buf = ring_in_list ? reinterpret_cast<uint8_t*>(list) : reinterpret_cast<uint8_t*>(bins);
         rg.tile = ring_in_list ? static_cast<int>(kListBytes / kStages) : kTileBytes;
+        rg.nst = kStages;
         return ring_sweep(rg, row, V * ES, [&](const uint4& u) {
             float x[16 / ES];
             unpack_vec<ES>(u, x);
@@ -1025,15 +1032,15 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
     uint64_t* hm = reinterpret_cast<uint64_t*>(smem + kCandBytes + kCountBytes);
     uint32_t* list = reinterpret_cast<uint32_t*>(smem + kBinsBytes);
     __shared__ Scratch s;
-    __shared__ __align__(8) uint64_t ring_bar[kStages];
+    __shared__ __align__(8) uint64_t ring_bar[kFirstStages];
     const Geometry& g = a.g;
     const int64_t V = g.V;
     const int T = blockDim.x, t = threadIdx.x;
     // Whole 16-byte vectors per row: every row starts 16-byte aligned.
     const bool use_ring = (V * ES) % 16 == 0;
-    Ring rg{ring_bar, smem, 0u, kTileBytes};
+    Ring rg{ring_bar, smem, 0u, kTileBytes, kStages};
     if (t == 0) {
-        for (int i = 0; i < kStages; ++i) mbar_init(&ring_bar[i], 1);
+        for (int i = 0; i < kFirstStages; ++i) mbar_init(&ring_bar[i], 1);
         fence_barrier_init();
     }
     __syncthreads();
@@ -1080,8 +1087,11 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                     a1[q] = bf16x2_max_nan(a1[q], w[q]);
                 }
             };
-            if (use_ring)
+            if (use_ring) {
+                rg.nst = kFirstStages;  // the list region is free until the first read ends
                 landed = ring_sweep(rg, row, V * ES, fv);
+                rg.nst = kStages;
+            }
             else
                 sweep_vec<ES>(row, V, fv, fs);
 #pragma unroll
@@ -1103,8 +1113,11 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                     m1[q] = fmax_nan(m1[q], x[q]);
                 }
             };
-            if (use_ring)
+            if (use_ring) {
+                rg.nst = kFirstStages;  // the list region is free until the first read ends
                 landed = ring_sweep(rg, row, V * ES, fv);
+                rg.nst = kStages;
+            }
             else
                 sweep_vec<ES>(row, V, fv, fs);
         }
