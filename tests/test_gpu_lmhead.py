@@ -203,3 +203,55 @@ def test_lmhead_greedy_ties_take_the_lowest_index(v1, v2):
     assert np.array_equal(r["num_accepted"].cpu().numpy(), orc["num_accepted"])
     assert np.array_equal(r["out_tokens"].cpu().numpy(), orc["out_tokens"])
     assert (r["out_tokens"].cpu().numpy() != v2).all()
+
+
+def test_lmhead_emitted_tokens_follow_target_law():
+    """The pages' invariant (the output follows the target distribution) through
+    the whole LM-head path: statistics GEMM, scan, emitted-pair GEMM and
+    sampler. 2^19 sequences share one set of hidden states; drafts x_i ~ q_i
+    from numpy's generator. Among sequences that reach position i, the token
+    at i must follow p_i = softmax(h_t,i W_t^T) (exact float64 logits from the
+    oracle), by chi-square with a Bonferroni-corrected threshold; the first
+    acceptance rate must match sum_x min(p_0(x), q_0(x)) to five standard
+    deviations."""
+    from scipy import stats
+    K, B, V, Dt, Dd = 2, 1 << 19, 8, 64, 32
+    rng = np.random.default_rng(77)
+
+    def bf16_bits(a):
+        u = np.asarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
+        return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+    ht = bf16_bits(rng.normal(size=(K + 1, Dt)))
+    wt = bf16_bits(rng.normal(size=(V, Dt)) * 1.2 / Dt ** 0.5)
+    hd = bf16_bits(rng.normal(size=(K, Dd)))
+    wd = bf16_bits(rng.normal(size=(V, Dd)) * 1.2 / Dd ** 0.5)
+    lt = oracle.lm_head_logits(ht, wt)
+    ld = oracle.lm_head_logits(hd, wd)
+    p = np.exp(lt - lt.max(1, keepdims=True))
+    p /= p.sum(1, keepdims=True)
+    q = np.exp(ld - ld.max(1, keepdims=True))
+    q /= q.sum(1, keepdims=True)
+    x = np.stack([rng.choice(V, size=B, p=q[i]) for i in range(K)], 1).astype(np.int32)
+
+    def dev(bits, shape):
+        t = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).cuda()
+        return t.unsqueeze(0).expand(*shape).contiguous() if len(shape) == 3 else t
+
+    h_t = dev(ht, (B, K + 1, Dt))
+    h_d = dev(hd, (B, K, Dd))
+    out, nacc = sv.spec_verify_lmhead(h_t, dev(wt, ()), h_d, dev(wd, ()),
+                                      torch.from_numpy(x).cuda(), 1.0, 0x5EED, "sample")
+    torch.cuda.synchronize()
+    out, nacc = out.cpu().numpy(), nacc.cpu().numpy()
+    assert np.all((nacc >= 0) & (nacc <= K))
+    pvals = []
+    for i in range(K + 1):
+        toks = out[nacc >= i, i]
+        assert np.all((toks >= 0) & (toks < V))
+        counts = np.bincount(toks, minlength=V)
+        pvals.append(stats.chisquare(counts, p[i] * counts.sum()).pvalue)
+    assert min(pvals) > 1e-3 / (K + 1), pvals
+    beta0 = np.minimum(p[0], q[0]).sum()
+    rate = np.mean(nacc >= 1)
+    assert abs(rate - beta0) < 5 * np.sqrt(beta0 * (1 - beta0) / B)
