@@ -23,6 +23,7 @@ from .api import (  # noqa: F401
     spec_verify_filtered,
     spec_verify_filtered_debug,
     spec_verify_filtered_timed,
+    spec_verify_gated,
     spec_verify_host,
     spec_verify_lmhead,
     spec_verify_lmhead_debug,

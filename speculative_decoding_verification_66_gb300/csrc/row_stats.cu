@@ -438,6 +438,22 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const __grid_con
         // ---------------- producer ----------------
         if (lane != 0) return;
         int64_t n = 0;
+        if (a.gate != nullptr) {
+            // Test hook: hold every copy until *gate != 0, bounded like every
+            // other wait. Nothing sets it in the tests that use it, so the
+            // consumers see the abort and mark their rows as timed out.
+            const volatile int32_t* gate = a.gate;
+            const long long t0 = clock64();
+            while (*gate == 0) {
+                if (clock64() - t0 > kWaitLimitCycles) {
+                    abort_flag = 1;
+                    n = -1;
+                    break;
+                }
+                __nanosleep(1000);
+            }
+            if (n < 0) return;  // no copy was issued
+        }
         for (; n < ntiles; ++n) {
             const int stage = static_cast<int>(n % kRowStages);
             if (n >= kRowStages) {

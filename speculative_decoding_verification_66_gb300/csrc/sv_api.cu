@@ -206,7 +206,8 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         double* lse_t, double* lse_d, double* log_ratio, int32_t* seq_status,
         void* const* events, int n_events, bool early_exit = false,
         const void* const* t_shards = nullptr, const void* const* d_shards = nullptr, int G = 1,
-        int64_t top_k = 0, float top_p = 1.0f, float* thr_t = nullptr, float* thr_d = nullptr)
+        int64_t top_k = 0, float top_p = 1.0f, float* thr_t = nullptr, float* thr_d = nullptr,
+        const int32_t* gate = nullptr)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -298,7 +299,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         sp_d = pairs + row_bytes;
         lay = sv::RowPairLayout{2, 0, 2, 0, pairs + 2 * B * row_bytes, pairs + 2 * B * row_bytes};
     }
-    sv::RowStatsArgs ra{tp, dp, g, c, partials, full, sh};
+    sv::RowStatsArgs ra{tp, dp, g, c, partials, full, sh, gate};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
                     sampling ? log_ratio : nullptr, seq_status, full, nullptr,
@@ -546,6 +547,21 @@ SV_EXPORT int spec_verify_debug(const void* target_logits, const void* draft_log
     return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
                out_tokens, num_accepted, workspace, workspace_bytes, stream, lse_t, lse_d,
                log_ratio, seq_status, nullptr, 0);
+}
+
+SV_EXPORT int spec_verify_gated(const void* target_logits, const void* draft_logits,
+                                const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
+                                int dtype, float temperature, uint64_t seed, int mode,
+                                int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                                size_t workspace_bytes, void* stream, int32_t* seq_status,
+                                const int32_t* gate)
+{
+    if (gate == nullptr) return SV_ERR_ARG;
+    if (!aligned_to(gate, 4)) return SV_ERR_ALIGN;
+    return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
+               out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
+               nullptr, seq_status, nullptr, 0, false, nullptr, nullptr, 1, 0, 1.0f, nullptr,
+               nullptr, gate);
 }
 
 SV_EXPORT int spec_verify_timed(const void* target_logits, const void* draft_logits,

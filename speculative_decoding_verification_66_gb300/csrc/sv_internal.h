@@ -149,6 +149,9 @@ struct RowStatsArgs {
     Partial* partials;      // [grid][maxseg][kRowConsumerWarps]
     RowMap map;
     Shards sh;
+    // Test hook (nullptr in every product call): the producer holds its
+    // copies until *gate != 0, a bounded wait like the others.
+    const int32_t* gate;
 };
 
 // Launch with programmatic stream serialization (the kernel must call

@@ -248,3 +248,30 @@ def test_binding_rejects_bad_tensors():
     bad = torch.empty(2 * 5 * 64 + 1, dtype=torch.bfloat16, device="cuda")[1:].view(2, 5, 64)
     with pytest.raises(sv.SpecVerifyError):
         sv.spec_verify(bad, inputs["draft"], inputs["tokens"])
+
+
+@pytest.mark.parametrize("mode", ["sample", "greedy"])
+def test_timeout_path(mode):
+    """Pass 1's timeout path, without a fault: its producers wait on a device
+    flag that nothing sets. The wait runs out (about 2 s), the consumers mark
+    their rows as timed out, and every sequence comes back as SV_SEQ_TIMEOUT.
+    The context stays usable: an ordinary call afterwards still matches the
+    oracle, and a gated call whose flag is already set matches spec_verify."""
+    base = WORKLOADS["small_f32"] if mode == "sample" else WORKLOADS["greedy_bf16"]
+    wl = base.resized(B=6, K=3, V=3000, dtype="bf16", mode=mode)
+    inputs = make_inputs(wl, 4, "cuda")
+    gate = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
+                             wl.temperature, 9, mode)
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == sv.SV_SEQ_TIMEOUT).all()
+    assert (r["num_accepted"].cpu() == -1).all() and (r["out_tokens"].cpu() == -1).all()
+    check(wl, 4, device_inputs=inputs)
+    gate.fill_(1)
+    r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
+                             wl.temperature, 9, mode)
+    out, nacc = sv.spec_verify(inputs["target"], inputs["draft"], inputs["tokens"],
+                               wl.temperature, 9, mode)
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == 0).all()
+    assert torch.equal(r["out_tokens"], out) and torch.equal(r["num_accepted"], nacc)

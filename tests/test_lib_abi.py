@@ -34,7 +34,7 @@ def lib():
 def test_header_declares_the_api():
     assert declared_functions() == sorted([
         "sv_workspace_bytes", "spec_verify", "spec_verify_debug", "spec_verify_timed",
-        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static",
+        "sv_host_staging_bytes", "spec_verify_host", "spec_verify_static", "spec_verify_gated",
         "sv_early_exit_workspace_bytes", "spec_verify_early_exit",
         "sv_sharded_workspace_bytes", "spec_verify_sharded", "sv_philox",
         "sv_filtered_workspace_bytes", "spec_verify_filtered", "spec_verify_filtered_timed",
@@ -241,6 +241,10 @@ def test_lmhead_host_side_validation(lib):
     assert dbg(*args, FAKE + 4, FAKE, FAKE, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE, FAKE, FAKE + 2, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE, FAKE, FAKE, FAKE + 1) == SV_ERR_ALIGN
+    sg = lib.spec_verify_gated
+    sargs = (FAKE, FAKE, FAKE, 2, 3, 64, 1, 1.0, 7, 0, FAKE, FAKE, FAKE, 1 << 20, None, FAKE)
+    assert sg(*sargs, None) == SV_ERR_ARG
+    assert sg(*sargs, FAKE + 2) == SV_ERR_ALIGN
     gated = lib.spec_verify_lmhead_gated
     gargs = (FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 64, 64, 32, 1.0, 7, 0, FAKE, FAKE, FAKE, 1 << 20,
              None, FAKE)
