@@ -115,7 +115,9 @@ __device__ void merge_row(const ScanArgs& a, int64_t lrow, int64_t tiles, int la
         const float l = log2f(hi) + lo / (hi * 0.69314718055994531f);
         const bool ok = M > __uint_as_float(kF32NegInfBits) && M < __uint_as_float(0x7F800000u) &&
                         hi > 0.f && l < __uint_as_float(0x7F800000u);
-        if (!ok) fl |= kFlagNonFinite;  // all -inf, or a sum that is not finite
+        // All -inf, or a sum that is not finite; a row that timed out in
+        // pass 1 reports only the timeout.
+        if (!ok && !(fl & kFlagTimeout)) fl |= kFlagNonFinite;
         norm->m = M;
         norm->l = l;
         norm->thr = __uint_as_float(kF32NegInfBits);
