@@ -438,22 +438,29 @@ int spec_verify_lmhead_timed(const void* hidden_target, const void* weight_targe
                              void* const* events, int n_events);
 
 /*
- * Test hook for the timeout path (no counterpart on the pages): spec_verify
- * with pass 1's producers holding every copy until the device int32 *gate
- * becomes nonzero. That wait is bounded like every other wait in the kernels
- * (about 2 s); when it runs out, the consumers see the abort, mark their rows
- * as timed out and the CTA returns, and every sequence is reported as
- * SV_SEQ_TIMEOUT (num_accepted -1, tokens -1, seq_status if given), with the
- * context still usable. A caller that sets *gate before the wait runs out
- * gets spec_verify's results.
- *   gate  device int32, 4-byte aligned (SV_ERR_ARG if NULL, SV_ERR_ALIGN).
- * Other arguments as spec_verify_debug (seq_status optional).
+ * Test hook for the timeout paths (no counterpart on the pages):
+ * spec_verify_filtered (spec_verify when both cuts are off) with one stage's
+ * bulk copies held until the device int32 *gate becomes nonzero:
+ *   stage 1  pass 1's producers (with a cut: the thresholds kernel's);
+ *   stage 2  the sampler's streaming warps.
+ * That wait is bounded like every other wait in the kernels (about 2 s). When
+ * it runs out, the held stage marks its work as timed out and returns with no
+ * copy in flight, and the sequences it affects are reported as SV_SEQ_TIMEOUT
+ * (num_accepted -1, tokens -1, seq_status if given). Stage 1 affects every
+ * sequence; stage 2 every sequence the scan found valid. The context stays
+ * usable. A caller that sets *gate before the wait runs out gets the ordinary
+ * results.
+ *   stage  1 or 2 (SV_ERR_ARG otherwise).
+ *   gate   device int32, 4-byte aligned (SV_ERR_ARG if NULL, SV_ERR_ALIGN).
+ * Other arguments as spec_verify_filtered (workspace: sv_filtered_workspace_bytes,
+ * which is sv_workspace_bytes when both cuts are off); seq_status optional.
  */
 int spec_verify_gated(const void* target_logits, const void* draft_logits,
                       const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,
-                      float temperature, uint64_t seed, int mode, int32_t* out_tokens,
-                      int32_t* num_accepted, void* workspace, size_t workspace_bytes, void* stream,
-                      int32_t* seq_status, const int32_t* gate);
+                      float temperature, int64_t top_k, float top_p, uint64_t seed, int mode,
+                      int32_t* out_tokens, int32_t* num_accepted, void* workspace,
+                      size_t workspace_bytes, void* stream, int32_t* seq_status, int stage,
+                      const int32_t* gate);
 
 /*
  * Test hook for the timeout path (no counterpart on the pages): spec_verify_lmhead

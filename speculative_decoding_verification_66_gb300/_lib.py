@@ -47,8 +47,8 @@ SIGNATURES = {
                                         _vp]),
     "spec_verify_lmhead_timed": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                         _f32, _u64, _i32, _vp, _vp, _vp, _sz, _vp, _vp, _i32]),
-    "spec_verify_gated": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _f32, _u64, _i32, _vp,
-                                 _vp, _vp, _sz, _vp, _vp, _vp]),
+    "spec_verify_gated": (_i32, [_vp, _vp, _vp, _i64, _i64, _i64, _i32, _f32, _i64, _f32, _u64,
+                                 _i32, _vp, _vp, _vp, _sz, _vp, _vp, _i32, _vp]),
     "spec_verify_lmhead_gated": (_i32, [_vp, _vp, _vp, _vp, _vp, _i64, _i64, _i64, _i64, _i64,
                                         _f32, _u64, _i32, _vp, _vp, _vp, _sz, _vp, _vp, _vp]),
     "sv_lmhead_logits": (_i32, [_vp, _vp, _i64, _i64, _i64, _vp, _vp, _vp]),

@@ -542,24 +542,34 @@ def spec_verify_lmhead_timed(hidden_target, weight_target, hidden_draft, weight_
 
 
 def spec_verify_gated(target_logits, draft_logits, draft_tokens, gate, temperature: float = 1.0,
-                      seed: int = 0, mode="sample", *, workspace=None, stream=None) -> dict:
-    """Test hook for the timeout path: spec_verify with pass 1's copies held
-    until the device int32 ``gate`` (one element) is nonzero. Returns
-    out_tokens, num_accepted and seq_status."""
+                      seed: int = 0, mode="sample", *, stage: int = 1, top_k: int = 0,
+                      top_p: float = 1.0, workspace=None, stream=None) -> dict:
+    """Test hook for the timeout paths: spec_verify_filtered (spec_verify with
+    the cuts off) with one stage's copies held until the device int32 ``gate``
+    (one element) is nonzero: stage 1 = pass 1 (or the thresholds kernel),
+    stage 2 = the sampler. Returns out_tokens, num_accepted and seq_status."""
     if gate.dtype != torch.int32 or not gate.is_cuda or gate.numel() < 1:
         raise ValueError("gate must be an int32 CUDA tensor")
-    m, B, K, V, d, stream, out_tokens, num_accepted, workspace = _prepare(
-        target_logits, draft_logits, draft_tokens, mode, None, None, workspace, stream)
+    m = mode_code(mode)
+    B, K, V = _shapes(target_logits, draft_logits, draft_tokens, m)
     dev = target_logits.device
-    seq_status = torch.full((B,), -7, dtype=torch.int32, device=dev)
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    d = dtype_code(target_logits.dtype)
+    if workspace is None:
+        workspace = workspace_for(dev, stream, sv_filtered_workspace_bytes(B, K, V, d, m))
+    out = {"out_tokens": torch.empty((B, K + 1), dtype=torch.int32, device=dev),
+           "num_accepted": torch.empty((B,), dtype=torch.int32, device=dev),
+           "seq_status": torch.full((B,), -7, dtype=torch.int32, device=dev)}
     with torch.cuda.device(dev):
         _check(_lib.load().spec_verify_gated(
             _ptr(target_logits), _ptr(draft_logits if m == SV_SAMPLE else None),
-            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature),
-            int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out_tokens), _ptr(num_accepted),
-            _ptr(workspace), workspace.numel(), ctypes.c_void_p(stream.cuda_stream),
-            _ptr(seq_status), _ptr(gate)), "spec_verify_gated")
-    return {"out_tokens": out_tokens, "num_accepted": num_accepted, "seq_status": seq_status}
+            _ptr(draft_tokens if K > 0 else None), B, K, V, d, float(temperature), int(top_k),
+            float(top_p), int(seed) & 0xFFFFFFFFFFFFFFFF, m, _ptr(out["out_tokens"]),
+            _ptr(out["num_accepted"]), _ptr(workspace), workspace.numel(),
+            ctypes.c_void_p(stream.cuda_stream), _ptr(out["seq_status"]), int(stage), _ptr(gate)),
+            "spec_verify_gated")
+    return out
 
 
 def spec_verify_lmhead_gated(hidden_target, weight_target, hidden_draft, weight_draft,

@@ -1059,6 +1059,28 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
     // at most 22 bits so that to_fixed stays exact.
     const int sc = 30 - lg < 22 ? 30 - lg : 22;
     pdl_trigger();  // the scan may launch; it waits for this grid before reading
+    if (a.gate != nullptr) {
+        // Test hook: hold every copy until *gate != 0, bounded like every
+        // other wait. Nothing sets it in the tests that use it: the CTA then
+        // marks its rows as timed out and returns, with no copy issued.
+        if (t == 0) {
+            s.list_n = 0;
+            const volatile int32_t* gate = a.gate;
+            const long long t0 = clock64();
+            while (*gate == 0) {
+                if (clock64() - t0 > kWaitLimitCycles) {
+                    s.list_n = 1;
+                    break;
+                }
+                __nanosleep(1000);
+            }
+        }
+        __syncthreads();
+        if (s.list_n != 0) {
+            fail_rows(a, blockIdx.x);
+            return;
+        }
+    }
 
     for (int64_t r = blockIdx.x; r < g.rows; r += gridDim.x) {
         const uint8_t* row =

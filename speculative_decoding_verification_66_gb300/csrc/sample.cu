@@ -439,6 +439,35 @@ __global__ void __launch_bounds__(kT, 3) sample_stream_kernel(const __grid_const
     __syncwarp();
     pdl_wait();  // the scan has finished and the sequence records are visible
     pdl_trigger();  // the race kernel may be scheduled; it waits for this grid
+    if (a.gate != nullptr) {
+        // Test hook: hold this warp's copies until *gate != 0, bounded like
+        // every other wait. Nothing sets it in the tests that use it: the
+        // warp then marks its slices with NaN sums (the race kernel reports
+        // their sequences as timed out) and returns, with no copy issued.
+        int held = 0;
+        if (lane == 0) {
+            const volatile int32_t* gate = a.gate;
+            const long long t0 = clock64();
+            while (*gate == 0) {
+                if (clock64() - t0 > kWaitLimitCycles) {
+                    held = 1;
+                    break;
+                }
+                __nanosleep(1000);
+            }
+        }
+        if (__shfl_sync(0xFFFFFFFFu, held, 0)) {
+            const float nan = __uint_as_float(0x7FC00000u);
+            float sums[G::kBlocks];
+#pragma unroll
+            for (int q = 0; q < G::kBlocks; ++q) sums[q] = nan;
+            for (int64_t k = i0; k < i1; ++k) {
+                const int64_t kb = k / per_seq, ke0 = (k - kb * per_seq) * G::kTok;
+                store_sums<ES>(a, kb, ke0, static_cast<int>(lmin(G::kTok, g.V - ke0)), sums, lane);
+            }
+            return;
+        }
+    }
 
     auto tokens_at = [&](int64_t sl) { return static_cast<int>(lmin(G::kTok, g.V - sl * G::kTok)); };
     TensorEnds ends{nullptr, nullptr};

@@ -207,7 +207,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         void* const* events, int n_events, bool early_exit = false,
         const void* const* t_shards = nullptr, const void* const* d_shards = nullptr, int G = 1,
         int64_t top_k = 0, float top_p = 1.0f, float* thr_t = nullptr, float* thr_d = nullptr,
-        const int32_t* gate = nullptr)
+        const int32_t* gate = nullptr, int gate_stage = 0)
 {
     int rc = check_sizes(B, K, V, dtype, mode);
     if (rc != SV_OK) return rc;
@@ -299,14 +299,17 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         sp_d = pairs + row_bytes;
         lay = sv::RowPairLayout{2, 0, 2, 0, pairs + 2 * B * row_bytes, pairs + 2 * B * row_bytes};
     }
-    sv::RowStatsArgs ra{tp, dp, g, c, partials, full, sh, gate};
+    // Test hook: stage 1 holds pass 1's (or the thresholds kernel's) copies,
+    // stage 2 the sampler's.
+    sv::RowStatsArgs ra{tp, dp, g, c, partials, full, sh, gate_stage == 1 ? gate : nullptr};
     sv::ScanArgs sa{tp, dp, tokens, g, c, seed, partials, out_tokens, num_accepted, seqs,
                     sampling ? lse_t : nullptr, sampling ? lse_d : nullptr,
                     sampling ? log_ratio : nullptr, seq_status, full, nullptr,
                     sampling ? thr_t : nullptr, sampling ? thr_d : nullptr,
                     nullptr, nullptr, nullptr, nullptr, sh};
     sv::SampleArgs pa{sp_t, sp_d, g, c, seed, seqs, block_sums,
-                      out_tokens, num_accepted, seq_status, lay, direct ? 1 : 0, sh, 0};
+                      out_tokens, num_accepted, seq_status, lay, direct ? 1 : 0, sh, 0,
+                      gate_stage == 2 ? gate : nullptr};
     sv::GatherArgs ga{g, sh, seqs, ws + L.pairs};
 
     if (filtered) {
@@ -315,7 +318,7 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         const int64_t cap = filter_blocks(g.es);
         if (cap <= 0) return SV_ERR_CUDA;
         const int grid = static_cast<int>(g.rows < cap ? g.rows : cap);
-        sv::FilterArgs fa{tp, dp, g, c, top_k, top_p, filt};
+        sv::FilterArgs fa{tp, dp, g, c, top_k, top_p, filt, gate_stage == 1 ? gate : nullptr};
         sa.filt = filt;
         pa.filtered = 1;
         if (!record(0)) return SV_ERR_CUDA;
@@ -551,17 +554,17 @@ SV_EXPORT int spec_verify_debug(const void* target_logits, const void* draft_log
 
 SV_EXPORT int spec_verify_gated(const void* target_logits, const void* draft_logits,
                                 const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V,
-                                int dtype, float temperature, uint64_t seed, int mode,
-                                int32_t* out_tokens, int32_t* num_accepted, void* workspace,
-                                size_t workspace_bytes, void* stream, int32_t* seq_status,
-                                const int32_t* gate)
+                                int dtype, float temperature, int64_t top_k, float top_p,
+                                uint64_t seed, int mode, int32_t* out_tokens,
+                                int32_t* num_accepted, void* workspace, size_t workspace_bytes,
+                                void* stream, int32_t* seq_status, int stage, const int32_t* gate)
 {
-    if (gate == nullptr) return SV_ERR_ARG;
+    if (gate == nullptr || (stage != 1 && stage != 2)) return SV_ERR_ARG;
     if (!aligned_to(gate, 4)) return SV_ERR_ALIGN;
     return run(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature, seed, mode,
                out_tokens, num_accepted, workspace, workspace_bytes, stream, nullptr, nullptr,
-               nullptr, seq_status, nullptr, 0, false, nullptr, nullptr, 1, 0, 1.0f, nullptr,
-               nullptr, gate);
+               nullptr, seq_status, nullptr, 0, false, nullptr, nullptr, 1, top_k, top_p, nullptr,
+               nullptr, gate, stage);
 }
 
 SV_EXPORT int spec_verify_timed(const void* target_logits, const void* draft_logits,

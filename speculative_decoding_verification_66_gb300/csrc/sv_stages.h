@@ -15,6 +15,7 @@ struct FilterArgs {
     int64_t top_k;      // 0 < top_k < V, else off
     float top_p;        // in (0, 1); 1 = off
     FiltRow* rows;      // [B (2K + 1)]
+    const int32_t* gate;  // test hook (nullptr in product calls): hold the copies until *gate != 0
 };
 
 struct ScanArgs {
@@ -80,6 +81,7 @@ struct SampleArgs {
     int32_t direct;
     Shards sh;
     int32_t filtered;       // weights are masked by the records' thresholds
+    const int32_t* gate;    // test hook (nullptr in product calls): hold the copies until *gate != 0
 };
 
 // Sharded verification: copies each sequence's emitted row pair from the

@@ -289,3 +289,26 @@ def test_filtered_single_sequence_full_vocab():
     wl = WORKLOADS["llama3_bf16"].resized(B=1)
     st, _, _ = check(wl, 41, 50, 0.9)
     assert st["decisions"] > 0
+
+
+def test_thresholds_kernel_timeout_path():
+    """The thresholds kernel's timeout path, without a fault: its copies are
+    held behind a device flag that nothing sets; every CTA marks its rows as
+    timed out, and every sequence is reported as SV_SEQ_TIMEOUT. A gated call
+    whose flag is already set matches spec_verify_filtered."""
+    wl = WORKLOADS["spiky_bf16"].resized(B=6, K=3, V=3000)
+    inputs = make_inputs(wl, 2, "cuda", top_k=40, top_p=0.9)
+    gate = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
+                             wl.temperature, 9, "sample", stage=1, top_k=40, top_p=0.9)
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == sv.SV_SEQ_TIMEOUT).all()
+    assert (r["num_accepted"].cpu() == -1).all()
+    gate.fill_(1)
+    r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
+                             wl.temperature, 9, "sample", stage=1, top_k=40, top_p=0.9)
+    out, nacc = sv.spec_verify_filtered(inputs["target"], inputs["draft"], inputs["tokens"],
+                                        wl.temperature, 40, 0.9, 9, "sample")
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == 0).all()
+    assert torch.equal(r["out_tokens"], out) and torch.equal(r["num_accepted"], nacc)

@@ -275,3 +275,20 @@ def test_timeout_path(mode):
     torch.cuda.synchronize()
     assert (r["seq_status"].cpu() == 0).all()
     assert torch.equal(r["out_tokens"], out) and torch.equal(r["num_accepted"], nacc)
+
+
+def test_sampler_timeout_path():
+    """The sampler's timeout path, without a fault: its streaming warps wait on
+    a device flag that nothing sets. They mark their slices with NaN block
+    sums, and the race kernel reports every sequence as SV_SEQ_TIMEOUT; pass 1
+    and the scan ran normally. An ordinary call afterwards still matches the
+    oracle."""
+    wl = WORKLOADS["small_f32"].resized(B=6, K=3, V=3000, dtype="bf16")
+    inputs = make_inputs(wl, 6, "cuda")
+    gate = torch.zeros(1, dtype=torch.int32, device="cuda")
+    r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
+                             wl.temperature, 9, "sample", stage=2)
+    torch.cuda.synchronize()
+    assert (r["seq_status"].cpu() == sv.SV_SEQ_TIMEOUT).all()
+    assert (r["num_accepted"].cpu() == -1).all() and (r["out_tokens"].cpu() == -1).all()
+    check(wl, 6, device_inputs=inputs)

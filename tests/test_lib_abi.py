@@ -242,9 +242,12 @@ def test_lmhead_host_side_validation(lib):
     assert dbg(*args, FAKE, FAKE, FAKE + 2, FAKE) == SV_ERR_ALIGN
     assert dbg(*args, FAKE, FAKE, FAKE, FAKE + 1) == SV_ERR_ALIGN
     sg = lib.spec_verify_gated
-    sargs = (FAKE, FAKE, FAKE, 2, 3, 64, 1, 1.0, 7, 0, FAKE, FAKE, FAKE, 1 << 20, None, FAKE)
-    assert sg(*sargs, None) == SV_ERR_ARG
-    assert sg(*sargs, FAKE + 2) == SV_ERR_ALIGN
+    sargs = (FAKE, FAKE, FAKE, 2, 3, 64, 1, 1.0, 5, 0.9, 7, 0, FAKE, FAKE, FAKE, 1 << 20, None,
+             FAKE)
+    assert sg(*sargs, 1, None) == SV_ERR_ARG
+    assert sg(*sargs, 3, FAKE) == SV_ERR_ARG
+    assert sg(*sargs, 0, FAKE) == SV_ERR_ARG
+    assert sg(*sargs, 2, FAKE + 2) == SV_ERR_ALIGN
     gated = lib.spec_verify_lmhead_gated
     gargs = (FAKE, FAKE, FAKE, FAKE, FAKE, 2, 3, 64, 64, 32, 1.0, 7, 0, FAKE, FAKE, FAKE, 1 << 20,
              None, FAKE)
