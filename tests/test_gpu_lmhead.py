@@ -22,12 +22,49 @@ import oracle
 import speculative_decoding_verification_66_gb300 as sv
 from speculative_decoding_verification_66_gb300.workloads import (LM_WORKLOADS, lm_host_arrays,
                                                                    make_lmhead_inputs)
-from parity_util import compare
+from parity_util import compare, valid_output
 
 pytestmark = pytest.mark.gpu
 
 FLAG_LM = 1e-3
 RTOL_LM = 1e-4
+# Greedy decides on an argmax: the GPU takes it on float32-accumulated logits,
+# the oracle on exact ones, so a row whose two largest exact logits lie within
+# the accumulation error may go either way. 1e-3 is about 100x that error at
+# D = 4096 for these weight scales.
+GREEDY_GAP = 1e-3
+
+
+def _greedy_compare(gpu, host, lw, rows):
+    """Greedy LM-head results against the oracle, with near-ties flagged: up to
+    the first position whose row has a top-2 gap below GREEDY_GAP the tokens
+    must be identical; past it the output only has to be a valid result."""
+    ht, wt, _, _, tok = host
+    K, V = lw.K, lw.V
+    rows = list(rows)
+    b0, b1 = min(rows), max(rows) + 1
+    orc = oracle.verify_lmhead(ht, wt, None, None, tok, 1.0, 0, oracle.GREEDY,
+                               seq_range=(b0, b1))
+    logits = oracle.lm_head_logits(ht[b0:b1], wt)  # [n, K+1, V], exact
+    top2 = np.sort(logits, axis=-1)[..., -2:]
+    gap = top2[..., 1] - top2[..., 0]
+    flagged = 0
+    for b in rows:
+        assert int(gpu["seq_status"][b]) == int(orc["seq_status"][b]), b
+        og, oo = gpu["out_tokens"][b], orc["out_tokens"][b]
+        ng, no = int(gpu["num_accepted"][b]), int(orc["num_accepted"][b])
+        if int(orc["seq_status"][b]) != 0:
+            assert ng == -1 and np.all(og == -1), b
+            continue
+        near = [i for i in range(min(no, K) + 1) if gap[b - b0, i] < GREEDY_GAP]
+        if not near:
+            assert ng == no and np.array_equal(og, oo), (b, og, oo)
+            continue
+        flagged += 1
+        f = near[0]
+        assert ng >= min(f, no) and np.array_equal(og[:f], oo[:f]), (b, og, oo)
+        assert valid_output(og, ng, tok[b], K, V), (b, og)
+    return {"flagged_sequences": flagged}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -90,11 +127,13 @@ def _check(lw, seed, seq_ranges=None, inp=None):
     host = lm_host_arrays(inp)
     st = None
     for rng in (seq_ranges or [None]):
-        orc = oracle.verify_lmhead(*host[:4], host[4], lw.temperature, s,
-                                   oracle.GREEDY if greedy else oracle.SAMPLE, seq_range=rng,
-                                   threads=8)
-        rows = None if rng is None else range(*rng)
-        st = compare(gpu, orc, host[4], lw.K, lw.V, rows=rows, greedy=greedy, flag=FLAG_LM,
+        rows = range(lw.B) if rng is None else range(*rng)
+        if greedy:
+            st = _greedy_compare(gpu, host, lw, rows) if lw.B > 0 else None
+            continue
+        orc = oracle.verify_lmhead(*host[:4], host[4], lw.temperature, s, oracle.SAMPLE,
+                                   seq_range=rng, threads=8)
+        st = compare(gpu, orc, host[4], lw.K, lw.V, rows=rows, greedy=False, flag=FLAG_LM,
                      rtol=RTOL_LM)
     # The plain call gives the same tokens as the diagnostic one.
     out, nacc = _lm_call(inp, lw, s)
