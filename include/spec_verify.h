@@ -39,16 +39,18 @@
  *   (word >> 8) * 2^-24; position i is kept iff that uniform is below
  *   min(1, p_i(x_i) / q_i(x_i)). The token at the emitted position j is drawn
  *   from the weights w (max(0, p_j - q_j) after a rejection, p_K for the
- *   bonus) by a two-level exponential race over blocks of 8192 tokens. Level 1
+ *   bonus) by a two-level exponential race over blocks of 512 tokens. Level 1
  *   takes the block c with the largest W_c / E_c over blocks with weight
  *   W_c = sum of w over the block > 0, E_c = -ln v_c, v_c lane (c mod 4) of
  *   counter (j, b, 1 + c div 4, 1). Level 2 takes the token k of that block
  *   with the largest w_k / E_k over w_k > 0, v_k lane (k mod 4) of counter
  *   (j, b, 1 + k div 4, 0). Both levels map a word to (2 (word >> 9) + 1) 2^-24
  *   and let the lowest index win an exact tie. The race picks token k with
- *   probability w_k / sum(w). Results are a pure function of (inputs, T, seed,
- *   mode) on a given GPU model: no float atomics, fixed reduction trees, the
- *   same answer on every run.
+ *   probability w_k / sum(w) for any block length; the length (512, so that
+ *   one 128-thread block reads a block as one four-token group per thread)
+ *   only decides which random numbers the draw uses. Results are a pure
+ *   function of (inputs, T, seed, mode) on a given GPU model: no float
+ *   atomics, fixed reduction trees, the same answer on every run.
  *
  * Memory and streams:
  *   Every pointer passed to spec_verify / spec_verify_debug / spec_verify_timed

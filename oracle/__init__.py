@@ -15,8 +15,10 @@ Parity status of each function (how it is pinned, see ``tests/test_oracle_*.py``
 * ``accept_prob`` / ``sample_weights`` / ``race_sample`` / ``verify`` --
   pinned by the pages' two worked two-token examples, the p == q special case,
   exact path sums on tiny vocabularies (output law == target law), Monte-Carlo
-  chi-square of the output marginal and of the race alone, the race's
-  near-tie law, and closed-form acceptance rates.
+  chi-square of the output marginal and of the race alone (for race block
+  lengths 1, 7, 512 and V), the race's near-tie law, closed-form acceptance
+  rates, and, at one block (block length >= V), token-for-token equality with
+  a plain one-level race written out in the test.
 * ``row_argmax`` -- pinned against ``torch.argmax`` (first occurrence).
 
 * ``lm_head_logits`` / ``verify_lmhead`` -- the LM head h W^T (the pages take
@@ -96,16 +98,17 @@ def lib() -> ctypes.CDLL:
             L.svo_race_uniform.restype = dbl
             L.svo_block_uniform.argtypes = [u64, ctypes.c_uint32, ctypes.c_uint32, ctypes.c_uint32]
             L.svo_block_uniform.restype = dbl
-            L.svo_race_sample.argtypes = [vp, i64, u64, ctypes.c_uint32, ctypes.c_uint32, vp]
+            L.svo_race_sample.argtypes = [vp, i64, i64, u64, ctypes.c_uint32, ctypes.c_uint32,
+                                          vp]
             L.svo_race_sample.restype = i64
             L.svo_row_argmax.argtypes = [vp, i64, i32, vp]
             L.svo_row_argmax.restype = i64
             L.svo_verify.argtypes = [vp, vp, vp, i64, i64, i64, i32, dbl, u64, i32, i64, i64,
-                                     vp, vp, vp, vp, vp, vp, vp, vp]
+                                     i64, vp, vp, vp, vp, vp, vp, vp, vp]
             L.svo_verify.restype = i32
             L.svo_verify_filtered.argtypes = [vp, vp, vp, i64, i64, i64, i32, dbl, u64, i32, i64,
-                                              dbl, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp, vp,
-                                              vp, vp, vp]
+                                              i64, dbl, i64, i64, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, vp, vp]
             L.svo_verify_filtered.restype = i32
             L.svo_filter_row.argtypes = [vp, i64, i32, dbl, dbl, i64, dbl, vp, vp, vp]
             L.svo_filter_row.restype = i32
@@ -185,18 +188,22 @@ def race_uniform(seed: int, seq: int, pos: int, k: int) -> float:
     return lib().svo_race_uniform(seed, seq, pos, k)
 
 
-RACE_BLOCK = 512  # SVO_RACE_BLOCK in sv_oracle.h
+# Block length of the corrected / bonus token's two-level race in ``verify``.
+# The pages fix only the law of that draw, which the race meets for every block
+# length; the length decides which random numbers are used. 512 is the length
+# the CUDA library streams its block sums at, so it is the verifier's default.
+RACE_BLOCK = 512
 
 
 def block_uniform(seed: int, seq: int, pos: int, c: int) -> float:
     return lib().svo_block_uniform(seed, seq, pos, c)
 
 
-def race_sample(w: np.ndarray, seed: int, seq: int, pos: int):
-    """Returns (token, margin)."""
+def race_sample(w: np.ndarray, seed: int, seq: int, pos: int, block: int = RACE_BLOCK):
+    """Two-level race over blocks of ``block`` tokens; returns (token, margin)."""
     w = np.ascontiguousarray(w, dtype=np.float64)
     m = np.zeros(1, dtype=np.float64)
-    tok = lib().svo_race_sample(_ptr(w), w.shape[0], seed, seq, pos, _ptr(m))
+    tok = lib().svo_race_sample(_ptr(w), w.shape[0], int(block), seed, seq, pos, _ptr(m))
     return int(tok), float(m[0])
 
 
@@ -218,7 +225,8 @@ def filter_row(row: np.ndarray, T: float, lse: float, top_k: int, top_p: float):
 
 
 def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mode: int = SAMPLE,
-           threads: int = 1, seq_range=None, top_k: int = 0, top_p: float = 1.0) -> dict:
+           threads: int = 1, seq_range=None, top_k: int = 0, top_p: float = 1.0,
+           race_block: int = RACE_BLOCK) -> dict:
     """Run the oracle over a batch.
 
     target: [B, K+1, V] float32 or uint16 (bf16 bits); draft: [B, K, V] or None
@@ -228,6 +236,7 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
     shared state). ``seq_range=(b0, b1)`` restricts the work; outputs outside it
     are left at their fill values. ``top_k`` / ``top_p`` filter both rows of
     every position (0 and 1.0: off); ``top_p`` is widened from float32 like T.
+    ``race_block`` is the block length of the corrected / bonus token's race.
     """
     target = np.ascontiguousarray(target)
     if target.ndim != 3:
@@ -261,9 +270,9 @@ def verify(target: np.ndarray, draft, tokens, temperature: float, seed: int, mod
 
     def run(lo, hi):
         rc = L.svo_verify_filtered(_ptr(target), _ptr(draft), _ptr(tokens), B, K, V, dt, T,
-                                   seed, mode, int(top_k), P, lo, hi, _ptr(out["out_tokens"]),
-                                   _ptr(out["num_accepted"]), _ptr(out["lse_t"]),
-                                   _ptr(out["lse_d"]), _ptr(out["log_ratio"]),
+                                   seed, mode, int(race_block), int(top_k), P, lo, hi,
+                                   _ptr(out["out_tokens"]), _ptr(out["num_accepted"]),
+                                   _ptr(out["lse_t"]), _ptr(out["lse_d"]), _ptr(out["log_ratio"]),
                                    _ptr(out["accept_margin"]), _ptr(out["sample_margin"]),
                                    _ptr(out["filter_margin_t"]), _ptr(out["filter_margin_d"]),
                                    _ptr(out["filter_thr"]), _ptr(out["filter_log_mass"]),

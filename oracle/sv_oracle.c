@@ -3,9 +3,12 @@
  *
  * TEST INFRASTRUCTURE ONLY. Plain, single-threaded, slow on purpose: every
  * step is written out in the order the pages give it, in double precision,
- * with no blocking, fusion or reordering. Only the test-suite, the smoke
- * check and the benchmark's CPU-baseline leg load this file's library; the
- * CUDA library shares no code with it and never calls it.
+ * with no fusion or reordering. The one blocked step is the draw of the
+ * corrected / bonus token: the pages fix only its law, and it is read here as
+ * a two-level race over blocks of tokens whose length is an argument (below).
+ * Only the test-suite, the smoke check and the benchmark's CPU-baseline leg
+ * load this file's library; the CUDA library shares no code with it and never
+ * calls it.
  *
  * Pages this follows (cited by title and section):
  *  [RU] "Как работает speculative decoding на уровне логитов, а не токенов?"
@@ -36,7 +39,10 @@
  *  - u_i = lane 0 of Philox(key = seed, counter = (i, b, 0, 0)), mapped to
  *    (32-bit word >> 8) * 2^-24, exact in float and double;
  *  - the pages draw the corrected token with a generic multinomial draw; it is
- *    read here as a two-level exponential race over blocks of 512 tokens.
+ *    read here as a two-level exponential race over blocks of L consecutive
+ *    tokens, L an argument of the verifier (the CUDA library uses L = 512, a
+ *    length picked for its kernels; the law below holds for every L, and
+ *    L >= V is the plain one-level race over per-token clocks).
  *    Level 1 races the blocks: block c = argmax over blocks with W_c > 0 of
  *    W_c / E_c, W_c the sum of w over the block, E_c = -ln v_c, v_c lane c mod 4
  *    of counter (j, b, 1 + c div 4, 1). Level 2 races the tokens of the winning
@@ -296,17 +302,21 @@ static void race_step(double w, double v, int64_t id, double* best, double* seco
     }
 }
 
-int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq, uint32_t pos,
-                        double* margin)
+int64_t svo_race_sample(const double* w, int64_t V, int64_t block, uint64_t seed, uint32_t seq,
+                        uint32_t pos, double* margin)
 {
-    const int64_t nblocks = (V + SVO_RACE_BLOCK - 1) / SVO_RACE_BLOCK;
     double best = -INFINITY, second = 0.0, gap1, gap2;
-    int64_t c, k, best_c = -1, best_k = -1, k0, k1;
+    int64_t nblocks, c, k, best_c = -1, best_k = -1, k0, k1;
+    if (block < 1) {
+        *margin = 0.0;
+        return -1;
+    }
+    nblocks = (V + block - 1) / block;
     /* Level 1: the blocks, each with the total weight of its tokens. */
     for (c = 0; c < nblocks; ++c) {
         double W = 0.0;
-        k0 = c * SVO_RACE_BLOCK;
-        k1 = k0 + SVO_RACE_BLOCK < V ? k0 + SVO_RACE_BLOCK : V;
+        k0 = c * block;
+        k1 = k0 + block < V ? k0 + block : V;
         for (k = k0; k < k1; ++k) W += w[k];
         if (W > 0.0) race_step(W, svo_block_uniform(seed, seq, pos, (uint32_t)c), c, &best, &second, &best_c);
     }
@@ -318,8 +328,8 @@ int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq,
     /* Level 2: the tokens of the winning block. */
     best = -INFINITY;
     second = 0.0;
-    k0 = best_c * SVO_RACE_BLOCK;
-    k1 = k0 + SVO_RACE_BLOCK < V ? k0 + SVO_RACE_BLOCK : V;
+    k0 = best_c * block;
+    k1 = k0 + block < V ? k0 + block : V;
     for (k = k0; k < k1; ++k)
         if (w[k] > 0.0) race_step(w[k], svo_race_uniform(seed, seq, pos, (uint32_t)k), k, &best, &second, &best_k);
     gap2 = (best - second) / best;
@@ -359,7 +369,7 @@ static void fail_sequence(int64_t b, int64_t K, int32_t status, int32_t* out_tok
 
 static void verify_sampling(const void* target, const void* draft, const int32_t* tokens,
                             int64_t b, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
-                            int64_t top_k, double top_p, int32_t* out_tokens,
+                            int64_t race_block, int64_t top_k, double top_p, int32_t* out_tokens,
                             int32_t* num_accepted, double* lse_t_out, double* lse_d_out,
                             double* log_ratio_out, double* accept_margin, double* sample_margin,
                             double* fm_t, double* fm_d, double* thr_out, double* lm_out,
@@ -470,12 +480,12 @@ static void verify_sampling(const void* target, const void* draft, const int32_t
         filtered_weights(trow0 + (size_t)K * V * esz, NULL, V, dtype, T, lse_t[K], thr[K], lm[K],
                          0.0, 0.0, 0.0, w);
     }
-    token = svo_race_sample(w, V, seed, (uint32_t)b, (uint32_t)j, &margin);
+    token = svo_race_sample(w, V, race_block, seed, (uint32_t)b, (uint32_t)j, &margin);
     if (token < 0) {
         /* Every residual weight rounded to zero: race p'_j instead. */
         filtered_weights(trow0 + (size_t)j * V * esz, NULL, V, dtype, T, lse_t[j], thr[j], lm[j],
                          0.0, 0.0, 0.0, w);
-        token = svo_race_sample(w, V, seed, (uint32_t)b, (uint32_t)j, &margin);
+        token = svo_race_sample(w, V, race_block, seed, (uint32_t)b, (uint32_t)j, &margin);
         margin = 0.0;
     }
     if (sample_margin) sample_margin[b] = margin;
@@ -538,25 +548,26 @@ static void verify_greedy(const void* target, const int32_t* tokens, int64_t b, 
 
 int svo_verify(const void* target, const void* draft, const int32_t* tokens,
                int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed, int mode,
-               int64_t b0, int64_t b1, int32_t* out_tokens, int32_t* num_accepted,
-               double* lse_t, double* lse_d, double* log_ratio,
+               int64_t race_block, int64_t b0, int64_t b1, int32_t* out_tokens,
+               int32_t* num_accepted, double* lse_t, double* lse_d, double* log_ratio,
                double* accept_margin, double* sample_margin, int32_t* seq_status)
 {
-    return svo_verify_filtered(target, draft, tokens, B, K, V, dtype, T, seed, mode, 0, 1.0, b0,
-                               b1, out_tokens, num_accepted, lse_t, lse_d, log_ratio,
+    return svo_verify_filtered(target, draft, tokens, B, K, V, dtype, T, seed, mode, race_block,
+                               0, 1.0, b0, b1, out_tokens, num_accepted, lse_t, lse_d, log_ratio,
                                accept_margin, sample_margin, NULL, NULL, NULL, NULL, seq_status);
 }
 
 int svo_verify_filtered(const void* target, const void* draft, const int32_t* tokens,
                         int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
-                        int mode, int64_t top_k, double top_p, int64_t b0, int64_t b1,
-                        int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
+                        int mode, int64_t race_block, int64_t top_k, double top_p, int64_t b0,
+                        int64_t b1, int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
                         double* lse_d, double* log_ratio, double* accept_margin,
                         double* sample_margin, double* filter_margin_t, double* filter_margin_d,
                         double* filter_thr, double* filter_log_mass, int32_t* seq_status)
 {
     int64_t b;
     if (!(top_p > 0.0 && top_p <= 1.0)) return -1;
+    if (race_block < 1) return -1;
     if (B < 0 || K < 0 || V < 1 || b0 < 0 || b1 > B || b0 > b1) return -1;
     if (dtype != SVO_F32 && dtype != SVO_BF16 && dtype != SVO_F64) return -1;
     if (mode != SVO_SAMPLE && mode != SVO_GREEDY) return -1;
@@ -566,8 +577,8 @@ int svo_verify_filtered(const void* target, const void* draft, const int32_t* to
     if (mode == SVO_SAMPLE && !(T > 0.0 && isfinite(T))) return -1;
     for (b = b0; b < b1; ++b) {
         if (mode == SVO_SAMPLE)
-            verify_sampling(target, draft, tokens, b, K, V, dtype, T, seed, top_k, top_p,
-                            out_tokens, num_accepted, lse_t, lse_d, log_ratio, accept_margin,
+            verify_sampling(target, draft, tokens, b, K, V, dtype, T, seed, race_block, top_k,
+                            top_p, out_tokens, num_accepted, lse_t, lse_d, log_ratio, accept_margin,
                             sample_margin, filter_margin_t, filter_margin_d, filter_thr,
                             filter_log_mass, seq_status);
         else

@@ -59,11 +59,6 @@ double svo_accept_prob(double log_p, double log_q);
 void svo_sample_weights(const void* target_row, const void* draft_row, int64_t V, int dtype,
                         double T, double lse_t, double lse_d, double* w);
 
-/* Tokens per block of the two-level race. The pages fix only the law of the
- * draw, which the race meets for any block length; this length is part of the
- * reading (it decides which random numbers are drawn). */
-#define SVO_RACE_BLOCK 512
-
 /* Race uniform of token k at emitted position `pos` of sequence `seq`: lane
  * k mod 4 of Philox4x32-10 with key (lo32(seed), hi32(seed)) and counter
  * (pos, seq, 1 + k div 4, 0), mapped to (2 (word >> 9) + 1) * 2^-24 in (0, 1). */
@@ -72,14 +67,22 @@ double svo_race_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t k);
 /* Race uniform of block c: as above with counter (pos, seq, 1 + c div 4, 1). */
 double svo_block_uniform(uint64_t seed, uint32_t seq, uint32_t pos, uint32_t c);
 
-/* Two-level exponential race over blocks of SVO_RACE_BLOCK tokens: the block
- * with the largest W_c / E_c (W_c = sum of w over the block), then the token of
- * that block with the largest w_k / E_k, E = -ln(uniform). The lowest index
- * wins exact ties. *margin gets the smaller of the two levels' relative gaps
- * (best - second) / best (1 when a level has one candidate, 0 when no weight
- * is positive). Returns -1 if no weight is positive. */
-int64_t svo_race_sample(const double* w, int64_t V, uint64_t seed, uint32_t seq, uint32_t pos,
-                        double* margin);
+/* Two-level exponential race over blocks of `block` consecutive tokens (the
+ * last block may be shorter): the block with the largest W_c / E_c (W_c = sum
+ * of w over the block), then the token of that block with the largest
+ * w_k / E_k, E = -ln(uniform). The lowest index wins exact ties. *margin gets
+ * the smaller of the two levels' relative gaps (best - second) / best (1 when
+ * a level has one candidate, 0 when no weight is positive). Returns -1 if no
+ * weight is positive or block < 1.
+ *
+ * The draw follows w / Z for every block length: level 1 picks block c with
+ * probability W_c / Z and level 2 token k of it with probability w_k / W_c,
+ * from disjoint clocks. With block >= V there is one block, and the draw is
+ * the plain one-level race argmax_k w_k / E_k over the per-token clocks. The
+ * length only decides which random numbers are used, so it is a parameter of
+ * the reading, passed in by the caller. */
+int64_t svo_race_sample(const double* w, int64_t V, int64_t block, uint64_t seed, uint32_t seq,
+                        uint32_t pos, double* margin);
 
 /* Lowest index attaining the maximum of the raw row; *has_nan set to 1 when the
  * row holds a NaN (the index is then meaningless). */
@@ -97,12 +100,14 @@ int64_t svo_row_argmax(const void* row, int64_t V, int dtype, int* has_nan);
  *                         race's two levels (0 when the zero-residual fall-back
  *                         fired; NaN in greedy)
  *   seq_status [B]
+ * race_block (>= 1) is the block length of the corrected / bonus token's race
+ * (svo_race_sample); the CUDA library draws with 512.
  * Returns 0, or -1 on an invalid argument.
  */
 int svo_verify(const void* target, const void* draft, const int32_t* tokens,
                int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed, int mode,
-               int64_t b0, int64_t b1, int32_t* out_tokens, int32_t* num_accepted,
-               double* lse_t, double* lse_d, double* log_ratio,
+               int64_t race_block, int64_t b0, int64_t b1, int32_t* out_tokens,
+               int32_t* num_accepted, double* lse_t, double* lse_d, double* log_ratio,
                double* accept_margin, double* sample_margin, int32_t* seq_status);
 
 /*
@@ -128,8 +133,8 @@ int svo_filter_row(const void* row, int64_t V, int dtype, double T, double lse, 
  */
 int svo_verify_filtered(const void* target, const void* draft, const int32_t* tokens,
                         int64_t B, int64_t K, int64_t V, int dtype, double T, uint64_t seed,
-                        int mode, int64_t top_k, double top_p, int64_t b0, int64_t b1,
-                        int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
+                        int mode, int64_t race_block, int64_t top_k, double top_p, int64_t b0,
+                        int64_t b1, int32_t* out_tokens, int32_t* num_accepted, double* lse_t,
                         double* lse_d, double* log_ratio, double* accept_margin,
                         double* sample_margin, double* filter_margin_t, double* filter_margin_d,
                         double* filter_thr, double* filter_log_mass, int32_t* seq_status);

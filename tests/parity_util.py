@@ -2,8 +2,10 @@
 
 Bit-exact where the method is discrete (accepted counts, tokens, argmaxes,
 status), except for decisions the oracle flags as near-ties: an acceptance
-draw with |u - r| < 1e-5 or a sampling draw within 1e-5 * Z of an edge of the
-chosen token's CDF interval. A flagged sequence is compared exactly up to its
+draw with |u - r| < 1e-5, or a sampling draw whose two-level exponential race
+(blocks of 512 tokens) has, at either level, a relative gap
+(best - second) / best below 1e-5 between its two largest scores w / E. A
+flagged sequence is compared exactly up to its
 first flagged decision; past it, either branch is correct, so the GPU output
 is only checked to be a valid verification result. Normalisers and
 log-ratios must agree to 1e-5 relative (absolute below magnitude 1).

@@ -31,7 +31,12 @@ MUTANTS = {
     "block_race_shares_token_stream": ("ctr[2] = 1u + (c >> 2); ctr[3] = 1;",
                                        "ctr[2] = 1u + (c >> 2); ctr[3] = 0;"),
     "block_weight_ignored": ("if (W > 0.0) race_step(W,", "if (W > 0.0) race_step(1.0,"),
-    "level2_races_wrong_block": ("k0 = best_c * SVO_RACE_BLOCK;", "k0 = 0;"),
+    "level2_races_wrong_block": ("k0 = best_c * block;", "k0 = 0;"),
+    "level2_block_start_shifted": ("k0 = best_c * block;", "k0 = best_c * block + 1;"),
+    "block_weight_skips_first_token": ("for (k = k0; k < k1; ++k) W += w[k];",
+                                       "for (k = k0 + 1; k < k1; ++k) W += w[k];"),
+    "block_length_fixed": ("nblocks = (V + block - 1) / block;",
+                           "block = 512;\n    nblocks = (V + block - 1) / block;"),
     "temperature_dropped_in_max": ("double s = svo_elem(row, k, dtype) / T;",
                                    "double s = svo_elem(row, k, dtype);"),
     "lse_shift_sign": ("acc += exp(svo_elem(row, k, dtype) / T - m);",

@@ -293,6 +293,111 @@ def test_two_level_race_law(oracle_mod):
     assert stats.chisquare(counts, w[picks] / w.sum() * n).pvalue > 1e-3
 
 
+def _plain_race(o, w, seed, seq, pos):
+    """A one-level exponential race written out here, independently of the
+    oracle's race: token = argmax over w_k > 0 of w_k / E_k, E_k = -ln v_k, v_k
+    from lane k mod 4 of Philox4x32-10 at counter (pos, seq, 1 + k div 4, 0)
+    mapped to (2 (word >> 9) + 1) 2^-24; the lowest index wins an exact tie.
+    Only the Philox words come from the oracle (``philox_many``, itself pinned
+    against triton's generator). Returns (token, relative top-2 gap)."""
+    V = len(w)
+    n = (V + 3) // 4
+    ctr = np.zeros((n, 4), dtype=np.uint32)
+    ctr[:, 0] = pos
+    ctr[:, 1] = seq
+    ctr[:, 2] = 1 + np.arange(n)
+    words = o.philox_many(ctr, [seed & 0xFFFFFFFF, seed >> 32]).reshape(-1)[:V]
+    best, second, tok = -math.inf, 0.0, -1
+    for k in range(V):
+        if w[k] > 0.0:
+            v = (2.0 * float(int(words[k]) >> 9) + 1.0) * 2.0 ** -24
+            score = w[k] / -math.log(v)
+            if score > best:
+                if tok >= 0:
+                    second = best
+                best, tok = score, k
+            elif score > second:
+                second = score
+    return tok, ((best - second) / best if tok >= 0 else 0.0)
+
+
+@pytest.mark.parametrize("V", [1, 5, 300, 2000])
+def test_race_one_block_is_the_plain_race(oracle_mod, V):
+    """With one block (block length >= V) the two-level race is the plain
+    one-level race argmax_k w_k / E_k: same token, same margin, seed by seed."""
+    rng = np.random.default_rng(V + 5)
+    w = rng.gamma(0.6, size=V)
+    if V > 2:
+        w[rng.choice(V, size=V // 4, replace=False)] = 0.0
+    for block in (V, V + 3, 4096):
+        for seq in range(150):
+            want, gap = _plain_race(oracle_mod, w, 4242 + seq, seq, 3)
+            got, margin = oracle_mod.race_sample(w, 4242 + seq, seq, 3, block=block)
+            assert got == want, (block, seq)
+            # level 1 has a single candidate (margin 1), so the margin is level 2's gap
+            assert margin == pytest.approx(gap, rel=1e-12, abs=1e-300), (block, seq)
+
+
+@pytest.mark.parametrize("block", [1, 7, 512, 1100])
+def test_two_level_race_law_any_block(oracle_mod, block):
+    """The draw follows w / Z whatever the block length: 1 (level 1 alone),
+    7 (many blocks, a ragged last block of one token), 512 (the library's
+    length, a ragged last block) and V (one block). Chi-square of the tokens,
+    pooled into cells of >= 50 expected draws, and of the blocks."""
+    from scipy import stats
+    V = 1100
+    rng = np.random.default_rng(block)
+    w = rng.gamma(0.5, size=V)
+    w[rng.choice(V, size=200, replace=False)] = 0.0
+    w[V - 1] = 3.0 * w.max()  # the last token alone in a ragged block for block 7
+    n = 30_000
+    toks = np.array([oracle_mod.race_sample(w, 555, b, 1, block=block)[0] for b in range(n)])
+    assert toks.min() >= 0 and np.all(w[toks] > 0)
+    counts = np.bincount(toks, minlength=V)
+    exp = w / w.sum() * n
+    keep = w > 0
+    order = np.argsort(exp[keep])
+    grp = (np.cumsum(exp[keep][order]) // 50).astype(int)
+    c2 = np.bincount(grp, weights=counts[keep][order])
+    e2 = np.bincount(grp, weights=exp[keep][order])
+    nz = e2 > 0
+    assert stats.chisquare(c2[nz], e2[nz] * c2[nz].sum() / e2[nz].sum()).pvalue > 1e-3
+    nb = (V + block - 1) // block
+    if 1 < nb <= 200:
+        W = np.add.reduceat(w, np.arange(0, V, block))
+        cb = np.bincount(toks // block, minlength=nb)
+        eb = W / W.sum() * n
+        ok = eb > 0
+        assert cb[~ok].sum() == 0
+        assert stats.chisquare(cb[ok], eb[ok] * cb[ok].sum() / eb[ok].sum()).pvalue > 1e-3
+
+
+def test_verify_one_block_draws_the_plain_race(oracle_mod):
+    """The verifier with race_block >= V emits, at position j, the token of the
+    plain one-level race over its own weights (max(0, p - q) after a rejection,
+    p of the bonus row otherwise), clocks keyed by (j, b)."""
+    o = oracle_mod
+    rng = np.random.default_rng(8)
+    B, K, V, T, seed = 60, 3, 600, 0.8, 0xABCDEF12345
+    t = (rng.normal(size=(B, K + 1, V)) * 1.5).astype(np.float32)
+    d = (t[:, :K] + rng.normal(size=(B, K, V)).astype(np.float32)).astype(np.float32)
+    tok = draw_tokens(rng, softmax64(d, T))
+    res = o.verify(t, d, tok, T, seed, race_block=V)
+    res512 = o.verify(t, d, tok, T, seed)
+    np.testing.assert_array_equal(res["num_accepted"], res512["num_accepted"])
+    Tf = float(np.float32(T))
+    for b in range(B):
+        j = int(res["num_accepted"][b])
+        lse_t = res["lse_t"][b, j]
+        if j < K:
+            w = o.sample_weights(t[b, j], d[b, j], Tf, lse_t, res["lse_d"][b, j])
+        else:
+            w = o.sample_weights(t[b, K], None, Tf, lse_t, 0.0)
+        want, gap = _plain_race(o, w, seed, b, j)
+        assert res["out_tokens"][b, j] == want, b
+        assert res["sample_margin"][b] == pytest.approx(gap, rel=1e-12, abs=1e-300)
+
+
 def test_block_uniforms_are_their_own_stream(oracle_mod):
     b = np.array([oracle_mod.block_uniform(3, s, 1, c) for s in range(500) for c in range(8)])
     t = np.array([oracle_mod.race_uniform(3, s, 1, c) for s in range(500) for c in range(8)])
