@@ -213,7 +213,9 @@ int spec_verify_host(const void* h_target_logits, const void* h_draft_logits,
  * before any stream capture. All calls share the one array: two calls whose
  * work overlaps on the GPU (different streams, no ordering between them) race
  * on it. The array keeps the last call's contents; nothing in it needs to
- * start at zero.
+ * start at zero. The looked-up address is kept for the life of the process:
+ * after cudaDeviceReset on a device, unload and reload the library before
+ * calling this entry point on that device again.
  */
 int spec_verify_static(const void* target_logits, const void* draft_logits,
                        const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,

@@ -34,7 +34,11 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_scratch on the current device; the first call on each
-// device does the lookup.
+// device does the lookup. The cached address belongs to the device's primary
+// context as it was at that lookup: after cudaDeviceReset (or anything else
+// that destroys and recreates the primary context) the library's module is
+// loaded again at a new address, so the library must be unloaded and loaded
+// again before spec_verify_static is called on that device.
 int scratch_address(void** out)
 {
     int dev = 0;
@@ -67,9 +71,10 @@ SV_EXPORT int spec_verify_static(const void* target_logits, const void* draft_lo
     void* scratch = nullptr;
     rc = scratch_address(&scratch);
     if (rc != SV_OK) return rc;
-    // Nothing in the scratch has to start at zero: every pass writes what the
-    // next one reads before it is read, and the last-CTA counters are reset by
-    // the scan kernel in the same call.
+    // Nothing in the scratch has to start at zero: spec_verify writes every
+    // region of its workspace (pass-1 partials, sequence records, race-block
+    // sums) before it reads it within the same call, and it keeps no counters
+    // there.
     return spec_verify(target_logits, draft_logits, draft_tokens, B, K, V, dtype, temperature,
                        seed, mode, out_tokens, num_accepted, scratch, kStaticScratchBytes, stream);
 }

@@ -99,3 +99,40 @@ def compare(gpu: dict, orc: dict, tokens: np.ndarray, K: int, V: int, rows=None,
             assert np.array_equal(og, oo), f"seq {b}: tokens gpu {og} oracle {oo}"
     return {"decisions": n_dec, "flagged_decisions": n_flag_dec, "flagged_sequences": n_flag_seq,
             "flagged_differing": n_flag_diff}
+
+
+# The parity rule's budget for near-ties: under 0.01% of decisions.
+FLAG_BUDGET = 1e-4
+
+
+def oracle_flag_counts(orc: dict, K: int, flag=FLAG) -> tuple:
+    """(decisions, flagged) over every decision the oracle took, counting each
+    flagged decision (not only a sequence's first): the acceptance draws at
+    positions 0 .. min(j, K - 1) and the one draw of the emitted token.
+    Invalid sequences take no decision."""
+    ok = orc["seq_status"] == 0
+    j = orc["num_accepted"][ok].astype(np.int64)
+    am = orc["accept_margin"][ok]
+    taken = np.arange(K)[None, :] <= np.minimum(j, K - 1)[:, None] if K > 0 else \
+        np.zeros((len(j), 0), dtype=bool)
+    n_acc = int(taken.sum())
+    f_acc = int((taken & (am < flag)).sum())
+    f_smp = int((orc["sample_margin"][ok] < flag).sum())
+    return n_acc + len(j), f_acc + f_smp
+
+
+def flag_count_plausible(flagged: int, decisions: int, budget=FLAG_BUDGET, alpha=1e-6) -> bool:
+    """True unless ``flagged`` near-ties in ``decisions`` would be implausible
+    (one-sided binomial tail below ``alpha``) at a flag rate of ``budget``."""
+    from scipy import stats
+    if flagged == 0:
+        return True
+    return bool(stats.binom.sf(flagged - 1, decisions, budget) >= alpha)
+
+
+def flag_rate_upper_bound(flagged: int, decisions: int, conf=0.99) -> float:
+    """One-sided Clopper-Pearson upper confidence bound of a binomial rate."""
+    from scipy import stats
+    if flagged >= decisions:
+        return 1.0
+    return float(stats.beta.ppf(conf, flagged + 1, decisions - flagged))

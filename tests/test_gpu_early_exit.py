@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import speculative_decoding_verification_66_gb300 as sv
-from parity_util import compare
+from parity_util import compare, flag_count_plausible
 from speculative_decoding_verification_66_gb300.workloads import (WORKLOADS, make_inputs,
                                                                    to_host_arrays)
 
@@ -80,7 +80,7 @@ SIZES = {
 def test_early_exit_parity(name, seed):
     wl = WORKLOADS[name].resized(**SIZES[name])
     st = check(wl, seed)
-    assert st["flagged_decisions"] <= max(2, 1e-3 * st["decisions"]), st
+    assert flag_count_plausible(st["flagged_decisions"], st["decisions"]), st
 
 
 @pytest.mark.parametrize("name", ["llama3_bf16", "qwen_long_bf16", "greedy_bf16"])

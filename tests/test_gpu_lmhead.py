@@ -64,7 +64,16 @@ def _greedy_compare(gpu, host, lw, rows):
         f = near[0]
         assert ng >= min(f, no) and np.array_equal(og[:f], oo[:f]), (b, og, oo)
         assert valid_output(og, ng, tok[b], K, V), (b, og)
-    return {"flagged_sequences": flagged}
+    return {"flagged_sequences": flagged, "sequences": len(rows)}
+
+
+def _greedy_flag_cap(n):
+    """Most greedy near-ties a check of n sequences may flag. A row's top-2
+    gap falls below GREEDY_GAP with probability of a few 1e-3 for these
+    logit scales (spacing of the top order statistics about sigma / sqrt(2 ln V)),
+    so 2 + 2% of the sequences leaves room for the spread and still catches a
+    systematic greedy error near ties."""
+    return 2 + n // 50
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -126,15 +135,22 @@ def _check(lw, seed, seq_ranges=None, inp=None):
     gpu = {k: v.cpu().numpy() for k, v in gpu.items()}
     host = lm_host_arrays(inp)
     st = None
+    g_flagged = g_seqs = 0
     for rng in (seq_ranges or [None]):
         rows = range(lw.B) if rng is None else range(*rng)
         if greedy:
-            st = _greedy_compare(gpu, host, lw, rows) if lw.B > 0 else None
+            if lw.B > 0:
+                st = _greedy_compare(gpu, host, lw, rows)
+                g_flagged += st["flagged_sequences"]
+                g_seqs += st["sequences"]
             continue
         orc = oracle.verify_lmhead(*host[:4], host[4], lw.temperature, s, oracle.SAMPLE,
                                    seq_range=rng, threads=8)
         st = compare(gpu, orc, host[4], lw.K, lw.V, rows=rows, greedy=False, flag=FLAG_LM,
                      rtol=RTOL_LM)
+    if greedy and g_seqs > 0:
+        print(f"greedy near-ties: {g_flagged} of {g_seqs} sequences flagged")
+        assert g_flagged <= _greedy_flag_cap(g_seqs), (g_flagged, g_seqs)
     # The plain call gives the same tokens as the diagnostic one.
     out, nacc = _lm_call(inp, lw, s)
     torch.cuda.synchronize()

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import speculative_decoding_verification_66_gb300 as sv
-from parity_util import compare
+from parity_util import compare, flag_count_plausible
 from speculative_decoding_verification_66_gb300.workloads import (WORKLOADS, make_inputs,
                                                                    to_host_arrays)
 
@@ -58,7 +58,7 @@ def test_sharded_parity(name, G):
     size = {"greedy_bf16": {"B": 24, "V": 32000}}.get(name, {})
     wl = WORKLOADS[name].resized(**size)
     st = check(wl, G, 3)
-    assert st["flagged_decisions"] <= max(2, 1e-3 * st["decisions"]), st
+    assert flag_count_plausible(st["flagged_decisions"], st["decisions"]), st
 
 
 def test_sharded_headline_shapes():

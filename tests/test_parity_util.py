@@ -68,3 +68,30 @@ def test_valid_output_rules():
     assert not valid_output(np.array([3, 9, 2, -1]), 1, x, 3, 10)
     assert not valid_output(np.array([4, 9, -1, -1]), 1, x, 3, 10)
     assert not valid_output(np.array([3, 10, -1, -1]), 1, x, 3, 10)
+
+
+def test_oracle_flag_counts_counts_every_taken_decision():
+    from parity_util import oracle_flag_counts
+    orc = {
+        "seq_status": np.array([0, 0, 1]),
+        "num_accepted": np.array([1, 3, -1]),
+        # seq 0 takes positions 0, 1 (1 is the rejection); seq 1 takes 0, 1, 2
+        "accept_margin": np.array([[0.5, FLAG / 2, FLAG / 3],
+                                   [FLAG / 2, 0.5, FLAG / 4],
+                                   [0.0, 0.0, 0.0]]),
+        "sample_margin": np.array([FLAG / 2, 0.5, 0.0]),
+    }
+    n, f = oracle_flag_counts(orc, 3)
+    assert n == (2 + 1) + (3 + 1)
+    assert f == 1 + 1 + 2  # seq 0: position 1 and the draw; seq 1: positions 0 and 2
+
+
+def test_flag_budget_bounds():
+    from parity_util import flag_count_plausible, flag_rate_upper_bound
+    assert flag_count_plausible(0, 10) and flag_count_plausible(1, 100)
+    assert not flag_count_plausible(3, 100)          # 3 in 100 at rate 1e-4: p ~ 1.6e-7
+    assert flag_count_plausible(30, 300_000)         # mean 30 at the budget
+    assert not flag_count_plausible(80, 300_000)
+    ub = flag_rate_upper_bound(5, 300_000)
+    assert 5 / 300_000 < ub < 1e-4
+    assert flag_rate_upper_bound(40, 300_000) > 1e-4
