@@ -1321,7 +1321,10 @@ cudaError_t launch_filter(const FilterArgs& a, int grid, cudaStream_t s)
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kFilterSmem));
     if (e != cudaSuccess) return e;
-    return launch_dependent(a.g.pdl != 0, k, dim3(static_cast<unsigned>(grid)), dim3(kFilterThreads),
+    // The first kernel of a call: launched without programmatic dependent
+    // launch, so the caller's earlier work on the stream (the logits) is
+    // complete and visible before the first read.
+    return launch_dependent(false, k, dim3(static_cast<unsigned>(grid)), dim3(kFilterThreads),
                             kFilterSmem, s, a);
 }
 
