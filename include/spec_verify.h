@@ -322,8 +322,10 @@ int sv_filtered_workspace_bytes(int64_t B, int64_t K, int64_t V, int dtype, int 
  * Thresholds are exact (integer work on the logits' order); the top-p
  * boundary's masses are 64-bit fixed point, so a boundary that the exact
  * masses put within 1e-5 of top_p (relative to the top-k mass) may fall on
- * the other side. Not combined with early exit or sharded logits. Calls make
- * 4 launches: thresholds, scan, and the two sampler launches.
+ * the other side. Rows must hold fewer than 2^22 logits (SV_ERR_SIZE
+ * otherwise: the 2^40-scaled mass sums of longer rows could overflow 64 bits).
+ * Not combined with early exit or sharded logits. Calls make 4 launches:
+ * thresholds, scan, and the two sampler launches.
  */
 int spec_verify_filtered(const void* target_logits, const void* draft_logits,
                          const int32_t* draft_tokens, int64_t B, int64_t K, int64_t V, int dtype,

@@ -18,8 +18,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libspecverify.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
-SOURCES = ["row_stats.cu", "scan.cu", "sample.cu", "filter.cu", "lmhead.cu", "sv_api.cu", "sv_static.cu",
-           "philox.cu"]
+SOURCES = ["row_stats.cu", "scan.cu", "sample.cu", "filter.cu", "hist.cu", "lmhead.cu", "sv_api.cu",
+           "sv_static.cu", "philox.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -1315,8 +1315,10 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
 
 }  // namespace
 
-cudaError_t launch_filter(const FilterArgs& a, int grid, cudaStream_t s)
+cudaError_t launch_filter(const FilterArgs& a, int grid, int sms, cudaStream_t s)
 {
+    const bool tk = a.top_k > 0 && a.top_k < a.g.V;
+    if (a.g.es == 2 && (!tk || a.top_k > kSortK)) return launch_hist(a, sms, s);
     auto* k = a.g.es == 2 ? filter_kernel<2> : filter_kernel<4>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kFilterSmem));

@@ -267,6 +267,9 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
     if (rc != SV_OK) return rc;
     if (workspace_bytes < L.total) return SV_ERR_WORKSPACE;
     if (filtered && (early_exit || G > 1)) return SV_ERR_ARG;
+    // The thresholds kernels' fixed-point mass sums (2^40 per token at most)
+    // hold rows below 2^22 tokens.
+    if (filtered && V >= (int64_t(1) << 22)) return SV_ERR_SIZE;
     // Events between the kernels would sit between programmatically chained
     // launches; the timed variant launches them one after the other instead.
     g.pdl = events == nullptr ? 1 : 0;
@@ -318,11 +321,13 @@ int run(const void* target, const void* draft, const int32_t* tokens, int64_t B,
         const int64_t cap = filter_blocks(g.es);
         if (cap <= 0) return SV_ERR_CUDA;
         const int grid = static_cast<int>(g.rows < cap ? g.rows : cap);
+        int sms = 0, blocks = 0, sample_blocks = 0;
+        if (device_limits(g.es, mode, &sms, &blocks, &sample_blocks) != SV_OK) return SV_ERR_CUDA;
         sv::FilterArgs fa{tp, dp, g, c, top_k, top_p, filt, gate_stage == 1 ? gate : nullptr};
         sa.filt = filt;
         pa.filtered = 1;
         if (!record(0)) return SV_ERR_CUDA;
-        if (sv::launch_filter(fa, grid, s) != cudaSuccess) return SV_ERR_CUDA;
+        if (sv::launch_filter(fa, grid, sms, s) != cudaSuccess) return SV_ERR_CUDA;
         if (!record(1)) return SV_ERR_CUDA;
         if (sv::launch_scan(sa, s) != cudaSuccess) return SV_ERR_CUDA;
         if (!record(2)) return SV_ERR_CUDA;

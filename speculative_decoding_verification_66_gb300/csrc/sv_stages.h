@@ -139,7 +139,11 @@ struct LmArgs {
 cudaError_t launch_scan(const ScanArgs& a, cudaStream_t s);
 cudaError_t launch_sample(const SampleArgs& a, cudaStream_t s);
 cudaError_t launch_gather_pairs(const GatherArgs& a, cudaStream_t s);
-cudaError_t launch_filter(const FilterArgs& a, int grid, cudaStream_t s);
+// The thresholds: bfloat16 rows cut by top-p alone or by top-k with k > 64 go
+// to the value-count kernel (hist.cu, one CTA on each of `sms` SMs); every
+// other cut to the group-maxima kernel (filter.cu, `grid` CTAs).
+cudaError_t launch_filter(const FilterArgs& a, int grid, int sms, cudaStream_t s);
+cudaError_t launch_hist(const FilterArgs& a, int sms, cudaStream_t s);
 // Resident filter CTAs per SM.
 cudaError_t filter_blocks_per_sm(int es, int* blocks);
 // The LM head; *mapped = false when a tensor map could not be made (nothing

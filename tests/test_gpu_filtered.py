@@ -14,8 +14,8 @@ import torch
 import oracle
 import speculative_decoding_verification_66_gb300 as sv
 from parity_util import compare
-from speculative_decoding_verification_66_gb300.workloads import (WORKLOADS, make_inputs,
-                                                                   to_host_arrays)
+from speculative_decoding_verification_66_gb300.workloads import (WORKLOADS, draw_from_logits,
+                                                                   make_inputs, to_host_arrays)
 
 pytestmark = pytest.mark.gpu
 THREADS = max(1, min(16, os.cpu_count() or 1))
@@ -200,6 +200,29 @@ def test_filtered_many_ties_at_the_top(top_k, top_p):
         inputs[key][:, :, 1000:11000] = inputs[key].float().amax(dim=-1, keepdim=True).to(
             inputs[key].dtype)
     st, g, orc = check(wl, 23, top_k, top_p, device_inputs=inputs)
+    assert (g["num_accepted"] >= 0).all()
+
+
+@pytest.mark.parametrize("fill", ["max", "-inf", "-5"])
+@pytest.mark.parametrize("top_k,top_p", [(0, 0.9), (100, 1.0), (150000, 0.95), (2000, 0.8)])
+def test_filtered_value_shared_by_2_16_tokens(fill, top_k, top_p):
+    """bfloat16 rows where 70000 tokens share one value (the row maximum, -inf
+    or -5): a 16-bit count of that value wraps, the wrap shows in the sum of
+    all counts, and the row is counted again with 32-bit counts; top-k up to
+    almost V reaches into the shared value from above and below."""
+    wl = WORKLOADS["qwen_long_bf16"].resized(B=2, K=2)
+    inputs = make_inputs(wl, 29, "cuda", top_k=top_k, top_p=top_p)
+    for key in ("target", "draft"):
+        x = inputs[key]
+        if fill == "max":
+            v = x.float().amax(dim=-1, keepdim=True).to(x.dtype)
+        else:
+            v = torch.full_like(x[..., :1], float(fill))
+        x[..., 50000:120000] = v
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(29)
+    inputs["tokens"] = draw_from_logits(inputs["draft"], wl.temperature, gen, top_k, top_p)
+    st, g, orc = check(wl, 29, top_k, top_p, device_inputs=inputs)
     assert (g["num_accepted"] >= 0).all()
 
 
