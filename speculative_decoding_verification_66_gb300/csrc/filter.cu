@@ -9,6 +9,10 @@
 // whose upper set {x >= v} holds at least top_p of the top-k set's mass. Both
 // cuts are thresholds on the logit value: equal logits stay together.
 //
+// This kernel takes top-k up to 64 (with or without top-p) for both dtypes,
+// and every cut of float32 rows; bfloat16 rows cut by top-p alone or by top-k
+// above 64 go to the value-count kernel (hist.cu).
+//
 // Design: one CTA per row (a persistent grid walks the rows). The exact
 // thresholds come from a radix select over 32-bit order-preserving keys of
 // the widened logits, 8 bits per level, with shared-memory histograms of

@@ -14,26 +14,34 @@
 // A bfloat16 logit is one of 2^16 values, so the count of every value orders
 // the whole row: the k-th largest logit, and the mass of every upper set, and
 // with it the top-p threshold, follow from the counts alone. One read of the
-// row (from HBM, each element once) builds them in shared memory: 2^15 words,
-// word g holding the count of +g in its low half and of -g in its high half
-// (g the 15 magnitude bits), two shared-memory reductions per pair of
-// elements, with a packed maximum for the row maximum and the NaN / +inf
-// check. A sweep over the table then gives each thread's 32 magnitudes their
-// counts and masses (one exponential per value present, not per element), a
-// block-wide scan in value order finds the 32 magnitudes that hold each
-// crossing, and one warp walks them to the exact threshold.
+// row (from HBM, each element once) counts its values in shared memory, two
+// shared-memory reductions per pair of elements plus a packed maximum (the row
+// maximum, and the NaN / +inf check). The table is a window of 2^14 words over
+// the magnitudes of 128 binades, 2^-64 <= |x| < 2^64, word g holding the count
+// of +g in its low half and of -g in its high half; two more words count the
+// magnitudes below the window (zeros, mostly) and above it (-inf, mostly).
+// Two CTAs share an SM, so that one's selection runs while the other counts
+// (the counting is bound by the SM's shared-memory atomics).
 //
-// A 16-bit count wraps only when 2^16 elements share one value; each wrap
-// takes 2^16 - 1 (low half) or 2^16 (high half) from the sum of all counts,
-// so the sum equals V exactly when nothing wrapped. A row where it does not
-// (a large masked vocabulary, say) is counted again with one 32-bit count per
-// magnitude, one sign per read, read from L2.
+// The selection: the 2^10 segments of 32 magnitudes of each sign get their
+// counts and masses (one exponential per value present, not per element); a
+// block-wide scan in value order finds the segment that holds each crossing,
+// and one warp walks it to the exact threshold.
+//
+// Three things send a row to a slower exact path that counts it again, with
+// one 32-bit count per magnitude, in four reads (one sign and half of the
+// magnitudes each, from L2): a 16-bit count that wrapped (2^16 elements share
+// a value; each wrap takes 2^16 - 1 or 2^16 from the sum of all counts, so the
+// sum equals V exactly when nothing wrapped), a crossing among the values
+// outside the window, or a row maximum of 2^64 or more.
 //
 // Masses are integers, so every sum -- and every decision -- is the same on
-// every run: a value's mass is 2^(x c - m) 2^40 rounded (m the ceiling of the
-// row maximum times c), times its count. The rounding (below 2^-41 of the
-// largest mass) and the SFU exponential (a few ulp per value) move a top-p
-// boundary by well under 1e-5 of the mass.
+// every run: the mass of a value's n tokens is n 2^(x c - m) on a grid of
+// 2^-40 (m the ceiling of the row maximum times c), the bits below the grid
+// dropped; a value below the window has the mass of 0, one above it (below
+// -2^64) none. The truncation (below 2^-40 of the largest mass, per value)
+// and the SFU exponential (a few ulp per value) move a top-p boundary by well
+// under 1e-5 of the mass.
 #include <cuda_bf16.h>
 
 #include "sv_device.cuh"
@@ -42,33 +50,38 @@
 namespace sv {
 namespace {
 
-constexpr int kHT = 1024;                    // threads (32 warps)
+constexpr int kHT = 512;                     // threads (16 warps); two CTAs per SM
 constexpr int kHW = kHT / 32;
-constexpr int kMags = 32768;                 // table words: one per bfloat16 magnitude
-constexpr int kWPT = kMags / kHT;            // words per thread in the table sweeps
-static_assert(kWPT == 32, "the crossing walk takes one word per lane");
+constexpr uint32_t kG0 = 63u * 128u;         // first magnitude of the window (2^-64)
+constexpr int kWin = 16384;                  // magnitudes in the window
+constexpr int kSegs = 1024;                  // segments of 32 magnitudes, per sign
 constexpr int kHU = 8;                       // 16-byte loads in flight per thread
-// Dynamic shared memory: the table (128 KB), then the sums of every
-// segment of 32 magnitudes (counts and masses of each sign, 24 KB).
-constexpr int kSegs = kMags / 32;
-constexpr int kHSmem = kMags * 4 + kSegs * (4 + 8 + 4 + 8);
-constexpr float kFixH = 1099511627776.0f;    // 2^40
 
-// What the table holds: both signs in 16-bit halves, or one 32-bit count per
-// magnitude for the positive values (with -0 as +0) or the negative ones.
-enum { kPacked = 0, kPos32 = 1, kNeg32 = 2 };
+// Dynamic shared memory: 16 bytes whose last word counts the magnitudes below
+// the window, the window (64 KB), 16 bytes whose first word counts those
+// above it, then the sums of every segment (counts and masses of each sign).
+constexpr int kTabBytes = 16 + kWin * 4 + 16;
+constexpr int kHSmem = kTabBytes + kSegs * (4 + 8 + 4 + 8);
+
+// What the table holds: the window, both signs in 16-bit halves; or 32-bit
+// counts of one sign and half of the magnitudes (kQ0 + 2 sign + half), with
+// -0 counted as +0.
+enum { kPacked = -1, kQ0 = 0, kQ1 = 1, kQ2 = 2, kQ3 = 3 };
 
 struct HScratch {
     float wmax[kHW];
+    uint32_t sum_c[kHW];           // block_sum2's per-warp sums (its own slots: the
+    uint64_t sum_m[kHW];           // scan that follows writes wcp / wmp at once)
     uint32_t wcp[kHW], wcn[kHW];   // per-warp totals, then what lies before each warp
     uint64_t wmp[kHW], wmn[kHW];
     uint32_t tot_pc, tot_nc;       // all positive / negative counts and masses
     uint64_t tot_pm, tot_nm;
-    int seg;              // the crossing's 32 magnitudes: thread index, + kHT if negative
-    uint32_t seg_c;       // count before them (in value order)
-    uint64_t seg_m;       // mass before them
-    float tau;            // the threshold found by the walk
+    int seg[2];           // the crossing's segment (top-k, top-p): index, + kSegs if negative; -1 none
+    uint32_t seg_c[2];    // count before it (in value order)
+    uint64_t seg_m[2];    // mass before it
+    float tau;            // the threshold found by the walk or the scan
     uint64_t through;     // mass of the upper set {x >= tau}
+    int found;            // the scan: 0 not yet, 1 found, 2 in an outer word
     int fail;
 };
 
@@ -94,10 +107,18 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p)
     return v;
 }
 
-// Fixed-point mass of one token: 2^(x c - m) 2^40, rounded.
-__device__ __forceinline__ uint64_t mass_fix(float x, float c, float m)
+// Fixed-point mass of n tokens of logit x: n 2^(x c - m) in units of 2^-40,
+// from the bits of the float y = 2^(x c - m) <= 1 (x at most the row maximum):
+// its 24-bit significand times n, shifted to the 2^-40 grid (the part below
+// it dropped). Integer work only, after the exponential.
+__device__ __forceinline__ uint64_t mass_n(uint32_t n, float x, float c, float m)
 {
-    return __float2ull_rn(ex2(fmaf(x, c, -m)) * kFixH);
+    const uint32_t b = __float_as_uint(ex2(fmaf(x, c, -m)));
+    const int e = static_cast<int>(b >> 23);  // biased; 0 for a flushed subnormal or 0
+    const uint64_t f = static_cast<uint64_t>(n) * ((b & 0x7FFFFFu) | (e ? 0x800000u : 0u));
+    // y = f 2^(e - 150), so y 2^40 = f 2^(e - 110).
+    const int sh = e - 110;
+    return sh >= 0 ? f << sh : (sh > -64 ? f >> -sh : 0u);
 }
 
 // ceil(top_p * mass) for top_p in (0, 1), exactly, in integer arithmetic:
@@ -122,72 +143,106 @@ __device__ __forceinline__ uint64_t ceil_frac(float top_p, uint64_t mass)
     return q + (rem ? 1u : 0u);
 }
 
-// Adds the two elements of a 32-bit word to the packed table: the low
-// element at word (w & 0x7FFF), the high one at word ((w >> 16) & 0x7FFF);
-// +1 for a positive value, +2^16 for a negative one (prmt replicates the sign
-// bit of byte 1 or byte 3 into 0xFFFF, which plus one is 2^16).
-__device__ __forceinline__ void count_pair(uint32_t base, uint32_t w)
+// Shared address of the window word of magnitude g; magnitudes below the
+// window go to the word before it, those above to the word after it.
+__device__ __forceinline__ uint32_t win_addr(uint32_t win, uint32_t g)
 {
-    red_add(base + ((w & 0x7FFFu) << 2), prmt(w, 0u, 0x4499u) + 1u);
-    red_add(base + ((w >> 14) & 0x1FFFCu), prmt(w, 0u, 0x44BBu) + 1u);
+    int i = static_cast<int>(g) - static_cast<int>(kG0);
+    i = max(-1, min(i, kWin));
+    return win + static_cast<uint32_t>(i * 4);
+}
+
+// Adds the two elements of a 32-bit word to the packed window: +1 for a
+// positive value, +2^16 for a negative one (prmt replicates the sign bit of
+// byte 1 or byte 3 into 0xFFFF, which plus one is 2^16).
+__device__ __forceinline__ void count_pair(uint32_t win, uint32_t w)
+{
+    red_add(win_addr(win, w & 0x7FFFu), prmt(w, 0u, 0x4499u) + 1u);
+    red_add(win_addr(win, (w >> 16) & 0x7FFFu), prmt(w, 0u, 0x44BBu) + 1u);
 }
 
 // One element given by its 16 bits, in table mode MODE.
 template <int MODE>
-__device__ __forceinline__ void count_one(uint32_t base, uint32_t h)
-{
-    const uint32_t addr = base + ((h & 0x7FFFu) << 2);
-    const bool neg = (h & 0x8000u) != 0u && h != 0x8000u;  // -0 counts as +0
-    if (MODE == kPacked) red_add(addr, (h & 0x8000u) ? 0x10000u : 1u);
-    else if (MODE == kPos32) { if (!neg) red_add(addr, 1u); }
-    else { if (neg) red_add(addr, 1u); }
-}
-
-template <int MODE>
-__device__ __forceinline__ void count_word(uint32_t base, uint32_t w)
+__device__ __forceinline__ void count_one(uint32_t win, uint32_t h)
 {
     if (MODE == kPacked) {
-        count_pair(base, w);
+        red_add(win_addr(win, h & 0x7FFFu), (h & 0x8000u) ? 0x10000u : 1u);
     } else {
-        count_one<MODE>(base, w & 0xFFFFu);
-        count_one<MODE>(base, w >> 16);
+        const bool neg = (h & 0x8000u) != 0u && h != 0x8000u;  // -0 counts as +0
+        const uint32_t i = (h & 0x7FFFu) - (MODE & 1 ? static_cast<uint32_t>(kWin) : 0u);
+        if (neg == (MODE >= kQ2) && i < static_cast<uint32_t>(kWin)) red_add(win + i * 4u, 1u);
     }
 }
 
-__device__ __forceinline__ void zero_table(uint32_t* tab)
+template <int MODE>
+__device__ __forceinline__ void count_word(uint32_t win, uint32_t w)
 {
-    uint4* t4 = reinterpret_cast<uint4*>(tab);
-    for (int i = threadIdx.x; i < kMags / 4; i += kHT) t4[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (MODE == kPacked) {
+        count_pair(win, w);
+    } else {
+        count_one<MODE>(win, w & 0xFFFFu);
+        count_one<MODE>(win, w >> 16);
+    }
 }
 
-// Counts one row (V bfloat16 values, 2-byte aligned) into the zeroed table.
-// In packed mode also returns this thread's NaN-propagating maximum.
-template <int MODE>
-__device__ void count_row(const uint8_t* row, int64_t V, uint32_t base, float* tmax)
+// Zeroes the window and the two words beside it.
+__device__ __forceinline__ void zero_table(uint8_t* tabmem)
+{
+    uint4* t4 = reinterpret_cast<uint4*>(tabmem);
+    for (int i = threadIdx.x; i < kTabBytes / 16; i += kHT) t4[i] = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// A row of V bfloat16 values (2-byte aligned) as 16-byte vectors, with the
+// elements before the first 16-byte boundary (head) and after the last
+// whole vector (tail) apart.
+struct RowVecs {
+    const uint16_t* r16;
+    const uint4* vp;
+    int64_t head, nvec, tail, V;
+};
+
+__device__ __forceinline__ RowVecs row_vecs(const uint8_t* row, int64_t V)
+{
+    RowVecs rv;
+    rv.r16 = reinterpret_cast<const uint16_t*>(row);
+    const uintptr_t rp = reinterpret_cast<uintptr_t>(row);
+    rv.head = static_cast<int64_t>(((16u - static_cast<uint32_t>(rp & 15u)) & 15u) >> 1);
+    if (rv.head > V) rv.head = V;
+    rv.nvec = (V - rv.head) >> 3;
+    rv.tail = rv.head + (rv.nvec << 3);
+    rv.vp = reinterpret_cast<const uint4*>(row + rv.head * 2);
+    rv.V = V;
+    return rv;
+}
+
+// This thread's vectors v0 + q kHT + t of a batch (zeros past the end).
+__device__ __forceinline__ void load_batch(const RowVecs& rv, int64_t v0, uint4 (&u)[kHU])
+{
+#pragma unroll
+    for (int q = 0; q < kHU; ++q) {
+        const int64_t v = v0 + q * kHT + threadIdx.x;
+        u[q] = v < rv.nvec ? ldg_stream(rv.vp + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
+// Counts a row into the zeroed table. With PRE, u already holds the first
+// batch (loaded before the table was cleared, so that those loads overlap
+// it). In packed mode also returns this thread's NaN-propagating maximum.
+template <int MODE, bool PRE>
+__device__ __forceinline__ void count_vecs(const RowVecs& rv, uint32_t win, uint4 (&u)[kHU],
+                                           float* tmax)
 {
     const int t = threadIdx.x;
-    const uint16_t* r16 = reinterpret_cast<const uint16_t*>(row);
-    const uintptr_t rp = reinterpret_cast<uintptr_t>(row);
-    int64_t head = static_cast<int64_t>(((16u - static_cast<uint32_t>(rp & 15u)) & 15u) >> 1);
-    if (head > V) head = V;
-    const int64_t nvec = (V - head) >> 3;
-    const int64_t tail = head + (nvec << 3);
-    const uint4* vp = reinterpret_cast<const uint4*>(row + head * 2);
     uint32_t pm = kBf16NegInfPair;
-    for (int64_t v0 = 0; v0 < nvec; v0 += static_cast<int64_t>(kHU) * kHT) {
-        uint4 u[kHU];
+    for (int64_t v0 = 0; v0 < rv.nvec; v0 += static_cast<int64_t>(kHU) * kHT) {
+        if (!PRE || v0 != 0) load_batch(rv, v0, u);
 #pragma unroll
         for (int q = 0; q < kHU; ++q) {
-            const int64_t v = v0 + q * kHT + t;
-            u[q] = v < nvec ? ldg_stream(vp + v) : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int q = 0; q < kHU; ++q) {
-            if (v0 + q * kHT + t < nvec) {
-                count_word<MODE>(base, u[q].x);
-                count_word<MODE>(base, u[q].y);
-                count_word<MODE>(base, u[q].z);
-                count_word<MODE>(base, u[q].w);
+            if (v0 + q * kHT + t < rv.nvec) {
+                count_word<MODE>(win, u[q].x);
+                count_word<MODE>(win, u[q].y);
+                count_word<MODE>(win, u[q].z);
+                count_word<MODE>(win, u[q].w);
                 if (MODE == kPacked)
                     pm = bf16x2_max_nan(pm, bf16x2_max_nan(bf16x2_max_nan(u[q].x, u[q].y),
                                                            bf16x2_max_nan(u[q].z, u[q].w)));
@@ -195,32 +250,40 @@ __device__ void count_row(const uint8_t* row, int64_t V, uint32_t base, float* t
         }
     }
     float m = fmax_nan(bf16_lo(pm), bf16_hi(pm));
-    for (int64_t i = t; i < head; i += kHT) {
-        const uint32_t h = r16[i];
-        count_one<MODE>(base, h);
+    for (int64_t i = t; i < rv.head; i += kHT) {
+        const uint32_t h = rv.r16[i];
+        count_one<MODE>(win, h);
         m = fmax_nan(m, __uint_as_float(h << 16));
     }
-    for (int64_t i = tail + t; i < V; i += kHT) {
-        const uint32_t h = r16[i];
-        count_one<MODE>(base, h);
+    for (int64_t i = rv.tail + t; i < rv.V; i += kHT) {
+        const uint32_t h = rv.r16[i];
+        count_one<MODE>(win, h);
         m = fmax_nan(m, __uint_as_float(h << 16));
     }
     if (tmax != nullptr) *tmax = m;
 }
 
-// Counts of magnitude g from its table word: (positive, negative), with -0
-// merged into +0.
+// Counts one row (V bfloat16 values, 2-byte aligned) into the zeroed table.
 template <int MODE>
-__device__ __forceinline__ void split_word(uint32_t w, uint32_t g, uint32_t* np, uint32_t* nn)
+__device__ void count_row(const uint8_t* row, int64_t V, uint32_t win)
 {
-    if (MODE == kPacked) {
-        *np = w & 0xFFFFu;
-        *nn = w >> 16;
-        if (g == 0u) {
-            *np += *nn;
-            *nn = 0u;
-        }
-    } else if (MODE == kPos32) {
+    uint4 u[kHU];
+    count_vecs<MODE, false>(row_vecs(row, V), win, u, nullptr);
+}
+
+// First magnitude that word 0 of a 32-bit table stands for, in mode MODE.
+template <int MODE>
+__device__ __forceinline__ uint32_t table_g0()
+{
+    return MODE & 1 ? static_cast<uint32_t>(kWin) : 0u;
+}
+
+// The counts a 32-bit table word gives magnitude g's positive and negative
+// value.
+template <int MODE>
+__device__ __forceinline__ void split_word(uint32_t w, uint32_t* np, uint32_t* nn)
+{
+    if (MODE < kQ2) {
         *np = w;
         *nn = 0u;
     } else {
@@ -229,70 +292,91 @@ __device__ __forceinline__ void split_word(uint32_t w, uint32_t g, uint32_t* np,
     }
 }
 
-// Counts and masses of the positive and of the negative values of every
-// segment of 32 magnitudes [32 j, 32 j + 32), into the segment arrays. Warp w
-// takes the segments j = w (mod 32), one magnitude per lane, so that the few
-// dense segments near the bulk of a row spread over all warps; an empty
-// segment costs one vote, a non-empty one a warp reduction.
 struct SegArrays {
-    uint32_t* cp;
-    uint64_t* mp;
-    uint32_t* cn;
-    uint64_t* mn;
+    uint32_t* cp;   // [kSegs] per segment: positive count
+    uint64_t* mp;   //                      positive mass
+    uint32_t* cn;   //                      negative count
+    uint64_t* mn;   //                      negative mass
 };
 
+// The sums of a 32-bit table's 512 segments into the segment arrays (global
+// segment = table_g0 / 32 + local). Warp w takes blocks of 4 segments (one
+// 16-byte load per lane, 8 lanes per segment), blocks w, w + 16, ...; an
+// empty block costs one vote, a non-empty one a reduction over 8 lanes.
 template <int MODE>
-__device__ void segment_sums(const uint32_t* tab, float c, float mref, const SegArrays& A)
+__device__ void segment_sums(const uint32_t* win, float c, float mref, const SegArrays& A)
 {
     const uint32_t lane = threadIdx.x & 31u, w = threadIdx.x >> 5;
-    for (uint32_t j = w; j < static_cast<uint32_t>(kSegs); j += kHW) {
-        const uint32_t g = 32u * j + lane;
-        const uint32_t word = tab[g];
-        if (!__any_sync(0xFFFFFFFFu, word != 0u)) {
-            if (lane == 0) {
-                A.cp[j] = 0u;
-                A.mp[j] = 0u;
-                A.cn[j] = 0u;
-                A.mn[j] = 0u;
-            }
-            continue;
-        }
-        uint32_t np, nn;
-        split_word<MODE>(word, g, &np, &nn);
-        const float v = __uint_as_float(g << 16);
-        uint64_t mp = np ? static_cast<uint64_t>(np) * mass_fix(v, c, mref) : 0u;
-        uint64_t mn = nn ? static_cast<uint64_t>(nn) * mass_fix(-v, c, mref) : 0u;
-        uint64_t cc = (static_cast<uint64_t>(np) << 32) | nn;  // counts below 2^21 each
+    const uint32_t g0 = table_g0<MODE>();
+    const uint4* w4 = reinterpret_cast<const uint4*>(win);
+    for (uint32_t b = w; b < static_cast<uint32_t>(kWin / 128); b += kHW) {
+        const uint4 q = w4[32u * b + lane];
+        const uint32_t j = g0 / 32u + 4u * b + (lane >> 3);  // this lane's segment
+        const bool nz = (q.x | q.y | q.z | q.w) != 0u;
+        uint32_t c_p = 0, c_n = 0;
+        uint64_t m_p = 0, m_n = 0;
+        if (__any_sync(0xFFFFFFFFu, nz)) {
+            if (nz) {
+                const uint32_t ws[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            cc += __shfl_xor_sync(0xFFFFFFFFu, cc, off);
-            mp += __shfl_xor_sync(0xFFFFFFFFu, mp, off);
-            mn += __shfl_xor_sync(0xFFFFFFFFu, mn, off);
+                for (int k = 0; k < 4; ++k) {
+                    uint32_t np, nn;
+                    split_word<MODE>(ws[k], &np, &nn);
+                    const uint32_t g = g0 + 128u * b + 4u * lane + static_cast<uint32_t>(k);
+                    const float v = __uint_as_float(g << 16);
+                    if (np) {
+                        c_p += np;
+                        m_p += mass_n(np, v, c, mref);
+                    }
+                    if (nn) {
+                        c_n += nn;
+                        m_n += mass_n(nn, -v, c, mref);
+                    }
+                }
+            }
+            uint64_t cc = (static_cast<uint64_t>(c_p) << 32) | c_n;  // counts below 2^22 each
+#pragma unroll
+            for (int off = 4; off > 0; off >>= 1) {
+                cc += __shfl_xor_sync(0xFFFFFFFFu, cc, off);
+                m_p += __shfl_xor_sync(0xFFFFFFFFu, m_p, off);
+                m_n += __shfl_xor_sync(0xFFFFFFFFu, m_n, off);
+            }
+            c_p = static_cast<uint32_t>(cc >> 32);
+            c_n = static_cast<uint32_t>(cc);
         }
-        if (lane == 0) {
-            A.cp[j] = static_cast<uint32_t>(cc >> 32);
-            A.mp[j] = mp;
-            A.cn[j] = static_cast<uint32_t>(cc);
-            A.mn[j] = mn;
+        if ((lane & 7u) == 0u) {
+            if (MODE < kQ2) {
+                A.cp[j] = c_p;
+                A.mp[j] = m_p;
+            } else {
+                A.cn[j] = c_n;
+                A.mn[j] = m_n;
+            }
         }
     }
 }
 
-// Block-wide positions of every thread's two segments in value order: the
-// positive segments from the largest magnitudes down (thread kHT - 1 first),
-// then the negative ones from the smallest magnitude up (thread 0 first).
-// Returns the count and mass before each segment and the grand totals.
+// A thread's two segments 2t, 2t + 1 of each sign.
+struct OwnSegs {
+    uint32_t cp[2], cn[2];
+    uint64_t mp[2], mn[2];
+};
+
+// Block-wide positions of every thread's segments in value order: the
+// positive ones from the largest magnitudes down (thread kHT - 1 first), then
+// the negative ones from the smallest magnitude up (thread 0 first).
 struct SegPos {
-    uint32_t bcp, bcn;    // count before this thread's positive / negative segment
+    uint32_t bcp, bcn;    // count before this thread's positive / negative pair
     uint64_t bmp, bmn;    // mass before them
     uint32_t tot_c;
     uint64_t tot_m;
 };
 
-__device__ SegPos segment_positions(uint32_t cp, uint64_t mp, uint32_t cn, uint64_t mn,
-                                    HScratch& s)
+__device__ SegPos segment_positions(const OwnSegs& o, HScratch& s)
 {
     const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    const uint32_t cp = o.cp[0] + o.cp[1], cn = o.cn[0] + o.cn[1];
+    const uint64_t mp = o.mp[0] + o.mp[1], mn = o.mn[0] + o.mn[1];
     // Within the warp: positive, suffix sums over the lanes; negative, prefix sums.
     uint32_t sc = cp, pc = cn;
     uint64_t sm = mp, pmv = mn;
@@ -323,8 +407,9 @@ __device__ SegPos segment_positions(uint32_t cp, uint64_t mp, uint32_t cn, uint6
     __syncthreads();
     // Warp 0: what lies before each warp, and the totals.
     if (w == 0) {
-        const uint32_t c1 = s.wcp[lane], c2 = s.wcn[lane];
-        const uint64_t m1 = s.wmp[lane], m2 = s.wmn[lane];
+        const bool in = lane < kHW;
+        const uint32_t c1 = in ? s.wcp[lane] : 0u, c2 = in ? s.wcn[lane] : 0u;
+        const uint64_t m1 = in ? s.wmp[lane] : 0u, m2 = in ? s.wmn[lane] : 0u;
         uint32_t a1 = c1, a2 = c2;
         uint64_t b1 = m1, b2 = m2;
 #pragma unroll
@@ -343,15 +428,17 @@ __device__ SegPos segment_positions(uint32_t cp, uint64_t mp, uint32_t cn, uint6
             }
         }
         __syncwarp();
-        s.wcp[lane] = a1 - c1;  // positive: the warps above this one
-        s.wmp[lane] = b1 - m1;
-        s.wcn[lane] = a2 - c2;  // negative: the warps below this one
-        s.wmn[lane] = b2 - m2;
+        if (in) {
+            s.wcp[lane] = a1 - c1;  // positive: the warps above this one
+            s.wmp[lane] = b1 - m1;
+            s.wcn[lane] = a2 - c2;  // negative: the warps below this one
+            s.wmn[lane] = b2 - m2;
+        }
         if (lane == 0) {
             s.tot_pc = a1;
             s.tot_pm = b1;
         }
-        if (lane == 31) {
+        if (lane == kHW - 1) {
             s.tot_nc = a2;
             s.tot_nm = b2;
         }
@@ -367,56 +454,58 @@ __device__ SegPos segment_positions(uint32_t cp, uint64_t mp, uint32_t cn, uint6
     return r;
 }
 
-// The segment (of 32 magnitudes, one sign) where the running count (BY_MASS
-// false) or mass (true) in value order first reaches `need`: the thread that
-// owns it records it. Exactly one segment qualifies when 0 < need <= total.
+// The segment where the running count (BY_MASS false) or mass (true) in
+// value order first reaches `need`: the thread that owns it records it.
+// Exactly one segment qualifies when 0 < need <= total.
 template <bool BY_MASS>
-__device__ __forceinline__ void claim_segment(const SegPos& p, uint32_t cp, uint64_t mp, uint32_t cn,
-                                              uint64_t mn, uint64_t need, HScratch& s)
+__device__ void claim_segment(const SegPos& p, const OwnSegs& o, uint64_t need, HScratch& s)
 {
-    if (BY_MASS) {
-        if (p.bmp < need && need <= p.bmp + mp && mp > 0) {
-            s.seg = threadIdx.x;
-            s.seg_c = p.bcp;
-            s.seg_m = p.bmp;
+    const int t = threadIdx.x;
+    constexpr int slot = BY_MASS ? 1 : 0;
+    auto test = [&](uint32_t bc, uint64_t bm, uint32_t cnt, uint64_t mass, int seg) {
+        const bool hit = BY_MASS ? (bm < need && need <= bm + mass && mass > 0)
+                                 : (bc < need && need <= static_cast<uint64_t>(bc) + cnt);
+        if (hit) {
+            s.seg[slot] = seg;
+            s.seg_c[slot] = bc;
+            s.seg_m[slot] = bm;
         }
-        if (p.bmn < need && need <= p.bmn + mn && mn > 0) {
-            s.seg = threadIdx.x + kHT;
-            s.seg_c = p.bcn;
-            s.seg_m = p.bmn;
-        }
-    } else {
-        if (p.bcp < need && need <= p.bcp + cp) {
-            s.seg = threadIdx.x;
-            s.seg_c = p.bcp;
-            s.seg_m = p.bmp;
-        }
-        if (p.bcn < need && need <= p.bcn + cn) {
-            s.seg = threadIdx.x + kHT;
-            s.seg_c = p.bcn;
-            s.seg_m = p.bmn;
-        }
-    }
+    };
+    // Positive: segment 2t + 1 (larger magnitudes) comes before 2t.
+    test(p.bcp, p.bmp, o.cp[1], o.mp[1], 2 * t + 1);
+    test(p.bcp + o.cp[1], p.bmp + o.mp[1], o.cp[0], o.mp[0], 2 * t);
+    // Negative: segment 2t (smaller magnitudes) comes before 2t + 1.
+    test(p.bcn, p.bmn, o.cn[0], o.mn[0], kSegs + 2 * t);
+    test(p.bcn + o.cn[0], p.bmn + o.mn[0], o.cn[1], o.mn[1], kSegs + 2 * t + 1);
+}
+
+// The table mode that holds segment seg (index + kSegs if negative) in full.
+__device__ __forceinline__ int mode_of_seg(int seg)
+{
+    const bool neg = seg >= kSegs;
+    const int j = neg ? seg - kSegs : seg;
+    return (neg ? kQ2 : kQ0) + (j >= kSegs / 2 ? 1 : 0);
 }
 
 // Warp 0: walks the claimed segment, one magnitude per lane in value order,
 // to the first value where the running count or mass reaches `need`; records
-// that value and the mass of its upper set. The table must hold the
-// segment's sign (packed, or the matching 32-bit mode).
+// that value and the mass of its upper set. The table (mode MODE) must hold
+// the segment.
 template <int MODE, bool BY_MASS>
-__device__ void walk_segment(const uint32_t* tab, float c, float mref, uint64_t need, HScratch& s)
+__device__ void walk_segment(const uint32_t* win, float c, float mref, uint64_t need, HScratch& s)
 {
     const uint32_t lane = threadIdx.x & 31u;
-    const int seg = s.seg;
-    const bool pos = seg < kHT;
-    const uint32_t owner = static_cast<uint32_t>(pos ? seg : seg - kHT);
+    constexpr int slot = BY_MASS ? 1 : 0;
+    const int seg = s.seg[slot];
+    const bool pos = seg < kSegs;
+    const uint32_t j = static_cast<uint32_t>(pos ? seg : seg - kSegs);
     // Positive values descend with the magnitude, negative ones ascend.
-    const uint32_t g = owner * kWPT + (pos ? 31u - lane : lane);
+    const uint32_t g = 32u * j + (pos ? 31u - lane : lane);
     uint32_t np, nn;
-    split_word<MODE>(tab[g], g, &np, &nn);
+    split_word<MODE>(win[g - table_g0<MODE>()], &np, &nn);
     const uint32_t n = pos ? np : nn;
     const float v = pos ? __uint_as_float(g << 16) : -__uint_as_float(g << 16);
-    const uint64_t m = n ? static_cast<uint64_t>(n) * mass_fix(v, c, mref) : 0u;
+    const uint64_t m = n ? mass_n(n, v, c, mref) : 0u;
     uint64_t cc = n, cm = m;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -427,11 +516,11 @@ __device__ void walk_segment(const uint32_t* tab, float c, float mref, uint64_t 
             cm += om;
         }
     }
-    const bool hit = BY_MASS ? (s.seg_m + cm >= need) : (s.seg_c + cc >= need);
+    const bool hit = BY_MASS ? (s.seg_m[slot] + cm >= need) : (s.seg_c[slot] + cc >= need);
     const unsigned b = __ballot_sync(0xFFFFFFFFu, hit);
     if (b != 0u && lane == static_cast<uint32_t>(__ffs(b) - 1)) {
         s.tau = v == 0.0f ? 0.0f : v;
-        s.through = s.seg_m + cm;
+        s.through = s.seg_m[slot] + cm;
     }
 }
 
@@ -448,6 +537,223 @@ __device__ __forceinline__ float block_max(float m, HScratch& s)
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// Selection on the packed window (every row whose counts did not wrap)
+// ---------------------------------------------------------------------------
+// How a selection ended: thresholds found; count the row again with 32-bit
+// counts; no crossing found (impossible with exact integer sums); (a scan)
+// scan again.
+enum { kSelOk = 0, kSelRecount = 1, kSelFail = 2, kSelAgain = 3 };
+
+// Sum over the CTA of a count and a mass; every thread gets them. Its slots
+// are read again only after the next row's barriers.
+__device__ void block_sum2(uint32_t* c, uint64_t* m, HScratch& s)
+{
+    const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+    uint32_t x = __reduce_add_sync(0xFFFFFFFFu, *c);
+    uint64_t y = *m;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) y += __shfl_xor_sync(0xFFFFFFFFu, y, off);
+    if (lane == 0) {
+        s.sum_c[w] = x;
+        s.sum_m[w] = y;
+    }
+    __syncthreads();
+    x = lane < kHW ? s.sum_c[lane] : 0u;
+    y = lane < kHW ? s.sum_m[lane] : 0u;
+    x = __reduce_add_sync(0xFFFFFFFFu, x);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) y += __shfl_xor_sync(0xFFFFFFFFu, y, off);
+    *c = x;
+    *m = y;
+}
+
+// The count of every element and the row's whole mass, from the packed
+// window and its two outer words: below the window (|x| < 2^-64) the mass of
+// 0 each, above it none (x <= -2^64; a positive value there means a maximum
+// of 2^64 or more, and such rows are counted again).
+template <bool MASS>
+__device__ void window_totals(const uint32_t* win, float c, float mref, uint32_t* cnt,
+                              uint64_t* mass, HScratch& s)
+{
+    const uint32_t t = threadIdx.x, lane = t & 31u, w = t >> 5;
+    const uint4* w4 = reinterpret_cast<const uint4*>(win);
+    // Warp w takes blocks of 128 consecutive words, w, w + 16, ...: the words
+    // present cluster (a row's values fill a few binades), so most blocks are
+    // skipped whole and a dense one keeps all its lanes busy.
+    constexpr int kBlocks = kWin / 128 / kHW;  // per warp
+    constexpr int kBatch = 4;
+    uint32_t n = 0;
+    uint64_t m = 0;
+    for (int i0 = 0; i0 < kBlocks; i0 += kBatch) {
+        uint4 q[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) q[i] = w4[32u * (w + kHW * (i0 + i)) + lane];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const uint32_t ws[4] = {q[i].x, q[i].y, q[i].z, q[i].w};
+            n += (ws[0] & 0xFFFFu) + (ws[0] >> 16) + (ws[1] & 0xFFFFu) + (ws[1] >> 16) +
+                 (ws[2] & 0xFFFFu) + (ws[2] >> 16) + (ws[3] & 0xFFFFu) + (ws[3] >> 16);
+            if (!MASS || !__any_sync(0xFFFFFFFFu, (ws[0] | ws[1] | ws[2] | ws[3]) != 0u)) continue;
+            const uint32_t g4 = kG0 + 4u * (32u * (w + kHW * static_cast<uint32_t>(i0 + i)) + lane);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const uint32_t np = ws[k] & 0xFFFFu, nn = ws[k] >> 16;
+                const float v = __uint_as_float((g4 + k) << 16);
+                if (np) m += mass_n(np, v, c, mref);
+                if (nn) m += mass_n(nn, -v, c, mref);
+            }
+        }
+    }
+    if (t == 0) {
+        const uint32_t lo = win[-1], hi = win[kWin];
+        const uint32_t nt = (lo & 0xFFFFu) + (lo >> 16);
+        n += nt + (hi & 0xFFFFu) + (hi >> 16);
+        if (MASS) m += mass_n(nt, 0.0f, c, mref);
+    }
+    block_sum2(&n, &m, s);
+    *cnt = n;
+    *mass = m;
+}
+
+// The packed window's values in value order, from the row maximum down:
+// positions [0, np) the positive magnitudes from the maximum's down to the
+// window's first; then, if any value can lie there, the word below the
+// window (|x| < 2^-64, both signs); then the negative magnitudes from i0
+// (the maximum's, when the maximum is negative) up; then the word above it.
+struct DownSeq {
+    int np;
+    int tiny;   // 1 when the word below the window has a position
+    int i0;
+    int n;      // number of positions
+};
+
+__device__ __forceinline__ DownSeq down_seq(float mx)
+{
+    DownSeq d;
+    const int gm = static_cast<int>((__float_as_uint(mx) >> 16) & 0x7FFFu);
+    const bool neg = __float_as_uint(mx) >> 31;
+    const bool in = gm >= static_cast<int>(kG0);  // |mx| >= 2^-64 (and < 2^64: checked)
+    d.np = !neg && in ? gm - static_cast<int>(kG0) + 1 : 0;
+    d.tiny = neg && in ? 0 : 1;
+    d.i0 = neg && in ? gm - static_cast<int>(kG0) : 0;
+    d.n = d.np + d.tiny + (kWin - d.i0) + 1;
+    return d;
+}
+
+// Finds, by a block-wide scan of 512 positions at a time in value order, the
+// first value where the running count (KIND kByCount) or mass (kByMass)
+// reaches `need` (0 < need <= total). Sets s.tau and s.through (the mass of
+// the upper set of that value) and returns kSelOk; kSelRecount when the
+// crossing falls on one of the outer words, whose values are not told apart.
+// kByCountThenMass: top-k (need = k), then top-p (a fraction top_p of the
+// top-k mass), which crosses at or above the top-k threshold; when it crosses
+// in the same 512 positions their sums give it at once (s.tau, s.through the
+// top-p results), otherwise kSelAgain (s.through the top-k mass).
+enum { kByCount = 0, kByMass = 1, kByCountThenMass = 2 };
+
+template <int KIND>
+__device__ int scan_down(const uint32_t* win, const DownSeq& d, float c, float mref, uint64_t need,
+                         float top_p, HScratch& s)
+{
+    constexpr bool BY_MASS = KIND == kByMass;
+    const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+    uint64_t base_c = 0, base_m = 0;
+    for (int p0 = 0; p0 < d.n; p0 += kHT) {
+        const int p = p0 + t;
+        uint32_t n = 0;
+        uint64_t m = 0;
+        float v = 0.0f;
+        bool outer = false;
+        if (p < d.np) {
+            const int i = d.np - 1 - p;
+            n = win[i] & 0xFFFFu;
+            v = __uint_as_float((kG0 + static_cast<uint32_t>(i)) << 16);
+            m = n ? mass_n(n, v, c, mref) : 0u;
+        } else if (p < d.np + d.tiny) {
+            const uint32_t lo = win[-1];
+            n = (lo & 0xFFFFu) + (lo >> 16);
+            m = mass_n(n, 0.0f, c, mref);
+            outer = true;
+        } else if (p < d.n) {
+            const int i = d.i0 + (p - d.np - d.tiny);
+            if (i < kWin) {
+                n = win[i] >> 16;
+                v = -__uint_as_float((kG0 + static_cast<uint32_t>(i)) << 16);
+                m = n ? mass_n(n, v, c, mref) : 0u;
+            } else {
+                n = win[kWin] >> 16;  // no mass
+                outer = true;
+            }
+        }
+        // Inclusive scan over the warp, then over the warps.
+        uint32_t ic = n;
+        uint64_t im = m;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint32_t oc = __shfl_up_sync(0xFFFFFFFFu, ic, off);
+            const uint64_t om = __shfl_up_sync(0xFFFFFFFFu, im, off);
+            if (lane >= off) {
+                ic += oc;
+                im += om;
+            }
+        }
+        if (lane == 31) {
+            s.wcp[w] = ic;
+            s.wmp[w] = im;
+        }
+        __syncthreads();
+        // Lane l holds warp l's totals; an inclusive scan over them gives
+        // what lies before this warp (lane w - 1) and the chunk's total.
+        uint32_t xc = lane < kHW ? s.wcp[lane] : 0u;
+        uint64_t xm = lane < kHW ? s.wmp[lane] : 0u;
+#pragma unroll
+        for (int off = 1; off < kHW; off <<= 1) {
+            const uint32_t oc = __shfl_up_sync(0xFFFFFFFFu, xc, off);
+            const uint64_t om = __shfl_up_sync(0xFFFFFFFFu, xm, off);
+            if (lane >= off) {
+                xc += oc;
+                xm += om;
+            }
+        }
+        const uint32_t pc = w > 0 ? __shfl_sync(0xFFFFFFFFu, xc, w - 1) : 0u;
+        const uint64_t pm = w > 0 ? __shfl_sync(0xFFFFFFFFu, xm, w - 1) : 0u;
+        const uint32_t tc = __shfl_sync(0xFFFFFFFFu, xc, kHW - 1);
+        const uint64_t tm = __shfl_sync(0xFFFFFFFFu, xm, kHW - 1);
+        const uint64_t cc = base_c + pc + ic, cm = base_m + pm + im;
+        const bool hit = BY_MASS ? (m > 0 && cm >= need && cm - m < need)
+                                 : (n > 0 && cc >= need && cc - n < need);
+        if (hit) {
+            s.tau = v == 0.0f ? 0.0f : v;
+            s.through = cm;
+            s.found = outer ? 2 : 1;
+        }
+        __syncthreads();
+        if (KIND == kByCountThenMass && s.found == 1) {
+            // The top-p target, and whether it is crossed in this chunk.
+            const uint64_t target = ceil_frac(top_p, s.through);
+            if (base_m >= target) {
+                s.found = 3;  // crossed before this chunk: a second scan
+            } else {
+                __syncthreads();  // every thread has read s.through and s.found
+                if (m > 0 && cm >= target && cm - m < target) {
+                    s.tau = v == 0.0f ? 0.0f : v;
+                    s.through = cm;
+                    s.found = outer ? 2 : 1;
+                }
+                __syncthreads();
+            }
+        }
+        if (s.found != 0) break;
+        base_c += tc;
+        base_m += tm;
+    }
+    const int f = s.found;
+    __syncthreads();  // every thread has read s.found before the next scan resets it
+    if (t == 0) s.found = 0;
+    return f == 1 ? kSelOk : (f == 2 ? kSelRecount : (f == 3 ? kSelAgain : kSelFail));
+}
+
 // Per-row constants of the selection.
 struct CutK {
     bool tk, tp;
@@ -456,42 +762,66 @@ struct CutK {
     float c;
 };
 
-// The thresholds of one counted row. Every thread calls it, with its segment
-// sums; the table holds the packed counts (MODE kPacked) or one sign's 32-bit
-// counts (*mode_now), and is counted again when the other sign is needed.
-// False if no segment holds a crossing (impossible with exact integer sums;
-// the row is then reported as failed rather than read out of range).
-template <int MODE>
-__device__ bool select_row(const uint8_t* row, int64_t V, uint32_t* tab, uint32_t base,
-                           const CutK& P, float mref, const SegPos& pos, uint32_t cp, uint64_t mp,
-                           uint32_t cn, uint64_t mn, int* mode_now, HScratch& s, float* tau,
-                           uint64_t* kept)
+// Everything a row's selection needs from the kernel.
+struct RowCtx {
+    const uint8_t* row;
+    int64_t V;
+    uint8_t* tabmem;
+    uint32_t* win;        // window word 0 (generic pointer)
+    uint32_t win_s;       // its shared address
+    float mref;
+};
+
+// The thresholds of a row counted again with 32-bit counts; every thread
+// calls it. The table (a quarter, *mode_now) is counted again for the quarter
+// that holds each claimed segment. kSelFail if no segment holds a crossing
+// (impossible with exact integer sums; the row is reported as failed rather
+// than read out of range).
+__device__ int select_row(const RowCtx& R, const CutK& P, const SegPos& pos, const OwnSegs& o,
+                          int* mode_now, HScratch& s, float* tau, uint64_t* kept)
 {
-    // Makes the table hold the sign of the claimed segment (32-bit modes).
-    auto hold_sign = [&]() {
-        if (MODE == kPacked) return;
-        const int want = s.seg < kHT ? kPos32 : kNeg32;
-        if (*mode_now == want) return;
+    // The claim slots were reset before the segment positions were taken
+    // (whose barriers order that before these writes).
+    auto claim = [&](bool by_mass, uint64_t need) -> int {
+        if (by_mass) claim_segment<true>(pos, o, need, s);
+        else claim_segment<false>(pos, o, need, s);
         __syncthreads();
-        zero_table(tab);
-        __syncthreads();
-        if (want == kPos32) count_row<kPos32>(row, V, base, nullptr);
-        else count_row<kNeg32>(row, V, base, nullptr);
-        __syncthreads();
-        *mode_now = want;
+        const int seg = s.seg[by_mass ? 1 : 0];
+        if (seg < 0) return kSelFail;
+        const int want = mode_of_seg(seg);
+        if (want != *mode_now) {
+            zero_table(R.tabmem);
+            __syncthreads();
+            switch (want) {
+            case kQ0: count_row<kQ0>(R.row, R.V, R.win_s); break;
+            case kQ1: count_row<kQ1>(R.row, R.V, R.win_s); break;
+            case kQ2: count_row<kQ2>(R.row, R.V, R.win_s); break;
+            default: count_row<kQ3>(R.row, R.V, R.win_s); break;
+            }
+            __syncthreads();
+            *mode_now = want;
+        }
+        return kSelOk;
     };
     auto walk = [&](bool by_mass, uint64_t need) {
         if (threadIdx.x < 32) {
-            const int m = MODE == kPacked ? kPacked : *mode_now;
-            if (m == kPacked) {
-                if (by_mass) walk_segment<kPacked, true>(tab, P.c, mref, need, s);
-                else walk_segment<kPacked, false>(tab, P.c, mref, need, s);
-            } else if (m == kPos32) {
-                if (by_mass) walk_segment<kPos32, true>(tab, P.c, mref, need, s);
-                else walk_segment<kPos32, false>(tab, P.c, mref, need, s);
-            } else {
-                if (by_mass) walk_segment<kNeg32, true>(tab, P.c, mref, need, s);
-                else walk_segment<kNeg32, false>(tab, P.c, mref, need, s);
+            switch (*mode_now) {
+            case kQ0:
+                if (by_mass) walk_segment<kQ0, true>(R.win, P.c, R.mref, need, s);
+                else walk_segment<kQ0, false>(R.win, P.c, R.mref, need, s);
+                break;
+            case kQ1:
+                if (by_mass) walk_segment<kQ1, true>(R.win, P.c, R.mref, need, s);
+                else walk_segment<kQ1, false>(R.win, P.c, R.mref, need, s);
+                break;
+            case kQ2:
+                if (by_mass) walk_segment<kQ2, true>(R.win, P.c, R.mref, need, s);
+                else walk_segment<kQ2, false>(R.win, P.c, R.mref, need, s);
+                break;
+            default:
+                if (by_mass) walk_segment<kQ3, true>(R.win, P.c, R.mref, need, s);
+                else walk_segment<kQ3, false>(R.win, P.c, R.mref, need, s);
+                break;
             }
         }
         __syncthreads();
@@ -500,25 +830,16 @@ __device__ bool select_row(const uint8_t* row, int64_t V, uint32_t* tab, uint32_
     float t_val = __uint_as_float(kF32NegInfBits);
     uint64_t mass_k = pos.tot_m;
     if (P.tk) {
-        if (threadIdx.x == 0) s.seg = -1;
-        __syncthreads();
-        claim_segment<false>(pos, cp, mp, cn, mn, P.k, s);
-        __syncthreads();
-        if (s.seg < 0) return false;
-        hold_sign();
+        const int st = claim(false, P.k);
+        if (st != kSelOk) return st;
         walk(false, P.k);
         t_val = s.tau;
         mass_k = s.through;
     }
     if (P.tp) {
         const uint64_t target = ceil_frac(P.top_p, mass_k);
-        __syncthreads();  // every thread has read s.tau / s.through
-        if (threadIdx.x == 0) s.seg = -1;
-        __syncthreads();
-        claim_segment<true>(pos, cp, mp, cn, mn, target, s);
-        __syncthreads();
-        if (s.seg < 0) return false;
-        hold_sign();
+        const int st = claim(true, target);
+        if (st != kSelOk) return st;
         walk(true, target);
         t_val = s.tau;
         *kept = s.through;
@@ -526,7 +847,29 @@ __device__ bool select_row(const uint8_t* row, int64_t V, uint32_t* tab, uint32_
         *kept = mass_k;
     }
     *tau = t_val;
-    return true;
+    return kSelOk;
+}
+
+// The thresholds of a row counted in the packed window without a wrap.
+__device__ int fast_select(const uint32_t* win, const CutK& P, float mx, float mref, uint64_t tot_m,
+                           HScratch& s, float* tau, uint64_t* kept)
+{
+    const DownSeq d = down_seq(mx);
+    if (P.tk && P.tp) {
+        int st = scan_down<kByCountThenMass>(win, d, P.c, mref, P.k, P.top_p, s);
+        if (st == kSelAgain)
+            st = scan_down<kByMass>(win, d, P.c, mref, ceil_frac(P.top_p, s.through), 0.f, s);
+        if (st != kSelOk) return st;
+    } else if (P.tk) {
+        const int st = scan_down<kByCount>(win, d, P.c, mref, P.k, 0.f, s);
+        if (st != kSelOk) return st;
+    } else {
+        const int st = scan_down<kByMass>(win, d, P.c, mref, ceil_frac(P.top_p, tot_m), 0.f, s);
+        if (st != kSelOk) return st;
+    }
+    *tau = s.tau;
+    *kept = s.through;
+    return kSelOk;
 }
 
 __device__ void fail_rows(const FilterArgs& a, int flags)
@@ -535,15 +878,19 @@ __device__ void fail_rows(const FilterArgs& a, int flags)
     for (int64_t r = blockIdx.x; r < a.g.rows; r += gridDim.x) a.rows[r] = FiltRow{0.f, 0.f, 0.f, flags};
 }
 
-__global__ void __launch_bounds__(kHT, 1) hist_kernel(const __grid_constant__ FilterArgs a)
+__global__ void __launch_bounds__(kHT, 2) hist_kernel(const __grid_constant__ FilterArgs a)
 {
-    extern __shared__ __align__(16) uint32_t tab[];
+    extern __shared__ __align__(16) uint8_t hsm[];
     __shared__ HScratch s;
-    const SegArrays A{tab + kMags, reinterpret_cast<uint64_t*>(tab + kMags + kSegs),
-                      tab + kMags + 3 * kSegs, reinterpret_cast<uint64_t*>(tab + kMags + 4 * kSegs)};
     const int t = threadIdx.x;
     const int64_t V = a.g.V;
-    const uint32_t base = smem_addr(tab);
+    uint32_t* win = reinterpret_cast<uint32_t*>(hsm + 16);
+    const SegArrays A{reinterpret_cast<uint32_t*>(hsm + kTabBytes),
+                      reinterpret_cast<uint64_t*>(hsm + kTabBytes + kSegs * 4),
+                      reinterpret_cast<uint32_t*>(hsm + kTabBytes + kSegs * 12),
+                      reinterpret_cast<uint64_t*>(hsm + kTabBytes + kSegs * 16)};
+    RowCtx R{nullptr, V, hsm, win, smem_addr(win), 0.f};
+    if (t == 0) s.found = 0;
     CutK P;
     P.tk = a.top_k > 0 && a.top_k < V;
     P.tp = a.top_p < 1.0f;
@@ -575,66 +922,86 @@ __global__ void __launch_bounds__(kHT, 1) hist_kernel(const __grid_constant__ Fi
     }
 
     for (int64_t r = blockIdx.x; r < a.g.rows; r += gridDim.x) {
-        const uint8_t* row = r < a.g.rows_t ? a.target + r * V * 2 : a.draft + (r - a.g.rows_t) * V * 2;
-        __syncthreads();  // the previous row is done with the table
-        zero_table(tab);
+        R.row = r < a.g.rows_t ? a.target + r * V * 2 : a.draft + (r - a.g.rows_t) * V * 2;
+        const RowVecs rv = row_vecs(R.row, V);
+        uint4 u[kHU];
+        load_batch(rv, 0, u);  // in flight while the table is cleared
+        __syncthreads();       // the previous row is done with the table
+        zero_table(hsm);
         __syncthreads();
         float tm;
-        count_row<kPacked>(row, V, base, &tm);
+        count_vecs<kPacked, true>(rv, R.win_s, u, &tm);
         const float mx = block_max(tm, s);  // its barriers also order the counts before the sweep
         if (!(mx > __uint_as_float(kF32NegInfBits)) || !(mx < __uint_as_float(0x7F800000u))) {
             // NaN or +inf in the row, or no finite logit.
             if (t == 0) a.rows[r] = FiltRow{0.f, 0.f, 0.f, kFlagNonFinite};
             continue;
         }
-        const float mref = ceilf(mx * P.c);
-        // This thread's segment (magnitudes [32 t, 32 t + 32)): its sums.
-        auto own_sums = [&](uint32_t* cp, uint64_t* mp, uint32_t* cn, uint64_t* mn) {
+        R.mref = ceilf(mx * P.c);
+        // This thread's segments 2t, 2t + 1 of each sign (32-bit counts).
+        auto own = [&]() {
             __syncthreads();  // the segment arrays are written
-            *cp = A.cp[t];
-            *mp = A.mp[t];
-            *cn = A.cn[t];
-            *mn = A.mn[t];
+            if (t == 0) {
+                s.seg[0] = -1;
+                s.seg[1] = -1;
+            }
+            OwnSegs o;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                o.cp[i] = A.cp[2 * t + i];
+                o.mp[i] = A.mp[2 * t + i];
+                o.cn[i] = A.cn[2 * t + i];
+                o.mn[i] = A.mn[2 * t + i];
+            }
+            return o;
         };
-        uint32_t cp, cn;
-        uint64_t mp, mn;
-        segment_sums<kPacked>(tab, P.c, mref, A);
-        own_sums(&cp, &mp, &cn, &mn);
-        SegPos pos = segment_positions(cp, mp, cn, mn, s);
+        uint32_t tot_c;
+        uint64_t tot_m;
+        // The whole mass is the top-p target's base when top-k is off.
+        if (P.tp && !P.tk) window_totals<true>(win, P.c, R.mref, &tot_c, &tot_m, s);
+        else window_totals<false>(win, P.c, R.mref, &tot_c, &tot_m, s);
         float tau = 0.f;
         uint64_t kept = 0;
-        bool ok;
-        if (pos.tot_c == static_cast<uint64_t>(V)) {
-            int mode_now = kPacked;
-            ok = select_row<kPacked>(row, V, tab, base, P, mref, pos, cp, mp, cn, mn, &mode_now, s,
-                                     &tau, &kept);
-        } else {
-            // A 16-bit count wrapped (the counts fall short of V): count
-            // again, one sign per read, 32 bits per magnitude.
-            zero_table(tab);
+        int st = kSelRecount;
+        // A wrapped 16-bit count shows as counts short of V.
+        if (tot_c == static_cast<uint64_t>(V) && mx < 18446744073709551616.0f)
+            st = fast_select(win, P, mx, R.mref, tot_m, s, &tau, &kept);
+        if (st == kSelRecount) {
+            // Count again: 32 bits per magnitude, a quarter per read.
             __syncthreads();
-            count_row<kPos32>(row, V, base, nullptr);
+            zero_table(hsm);
             __syncthreads();
-            segment_sums<kPos32>(tab, P.c, mref, A);
-            uint32_t c2, c3;
-            uint64_t m2, m3;
-            own_sums(&cp, &mp, &c2, &m2);
-            zero_table(tab);
+            count_row<kQ0>(R.row, V, R.win_s);
             __syncthreads();
-            count_row<kNeg32>(row, V, base, nullptr);
+            segment_sums<kQ0>(win, P.c, R.mref, A);
             __syncthreads();
-            segment_sums<kNeg32>(tab, P.c, mref, A);
-            own_sums(&c2, &m2, &c3, &m3);
-            cn = c3;
-            mn = m3;
-            pos = segment_positions(cp, mp, cn, mn, s);
-            int mode_now = kNeg32;
-            ok = select_row<kNeg32>(row, V, tab, base, P, mref, pos, cp, mp, cn, mn, &mode_now, s,
-                                    &tau, &kept);
+            zero_table(hsm);
+            __syncthreads();
+            count_row<kQ1>(R.row, V, R.win_s);
+            __syncthreads();
+            segment_sums<kQ1>(win, P.c, R.mref, A);
+            __syncthreads();
+            zero_table(hsm);
+            __syncthreads();
+            count_row<kQ2>(R.row, V, R.win_s);
+            __syncthreads();
+            segment_sums<kQ2>(win, P.c, R.mref, A);
+            __syncthreads();
+            zero_table(hsm);
+            __syncthreads();
+            count_row<kQ3>(R.row, V, R.win_s);
+            __syncthreads();
+            segment_sums<kQ3>(win, P.c, R.mref, A);
+            const OwnSegs o = own();
+            const SegPos pos = segment_positions(o, s);
+            int mode_now = kQ3;
+            st = pos.tot_c == static_cast<uint64_t>(V) ? select_row(R, P, pos, o, &mode_now, s, &tau, &kept)
+                                                        : kSelFail;
         }
         if (t == 0) {
             const float l = log2f(__ull2float_rn(kept)) - 40.0f;
-            a.rows[r] = ok && kept > 0 ? FiltRow{mref, l, tau, 0} : FiltRow{0.f, 0.f, 0.f, kFlagNonFinite};
+            a.rows[r] = st == kSelOk && kept > 0 ? FiltRow{R.mref, l, tau, 0}
+                                                 : FiltRow{0.f, 0.f, 0.f, kFlagNonFinite};
         }
     }
 }
@@ -645,7 +1012,8 @@ cudaError_t launch_hist(const FilterArgs& a, int sms, cudaStream_t s)
 {
     cudaError_t e = cudaFuncSetAttribute(hist_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kHSmem);
     if (e != cudaSuccess) return e;
-    const int64_t grid = a.g.rows < sms ? a.g.rows : sms;
+    const int64_t cap = 2 * static_cast<int64_t>(sms);
+    const int64_t grid = a.g.rows < cap ? a.g.rows : cap;
     if (grid <= 0) return cudaSuccess;
     // The first kernel of a call: launched without programmatic dependent
     // launch, so the caller's earlier work on the stream (the logits) is
