@@ -105,8 +105,20 @@ enum sv_status {
 enum sv_seq_status {
     SV_SEQ_BAD_TOKEN = 1,  /* a draft token outside [0, V)                  */
     SV_SEQ_NONFINITE = 2,  /* a NaN / +inf / all -inf row (see above)       */
-    SV_SEQ_TIMEOUT = 4     /* a bounded wait inside a kernel expired        */
+    SV_SEQ_TIMEOUT = 4,    /* a bounded wait inside a kernel expired        */
+    SV_SEQ_INDEX = 8       /* a device-side index check failed (the library
+                              built with device checks only; see
+                              sv_device_checks)                             */
 };
+
+/*
+ * 1 if this library was built with device-side index checks (the debug
+ * variant, libspecverify_debug.so), 0 for the product build. With them every
+ * kernel tests the indices it computes or reads before it uses them; a
+ * failed test skips that access and reports SV_SEQ_INDEX for the sequence
+ * (num_accepted -1, tokens -1), never a trap. Host-only: no CUDA call.
+ */
+int sv_device_checks(void);
 
 /* Supported ranges: 0 <= B < 2^31, 0 <= K <= 1024, 1 <= V < 2^31,
  * B * (2K + 1) * V * sizeof(element) < 2^62. Temperature (sampling mode):

@@ -13,6 +13,7 @@ from .api import (  # noqa: F401
     SV_GREEDY,
     SV_SAMPLE,
     SV_SEQ_BAD_TOKEN,
+    SV_SEQ_INDEX,
     SV_SEQ_NONFINITE,
     SV_SEQ_TIMEOUT,
     SpecVerifyError,
@@ -32,6 +33,7 @@ from .api import (  # noqa: F401
     spec_verify_sharded,
     spec_verify_static,
     spec_verify_timed,
+    sv_device_checks,
     sv_early_exit_workspace_bytes,
     sv_filtered_workspace_bytes,
     sv_host_staging_bytes,

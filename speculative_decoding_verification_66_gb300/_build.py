@@ -18,6 +18,10 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libspecverify.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
+# The debug variant: the same sources with device-side index checks compiled
+# in (-DSV_DEVICE_CHECKS), built beside the product library.
+DEBUG_LIB_PATH = os.path.join(PKG, "libspecverify_debug.so")
+DEBUG_FLAGS = ["-DSV_DEVICE_CHECKS=1"]
 SOURCES = ["row_stats.cu", "scan.cu", "sample.cu", "filter.cu", "hist.cu", "lmhead.cu", "sv_api.cu",
            "sv_static.cu", "philox.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -43,10 +47,10 @@ def _inputs():
     return files
 
 
-def stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def stale(path: str = LIB_PATH) -> bool:
+    if not os.path.exists(path):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(path)
     return any(os.path.getmtime(f) > t for f in _inputs())
 
 
@@ -56,16 +60,21 @@ def compile_flags(extra=()):
                    *extra]
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    """Compile (if needed) and return the library path."""
-    if not force and not stale():
-        return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile (if needed) and return the library path: the product library,
+    or with debug=True the variant with device-side index checks."""
+    lib_path = DEBUG_LIB_PATH if debug else LIB_PATH
+    build_dir = os.path.join(BUILD_DIR, "debug") if debug else BUILD_DIR
+    if debug:
+        extra_flags = (*DEBUG_FLAGS, *extra_flags)
+    if not force and not stale(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
     objs = []
 
     def one(src):
-        obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+        obj = os.path.join(build_dir, os.path.splitext(src)[0] + ".o")
         cmd = [cc, *compile_flags(extra_flags), "-c", os.path.join(CSRC, src), "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -80,16 +89,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
         objs.append(obj)
         if verbose and log:
             print(log)
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "shared",
            "-Xlinker", f"-rpath,{cuda_lib_dir()}"]
     p = subprocess.run(cmd, capture_output=True, text=True)
     if p.returncode != 0:
         raise RuntimeError(f"link failed:\n{p.stdout}\n{p.stderr}")
-    os.replace(tmp, LIB_PATH)
-    return LIB_PATH
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, verbose="-v" in sys.argv))
+    print(build(force=True, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -5,7 +5,12 @@ import ctypes
 import os
 import threading
 
-LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libspecverify.so")
+# The product library, or with SV_LIBRARY=debug in the environment the variant
+# built with device-side index checks (_build.build(debug=True)).
+_DIR = os.path.dirname(os.path.abspath(__file__))
+PRODUCT_PATH = os.path.join(_DIR, "libspecverify.so")
+DEBUG_PATH = os.path.join(_DIR, "libspecverify_debug.so")
+LIB_PATH = DEBUG_PATH if os.environ.get("SV_LIBRARY", "") == "debug" else PRODUCT_PATH
 
 # Exported names and their C signatures, as declared in include/spec_verify.h.
 _vp, _i64, _i32, _f32, _u64, _sz = (ctypes.c_void_p, ctypes.c_int64, ctypes.c_int,
@@ -55,6 +60,7 @@ SIGNATURES = {
     "sv_philox": (_i32, [_u64, _vp, _vp, _i64, _vp]),
     "sv_error_string": (ctypes.c_char_p, [_i32]),
     "sv_version": (_i32, []),
+    "sv_device_checks": (_i32, []),
 }
 
 _lock = threading.Lock()

@@ -16,7 +16,13 @@ from . import _lib
 
 SV_F32, SV_BF16 = 0, 1
 SV_SAMPLE, SV_GREEDY = 0, 1
-SV_SEQ_BAD_TOKEN, SV_SEQ_NONFINITE, SV_SEQ_TIMEOUT = 1, 2, 4
+SV_SEQ_BAD_TOKEN, SV_SEQ_NONFINITE, SV_SEQ_TIMEOUT, SV_SEQ_INDEX = 1, 2, 4, 8
+
+
+def sv_device_checks() -> bool:
+    """True when the loaded library is the variant built with device-side
+    index checks (see _build.build(debug=True) and the SV_LIBRARY variable)."""
+    return bool(_lib.load().sv_device_checks())
 
 def launches(mode, V: int, dtype) -> int:
     """Kernel launches one spec_verify call makes: row statistics and the scan,

@@ -175,6 +175,7 @@ struct Scratch {
     int lo;
     int list_n;
     int inc_n;
+    int check;  // kFlagIndex when a device-side index check failed on this row
 };
 
 template <typename H>
@@ -1089,6 +1090,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
     for (int64_t r = blockIdx.x; r < g.rows; r += gridDim.x) {
         const uint8_t* row =
             r < g.rows_t ? a.target + r * V * ES : a.draft + (r - g.rows_t) * V * ES;
+        if (t == 0) s.check = 0;  // thread 0 wrote the previous row's result
         __syncthreads();  // the previous row is done with shared memory
 
         // First read (HBM): per lane position of this thread's vectors (a
@@ -1224,7 +1226,9 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                         if (key >= lk) append(key, list, &s.list_n);
                     }
                 } else {
-                    inc[atomicAdd(&s.inc_n, 1)] = t;
+                    const int at = atomicAdd(&s.inc_n, 1);
+                    if (SV_IN_RANGE(at, kMaxShares)) inc[at] = t;
+                    else s.check = kFlagIndex;
                 }
                 __syncthreads();
                 reread_shares<ES>(row, V, inc, s.inc_n, lk, list, &s.list_n);
@@ -1312,7 +1316,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
         if (t == 0) {
             const float thr = tau == 0u ? ninf : key_value(tau);
             const float l = log2f(__ull2float_rn(kept)) - 40.0f;
-            a.rows[r] = FiltRow{mref, l, thr, kept > 0 ? 0 : kFlagNonFinite};
+            a.rows[r] = FiltRow{mref, l, thr, s.check != 0 ? s.check : (kept > 0 ? 0 : kFlagNonFinite)};
         }
     }
 }

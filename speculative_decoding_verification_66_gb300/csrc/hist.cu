@@ -83,6 +83,7 @@ struct HScratch {
     uint64_t through;     // mass of the upper set {x >= tau}
     int found;            // the scan: 0 not yet, 1 found, 2 in an outer word
     int fail;
+    int check;            // kFlagIndex when a device-side index check failed on this row
 };
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel)
@@ -501,8 +502,9 @@ __device__ void walk_segment(const uint32_t* win, float c, float mref, uint64_t 
     const uint32_t j = static_cast<uint32_t>(pos ? seg : seg - kSegs);
     // Positive values descend with the magnitude, negative ones ascend.
     const uint32_t g = 32u * j + (pos ? 31u - lane : lane);
-    uint32_t np, nn;
-    split_word<MODE>(win[g - table_g0<MODE>()], &np, &nn);
+    uint32_t np = 0, nn = 0;
+    if (SV_IN_RANGE(g - table_g0<MODE>(), kWin)) split_word<MODE>(win[g - table_g0<MODE>()], &np, &nn);
+    else s.check = kFlagIndex;
     const uint32_t n = pos ? np : nn;
     const float v = pos ? __uint_as_float(g << 16) : -__uint_as_float(g << 16);
     const uint64_t m = n ? mass_n(n, v, c, mref) : 0u;
@@ -667,7 +669,7 @@ __device__ int scan_down(const uint32_t* win, const DownSeq& d, float c, float m
         bool outer = false;
         if (p < d.np) {
             const int i = d.np - 1 - p;
-            n = win[i] & 0xFFFFu;
+            n = SV_IN_RANGE(i, kWin) ? win[i] & 0xFFFFu : (s.check = kFlagIndex, 0u);
             v = __uint_as_float((kG0 + static_cast<uint32_t>(i)) << 16);
             m = n ? mass_n(n, v, c, mref) : 0u;
         } else if (p < d.np + d.tiny) {
@@ -678,7 +680,7 @@ __device__ int scan_down(const uint32_t* win, const DownSeq& d, float c, float m
         } else if (p < d.n) {
             const int i = d.i0 + (p - d.np - d.tiny);
             if (i < kWin) {
-                n = win[i] >> 16;
+                n = SV_IN_RANGE(i, kWin) ? win[i] >> 16 : (s.check = kFlagIndex, 0u);
                 v = -__uint_as_float((kG0 + static_cast<uint32_t>(i)) << 16);
                 m = n ? mass_n(n, v, c, mref) : 0u;
             } else {
@@ -788,6 +790,10 @@ __device__ int select_row(const RowCtx& R, const CutK& P, const SegPos& pos, con
         __syncthreads();
         const int seg = s.seg[by_mass ? 1 : 0];
         if (seg < 0) return kSelFail;
+        if (!SV_IN_RANGE(seg, 2 * kSegs)) {
+            s.check = kFlagIndex;
+            return kSelFail;
+        }
         const int want = mode_of_seg(seg);
         if (want != *mode_now) {
             zero_table(R.tabmem);
@@ -926,6 +932,7 @@ __global__ void __launch_bounds__(kHT, 2) hist_kernel(const __grid_constant__ Fi
         const RowVecs rv = row_vecs(R.row, V);
         uint4 u[kHU];
         load_batch(rv, 0, u);  // in flight while the table is cleared
+        if (t == 0) s.check = 0;  // thread 0 wrote the previous row's result
         __syncthreads();       // the previous row is done with the table
         zero_table(hsm);
         __syncthreads();
@@ -1000,8 +1007,9 @@ __global__ void __launch_bounds__(kHT, 2) hist_kernel(const __grid_constant__ Fi
         }
         if (t == 0) {
             const float l = log2f(__ull2float_rn(kept)) - 40.0f;
-            a.rows[r] = st == kSelOk && kept > 0 ? FiltRow{R.mref, l, tau, 0}
-                                                 : FiltRow{0.f, 0.f, 0.f, kFlagNonFinite};
+            a.rows[r] = s.check != 0                 ? FiltRow{0.f, 0.f, 0.f, s.check}
+                        : st == kSelOk && kept > 0 ? FiltRow{R.mref, l, tau, 0}
+                                                   : FiltRow{0.f, 0.f, 0.f, kFlagNonFinite};
         }
     }
 }

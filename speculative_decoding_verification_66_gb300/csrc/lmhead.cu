@@ -417,8 +417,10 @@ __global__ void gather_hidden_kernel(const uint8_t* ht, const uint8_t* hd, const
 {
     for (int64_t b = blockIdx.y; b < B; b += gridDim.y) {
     const SeqRecord rec = seqs[b];
-    const bool ok = rec.status == 0;
     const int64_t j = rec.j;
+    // (An emitted position outside [0, K] leaves zeros; the sampler, reading
+    // the same record, reports the sequence.)
+    const bool ok = rec.status == 0 && SV_IN_RANGE(j, K + 1);
     const uint4 z = make_uint4(0, 0, 0, 0);
     for (int64_t v = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; v < row_t / 16;
          v += static_cast<int64_t>(gridDim.x) * blockDim.x)

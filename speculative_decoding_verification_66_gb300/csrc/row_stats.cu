@@ -532,7 +532,15 @@ __global__ void __launch_bounds__(kRowThreads) row_stats_kernel(const __grid_con
             abort_flag = 1;
             break;
         }
-        const TileRec sp = recs[stage];
+        TileRec sp = recs[stage];
+        if (!SV_IN_RANGE(sp.seg, g.maxseg)) {
+            // A tile record outside this CTA's segments: its elements are
+            // skipped and the segment being reduced is reported.
+            ss.flags |= kFlagIndex;
+            gs.flags |= kFlagIndex;
+            sp.seg = seg;
+            sp.nv = 0;
+        }
         if (sp.seg != seg) {
             Partial* out = my_partials + static_cast<int64_t>(seg) * kRowConsumerWarps;
             if (MODE == kSampleMode) {

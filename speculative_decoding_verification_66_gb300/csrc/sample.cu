@@ -144,7 +144,8 @@ __device__ __forceinline__ float elem(const uint8_t* p)
 struct SeqJob {
     RowPair rp;
     int64_t b;
-    bool ok;  // the scan found the sequence valid
+    bool ok;         // the scan found the sequence valid
+    bool bad_index;  // its emitted position failed the device-side index check
 };
 
 // Reads sequence b's record; returns the emitted position j.
@@ -155,6 +156,8 @@ __device__ __forceinline__ int load_seq(SeqJob& s, const SampleArgs& a, int64_t 
     s.b = b;
     s.ok = rec.status == 0;
     const int64_t K = g.K, row_bytes = g.V * es;
+    s.bad_index = s.ok && !SV_IN_RANGE(rec.j, K + 1);
+    if (s.bad_index) s.ok = false;
     const RowPairLayout& ly = a.lay;
     s.rp.trow = a.target + (b * ly.t_seq + rec.j * ly.t_pos) * row_bytes;
     s.rp.drow = rec.j < K ? a.draft + (b * ly.d_seq + rec.j * ly.d_pos) * row_bytes : nullptr;
@@ -591,7 +594,18 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_
     pdl_wait();  // the block sums are complete and visible
     SeqJob sj;
     const int j = load_seq(sj, a, b, ES);
-    if (!sj.ok) return;  // the scan wrote the outputs of an invalid sequence
+    if (!sj.ok) {
+        // The scan wrote the outputs of an invalid sequence; one whose record
+        // failed the index check is reported here.
+        if (sj.bad_index) {
+            for (int64_t i = t; i <= g.K; i += kRaceThreads) a.out_tokens[b * (g.K + 1) + i] = -1;
+            if (t == 0) {
+                a.num_accepted[b] = -1;
+                if (a.seq_status) a.seq_status[b] = kFlagIndex;
+            }
+        }
+        return;
+    }
     const int64_t nblk = g.nblocks;
     const float* W = a.block_sums + b * nblk;
     const uint2 key = make_uint2(static_cast<uint32_t>(a.seed), static_cast<uint32_t>(a.seed >> 32));
@@ -636,7 +650,8 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_
         blk = s_fb;
     }
     Best tok{0.0f, INT_MAX};
-    if (!bad && blk.idx != INT_MAX) {
+    const bool blk_ok = blk.idx == INT_MAX || SV_IN_RANGE(blk.idx, nblk);
+    if (!bad && blk_ok && blk.idx != INT_MAX) {
         const int64_t k0 = static_cast<int64_t>(blk.idx) * kRaceBlock + 4 * t;
         float xt[4], xd[4], w[4];
         group_load<ES, ALIGNED>(a, sj.rp, b, k0, g.V, xt, xd);
@@ -645,11 +660,12 @@ __global__ void __launch_bounds__(kRaceThreads) sample_race_kernel(const __grid_
     }
     tok = cta_best(tok, red);
     const int64_t K1 = g.K + 1;
-    if (bad || tok.idx == INT_MAX) {
+    const bool idx_ok = blk_ok && (tok.idx == INT_MAX || SV_IN_RANGE(tok.idx, g.V));
+    if (bad || !idx_ok || tok.idx == INT_MAX) {
         for (int64_t i = t; i < K1; i += kRaceThreads) a.out_tokens[b * K1 + i] = -1;
         if (t == 0) {
             a.num_accepted[b] = -1;
-            if (a.seq_status) a.seq_status[b] = kFlagTimeout;
+            if (a.seq_status) a.seq_status[b] = idx_ok ? kFlagTimeout : kFlagIndex;
         }
     } else if (t == 0) {
         a.out_tokens[b * K1 + j] = tok.idx;

@@ -199,6 +199,7 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
     const int64_t sq = blockIdx.x;
     if (sq >= nseq) return;
     const int64_t b = m.active != nullptr ? m.active[sq] : sq;
+    if (!SV_IN_RANGE(b, a.g.B)) return;  // a listed sequence outside the batch: nothing to report to
     const int64_t K = g.K, V = g.V;
     const bool sampling = g.mode == 0;
     const int p0 = m.p0;
@@ -249,7 +250,9 @@ __global__ void __launch_bounds__(kScanMaxThreads, 2) scan_kernel(const __grid_c
         const int64_t row = q < m.nt ? sq * m.nt + q : nseq * m.nt + sq * m.nd + (q - m.nt);
         RowNorm nm{0.f, 0.f, 0.f};
         int am = 0, fl = 0;
-        if (a.filt != nullptr) {
+        if (!SV_IN_RANGE(row, nseq * nrows)) {
+            fl = kFlagIndex;
+        } else if (a.filt != nullptr) {
             const FiltRow fr = a.filt[row];
             nm = RowNorm{fr.m, fr.l, fr.thr};
             fl = fr.flags;

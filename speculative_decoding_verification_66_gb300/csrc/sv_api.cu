@@ -955,3 +955,12 @@ SV_EXPORT const char* sv_error_string(int code)
 }
 
 SV_EXPORT int sv_version(void) { return 105; }
+
+SV_EXPORT int sv_device_checks(void)
+{
+#ifdef SV_DEVICE_CHECKS
+    return 1;
+#else
+    return 0;
+#endif
+}

@@ -12,6 +12,23 @@
 namespace sv {
 
 // ---------------------------------------------------------------------------
+// Device-side index checks
+// ---------------------------------------------------------------------------
+// Built with -DSV_DEVICE_CHECKS (the library's debug variant), SV_IN_RANGE(i,
+// n) tests 0 <= i < n where a kernel indexes memory by a value it computed or
+// read; a kernel whose test fails skips that access and reports kFlagIndex
+// (SV_SEQ_INDEX) for the row or sequence it was working on, never a trap.
+// In the product build the tests are the constant true and cost nothing.
+#ifdef SV_DEVICE_CHECKS
+constexpr bool kDeviceChecks = true;
+#define SV_IN_RANGE(i, n) \
+    (static_cast<long long>(i) >= 0 && static_cast<long long>(i) < static_cast<long long>(n))
+#else
+constexpr bool kDeviceChecks = false;
+#define SV_IN_RANGE(i, n) true
+#endif
+
+// ---------------------------------------------------------------------------
 // Arithmetic
 // ---------------------------------------------------------------------------
 // 2^x on the special-function unit (ex2.approx, subnormal results flushed).

@@ -38,6 +38,7 @@ constexpr int kMaxK = 1024;
 constexpr int kFlagNonFinite = 2;  // == SV_SEQ_NONFINITE
 constexpr int kFlagTimeout = 4;    // == SV_SEQ_TIMEOUT
 constexpr int kFlagBadToken = 1;   // == SV_SEQ_BAD_TOKEN
+constexpr int kFlagIndex = 8;      // == SV_SEQ_INDEX (device-side index checks)
 
 // One warp's reduction of one row segment.
 //   sampling: (hi + lo) * 2^m = sum over the segment of 2^(x*c), kept as a float

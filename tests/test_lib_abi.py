@@ -42,7 +42,7 @@ def test_header_declares_the_api():
         "sv_lmhead_workspace_bytes", "spec_verify_lmhead", "spec_verify_lmhead_debug",
         "spec_verify_lmhead_timed", "spec_verify_lmhead_gated", "sv_lmhead_logits",
         "sv_error_string",
-        "sv_version"])
+        "sv_version", "sv_device_checks"])
 
 
 def test_every_declared_symbol_is_exported(lib):
@@ -66,7 +66,7 @@ def test_python_binding_names_match_the_header():
     from speculative_decoding_verification_66_gb300 import _lib
     assert sorted(_lib.SIGNATURES) == declared_functions()
     for name in declared_functions():
-        if name not in ("sv_error_string", "sv_version"):
+        if name not in ("sv_error_string", "sv_version"):  # (sv_device_checks: api.py)
             assert callable(getattr(sv, name)), name
 
 
