@@ -492,11 +492,11 @@ def main():
         del shard_sets, ws_sh
 
     # Top-k / top-p on both rows (a variant, reported beside the full pass):
-    # the same logits, drafts redrawn from the filtered draft rows.
-    filtered = None
-    if args.filtered_steps > 0 and mode == "sample":
+    # the same logits, drafts redrawn from the filtered draft rows. Two cuts:
+    # top-k with top-p (the group-maxima thresholds kernel) and top-p alone
+    # (the value-count thresholds kernel).
+    def run_filtered(tk, tp):
         from speculative_decoding_verification_66_gb300.workloads import draw_from_logits
-        tk, tp = args.top_k, args.top_p
         gen = torch.Generator(device=dev)
         gen.manual_seed(4321 + rank)
         f_tokens = [draw_from_logits(c["draft"], wl.temperature, gen, tk, tp) for c in copies]
@@ -535,15 +535,24 @@ def main():
         # The thresholds pass must read every row once (further sweeps of a
         # row are meant to hit L2): the same algorithmic bytes as pass 1.
         thr_gbs = pass1_bytes / (thr_ms / 1e3) / 1e9
-        filtered = {"top_k": tk, "top_p": tp, "value": job_throughput(world, B, 1, f_ms / 1e3),
-                    "unit": "seqs/s", "ms_per_step": f_ms, "steps": args.filtered_steps,
-                    "mean_accepted": sum(f_acc) / len(f_acc),
-                    "stage_ms": {"thresholds": thr_ms, "scan": f_scan_ms, "sample": f_sample_ms,
-                                 "steps_timed": n_f},
-                    "thresholds_kernel": {"bound": "hbm", "achieved": thr_gbs, "peak": peak,
-                                          "unit": "GB/s", "frac": thr_gbs / peak,
-                                          "algorithmic_bytes": pass1_bytes}}
+        res = {"top_k": tk, "top_p": tp, "value": job_throughput(world, B, 1, f_ms / 1e3),
+               "unit": "seqs/s", "ms_per_step": f_ms, "steps": args.filtered_steps,
+               "mean_accepted": sum(f_acc) / len(f_acc),
+               "stage_ms": {"thresholds": thr_ms, "scan": f_scan_ms, "sample": f_sample_ms,
+                            "steps_timed": n_f},
+               "thresholds_kernel": {"kernel": "hist_kernel" if tk == 0 or tk > 64
+                                     else "filter_kernel",
+                                     "bound": "hbm", "achieved": thr_gbs, "peak": peak,
+                                     "unit": "GB/s", "frac": thr_gbs / peak,
+                                     "algorithmic_bytes": pass1_bytes}}
         del ws_f, f_tokens
+        return res
+
+    filtered = filtered_top_p = None
+    if args.filtered_steps > 0 and mode == "sample":
+        filtered = run_filtered(args.top_k, args.top_p)
+        if args.top_p < 1.0:
+            filtered_top_p = run_filtered(0, args.top_p)
 
     # Verification from the models' last hidden states (a variant, reported
     # beside the full pass): the LM heads run on the tensor cores with the row
@@ -713,6 +722,8 @@ def main():
         line["sharded"] = sharded
     if filtered is not None:
         line["filtered"] = filtered
+    if filtered_top_p is not None:
+        line["filtered_top_p"] = filtered_top_p
     if lmhead is not None:
         line["lmhead"] = lmhead
     if world == 1 and not args.no_cpu_baseline:

@@ -153,13 +153,33 @@ __device__ __forceinline__ uint32_t win_addr(uint32_t win, uint32_t g)
     return win + static_cast<uint32_t>(i * 4);
 }
 
+__device__ __forceinline__ uint32_t umin16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("min.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+__device__ __forceinline__ uint32_t umax16x2(uint32_t a, uint32_t b)
+{
+    uint32_t d;
+    asm("max.u16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
 // Adds the two elements of a 32-bit word to the packed window: +1 for a
 // positive value, +2^16 for a negative one (prmt replicates the sign bit of
-// byte 1 or byte 3 into 0xFFFF, which plus one is 2^16).
-__device__ __forceinline__ void count_pair(uint32_t win, uint32_t w)
+// byte 1 or byte 3 into 0xFFFF, which plus one is 2^16). Both word indices
+// come out of one packed computation: each magnitude g, offset by 2^15 - kG0
+// (no half can carry), clamped to [2^15 - 1, 2^15 + kWin], is 2^15 plus its
+// window index as win_addr clamps it; win_b is the window's address minus
+// 4 2^15.
+__device__ __forceinline__ void count_pair(uint32_t win_b, uint32_t w)
 {
-    red_add(win_addr(win, w & 0x7FFFu), prmt(w, 0u, 0x4499u) + 1u);
-    red_add(win_addr(win, (w >> 16) & 0x7FFFu), prmt(w, 0u, 0x44BBu) + 1u);
+    constexpr uint32_t kBias = (0x8000u - kG0) * 0x10001u;
+    constexpr uint32_t kLo = 0x7FFFu * 0x10001u, kHi = (0x8000u + kWin) * 0x10001u;
+    const uint32_t i2 = umin16x2(umax16x2((w & 0x7FFF7FFFu) + kBias, kLo), kHi);
+    red_add(win_b + ((i2 & 0xFFFFu) << 2), prmt(w, 0u, 0x4499u) + 1u);
+    red_add(win_b + ((i2 >> 16) << 2), prmt(w, 0u, 0x44BBu) + 1u);
 }
 
 // One element given by its 16 bits, in table mode MODE.
@@ -179,7 +199,7 @@ template <int MODE>
 __device__ __forceinline__ void count_word(uint32_t win, uint32_t w)
 {
     if (MODE == kPacked) {
-        count_pair(win, w);
+        count_pair(win - 4u * 0x8000u, w);
     } else {
         count_one<MODE>(win, w & 0xFFFFu);
         count_one<MODE>(win, w >> 16);

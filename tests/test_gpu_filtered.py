@@ -314,24 +314,26 @@ def test_filtered_single_sequence_full_vocab():
     assert st["decisions"] > 0
 
 
-def test_thresholds_kernel_timeout_path():
-    """The thresholds kernel's timeout path, without a fault: its copies are
+@pytest.mark.parametrize("top_k,top_p", [(40, 0.9), (0, 0.9)])
+def test_thresholds_kernel_timeout_path(top_k, top_p):
+    """The thresholds kernels' timeout path, without a fault: their reads are
     held behind a device flag that nothing sets; every CTA marks its rows as
     timed out, and every sequence is reported as SV_SEQ_TIMEOUT. A gated call
-    whose flag is already set matches spec_verify_filtered."""
+    whose flag is already set matches spec_verify_filtered. Top-k 40 runs the
+    group-maxima kernel, top-p alone (bf16) the value-count kernel."""
     wl = WORKLOADS["spiky_bf16"].resized(B=6, K=3, V=3000)
-    inputs = make_inputs(wl, 2, "cuda", top_k=40, top_p=0.9)
+    inputs = make_inputs(wl, 2, "cuda", top_k=top_k, top_p=top_p)
     gate = torch.zeros(1, dtype=torch.int32, device="cuda")
     r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
-                             wl.temperature, 9, "sample", stage=1, top_k=40, top_p=0.9)
+                             wl.temperature, 9, "sample", stage=1, top_k=top_k, top_p=top_p)
     torch.cuda.synchronize()
     assert (r["seq_status"].cpu() == sv.SV_SEQ_TIMEOUT).all()
     assert (r["num_accepted"].cpu() == -1).all()
     gate.fill_(1)
     r = sv.spec_verify_gated(inputs["target"], inputs["draft"], inputs["tokens"], gate,
-                             wl.temperature, 9, "sample", stage=1, top_k=40, top_p=0.9)
+                             wl.temperature, 9, "sample", stage=1, top_k=top_k, top_p=top_p)
     out, nacc = sv.spec_verify_filtered(inputs["target"], inputs["draft"], inputs["tokens"],
-                                        wl.temperature, 40, 0.9, 9, "sample")
+                                        wl.temperature, top_k, top_p, 9, "sample")
     torch.cuda.synchronize()
     assert (r["seq_status"].cpu() == 0).all()
     assert torch.equal(r["out_tokens"], out) and torch.equal(r["num_accepted"], nacc)
