@@ -226,6 +226,42 @@ def test_filtered_value_shared_by_2_16_tokens(fill, top_k, top_p):
     assert (g["num_accepted"] >= 0).all()
 
 
+@pytest.mark.parametrize("case", ["zeros", "tiny", "huge"])
+@pytest.mark.parametrize("top_k,top_p", [(0, 0.99), (2500, 1.0), (3000, 0.9)])
+def test_filtered_values_outside_the_count_window(case, top_k, top_p):
+    """bfloat16 rows whose crossing falls among values the value-count kernel
+    keeps only in its outer words (|x| < 2^-64: exact zeros of both signs, or
+    tiny magnitudes) or whose maximum is 2^64 or more; the row is then counted
+    again with 32-bit counts over the whole range of magnitudes."""
+    wl = WORKLOADS["spiky_bf16"].resized(B=4, K=3, V=4000)
+    inputs = make_inputs(wl, 37, "cuda", top_k=top_k, top_p=top_p)
+    g = torch.Generator(device="cuda")
+    g.manual_seed(37)
+    for key in ("target", "draft"):
+        x = inputs[key].float()
+        if case == "zeros":
+            # 2000 logits near 0.5, the rest +0 and -0: the crossings of
+            # top-p 0.99 and of k = 2500 / 3000 lie among the zeros.
+            x = torch.where(torch.rand(x.shape, generator=g, device="cuda") < 0.5,
+                            0.5 + 0.01 * x, torch.zeros_like(x))
+            x = torch.where((x == 0) & (torch.rand(x.shape, generator=g, device="cuda") < 0.5),
+                            -x, x)
+        elif case == "tiny":
+            # Half the logits are of magnitude 2^-80 .. 2^-70, both signs.
+            tiny = torch.sign(x) * 2.0 ** (-80 + 10 * torch.rand(x.shape, generator=g,
+                                                                  device="cuda"))
+            x = torch.where(torch.rand(x.shape, generator=g, device="cuda") < 0.5, 0.3 * x, tiny)
+        else:
+            # The maximum of every row at 2^70 (the other logits ordinary).
+            x[..., 17] = 2.0 ** 70
+        inputs[key] = x.to(inputs[key].dtype)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(37)
+    inputs["tokens"] = draw_from_logits(inputs["draft"], wl.temperature, gen, top_k, top_p)
+    st, g_out, orc = check(wl, 37, top_k, top_p, device_inputs=inputs)
+    assert (g_out["num_accepted"] >= 0).all()
+
+
 def test_filtered_off_is_spec_verify():
     wl = WORKLOADS["spiky_bf16"].resized(B=32)
     inputs = make_inputs(wl, 2, "cuda")
