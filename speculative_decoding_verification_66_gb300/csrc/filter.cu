@@ -502,95 +502,135 @@ __device__ __noinline__ uint32_t list_select_mass(const uint32_t* keys, int n, u
 }
 
 // Top-k then top-p on a list of n <= kSmallList keys by one warp, without
-// block barriers: for each element its rank (keys above it, keys at or above
-// it) and its upper-set mass, by a pass over the whole list. The k-th largest
-// key tau_k is the one with fewer than k keys above it and at least k at or
-// above it; the top-p threshold is the largest key whose upper-set mass
-// reaches ceil(top_p * mass(tau_k)). w: scratch for the n masses. Lane 0's
-// results are the answer.
+// block barriers. The warp sorts the keys in descending order (a bitonic
+// network over P keys per lane, lane l holding positions l*P .. l*P+P-1, the
+// padding keys 0 sinking below every real key); a key's rank window is then
+// its position, and masses follow from the sorted keys. The k-th largest key
+// tau_k sits at position k-1; the top-p threshold is the key at the first
+// position whose inclusive mass prefix reaches ceil(top_p * mass(tau_k)) —
+// the largest key whose upper-set mass reaches it, since every earlier tie
+// group ends before that position. Every lane returns the results.
 constexpr int kSmallList = 128;
 
-__device__ __noinline__ void small_select(const uint32_t* keys, int n, bool tk, uint64_t k, bool tp,
-                                          float top_p, float c, float mref, uint64_t* w,
-                                          uint32_t* tau_out, uint64_t* kept_out)
+template <int P>
+__device__ __forceinline__ void warp_sort_desc(uint32_t (&v)[P], int lane)
 {
-    const int lane = threadIdx.x & 31;
-    constexpr int kPer = kSmallList / 32;
-    for (int i = lane; i < n; i += 32) w[i] = mass_of(key_value(keys[i]), c, mref);
-    __syncwarp();
-    uint32_t kk[kPer];
-    int gt[kPer], ge[kPer];
-    uint64_t up[kPer];
+    constexpr int N = 32 * P;
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-        const int i = lane + 32 * q;
-        kk[q] = i < n ? keys[i] : 0u;
-        gt[q] = ge[q] = 0;
-        up[q] = 0;
-    }
-    for (int j = 0; j < n; ++j) {
-        const uint32_t kj = keys[j];
-        const uint64_t wj = w[j];
+    for (int size = 2; size <= N; size <<= 1) {
 #pragma unroll
-        for (int q = 0; q < kPer; ++q) {
-            gt[q] += kj > kk[q];
-            ge[q] += kj >= kk[q];
-            up[q] += kj >= kk[q] ? wj : 0u;
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride < P) {
+#pragma unroll
+                for (int r = 0; r < P; ++r) {
+                    if (r & stride) continue;
+                    const int e = lane * P + r;
+                    const uint32_t hi = max(v[r], v[r | stride]), lo = min(v[r], v[r | stride]);
+                    const bool desc = (e & size) == 0;
+                    v[r] = desc ? hi : lo;
+                    v[r | stride] = desc ? lo : hi;
+                }
+            } else {
+                const int lm = stride / P;
+                const bool lower = (lane & lm) == 0;
+#pragma unroll
+                for (int r = 0; r < P; ++r) {
+                    const int e = lane * P + r;
+                    const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v[r], lm);
+                    const bool desc = (e & size) == 0;
+                    v[r] = (lower == desc) ? max(v[r], o) : min(v[r], o);
+                }
+            }
         }
     }
-    // tau_k: the largest key with rank window containing k (all such keys are equal).
-    uint32_t tau = 0u;
+}
+
+template <int P>
+__device__ __forceinline__ void small_select_p(const uint32_t* keys, int n, bool tk, uint64_t k, bool tp,
+                                               float top_p, float c, float mref, uint32_t* tau_out,
+                                               uint64_t* kept_out)
+{
+    const int lane = threadIdx.x & 31;
+    uint32_t v[P];
 #pragma unroll
-    for (int q = 0; q < kPer; ++q) {
-        const bool real = lane + 32 * q < n;
-        if (real && (!tk || (static_cast<uint64_t>(gt[q]) < k && static_cast<uint64_t>(ge[q]) >= k)))
-            tau = tk ? kk[q] : 0u;
+    for (int r = 0; r < P; ++r) {
+        const int i = lane * P + r;
+        v[r] = i < n ? keys[i] : 0u;
     }
-    if (!tk) {
-        // No top-k cut: every key counts; tau_k is the smallest key.
-        uint32_t mn = 0xFFFFFFFFu;
+    warp_sort_desc<P>(v, lane);
+    uint64_t w[P];
 #pragma unroll
-        for (int q = 0; q < kPer; ++q)
-            if (lane + 32 * q < n) mn = kk[q] < mn ? kk[q] : mn;
+    for (int r = 0; r < P; ++r) w[r] = lane * P + r < n ? mass_of(key_value(v[r]), c, mref) : 0u;
+    // The key at sorted position pos (0 <= pos < 32 P), broadcast from its lane.
+    auto at = [&](int pos) {
+        uint32_t mine = v[0];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) mn = min(mn, __shfl_xor_sync(0xFFFFFFFFu, mn, off));
-        tau = mn;
-    } else {
+        for (int r = 1; r < P; ++r)
+            if (pos % P == r) mine = v[r];
+        return __shfl_sync(0xFFFFFFFFu, mine, pos / P);
+    };
+    // Sum of the masses of the real keys >= x, over the warp.
+    auto mass_ge = [&](uint32_t x) {
+        uint64_t acc = 0;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) tau = max(tau, __shfl_xor_sync(0xFFFFFFFFu, tau, off));
-    }
-    uint64_t mass_k = 0;
+        for (int r = 0; r < P; ++r)
+            if (lane * P + r < n && v[r] >= x) acc += w[r];
 #pragma unroll
-    for (int q = 0; q < kPer; ++q)
-        if (lane + 32 * q < n && kk[q] >= tau) mass_k += w[lane + 32 * q];
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) mass_k += __shfl_xor_sync(0xFFFFFFFFu, mass_k, off);
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, off);
+        return acc;
+    };
+    uint32_t tau;
+    if (tk)
+        tau = (k >= 1 && k <= static_cast<uint64_t>(n)) ? at(static_cast<int>(k) - 1) : 0u;
+    else
+        tau = n > 0 ? at(n - 1) : 0xFFFFFFFFu;
+    const uint64_t mass_k = mass_ge(tau);
     uint64_t kept = mass_k;
     if (tp) {
         const uint64_t target =
             static_cast<uint64_t>(ceil(static_cast<double>(top_p) * static_cast<double>(mass_k)));
-        uint32_t best = 0u;
-        uint64_t best_up = 0u;
+        uint64_t run = 0;
 #pragma unroll
-        for (int q = 0; q < kPer; ++q)
-            if (lane + 32 * q < n && up[q] >= target && kk[q] > best) {
-                best = kk[q];
-                best_up = up[q];
-            }
+        for (int r = 0; r < P; ++r) run += w[r];
+        // Exclusive prefix of the lane totals.
+        uint64_t inc = run;
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const uint32_t ob = __shfl_xor_sync(0xFFFFFFFFu, best, off);
-            const uint64_t ou = __shfl_xor_sync(0xFFFFFFFFu, best_up, off);
-            if (ob > best) {
-                best = ob;
-                best_up = ou;
-            }
+        for (int off = 1; off < 32; off <<= 1) {
+            const uint64_t o = __shfl_up_sync(0xFFFFFFFFu, inc, off);
+            if (lane >= off) inc += o;
         }
-        tau = best;
-        kept = best_up;
+        run = inc - run;
+        int first = -1;
+#pragma unroll
+        for (int r = 0; r < P; ++r) {
+            run += w[r];
+            if (first < 0 && lane * P + r < n && run >= target) first = r;
+        }
+        // No hit, or a hit on key 0 (no logit has it), leaves (0, 0).
+        const uint32_t hit = __ballot_sync(0xFFFFFFFFu, first >= 0);
+        tau = 0u;
+        kept = 0u;
+        if (hit != 0u) {
+            const int src = __ffs(hit) - 1;
+            const int r0 = __shfl_sync(0xFFFFFFFFu, first, src);
+            tau = at(src * P + r0);
+            if (tau != 0u) kept = mass_ge(tau);
+        }
     }
     *tau_out = tau;
     *kept_out = kept;
+}
+
+__device__ __noinline__ void small_select(const uint32_t* keys, int n, bool tk, uint64_t k, bool tp,
+                                          float top_p, float c, float mref, uint32_t* tau_out,
+                                          uint64_t* kept_out)
+{
+    if (n <= 32)
+        small_select_p<1>(keys, n, tk, k, tp, top_p, c, mref, tau_out, kept_out);
+    else if (n <= 64)
+        small_select_p<2>(keys, n, tk, k, tp, top_p, c, mref, tau_out, kept_out);
+    else
+        small_select_p<4>(keys, n, tk, k, tp, top_p, c, mref, tau_out, kept_out);
 }
 
 // small_select for lists of up to kMidList keys by the whole CTA: each thread
@@ -1277,7 +1317,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                 if (t < 32) {
                     uint32_t tw;
                     uint64_t kw;
-                    small_select(list, n, tk, k, tp, a.top_p, c, mref, hm, &tw, &kw);
+                    small_select(list, n, tk, k, tp, a.top_p, c, mref, &tw, &kw);
                     if (t == 0) {
                         s.above = kw;
                         s.e = static_cast<int>(tw);
