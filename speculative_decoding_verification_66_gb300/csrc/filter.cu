@@ -20,24 +20,32 @@
 // different warps never contend. Run over a whole row, that select would cost
 // some twenty instructions and a contended atomic per element -- several
 // times the HBM budget -- so it runs on a short list of candidates instead:
-//  * first read (HBM): each thread keeps the maximum of each lane position
-//    of its 16-byte vectors (NaN-propagating packed max: half an instruction
-//    per bf16 element), which gives the row maximum, the NaN / +inf check and
-//    4096 (bf16) or 2048 (fp32) group maxima of disjoint groups.
-//  * top-k (k up to the number of groups, with or without top-p): the k-th
-//    largest group maximum, to 16 bits, bounds the k-th largest logit from
-//    below. A second read (from L2) compares packed pairs against the bound
-//    and appends the few elements at or above it -- about k -- to the list,
-//    which then holds the whole top-k set.
-//  * top-p alone: the second read adds each element's mass into per-thread
-//    private bins (no atomics) by its log2 distance from the row maximum,
-//    32 bins of one unit; the bin where the running mass from the top reaches
-//    top_p times the row mass is read again into the list, or, when it holds
-//    too many elements, split into 32 sub-bins the same way, up to three times.
-//  * anything else (larger k, a list that overflows, a crossing in the
-//    bins' far tail) runs the radix select over the whole row.
-// Sweeps after the first read the row again, normally from L2 (two CTAs per SM
-// keep about 300 rows, some 80 MB of bf16 rows of 128K tokens, in flight).
+//  * first read (HBM): each thread keeps, per lane position of its 16-byte
+//    vectors (a group), the maximum and the second largest value (packed
+//    NaN-propagating max and min, about 1.5 instructions per bf16 element),
+//    which gives the row maximum, the NaN / +inf check and 2048 (bf16) or
+//    1024 (fp32) group maxima of disjoint groups.
+//  * top-k (with or without top-p): the k-th largest thread maximum (k up to
+//    64: one warp sorts the 256 of them) or group maximum (larger k, float32
+//    rows: a radix select) bounds the k-th largest logit from below. A group
+//    whose second value is below the bound holds at most one element above
+//    it, its maximum, which joins the list; the few thread shares with a
+//    group of two or more are read again (from L2), or, when more than 16
+//    are, the whole row with a packed compare. The list then holds the whole
+//    top-k set (about k keys), and the cuts are resolved on it: one warp sorts
+//    lists of up to 128 keys, the CTA ranks lists of up to 512, a radix select
+//    takes longer ones.
+//  * top-p alone (float32 rows): the second read adds each element's mass
+//    into per-thread private bins (no atomics) by its log2 distance from the
+//    row maximum, 32 bins of one unit; the bin where the running mass from the
+//    top reaches top_p times the row mass is read again into the list, or,
+//    when it holds too many elements, split into 32 sub-bins the same way, up
+//    to three times.
+//  * anything else (a list that overflows, a crossing in the bins' far tail)
+//    runs the radix select over the whole row.
+// Sweeps after the first read the row again, normally from L2 (four CTAs per
+// SM keep about 600 rows, some 150 MB of bf16 rows of 128K tokens, in flight,
+// so a share read again may also come from HBM).
 //
 // Masses are integers, so every sum -- and every decision -- is the same on
 // every run: a list element's mass is its 2^(x c - m) (m the ceiling of
@@ -512,6 +520,9 @@ __device__ __noinline__ uint32_t list_select_mass(const uint32_t* keys, int n, u
 // group ends before that position. Every lane returns the results.
 constexpr int kSmallList = 128;
 
+// Sorts 32 P keys held P per lane (key r of lane l is element l P + r) into
+// descending order across the warp: a bitonic network, compare-exchanges in
+// registers for partners in the same lane and by shuffles otherwise.
 template <int P>
 __device__ __forceinline__ void warp_sort_desc(uint32_t (&v)[P], int lane)
 {
@@ -954,41 +965,6 @@ __device__ __forceinline__ uint32_t bf16_bits_of_key16(uint32_t p)
     return (p & 0x8000u) ? (p & 0x7FFFu) : (~p & 0xFFFFu);
 }
 
-// Sorts 256 keys held 8 per lane (key j of lane l is element 8 l + j) into
-// descending order across the warp: a bitonic network, compare-exchanges in
-// registers for partners in the same lane and by shuffles otherwise.
-__device__ __forceinline__ void warp_sort256_desc(uint32_t (&v)[8])
-{
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int size = 2; size <= 256; size <<= 1) {
-#pragma unroll
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride >= 8) {
-                const int ls = stride >> 3;
-                const bool lower = (lane & ls) == 0;
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t o = __shfl_xor_sync(0xFFFFFFFFu, v[j], ls);
-                    const bool desc = ((lane * 8 + j) & size) == 0;
-                    v[j] = (lower == desc) ? max(v[j], o) : min(v[j], o);
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int pj = j ^ stride;
-                    if (pj > j) {
-                        const bool desc = ((lane * 8 + j) & size) == 0;
-                        const uint32_t x = v[j], y = v[pj];
-                        v[j] = desc ? max(x, y) : min(x, y);
-                        v[pj] = desc ? min(x, y) : max(x, y);
-                    }
-                }
-            }
-        }
-    }
-}
-
 // Packed x >= y on both bf16 halves: 0xFFFF per half where it holds.
 __device__ __forceinline__ unsigned ge2_mask(uint32_t a, uint32_t b)
 {
@@ -1237,7 +1213,7 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                     uint32_t v[8];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) v[j] = cand[8 * t + j];
-                    warp_sort256_desc(v);
+                    warp_sort_desc<8>(v, t);
                     const int kk = static_cast<int>(k) - 1;
                     if (t == (kk >> 3)) {
 #pragma unroll
