@@ -203,6 +203,56 @@ def test_filtered_many_ties_at_the_top(top_k, top_p):
     assert (g["num_accepted"] >= 0).all()
 
 
+def _top_block(wl, seed, top_k, top_p, values, step):
+    """Inputs whose every row has len(values) logits set to `values`, `step`
+    tokens apart, above all the other logits (clamped to 3); tokens drawn
+    from the filtered draft rows. A thread share of the group-maxima kernel
+    is every 256th 16-byte vector of the row (8 bf16 or 4 float32 logits)."""
+    inputs = make_inputs(wl, seed, "cuda", top_k=top_k, top_p=top_p)
+    n = len(values)
+    for j, key in enumerate(("target", "draft")):
+        x = inputs[key].float().clamp(max=3.0)
+        pos = torch.arange(n, device="cuda") * step + 3 * j + 1
+        x[..., pos] = torch.tensor(values, device="cuda", dtype=torch.float32)
+        inputs[key] = x.to(inputs[key].dtype)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed)
+    inputs["tokens"] = draw_from_logits(inputs["draft"], wl.temperature, gen, top_k, top_p)
+    return inputs
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("top_p", [1.0, 0.9])
+@pytest.mark.parametrize("top_k", [1, 31, 32, 33, 63, 64])
+def test_filtered_list_of_k_distinct_keys(dtype, top_k, top_p):
+    """80 distinct values above the rest of the row, 392 tokens apart (49
+    bf16 or 98 float32 vectors: 80 different thread shares either way): the
+    k-th largest thread maximum is the k-th of them, so the candidate list
+    holds exactly k keys -- across the one-warp select's 32 / 64-key network
+    sizes."""
+    wl = WORKLOADS["small_f32"].resized(B=4, K=2, V=32000, dtype=dtype)
+    values = [8.0 + 0.0625 * i for i in range(80)]
+    inputs = _top_block(wl, 41, top_k, top_p, values, 392)
+    st, g, orc = check(wl, 41, top_k, top_p, device_inputs=inputs)
+    assert (g["num_accepted"] >= 0).all()
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("top_k,top_p", [(5, 1.0), (64, 0.5)])
+@pytest.mark.parametrize("m", [32, 33, 64, 65, 128, 129])
+def test_filtered_list_of_m_tied_maxima(dtype, m, top_k, top_p):
+    """m logits tied at the row maximum, spread over the row: with k <= m the
+    bound is the maximum itself and the candidate list is the m ties (two in
+    one thread share are read again, not lost) -- across the one-warp
+    select's 32 / 64 / 128-key sizes and the hand-over to the CTA select
+    above 128; with k = 64 > m = 32 or 33 the list also takes the largest of
+    the other logits."""
+    wl = WORKLOADS["small_f32"].resized(B=4, K=2, V=32000, dtype=dtype)
+    inputs = _top_block(wl, 43, top_k, top_p, [9.0] * m, wl.V // m)
+    st, g, orc = check(wl, 43, top_k, top_p, device_inputs=inputs)
+    assert (g["num_accepted"] >= 0).all()
+
+
 @pytest.mark.parametrize("fill", ["max", "-inf", "-5"])
 @pytest.mark.parametrize("top_k,top_p", [(0, 0.9), (100, 1.0), (150000, 0.95), (2000, 0.8)])
 def test_filtered_value_shared_by_2_16_tokens(fill, top_k, top_p):
