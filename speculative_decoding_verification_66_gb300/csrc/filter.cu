@@ -26,7 +26,7 @@
 //    which gives the row maximum, the NaN / +inf check and 2048 (bf16) or
 //    1024 (fp32) group maxima of disjoint groups.
 //  * top-k (with or without top-p): the k-th largest thread maximum (k up to
-//    64: one warp sorts the 256 of them) or group maximum (larger k, float32
+//    64: the CTA sorts the 256 of them) or group maximum (larger k, float32
 //    rows: a radix select) bounds the k-th largest logit from below. A group
 //    whose second value is below the bound holds at most one element above
 //    it, its maximum, which joins the list; the few thread shares with a
@@ -988,7 +988,7 @@ __device__ __forceinline__ uint32_t bf16x2_min(uint32_t a, uint32_t b)
 // out. The CTA reads the shares' vectors together, one vector per thread per
 // round, the loads of a round issued before any is used.
 template <int ES>
-__device__ __noinline__ void reread_shares(const uint8_t* row, int64_t V, const int* inc, int ninc,
+__device__ __forceinline__ void reread_shares(const uint8_t* row, int64_t V, const int* inc, int ninc,
                                            uint32_t lk, uint32_t* list, int* count)
 {
     constexpr int kEPV = 16 / ES;
@@ -1202,25 +1202,30 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
             uint32_t lk;
             if (k <= static_cast<uint64_t>(kSortK) && T == 256) {
                 // For small k the thread maxima (distinct elements as well)
-                // give a bound almost as tight: one warp sorts them and
-                // takes the k-th.
+                // give a bound almost as tight: the CTA sorts them, one per
+                // thread (a bitonic network: shuffles within a warp, shared
+                // memory across warps), and takes the k-th.
                 uint32_t tm = fkey(m1[0]);
 #pragma unroll
                 for (int q = 1; q < G; ++q) tm = max(tm, fkey(m1[q]));
-                cand[t] = tm;
-                __syncthreads();
-                if (t < 32) {
-                    uint32_t v[8];
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) v[j] = cand[8 * t + j];
-                    warp_sort_desc<8>(v, t);
-                    const int kk = static_cast<int>(k) - 1;
-                    if (t == (kk >> 3)) {
+                for (int size = 2; size <= 256; size <<= 1) {
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            if (j == (kk & 7)) s.lo = static_cast<int>(v[j]);
+                    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+                        uint32_t o;
+                        if (stride < 32) {
+                            o = __shfl_xor_sync(0xFFFFFFFFu, tm, stride);
+                        } else {
+                            cand[t] = tm;
+                            __syncthreads();
+                            o = cand[t ^ stride];
+                            __syncthreads();
+                        }
+                        const bool lower = (t & stride) == 0, desc = (t & size) == 0;
+                        tm = (lower == desc) ? max(tm, o) : min(tm, o);
                     }
                 }
+                if (t == static_cast<int>(k) - 1) s.lo = static_cast<int>(tm);
                 __syncthreads();
                 lk = static_cast<uint32_t>(s.lo);
             } else {
@@ -1247,7 +1252,9 @@ __global__ void __launch_bounds__(kFilterThreads, 4) filter_kernel(const __grid_
                     else s.check = kFlagIndex;
                 }
                 __syncthreads();
-                reread_shares<ES>(row, V, inc, s.inc_n, lk, list, &s.list_n);
+                // Many rows need no share read again (about half at k = 50).
+                const int ninc = s.inc_n;
+                if (ninc > 0) reread_shares<ES>(row, V, inc, ninc, lk, list, &s.list_n);
             } else {
                 // Many groups hold two or more elements above the bound (k in the
                 // hundreds): one more read of the whole row, a packed compare
