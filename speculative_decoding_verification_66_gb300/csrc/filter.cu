@@ -509,17 +509,6 @@ __device__ __noinline__ uint32_t list_select_mass(const uint32_t* keys, int n, u
     return prefix;
 }
 
-// Top-k then top-p on a list of n <= kSmallList keys by one warp, without
-// block barriers. The warp sorts the keys in descending order (a bitonic
-// network over P keys per lane, lane l holding positions l*P .. l*P+P-1, the
-// padding keys 0 sinking below every real key); a key's rank window is then
-// its position, and masses follow from the sorted keys. The k-th largest key
-// tau_k sits at position k-1; the top-p threshold is the key at the first
-// position whose inclusive mass prefix reaches ceil(top_p * mass(tau_k)) —
-// the largest key whose upper-set mass reaches it, since every earlier tie
-// group ends before that position. Every lane returns the results.
-constexpr int kSmallList = 128;
-
 // Sorts 32 P keys held P per lane (key r of lane l is element l P + r) into
 // descending order across the warp: a bitonic network, compare-exchanges in
 // registers for partners in the same lane and by shuffles otherwise.
@@ -555,6 +544,17 @@ __device__ __forceinline__ void warp_sort_desc(uint32_t (&v)[P], int lane)
         }
     }
 }
+
+// Top-k then top-p on a list of n <= kSmallList keys by one warp, without
+// block barriers. The warp sorts the keys in descending order (a bitonic
+// network over P keys per lane, lane l holding positions l*P .. l*P+P-1, the
+// padding keys 0 sinking below every real key); a key's rank window is then
+// its position, and masses follow from the sorted keys. The k-th largest key
+// tau_k sits at position k-1; the top-p threshold is the key at the first
+// position whose inclusive mass prefix reaches ceil(top_p * mass(tau_k)) —
+// the largest key whose upper-set mass reaches it, since every earlier tie
+// group ends before that position. Every lane returns the results.
+constexpr int kSmallList = 128;
 
 template <int P>
 __device__ __forceinline__ void small_select_p(const uint32_t* keys, int n, bool tk, uint64_t k, bool tp,
