@@ -143,6 +143,10 @@ int make_plan(int64_t B, int64_t K, int64_t V, int dtype, int mode, Geometry* g,
     g->row_aligned = (g->row_len * es) % 16 == 0;
     // Misaligned rows need one extra 16-byte vector per tile in the buffer.
     g->tile_elems = (g->row_aligned ? sv::kRowTileBytes : sv::kRowTileBytes - 16) / es;
+    // Shard rows that fit a tile are a tile each: one bulk copy per tile
+    // instead of two pieces from two shards.
+    if (shards > 1 && g->row_shards == 1 && g->shard_len * es <= sv::kRowTileBytes)
+        g->tile_elems = g->shard_len;
     g->tiles_per_row = (g->row_len + g->tile_elems - 1) / g->tile_elems;
     g->tiles = g->rows * g->row_shards * g->tiles_per_row;
     if (early_exit) {
